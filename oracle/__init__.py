@@ -1,0 +1,272 @@
+"""CPU oracle for the W4A16 group-wise path -- TEST INFRASTRUCTURE ONLY.
+
+This package is a plain, slow, obviously correct restatement of what the path
+computes, used to judge the CUDA library.  Only ``tests/``, the smoke check
+in ``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` may import
+it.  The product library never imports, links or calls it, and it imports
+nothing from the product package.
+
+The arithmetic lives in ``w4a16_oracle.c`` (plain C, binary32 quantizer,
+binary64 dequantizer and GEMM); this module compiles it with gcc on first use
+and marshals numpy arrays through ctypes.  Sources, cited by page title and
+section:
+
+* "LLM quantization from IEEE 754 to GPTQ/AWQ/GGUF" tutorial (qaqbuyan.com
+  article 126), chapter "量化的数学基石": §1 FP16 bit layout, §2 symmetric
+  quantization formula, §3 per-group quantizer/dequantizer functions.
+* "W4A16 量化算子解码性能基准跑分与端侧大模型推理显存实测报告" (mhpq.cn):
+  §一 format (group 128, symmetric INT4, fp16 scales), §二/§五 the decode
+  product y = x W^T from the packed weights.
+
+Parity status of each function is stated in its docstring.
+"""
+from __future__ import annotations
+
+import ctypes
+import hashlib
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "w4a16_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LOCK = threading.Lock()
+_LIB = None
+
+GROUP = 128
+
+_CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+           "-fno-fast-math", "-fopenmp"]
+
+
+def _lib_path(src: str = _SRC) -> str:
+    with open(src, "rb") as f:
+        digest = hashlib.sha1(f.read() + " ".join(_CFLAGS).encode()).hexdigest()[:12]
+    return os.path.join(_BUILD_DIR, f"liboracle_{digest}.so")
+
+
+def build(src: str = _SRC, out: str | None = None, verbose: bool = False) -> str:
+    """Compile the oracle C source with gcc (idempotent); return the .so path.
+
+    ``src``/``out`` let the tests compile deliberately broken copies of the
+    oracle (planted mistakes) to show that the pins catch them."""
+    path = out or _lib_path(src)
+    if os.path.exists(path):
+        return path
+    os.makedirs(os.path.dirname(path), exist_ok=True)
+    tmp = path + f".tmp{os.getpid()}"
+    cmd = ["gcc", *_CFLAGS, "-o", tmp, src, "-lm"]
+    if verbose:
+        print(" ".join(cmd))
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, path)
+    return path
+
+
+def _bind(lib):
+    i64, p = ctypes.c_int64, ctypes.c_void_p
+    lib.orc_half_to_double.argtypes = [ctypes.c_uint16]
+    lib.orc_half_to_double.restype = ctypes.c_double
+    lib.orc_float_to_half.argtypes = [ctypes.c_float]
+    lib.orc_float_to_half.restype = ctypes.c_uint16
+    lib.orc_half_to_double_n.argtypes = [p, i64, p]
+    lib.orc_float_to_half_n.argtypes = [p, i64, p]
+    lib.orc_quantize.argtypes = [p, i64, i64, i64, p, p]
+    lib.orc_quantize.restype = ctypes.c_int
+    lib.orc_dequantize.argtypes = [p, p, i64, i64, i64, p]
+    lib.orc_dequantize.restype = ctypes.c_int
+    lib.orc_dequantize_f16.argtypes = [p, p, i64, i64, i64, p]
+    lib.orc_dequantize_f16.restype = ctypes.c_int
+    lib.orc_gemm.argtypes = [p, i64, i64, p, p, i64, i64, p]
+    lib.orc_gemm.restype = ctypes.c_int
+    lib.orc_gemm_rows.argtypes = [p, i64, i64, p, p, i64, i64, p, i64, p]
+    lib.orc_gemm_rows.restype = ctypes.c_int
+    lib.orc_num_threads.restype = ctypes.c_int
+    lib.orc_set_num_threads.argtypes = [ctypes.c_int]
+    return lib
+
+
+def _c(a: np.ndarray, dtype) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+class Oracle:
+    """One loaded build of the oracle library (the real one, or a test mutant)."""
+
+    def __init__(self, lib_path: str):
+        self.path = lib_path
+        self._lib = _bind(ctypes.CDLL(lib_path))
+
+    def num_threads(self) -> int:
+        return int(self._lib.orc_num_threads())
+
+    def set_num_threads(self, n: int) -> None:
+        self._lib.orc_set_num_threads(int(n))
+
+    # ------------------------------------------------------------------
+    # FP16 bit layout (tutorial §1).  Pinned: exhaustive / random
+    # comparison with numpy's IEEE float16 conversion.
+    # ------------------------------------------------------------------
+    def half_to_double(self, h: np.ndarray) -> np.ndarray:
+        """Exact binary64 value of fp16 bit patterns (uint16 array)."""
+        h = _c(h, np.uint16)
+        out = np.empty(h.shape, dtype=np.float64)
+        self._lib.orc_half_to_double_n(_ptr(h), h.size, _ptr(out))
+        return out
+
+    def float_to_half(self, f: np.ndarray) -> np.ndarray:
+        """fp16 bits (uint16) of binary32 values, round to nearest even."""
+        f = _c(f, np.float32)
+        out = np.empty(f.shape, dtype=np.uint16)
+        self._lib.orc_float_to_half_n(_ptr(f), f.size, _ptr(out))
+        return out
+
+    # ------------------------------------------------------------------
+    # Quantizer (tutorial §2 formula, §3 per_group_symmetric_quantize).
+    # Pinned: +-amax -> +-7, all-zero group, tie cases, small-scale clamp,
+    # round-trip bound, nearest-level brute force, scale through numpy,
+    # nibble-order fixture.
+    # ------------------------------------------------------------------
+    def quantize(self, W16: np.ndarray, group: int = GROUP):
+        """Group-wise symmetric RTN INT4 quantization of fp16 weights.
+
+        ``W16``: uint16 fp16 bit patterns, shape [N, K] (rows = out_features).
+        Returns ``(qweight uint8 [N, K/2], scales uint16 fp16 bits [N, K/group])``.
+        """
+        W16 = _c(W16, np.uint16)
+        if W16.ndim != 2:
+            raise ValueError("W must be 2-D [N, K]")
+        N, K = W16.shape
+        if group <= 0 or K % group:
+            raise ValueError(f"K={K} is not a multiple of group={group}")
+        q = np.empty((N, K // 2), dtype=np.uint8)
+        s = np.empty((N, K // group), dtype=np.uint16)
+        rc = self._lib.orc_quantize(_ptr(W16), N, K, group, _ptr(q), _ptr(s))
+        if rc != 0:
+            raise ValueError(f"oracle quantize rejected shape N={N} K={K} group={group}")
+        return q, s
+
+    # ------------------------------------------------------------------
+    # Dequantizer (tutorial §3 per_group_symmetric_dequantize).  Pinned:
+    # closed forms and the round-trip bound against the master weights.
+    # ------------------------------------------------------------------
+    def dequantize(self, qweight: np.ndarray, scales: np.ndarray,
+                   group: int = GROUP) -> np.ndarray:
+        """Exact dequantized weights (nibble - 8) * scale16 in binary64, [N, K]."""
+        qweight = _c(qweight, np.uint8)
+        scales = _c(scales, np.uint16)
+        N, K2 = qweight.shape
+        K = 2 * K2
+        out = np.empty((N, K), dtype=np.float64)
+        rc = self._lib.orc_dequantize(_ptr(qweight), _ptr(scales), N, K, group, _ptr(out))
+        if rc != 0:
+            raise ValueError("oracle dequantize rejected shape")
+        return out
+
+    def dequantize_f16(self, qweight: np.ndarray, scales: np.ndarray,
+                       group: int = GROUP) -> np.ndarray:
+        """The tutorial's own fp16 dequantized weight fp16(float(q) * float(s)).
+
+        Returns uint16 fp16 bits [N, K].  Pinned: equals the single fp16
+        rounding (numpy) of the exact dequantized value."""
+        qweight = _c(qweight, np.uint8)
+        scales = _c(scales, np.uint16)
+        N, K2 = qweight.shape
+        K = 2 * K2
+        out = np.empty((N, K), dtype=np.uint16)
+        rc = self._lib.orc_dequantize_f16(_ptr(qweight), _ptr(scales), N, K, group, _ptr(out))
+        if rc != 0:
+            raise ValueError("oracle dequantize_f16 rejected shape")
+        return out
+
+    # ------------------------------------------------------------------
+    # GEMM y = x W^T in binary64 (report §二/§五).  Pinned: numpy float64
+    # matmul of the dequantized weights on tiny shapes; closed form q = 1,
+    # s = 1 gives y = sum_k x exactly.
+    # ------------------------------------------------------------------
+    def gemm(self, x16: np.ndarray, qweight: np.ndarray, scales: np.ndarray,
+             group: int = GROUP) -> np.ndarray:
+        """y[m, n] = sum_k x[m, k] * Wd[n, k], binary64, unrounded.  x16: uint16 [M, K]."""
+        x16 = _c(x16, np.uint16)
+        qweight = _c(qweight, np.uint8)
+        scales = _c(scales, np.uint16)
+        M, K = x16.shape
+        N = qweight.shape[0]
+        if qweight.shape[1] * 2 != K:
+            raise ValueError("x and qweight disagree on K")
+        y = np.empty((M, N), dtype=np.float64)
+        rc = self._lib.orc_gemm(_ptr(x16), M, K, _ptr(qweight), _ptr(scales), N, group,
+                                _ptr(y))
+        if rc != 0:
+            raise ValueError("oracle gemm rejected shape")
+        return y
+
+    def gemm_rows(self, x16: np.ndarray, qweight: np.ndarray, scales: np.ndarray,
+                  rows, group: int = GROUP) -> np.ndarray:
+        """Columns ``rows`` of y only: returns [M, len(rows)] binary64."""
+        x16 = _c(x16, np.uint16)
+        qweight = _c(qweight, np.uint8)
+        scales = _c(scales, np.uint16)
+        rows = _c(np.asarray(rows), np.int64)
+        M, K = x16.shape
+        N = qweight.shape[0]
+        if qweight.shape[1] * 2 != K:
+            raise ValueError("x and qweight disagree on K")
+        y = np.empty((M, rows.size), dtype=np.float64)
+        rc = self._lib.orc_gemm_rows(_ptr(x16), M, K, _ptr(qweight), _ptr(scales), N,
+                                     group, _ptr(rows), rows.size, _ptr(y))
+        if rc != 0:
+            raise ValueError("oracle gemm_rows rejected arguments")
+        return y
+
+
+def default() -> Oracle:
+    """The oracle built from this directory's source (compiled on first use)."""
+    global _LIB
+    with _LOCK:
+        if _LIB is None:
+            _LIB = Oracle(build())
+    return _LIB
+
+
+def half_to_double(h):
+    return default().half_to_double(h)
+
+
+def float_to_half(f):
+    return default().float_to_half(f)
+
+
+def quantize(W16, group: int = GROUP):
+    return default().quantize(W16, group)
+
+
+def dequantize(qweight, scales, group: int = GROUP):
+    return default().dequantize(qweight, scales, group)
+
+
+def dequantize_f16(qweight, scales, group: int = GROUP):
+    return default().dequantize_f16(qweight, scales, group)
+
+
+def gemm(x16, qweight, scales, group: int = GROUP):
+    return default().gemm(x16, qweight, scales, group)
+
+
+def gemm_rows(x16, qweight, scales, rows, group: int = GROUP):
+    return default().gemm_rows(x16, qweight, scales, rows, group)
+
+
+def num_threads() -> int:
+    return default().num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    default().set_num_threads(n)

@@ -1,0 +1,20 @@
+"""Shared pytest set-up: markers and import paths.
+
+Tests marked ``gpu`` need a CUDA device and the compiled library; everything
+else runs on a CPU-only host.
+"""
+from __future__ import annotations
+
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+HERE = os.path.dirname(os.path.abspath(__file__))
+if HERE not in sys.path:
+    sys.path.insert(0, HERE)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU and the compiled sm_103a library")

@@ -1,0 +1,289 @@
+"""Pins for the CPU oracle: checks against what the pages and mathematics fix.
+
+Every function here takes an ``oracle.Oracle`` (the real build, or a mutant
+with a planted mistake) and raises ``AssertionError`` when the oracle breaks
+the pinned fact.  None of them re-types the oracle's own arithmetic: each is
+a hand-derived fixture, a closed form, an invariant, a library routine
+(numpy's IEEE float16 conversion and float64 matmul) on a special case, or a
+brute-force enumeration on tiny inputs.
+
+Sources: qaqbuyan.com quantization tutorial, chapter "量化的数学基石"
+(§1 FP16 bit layout; §2 symmetric formula and the rounding-error model
+|error| <= s/2; §3 per-group quantizer and dequantizer); W4A16 benchmark
+report (mhpq.cn) §二/§五 for y = x W^T.
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+GROUP = 128
+
+
+def _read_fixture(name: str) -> list[list[str]]:
+    rows = []
+    with open(os.path.join(GOLDEN, name), encoding="utf-8") as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line.split())
+    return rows
+
+
+def _f16_bits(values) -> np.ndarray:
+    return np.asarray(values, dtype=np.float16).view(np.uint16)
+
+
+def _nibbles(qweight: np.ndarray) -> np.ndarray:
+    """Unpack bytes into stored nibbles in k order (low nibble first)."""
+    lo = qweight & 0x0F
+    hi = qweight >> 4
+    return np.stack([lo, hi], axis=-1).reshape(qweight.shape[0], -1).astype(np.int16)
+
+
+def _random_weights(rng: np.random.Generator, N: int, K: int) -> np.ndarray:
+    w = rng.standard_normal((N, K)).astype(np.float32) * np.float32(0.02)
+    mask = rng.random((N, K)) < 0.001
+    w[mask] *= np.float32(20.0)
+    return w.astype(np.float16).view(np.uint16)
+
+
+# --------------------------------------------------------------------------
+# FP16 bit layout
+# --------------------------------------------------------------------------
+
+def pin_half_to_double_exhaustive(o) -> None:
+    """All 65536 fp16 patterns decode to numpy's IEEE float16 value."""
+    h = np.arange(65536, dtype=np.uint16)
+    got = o.half_to_double(h)
+    ref = h.view(np.float16).astype(np.float64)
+    same = (got == ref) | (np.isnan(got) & np.isnan(ref))
+    assert same.all(), f"{(~same).sum()} fp16 patterns decode wrongly"
+    # signed zeros keep their sign
+    assert math.copysign(1.0, got[0x8000]) == -1.0
+
+
+def pin_float_to_half_numpy(o) -> None:
+    """binary32 -> fp16 RNE agrees with numpy on boundaries and random floats."""
+    rng = np.random.default_rng(1234)
+    boundary = np.array([
+        0.0, -0.0, 65504.0, 65505.0, 65519.996, 65520.0, 65536.0, 1e9, -65520.0,
+        2.0 ** -24, 2.0 ** -25, 2.0 ** -25 * 1.0000001, 3 * 2.0 ** -26, 2.0 ** -14,
+        2.0 ** -14 - 2.0 ** -25, 2.0 ** -14 - 2.0 ** -26, 1.0 + 2.0 ** -11,
+        1.0 + 3 * 2.0 ** -11, 1.0 + 2.0 ** -11 + 2.0 ** -23, 1e-8, 5.96e-8,
+        np.inf, -np.inf, 0.1, 1.0 / 3.0, 2047.5, 2048.5, 4095.0,
+    ], dtype=np.float32)
+    bits = rng.integers(0, 2 ** 32, size=400_000, dtype=np.uint64).astype(np.uint32)
+    rand_bits = bits.view(np.float32)
+    rand_bits = rand_bits[np.isfinite(rand_bits)]
+    rand_mid = (rng.standard_normal(400_000) * np.exp(rng.uniform(-20, 12, 400_000))
+                ).astype(np.float32)
+    for f in (boundary, rand_bits, rand_mid):
+        got = o.float_to_half(f)
+        with np.errstate(over="ignore"):
+            ref = f.astype(np.float16).view(np.uint16)
+        assert np.array_equal(got, ref), (
+            f"float->half differs on {np.count_nonzero(got != ref)} values, e.g. "
+            f"{f[got != ref][:4]}")
+
+
+def pin_half_round_trip(o) -> None:
+    """Every finite fp16 value survives half -> double -> float -> half."""
+    h = np.arange(65536, dtype=np.uint16)
+    finite = (h & 0x7C00) != 0x7C00
+    h = h[finite]
+    back = o.float_to_half(o.half_to_double(h).astype(np.float32))
+    assert np.array_equal(back, h)
+
+
+# --------------------------------------------------------------------------
+# Quantizer
+# --------------------------------------------------------------------------
+
+def pin_nibble_order_fixture(o) -> None:
+    rows = {r[0]: r[1:] for r in _read_fixture("nibble_order_group128.txt")}
+    c = [int(v) for v in rows["c"]] + [0] * int(rows["c_rest"][1])
+    assert len(c) == GROUP
+    w = _f16_bits(np.array(c, dtype=np.float64) * 2.0 ** -6).reshape(1, GROUP)
+    expect = [int(b, 16) for b in rows["bytes"]]
+    expect += [int(rows["bytes_rest"][0], 16)] * int(rows["bytes_rest"][1])
+    q, s = o.quantize(w, GROUP)
+    assert q.tolist() == [expect], f"packed bytes {q[0, :8].tolist()}"
+    assert s.tolist() == [[int(rows["scale_bits"][0], 16)]]
+
+
+def pin_ties_to_even(o) -> None:
+    rows = _read_fixture("ties_pow2_scale.txt")
+    amax = float(rows[0][1])
+    cases = [(float(r[1]), int(r[2])) for r in rows[1:]]
+    vals = [amax] + [r for r, _ in cases]
+    vals += [0.0] * (GROUP - len(vals))
+    w = _f16_bits(np.array(vals) * 2.0 ** -6).reshape(1, GROUP)
+    q, s = o.quantize(w, GROUP)
+    nib = _nibbles(q)[0] - 8
+    assert nib[0] == 7
+    for i, (r, expect) in enumerate(cases, start=1):
+        assert nib[i] == expect, f"r={r}: q={nib[i]}, expected {expect}"
+    assert s[0, 0] == _f16_bits([2.0 ** -6])[0]
+
+
+def pin_tiny_scale_clamp(o) -> None:
+    rows = {r[0]: r[1:] for r in _read_fixture("tiny_scale_clamp.txt")}
+    w = np.full((1, GROUP), int(rows["w_bits"][0], 16), dtype=np.uint16)
+    q, s = o.quantize(w, GROUP)
+    assert (q == int(rows["bytes"][0], 16)).all(), f"bytes {q[0, :4]}"
+    assert s[0, 0] == int(rows["scale_bits"][0], 16)
+
+
+def pin_all_zero_group(o) -> None:
+    """An all-zero group packs to 0x88 bytes, a +0 scale, and dequantizes to 0."""
+    w = np.zeros((3, 2 * GROUP), dtype=np.uint16)
+    w[1, GROUP:] = _f16_bits(np.linspace(-1, 1, GROUP))  # one live group
+    w[2, :] = 0x8000                                      # negative zeros
+    q, s = o.quantize(w, GROUP)
+    assert (q[0] == 0x88).all() and (q[2] == 0x88).all() and (q[1, :GROUP // 2] == 0x88).all()
+    assert s[0].tolist() == [0, 0] and s[2].tolist() == [0, 0] and s[1, 0] == 0
+    wd = o.dequantize(q, s, GROUP)
+    assert (wd[0] == 0).all() and (wd[2] == 0).all() and (wd[1, :GROUP] == 0).all()
+
+
+def pin_amax_maps_to_seven(o) -> None:
+    """The largest |w| of every group quantizes to +-7 with w's sign, and no
+    |q| exceeds 7 (symmetric quantization never reaches -8)."""
+    rng = np.random.default_rng(7)
+    w16 = _random_weights(rng, 64, 1024)
+    q, s = o.quantize(w16, GROUP)
+    qv = _nibbles(q) - 8
+    w = w16.view(np.float16).astype(np.float64)
+    wg = w.reshape(64, -1, GROUP)
+    qg = qv.reshape(64, -1, GROUP)
+    idx = np.abs(wg).argmax(axis=-1)
+    amax_q = np.take_along_axis(qg, idx[..., None], axis=-1)[..., 0]
+    amax_w = np.take_along_axis(wg, idx[..., None], axis=-1)[..., 0]
+    assert (amax_q == 7 * np.sign(amax_w)).all()
+    assert np.abs(qv).max() == 7
+
+
+def pin_scale_is_fp16_of_amax_over_7(o) -> None:
+    """Stored scale == numpy fp16(max(fp32(amax) / fp32(7), fp32(1e-8)))."""
+    rng = np.random.default_rng(8)
+    w16 = _random_weights(rng, 32, 2048)
+    w16[3, :GROUP] = 0
+    w16[5, GROUP:2 * GROUP] = 0x0001
+    _, s = o.quantize(w16, GROUP)
+    a = np.abs(w16.view(np.float16).astype(np.float32)).reshape(32, -1, GROUP).max(-1)
+    ref = np.maximum(a / np.float32(7.0), np.float32(1e-8)).astype(np.float16).view(np.uint16)
+    assert np.array_equal(s, ref)
+
+
+def pin_nearest_level_brute_force(o) -> None:
+    """On tiny inputs, q is the level j in [-8, 7] nearest to fp32(w)/fp32(s),
+    ties to the even level, found by enumerating all 16 levels."""
+    rng = np.random.default_rng(9)
+    w16 = _random_weights(rng, 4, 2 * GROUP)
+    q, _ = o.quantize(w16, GROUP)
+    qv = _nibbles(q) - 8
+    w32 = w16.view(np.float16).astype(np.float32)
+    levels = np.arange(-8, 8, dtype=np.float64)
+    for n in range(w32.shape[0]):
+        for g in range(w32.shape[1] // GROUP):
+            blk = w32[n, g * GROUP:(g + 1) * GROUP]
+            s32 = max(np.float32(np.abs(blk).max()) / np.float32(7.0), np.float32(1e-8))
+            for i, wv in enumerate(blk):
+                r = float(np.float32(wv) / np.float32(s32))
+                d = np.abs(levels - r)
+                best = levels[d == d.min()]
+                j = best[0] if best.size == 1 else best[np.fmod(best, 2) == 0][0]
+                assert qv[n, g * GROUP + i] == j, (n, g, i, r, qv[n, g * GROUP + i])
+
+
+def pin_round_trip_bound(o) -> None:
+    """Rounding-error model (tutorial §2): every element comes back within
+    half a step.  With the stored fp16 scale s16 (|s16 - s32| <= 2^-11 s32 in
+    the normal range) the bound is s16 (1 + 2^-10) (1/2 + 2^-21 + 8 * 2^-11)."""
+    rng = np.random.default_rng(10)
+    w16 = _random_weights(rng, 128, 4096)
+    q, s = o.quantize(w16, GROUP)
+    wd = o.dequantize(q, s, GROUP)
+    w = w16.view(np.float16).astype(np.float64)
+    s64 = o.half_to_double(s)
+    assert (s64 >= 2.0 ** -14).all()
+    bound = np.repeat(s64, GROUP, axis=1) * (1 + 2.0 ** -10) * (0.5 + 2.0 ** -21 + 8 * 2.0 ** -11)
+    err = np.abs(w - wd)
+    assert (err <= bound).all(), float((err / bound).max())
+    # the error is a half-step uniform noise on average (|U| with U ~ U(-1/2, 1/2))
+    rel = (err / np.repeat(s64, GROUP, axis=1)).mean()
+    assert 0.2 < rel < 0.3, rel
+
+
+# --------------------------------------------------------------------------
+# Dequantizer and GEMM
+# --------------------------------------------------------------------------
+
+def pin_dequant_closed_forms(o) -> None:
+    """Nibble 9 with scale 1.0 is +1; nibble 0 is -8 * scale; nibble 8 is 0."""
+    N, K = 3, 2 * GROUP
+    q = np.full((N, K // 2), 0x99, dtype=np.uint8)
+    q[1] = 0x00
+    q[2] = 0x08  # low nibble 8 (0), high nibble 0 (-8)
+    s = np.full((N, K // GROUP), 0x3C00, dtype=np.uint16)   # 1.0
+    s[1, 1] = 0x4000                                         # 2.0 in group 1
+    s[2] = _f16_bits([0.25, 0.5])
+    wd = o.dequantize(q, s, GROUP)
+    assert (wd[0] == 1.0).all()
+    assert (wd[1, :GROUP] == -8.0).all() and (wd[1, GROUP:] == -16.0).all()
+    assert (wd[2, 0::2] == 0.0).all()
+    assert (wd[2, 1:GROUP:2] == -2.0).all() and (wd[2, GROUP + 1::2] == -4.0).all()
+
+
+def pin_gemm_numpy_tiny(o) -> None:
+    """Tiny shapes: y equals numpy's float64 matmul x @ Wd^T (Wd pinned above)."""
+    rng = np.random.default_rng(11)
+    for M, N, K in ((1, 1, 128), (2, 3, 256), (16, 8, 128), (3, 5, 384)):
+        w16 = _random_weights(rng, N, K)
+        q, s = o.quantize(w16, GROUP)
+        x16 = rng.standard_normal((M, K)).astype(np.float16).view(np.uint16)
+        y = o.gemm(x16, q, s, GROUP)
+        ref = x16.view(np.float16).astype(np.float64) @ o.dequantize(q, s, GROUP).T
+        assert y.shape == (M, N)
+        np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)
+        rows = np.array([N - 1, 0])
+        np.testing.assert_array_equal(o.gemm_rows(x16, q, s, rows, GROUP), y[:, rows])
+
+
+def pin_gemm_closed_form(o) -> None:
+    """q = 1 and scale s[n, g] = 2^-(n+g) give y[m, n] = sum_g 2^-(n+g) sum_{k in g} x[m, k],
+    which binary64 holds exactly (fp16 x, at most a few hundred terms)."""
+    rng = np.random.default_rng(12)
+    M, N, K = 3, 4, 3 * GROUP
+    x16 = rng.standard_normal((M, K)).astype(np.float16)
+    q = np.full((N, K // 2), 0x99, dtype=np.uint8)
+    s = np.array([[2.0 ** -(n + g) for g in range(K // GROUP)] for n in range(N)])
+    y = o.gemm(x16.view(np.uint16), q, _f16_bits(s), GROUP)
+    xs = x16.astype(np.float64)
+    for m in range(M):
+        for n in range(N):
+            expect = math.fsum(
+                s[n, g] * math.fsum(xs[m, g * GROUP:(g + 1) * GROUP]) for g in range(K // GROUP))
+            assert y[m, n] == expect, (m, n, y[m, n], expect)
+
+
+ALL_PINS = (
+    pin_half_to_double_exhaustive,
+    pin_float_to_half_numpy,
+    pin_half_round_trip,
+    pin_nibble_order_fixture,
+    pin_ties_to_even,
+    pin_tiny_scale_clamp,
+    pin_all_zero_group,
+    pin_amax_maps_to_seven,
+    pin_scale_is_fp16_of_amax_over_7,
+    pin_nearest_level_brute_force,
+    pin_round_trip_bound,
+    pin_dequant_closed_forms,
+    pin_gemm_numpy_tiny,
+    pin_gemm_closed_form,
+)

@@ -1,0 +1,57 @@
+"""Planted mistakes: each mutant is a copy of the oracle's C source with one
+plausible error (a wrong rounding mode, swapped nibbles, a dropped clamp, a
+wrong divisor, an off-by-one offset, a reversed operand, a truncating
+conversion, a wrong exponent bias, a wrong group stride, a transposed scale
+store, a scale taken from the wrong group).  The pin suite must reject every
+one of them; a mutant that passes all pins means the pins are too weak."""
+from __future__ import annotations
+
+import os
+
+import pytest
+
+import oracle
+import oracle_pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "w4a16_oracle.c")
+
+MUTANTS = {
+    "round_half_away": ("float rq = nearbyintf(r);", "float rq = roundf(r);"),
+    "swapped_nibbles": ("(uint8_t)((hi << 4) | lo)", "(uint8_t)((lo << 4) | hi)"),
+    "dropped_clamp": ("if (s < 1e-8f)", "if (s < 0.0f)"),
+    "divide_by_8": ("float s = amax / 7.0f;", "float s = amax / 8.0f;"),
+    "offset_7": ("out[k] = (double)(nib - 8)", "out[k] = (double)(nib - 7)"),
+    "reversed_x": ("acc += orc_half_to_double(x[m * K + k]) * wd[k];",
+                   "acc += orc_half_to_double(x[m * K + (K - 1 - k)]) * wd[k];"),
+    "truncating_f2h": ("double m = rint(ldexp(a, 10 - e)) - 1024.0;",
+                       "double m = floor(ldexp(a, 10 - e)) - 1024.0;"),
+    "exponent_bias": ("v = ldexp(1024.0 + (double)m, e - 25);",
+                      "v = ldexp(1024.0 + (double)m, e - 24);"),
+    "group_stride": ("const uint16_t *wg = W + n * K + g * group;",
+                     "const uint16_t *wg = W + n * K + g;"),
+    "scale_transposed": ("scales[n * ngroups + g] = quantize_group",
+                         "scales[g * N + n] = quantize_group"),
+    "scale_group_zero": ("out[k] = (double)(nib - 8) * orc_half_to_double(srow[k / group]);",
+                         "out[k] = (double)(nib - 8) * orc_half_to_double(srow[0]);"),
+    "amax_signed": ("float a = fabsf((float)orc_half_to_double(w16[i]));",
+                    "float a = (float)orc_half_to_double(w16[i]);"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_mutant(name, tmp_path):
+    old, new = MUTANTS[name]
+    with open(SRC, encoding="utf-8") as f:
+        src = f.read()
+    assert src.count(old) >= 1, f"mutation site for {name} not found"
+    mutant_src = tmp_path / f"oracle_{name}.c"
+    mutant_src.write_text(src.replace(old, new), encoding="utf-8")
+    lib = oracle.build(str(mutant_src), out=str(tmp_path / f"liboracle_{name}.so"))
+    orc = oracle.Oracle(lib)
+    failed = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(orc)
+        except (AssertionError, ValueError):
+            failed.append(pin.__name__)
+    assert failed, f"mutant {name} passed every pin"
