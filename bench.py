@@ -1,0 +1,502 @@
+#!/usr/bin/env python3
+"""Benchmark of the W4A16 decode path on GB300 -- prints ONE JSON line.
+
+Headline step: one pass of the Llama-3-8B decode linear layers at M = 1
+(QKV 6144x4096, O 4096x4096, gate/up 28672x4096, down 4096x14336, lm_head
+128256x4096) through ``w4a16_gemm``, weights already resident in HBM in the
+kernel layout.  The step moves 383.7 MB of packed weights and scales -- three
+times the 129 MB L2 -- so every step streams from HBM (no L2 flush needed).
+``value`` is algorithmic bytes / device time (GB/s): bytes per call =
+N*K/2 + 2*N*K/128 + 2*M*K + 2*M*N.
+
+Also reported in the same line: per-shape us/call over rotating weight copies
+(>= 4x L2), the 8B-stack token (129 GEMVs, tokens/s), the M = 2..16 sweep over
+the Llama and Qwen-2.5-7B shapes, the quantizer on [14336, 4096], the
+roofline of the GEMV kernel, the CPU oracle baseline on the host cores, the
+end-to-end number through the Python API with host buffers, and SM clocks
+sampled during the timed region.
+
+``--impl reference`` times the CPU oracle (the only reference this path has)
+on the same workload, a bounded sample of rows per step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from w4a16_weight_only_gemm_gb300 import synthetic, workloads  # noqa: E402
+
+METRIC = "W4A16 GEMV achieved HBM GB/s (% of 8 TB/s) and 8B-stack tokens/s at M=1"
+WORKLOAD = ("llama3_8b_decode_m1: qkv 6144x4096, o_proj 4096x4096, gate_up 28672x4096, "
+            "down 4096x14336, lm_head 128256x4096; M=1; W4A16 group 128, fp16 scales")
+NOMINAL_HBM_GBS = 8000.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--skip-extras", action="store_true",
+                   help="headline step only (no per-shape, stack, sweep, quantizer sections)")
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="budget of the CPU oracle baseline sample")
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (replicas: every rank runs the same step on its GPU)
+# ----------------------------------------------------------------------------
+def dist_init(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        with open(self.path) as f:
+            for line in f:
+                cols = [c.strip() for c in line.split(",")]
+                if len(cols) < 9:
+                    continue
+                try:
+                    sm.append(float(cols[1]))
+                    smax.append(float(cols[2]))
+                    power.append(float(cols[3]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, cols[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "power_w_max": max(power), "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------
+# GPU side
+# ----------------------------------------------------------------------------
+def make_layer(lin, workload: str, idx: int, M: int = 1):
+    import w4a16_weight_only_gemm_gb300 as w4
+    sw, sx = synthetic.seeds(workload, idx)
+    W = synthetic.master_weight(lin.N, lin.K, sw, device="cuda")
+    q, s = w4.quantize(W)
+    r = w4.repack(q)
+    del W, q
+    x = synthetic.activations(M, lin.K, sx, device="cuda")
+    y = torch.empty((M, lin.N), dtype=torch.float16, device="cuda")
+    return {"lin": lin, "r": r, "s": s, "x": x, "y": y, "M": M}
+
+
+def gemm_call(layer, r=None, s=None):
+    import w4a16_weight_only_gemm_gb300 as w4
+    w4.gemm(layer["x"], layer["r"] if r is None else r, layer["s"] if s is None else s,
+            out=layer["y"])
+
+
+def capture(fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()  # first use outside capture: per-device set-up
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph(g, stream, reps: int, warmup: int, world: int = 1) -> float:
+    """Seconds per replay (CUDA events on the replay stream, max over ranks)."""
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            g.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(reps):
+            g.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    secs = start.elapsed_time(end) / 1e3
+    return max_over_ranks(secs, world) / reps
+
+
+def l2_bytes() -> int:
+    try:
+        return int(torch.cuda.get_device_properties(0).L2_cache_size)
+    except AttributeError:
+        return 129 * 2 ** 20
+
+
+def per_shape_us(lin, workload, idx, M=1, reps=20):
+    """us per call over rotating weight copies totalling >= 4x L2."""
+    base = make_layer(lin, workload, idx, M)
+    nbytes = lin.N * lin.K // 2 + 2 * lin.N * (lin.K // 128)
+    copies = max(2, -(-4 * l2_bytes() // nbytes))
+    rs = [base["r"]] + [base["r"].clone() for _ in range(copies - 1)]
+    ss = [base["s"]] + [base["s"].clone() for _ in range(copies - 1)]
+    stream = torch.cuda.Stream()
+
+    def body():
+        for r, s in zip(rs, ss):
+            gemm_call(base, r, s)
+    g = capture(body, stream)
+    t = time_graph(g, stream, reps, 3) / copies
+    b = workloads.algorithmic_bytes(M, lin.N, lin.K)
+    del rs, ss, g
+    return {"us": round(t * 1e6, 3), "gbs": round(b / t / 1e9, 1), "bytes": b, "copies": copies}
+
+
+def run_ours(args, rank, world):
+    import w4a16_weight_only_gemm_gb300 as w4
+    from w4a16_weight_only_gemm_gb300 import build
+    build.build()
+    dev = torch.cuda.current_device()
+    layers = [make_layer(lin, "llama3_8b_decode", i) for i, lin in enumerate(workloads.LLAMA3_8B)]
+    step_bytes = sum(workloads.algorithmic_bytes(1, lin.N, lin.K) for lin in workloads.LLAMA3_8B)
+    stream = torch.cuda.Stream()
+
+    def step():
+        for layer in layers:
+            gemm_call(layer)
+    g = capture(step, stream)
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            g.replay()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(dev)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    secs = max_over_ranks(start.elapsed_time(end) / 1e3, world)
+    status = w4.device_status()
+    ms_per_step = secs / args.steps * 1e3
+    value = step_bytes * world / (secs / args.steps) / 1e9
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded N(0,0.02) weights with 0.1% x20 outliers, N(0,1) activations)",
+        "config": {"workload": WORKLOAD, "global_batch": 1 * world, "parallelism": f"replicas{world}",
+                   "l2": "inputs larger than L2: 383.7 MB of packed weights per step, no flush",
+                   "submission": "CUDA graph of the step's w4a16_gemm calls"},
+        "pct_of_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 1),
+        "gpu_launches": args.steps * len(layers),
+        "clocks": clk,
+        "device_status": status,
+    }
+    peaks = load_peaks()
+    per_rank_gbs = value / world
+    result["roofline"] = {
+        "bound": "hbm", "achieved": round(per_rank_gbs, 1),
+        "peak": peaks.get("hbm_gbs", 6800.0), "unit": "GB/s",
+        "frac": round(per_rank_gbs / peaks.get("hbm_gbs", 6800.0), 3),
+        "peak_source": "measured" if "hbm_gbs" in peaks else "fallback",
+        "kernel": "gemv_kernel<1> (all launches of the step)",
+        "traffic": None,
+    }
+    result["e2e"] = e2e_eager(layers, args, world)
+    if rank == 0 and not args.skip_extras:
+        result["sections"] = extras(layers)
+    if rank == 0:
+        result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    return result
+
+
+def e2e_eager(layers, args, world):
+    """The same step through the Python API, eager, with host buffers:
+    each step copies its activations from pinned host memory, runs the five
+    GEMVs and reads every output back to pinned host memory."""
+    import w4a16_weight_only_gemm_gb300 as w4
+    xh = [l["x"].cpu().pin_memory() for l in layers]
+    yh = [torch.empty_like(l["y"], device="cpu").pin_memory() for l in layers]
+    h2d = sum(x.numel() * 2 for x in xh)
+    d2h = sum(y.numel() * 2 for y in yh)
+
+    def step():
+        for l, x_host, y_host in zip(layers, xh, yh):
+            l["x"].copy_(x_host, non_blocking=True)
+            w4.gemm(l["x"], l["r"], l["s"], out=l["y"])
+            y_host.copy_(l["y"], non_blocking=True)
+    steps = max(10, min(args.steps, 500))
+    for _ in range(5):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        step()
+    end.record()
+    torch.cuda.synchronize()
+    secs = max_over_ranks(start.elapsed_time(end) / 1e3, world) / steps
+    step_bytes = sum(workloads.algorithmic_bytes(1, l["lin"].N, l["lin"].K) for l in layers)
+    return {"value": round(step_bytes * world / secs / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(secs * 1e3, 4), "steps": steps,
+            "how": "eager Python API calls (ctypes -> w4a16_gemm), pinned host buffers"}
+
+
+def extras(layers):
+    out = {}
+    out["per_shape_m1"] = {lin.name: per_shape_us(lin, "llama3_8b_decode", i)
+                           for i, lin in enumerate(workloads.LLAMA3_8B)}
+    out["gemv_4096_m1"] = per_shape_us(workloads.SINGLE_GEMV, "gemv_4096", 0)
+    out["stack_8b"] = stack_8b()
+    sweep = {}
+    shapes = [("llama", l) for l in workloads.LLAMA3_8B] + [("qwen", l) for l in workloads.QWEN25_7B]
+    for M in workloads.DECODE_SWEEP_M:
+        for i, (fam, lin) in enumerate(shapes):
+            sweep[f"{fam}_{lin.name}_m{M}"] = per_shape_us(lin, "decode_sweep", i, M=M, reps=10)
+    out["decode_sweep"] = sweep
+    out["quantizer"] = quantizer_throughput()
+    return out
+
+
+def stack_8b():
+    """One decode token of the 8B linear stack: 32 x (QKV, O, gate/up, down)
+    + lm_head, every matrix distinct (3.87 GB), in one CUDA graph."""
+    lins = workloads.stack_8b()
+    layers = [make_layer(lin, "stack_8b", i) for i, lin in enumerate(lins)]
+    stream = torch.cuda.Stream()
+
+    def token():
+        for l in layers:
+            gemm_call(l)
+    g = capture(token, stream)
+    t = time_graph(g, stream, 20, 3)
+    b = sum(workloads.algorithmic_bytes(1, l.N, l.K) for l in lins)
+    del layers, g
+    torch.cuda.empty_cache()
+    return {"ms_per_token": round(t * 1e3, 4), "tokens_per_s": round(1 / t, 1),
+            "gbs": round(b / t / 1e9, 1), "bytes_per_token": b, "gemv_calls": len(lins)}
+
+
+def quantizer_throughput():
+    import w4a16_weight_only_gemm_gb300 as w4
+    N, K = workloads.QUANTIZER_SHAPE
+    copies = 4
+    Ws = [synthetic.master_weight(N, K, 4000 + i, device="cuda") for i in range(copies)]
+    qs = [torch.empty((N, K // 2), dtype=torch.uint8, device="cuda") for _ in range(copies)]
+    ss = [torch.empty((N, K // 128), dtype=torch.float16, device="cuda") for _ in range(copies)]
+    lib = __import__("w4a16_weight_only_gemm_gb300._native", fromlist=["lib"]).lib()
+    stream = torch.cuda.Stream()
+
+    def body():
+        sp = torch.cuda.current_stream().cuda_stream
+        for W, q, s in zip(Ws, qs, ss):
+            rc = lib.w4a16_quantize(W.data_ptr(), N, K, 128, q.data_ptr(), s.data_ptr(), sp)
+            assert rc == 0
+    g = capture(body, stream)
+    t = time_graph(g, stream, 10, 2) / copies
+    b = N * K * 2 + N * K // 2 + 2 * N * (K // 128)
+    rt = w4.repack(qs[0])
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(10):
+        w4.repack(qs[0])
+    torch.cuda.synchronize()
+    trep = (time.perf_counter() - t0) / 10
+    del Ws, qs, ss, rt
+    return {"us": round(t * 1e6, 2), "gbs": round(b / t / 1e9, 1), "bytes": b,
+            "repack_us_wall": round(trep * 1e6, 1)}
+
+
+def load_peaks() -> dict:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle (baseline leg and the reference arm)
+# ----------------------------------------------------------------------------
+def oracle_inputs(rows_per_shape: int = 64):
+    """Sampled rows of each decode shape at M = 1, ready for the oracle:
+    (shape, packed rows, scale rows, x).  Packed bytes and scales are random
+    (the oracle's cost does not depend on the values)."""
+    rng = np.random.default_rng(0)
+    prepared = []
+    for i, lin in enumerate(workloads.LLAMA3_8B):
+        _, sx = synthetic.seeds("llama3_8b_decode", i)
+        q = rng.integers(0, 256, size=(rows_per_shape, lin.K // 2), dtype=np.uint8)
+        s = rng.uniform(1e-3, 1e-2, size=(rows_per_shape, lin.K // 128)).astype(np.float16)
+        x = synthetic.activations(1, lin.K, sx).view(torch.int16).numpy().view(np.uint16)
+        prepared.append((lin, q, s.view(np.uint16), x))
+    return prepared
+
+
+def oracle_pass(prepared) -> int:
+    """One pass of the oracle over the sampled rows; returns algorithmic bytes
+    of the work done (packed rows + their scales + x + the outputs)."""
+    import oracle
+    done = 0
+    for lin, q, s, x in prepared:
+        rows = np.arange(q.shape[0])
+        oracle.gemm_rows(x, q, s, rows)
+        done += q.shape[0] * (lin.K // 2 + 2 * (lin.K // 128) + 2) + 2 * lin.K
+    return done
+
+
+ORACLE_SAMPLE = ("{rows} sampled rows of each of the 5 decode shapes (M=1) per pass; "
+                 "binary64 oracle, OpenMP over rows")
+
+
+def cpu_baseline(seconds: float, rows_per_shape: int = 64):
+    import oracle
+    prepared = oracle_inputs(rows_per_shape)
+    oracle_pass(prepared)
+    done, passes = 0, 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        done += oracle_pass(prepared)
+        passes += 1
+    secs = time.perf_counter() - t0
+    return {"value": round(done / secs / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "sample": f"{passes} passes: " + ORACLE_SAMPLE.format(rows=rows_per_shape),
+            "seconds": round(secs, 2)}
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle on the headline workload: each step is one pass over a
+    bounded sample (64 rows of each decode shape), timed on the host cores."""
+    import oracle
+    if rank != 0:
+        return None
+    prepared = oracle_inputs(64)
+    for _ in range(args.warmup):
+        oracle_pass(prepared)
+    done = 0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        done += oracle_pass(prepared)
+    secs = time.perf_counter() - t0
+    value = done / secs / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": 1, "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "kind": "oracle",
+                         "cores": oracle.num_threads(),
+                         "sample": "per step: " + ORACLE_SAMPLE.format(rows=64)},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        # Only rank 0 times the CPU oracle; other ranks exit without work.
+        rank = int(os.environ.get("RANK", "0"))
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        res = run_reference(args, rank, world)
+        if rank == 0 and res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    rank, world = dist_init(args.gpus)
+    res = run_ours(args, rank, world)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,177 @@
+/*
+ * w4a16.h -- C ABI of the GB300 (sm_103a) W4A16 weight-only INT4 library.
+ *
+ * The library computes y = x * W^T for fp16 activations x [M, K] and weights
+ * W [N, K] stored as symmetric INT4 in groups of 128 along K with one fp16
+ * scale per group: the dequantize-on-the-fly product that dominates
+ * memory-bound single-batch LLM decode ("W4A16 量化算子解码性能基准跑分与端侧大模型
+ * 推理显存实测报告", mhpq.cn, §二 and §五), together with the group-wise
+ * round-to-nearest quantizer that produces the packed weights ("LLM
+ * quantization from IEEE 754 to GPTQ/AWQ/GGUF" tutorial, qaqbuyan.com
+ * article 126, chapter "量化的数学基石" §2 formula and §3
+ * per_group_symmetric_quantize / per_group_symmetric_dequantize).
+ *
+ * Conventions for every entry point
+ *  - Pointers are DEVICE pointers owned by the caller (for example a torch
+ *    tensor's data_ptr()); the library never allocates, frees or keeps them.
+ *    Every pointer must be 16-byte aligned.  Tensors are dense and row-major.
+ *  - `stream` is a cudaStream_t passed as void*; NULL means the legacy
+ *    default stream.  Work is enqueued asynchronously on it; the call returns
+ *    without synchronising.  Calls on one stream execute in order.
+ *  - Argument errors are reported synchronously, before anything is
+ *    launched, as a w4a16_status code; nothing is written in that case.
+ *  - A device-side failure (a bounded wait inside a kernel that gave up) is
+ *    recorded in a device status word, readable with w4a16_device_status().
+ *  - All kernels are built for sm_103a only; on another device the calls
+ *    return W4A16_ERR_DEVICE.
+ *  - The library keeps no state across calls other than the device status
+ *    word and per-device launch attributes set on first use (first use on a
+ *    device should happen before any CUDA graph capture).
+ */
+#ifndef W4A16_H
+#define W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum w4a16_status {
+    W4A16_OK = 0,
+    W4A16_ERR_NULL = 1,      /* a required pointer is NULL                    */
+    W4A16_ERR_SHAPE = 2,     /* unsupported M, N, K or group size             */
+    W4A16_ERR_ALIGN = 3,     /* a pointer is not 16-byte aligned              */
+    W4A16_ERR_CUDA = 4,      /* a CUDA runtime call or launch failed          */
+    W4A16_ERR_TIMEOUT = 5,   /* a kernel's bounded wait gave up (device)      */
+    W4A16_ERR_DEVICE = 6     /* current device is not an sm_103 GPU           */
+} w4a16_status;
+
+/* Group size along K: one fp16 scale per 128 consecutive weights of a row. */
+#define W4A16_GROUP 128
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *w4a16_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int w4a16_version(void);
+
+/*
+ * w4a16_quantize -- group-wise symmetric round-to-nearest INT4 quantizer.
+ *
+ * Source: qaqbuyan.com tutorial, "量化的数学基石" §2 (x_q = clamp(round(x / s),
+ * -8, 7), s = max|x| / 7) and §3 per_group_symmetric_quantize (groups along
+ * in_features, clamp(min = 1e-8) on the scale, two nibbles per byte with the
+ * even index in the low nibble, each stored as q + 8, scales cast to fp16).
+ *
+ * For each row n and group g of 128 weights, in IEEE binary32 on the exactly
+ * upcast fp16 inputs:
+ *     s32 = max(max_k |W[n,k]| / 7, 1e-8)             (correctly rounded /)
+ *     q   = clamp(round_half_even(W[n,k] / s32), -8, 7)
+ *     scales[n, g] = fp16_round_nearest_even(s32)
+ *     qweight[n, k/2] = (q[k+1] + 8) << 4 | (q[k] + 8)   for even k
+ *
+ *   W_f16      [N, K] fp16, row-major (rows are output features).  Finite.
+ *   N, K       N >= 1; K >= 128 and K % 128 == 0.
+ *   group      must be 128 (W4A16_GROUP).
+ *   qweight    [N, K/2] bytes, written (the canonical packed layout).
+ *   scales_f16 [N, K/128] fp16, written.
+ * The result is bit-identical to the library's CPU reference definition.
+ * Errors: NULL -> W4A16_ERR_NULL; bad N, K or group -> W4A16_ERR_SHAPE;
+ *         misaligned pointer -> W4A16_ERR_ALIGN.
+ */
+int w4a16_quantize(const void *W_f16, int64_t N, int64_t K, int32_t group, void *qweight,
+                   void *scales_f16, void *stream);
+
+/*
+ * Bytes of the kernel layout produced by w4a16_repack for an [N, K] weight:
+ * N rounded up to a multiple of 128, times K/2.  Returns -1 on a bad shape.
+ */
+int64_t w4a16_repacked_bytes(int64_t N, int64_t K);
+
+/*
+ * w4a16_repack -- one-time re-layout of canonical packed weights into the
+ * kernel layout read by w4a16_gemm (a pure permutation of nibbles; rows
+ * beyond N are padded with nibble 8, i.e. q = 0).
+ *
+ * The tutorial's packed layout is row-major [N, K/2]; its "block-major"
+ * cache-friendly re-layout advice (qaqbuyan.com, llama.cpp tuning section)
+ * motivates this step, but the exact layout is the library's own:
+ *   block b = n / 128 (128 rows), chunk c = k / 64, tile i = (n % 128) / 16;
+ *   512 bytes per (b, c, i), 16 bytes per lane L = 4 * g + t of a warp,
+ *   holding rows 16 i + g and 16 i + g + 8 at k = 64 c + 16 t ... + 15.
+ *   byte offset = ((b * (K/64) + c) * 8 + i) * 512 + 16 * L.
+ *   Within the lane's 16 bytes, 32-bit word s covers k' = 64c + 16t + 4s
+ *   .. k' + 3; its nibble positions 0..7 hold (row, k) =
+ *   (r0,k'), (r1,k'), (r0,k'+2), (r1,k'+2), (r0,k'+1), (r1,k'+1),
+ *   (r0,k'+3), (r1,k'+3) with r0 = 16 i + g and r1 = r0 + 8,
+ *   so one lop3 per nibble pair yields the f16 MMA fragment directly.
+ *
+ *   qweight   [N, K/2] canonical bytes (from w4a16_quantize).
+ *   repacked  w4a16_repacked_bytes(N, K) bytes, written.
+ * Errors: as w4a16_quantize.  unrepack(repack(P)) == P byte for byte.
+ */
+int w4a16_repack(const void *qweight, int64_t N, int64_t K, void *repacked, void *stream);
+
+/* Inverse of w4a16_repack: kernel layout -> canonical [N, K/2] bytes. */
+int w4a16_unrepack(const void *repacked, int64_t N, int64_t K, void *qweight, void *stream);
+
+/*
+ * w4a16_gemm -- y[M, N] = x[M, K] * dequant(W)[N, K]^T.
+ *
+ * Source: mhpq.cn report §二/§五 (dequantize in registers on the fly, never
+ * materialise the fp16 weights; the decode step is memory-bound) and the
+ * qaqbuyan.com tutorial §3 dequantizer: W[n, k] = (nibble - 8) * scale[n, k/128].
+ *
+ *   x_f16      [M, K] fp16 activations.
+ *   repacked   weights in the kernel layout (w4a16_repack).
+ *   scales_f16 [N, K/128] fp16 scales (canonical layout, as quantized).
+ *   y_f16      [M, N] fp16 output, written (FP32 accumulation, rounded to
+ *              nearest-even fp16 once at the end).
+ *   M          1..16 runs the decode GEMV (warp MMAs fed by a bulk-copy
+ *              shared-memory ring); M > 16 runs the tcgen05 tensor-core GEMM
+ *              (fp16 q*scale staged in shared memory, FP32 accumulators in
+ *              tensor memory).
+ *   N, K       N >= 1; K >= 128 and K % 128 == 0.
+ * Accuracy against the exact result: max|y - y_ref| <= 2e-3 * max|y_ref|
+ * and ||y - y_ref||_2 <= 1e-3 * ||y_ref||_2 for the library's test inputs.
+ * The call is graph-capturable; launches use programmatic dependent launch,
+ * and only L2 prefetches of the weights run before the previous kernel on
+ * the stream completes.
+ * Errors: NULL -> W4A16_ERR_NULL; bad M, N, K -> W4A16_ERR_SHAPE;
+ *         misaligned pointer -> W4A16_ERR_ALIGN; launch failure ->
+ *         W4A16_ERR_CUDA.
+ */
+int w4a16_gemm(const void *x_f16, const void *repacked, const void *scales_f16, void *y_f16,
+               int64_t M, int64_t N, int64_t K, void *stream);
+
+/*
+ * w4a16_device_status -- synchronises the current device, returns in
+ * *status the OR of the W4A16_ERR_* conditions recorded by kernels since
+ * the last call (W4A16_OK if none: W4A16_ERR_TIMEOUT when a bounded wait
+ * gave up) and clears the record.  Returns W4A16_ERR_CUDA if the device
+ * cannot be read.
+ */
+int w4a16_device_status(int *status);
+
+/*
+ * Upper bound, in nanoseconds, of every wait inside the library's kernels
+ * (default 2e9, i.e. two seconds).  Applies to launches made after the call.
+ */
+void w4a16_set_wait_timeout_ns(uint64_t timeout_ns);
+
+/*
+ * w4a16_selftest_wait_timeout -- diagnostic: launches one block that waits
+ * on an mbarrier nothing will ever arrive on, with a wait bound of
+ * `timeout_ns`.  The kernel gives up after that time, records
+ * W4A16_ERR_TIMEOUT in the device status word and exits normally, leaving
+ * the context usable.  Used by the tests of the failure path.
+ */
+int w4a16_selftest_wait_timeout(uint64_t timeout_ns, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_H */

@@ -44,7 +44,8 @@ _CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
 
 def _lib_path(src: str = _SRC) -> str:
     with open(src, "rb") as f:
-        digest = hashlib.sha1(f.read() + " ".join(_CFLAGS).encode()).hexdigest()[:12]
+        digest = hashlib.sha1(f.read() + " ".join(_CFLAGS).encode()
+                              + os.uname().machine.encode()).hexdigest()[:12]
     return os.path.join(_BUILD_DIR, f"liboracle_{digest}.so")
 
 

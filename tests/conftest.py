@@ -18,3 +18,20 @@ if HERE not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU and the compiled sm_103a library")
+
+
+import pytest  # noqa: E402
+
+
+@pytest.fixture(scope="session")
+def w4lib():
+    """Build (if stale) and load the CUDA library; GPU tests only.
+
+    Skips when this host has no CUDA device.  On a GPU host a missing or
+    broken library is an error, never a skip."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device on this host")
+    from w4a16_weight_only_gemm_gb300 import _native, build
+    build.build()
+    return _native.lib()

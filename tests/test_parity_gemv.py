@@ -1,0 +1,103 @@
+"""Decode GEMV (M = 1..16) vs the binary64 oracle.
+
+Bar (floating point, from the accuracy target of the path): max|y - y_ref| <=
+2e-3 max|y_ref| and ||y - y_ref|| <= 1e-3 ||y_ref||.  The budget is the final
+fp16 rounding of y (2^-11 relative, ~2.8e-4 RMS); products q*x are exact and
+sums are FP32."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import assert_close, bits16, from_bits16
+from parity_data import acts, as_device, quantized, sample_rows
+import w4a16_weight_only_gemm_gb300 as w4
+from w4a16_weight_only_gemm_gb300 import synthetic, workloads
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gemm(x16: np.ndarray, q: np.ndarray, s: np.ndarray) -> np.ndarray:
+    qt, st = as_device(q, s)
+    y = w4.gemm(from_bits16(x16), w4.repack(qt), st)
+    torch.cuda.synchronize()
+    return y.float().cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("M", list(range(1, 17)))
+def test_every_m_small(w4lib, M):
+    """Several row blocks, a ragged row tail, K split over a cluster."""
+    N, K = 1000, 1152
+    w16, q, s = quantized(N, K, 11)
+    x16 = acts(M, K, 12 + M)
+    assert_close(run_gemm(x16, q, s), oracle.gemm(x16, q, s), f"M={M}")
+
+
+@pytest.mark.parametrize("N,K", [(1, 128), (8, 128), (16, 256), (136, 384), (200, 1024),
+                                 (4168, 4096), (264, 18944), (4096, 640)])
+@pytest.mark.parametrize("M", [1, 3, 8, 9, 16])
+def test_shapes_and_tails(w4lib, M, N, K):
+    w16, q, s = quantized(N, K, 21)
+    x16 = acts(M, K, 22)
+    assert_close(run_gemm(x16, q, s), oracle.gemm(x16, q, s), f"M={M} N={N} K={K}")
+
+
+def test_every_nibble_value(w4lib):
+    """Hand-made packed data covering all 16 nibbles, including 0 (q = -8),
+    which the quantizer never emits, and varied fp16 scales."""
+    rng = np.random.default_rng(31)
+    N, K = 520, 1024
+    q = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    s = (rng.uniform(0.5, 2.0, size=(N, K // 128)) * 2.0 ** rng.integers(-12, 2, size=(N, K // 128))
+         ).astype(np.float16).view(np.uint16)
+    for M in (1, 5, 16):
+        x16 = acts(M, K, 32)
+        assert_close(run_gemm(x16, q, s), oracle.gemm(x16, q, s), f"nibbles M={M}")
+
+
+def test_output_guard_bands(w4lib):
+    """Nothing is written outside y: sentinels around the output survive."""
+    N, K, M = 136, 512, 3
+    w16, q, s = quantized(N, K, 41)
+    x = from_bits16(acts(M, K, 42))
+    qt, st = as_device(q, s)
+    r = w4.repack(qt)
+    pad = 64
+    buf = torch.full((M * N + 2 * pad,), float("nan"), dtype=torch.float16, device="cuda")
+    y = buf[pad:pad + M * N].view(M, N)
+    w4.gemm(x, r, st, out=y)
+    torch.cuda.synchronize()
+    assert torch.isnan(buf[:pad]).all() and torch.isnan(buf[pad + M * N:]).all()
+    assert_close(y.float().cpu().numpy(), oracle.gemm(bits16(x), q, s), "guard")
+
+
+def test_single_gemv_4096(w4lib):
+    """The single 4096x4096 M=1 GEMV, compared in full."""
+    sw, sx = synthetic.seeds("gemv_4096")
+    w16, q, s = quantized(4096, 4096, sw)
+    x16 = acts(1, 4096, sx)
+    assert_close(run_gemm(x16, q, s), oracle.gemm(x16, q, s), "gemv_4096")
+
+
+def _sampled(lin, M, workload, idx):
+    sw, sx = synthetic.seeds(workload, idx)
+    w16, q, s = quantized(lin.N, lin.K, sw)
+    x16 = acts(M, lin.K, sx)
+    y = run_gemm(x16, q, s)
+    rows = sample_rows(lin.N, 384, sw)
+    y_ref = oracle.gemm_rows(x16, q, s, rows)
+    assert_close(y[:, rows], y_ref, f"{lin.name} M={M}")
+
+
+@pytest.mark.parametrize("idx", range(len(workloads.LLAMA3_8B)))
+def test_llama3_8b_decode_shapes(w4lib, idx):
+    _sampled(workloads.LLAMA3_8B[idx], 1, "llama3_8b_decode", idx)
+
+
+@pytest.mark.parametrize("M", workloads.DECODE_SWEEP_M)
+@pytest.mark.parametrize("idx", range(len(workloads.LLAMA3_8B) + len(workloads.QWEN25_7B)))
+def test_decode_sweep(w4lib, M, idx):
+    shapes = workloads.LLAMA3_8B + workloads.QWEN25_7B
+    _sampled(shapes[idx], M, "decode_sweep", idx)

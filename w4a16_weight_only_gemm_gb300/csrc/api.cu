@@ -1,0 +1,178 @@
+// api.cu -- the C ABI (include/w4a16.h): argument checks, per-device set-up,
+// dispatch to the kernels, the device status word and its self-test.
+#include <mutex>
+
+#include "../../include/w4a16.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace w4a16 {
+namespace {
+
+// Status word written by kernels (atomicOr of kDev* bits); one per device.
+__device__ unsigned g_device_status;
+
+constexpr int kMaxDevices = 64;
+uint64_t g_timeout_ns = 2000000000ull;
+
+struct DeviceSlot {
+    std::once_flag once;
+    cudaError_t init_error = cudaSuccess;
+    bool supported = false;
+    DeviceCtx ctx{};
+};
+DeviceSlot g_slots[kMaxDevices];
+
+// Resolves the status word's device address (the symbol's host-side name is
+// only a handle) and the SM count once per device, with that device current.
+int device_ctx(DeviceCtx* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return W4A16_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return W4A16_ERR_DEVICE;
+    DeviceSlot& slot = g_slots[dev];
+    std::call_once(slot.once, [&]() {
+        cudaDeviceProp prop;
+        slot.init_error = cudaGetDeviceProperties(&prop, dev);
+        if (slot.init_error != cudaSuccess) return;
+        slot.supported = (prop.major == 10 && prop.minor == 3);
+        if (!slot.supported) return;
+        void* p = nullptr;
+        slot.init_error = cudaGetSymbolAddress(&p, g_device_status);
+        if (slot.init_error != cudaSuccess) return;
+        slot.ctx.status = static_cast<unsigned*>(p);
+        slot.ctx.num_sms = prop.multiProcessorCount;
+        slot.ctx.max_smem_optin = (int)prop.sharedMemPerBlockOptin;
+    });
+    if (slot.init_error != cudaSuccess) return W4A16_ERR_CUDA;
+    if (!slot.supported) return W4A16_ERR_DEVICE;
+    *out = slot.ctx;
+    out->timeout_ns = g_timeout_ns;
+    return W4A16_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool good_nk(int64_t N, int64_t K) {
+    return N >= 1 && N <= (int64_t)1 << 30 && K >= kGroup && K % kGroup == 0 &&
+           K <= (int64_t)1 << 20 && N * K <= (int64_t)1 << 40;
+}
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA; }
+
+__global__ void selftest_wait_kernel(unsigned* status, uint64_t timeout_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) (void)mbar_wait(b, 0, timeout_ns, status);  // nothing arrives
+}
+
+}  // namespace
+
+cudaError_t launch_selftest_wait(uint64_t timeout_ns, cudaStream_t stream, const DeviceCtx& ctx) {
+    selftest_wait_kernel<<<1, 32, 0, stream>>>(ctx.status, timeout_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace w4a16
+
+using namespace w4a16;
+
+extern "C" {
+
+const char* w4a16_status_string(int status) {
+    switch (status) {
+        case W4A16_OK: return "W4A16_OK";
+        case W4A16_ERR_NULL: return "W4A16_ERR_NULL: a required pointer is NULL";
+        case W4A16_ERR_SHAPE: return "W4A16_ERR_SHAPE: unsupported M, N, K or group size";
+        case W4A16_ERR_ALIGN: return "W4A16_ERR_ALIGN: a pointer is not 16-byte aligned";
+        case W4A16_ERR_CUDA: return "W4A16_ERR_CUDA: a CUDA runtime call or launch failed";
+        case W4A16_ERR_TIMEOUT: return "W4A16_ERR_TIMEOUT: a kernel's bounded wait gave up";
+        case W4A16_ERR_DEVICE: return "W4A16_ERR_DEVICE: the current device is not sm_103";
+        default: return "W4A16: unknown status";
+    }
+}
+
+int w4a16_version(void) { return 100; }
+
+int w4a16_quantize(const void* W_f16, int64_t N, int64_t K, int32_t group, void* qweight,
+                   void* scales_f16, void* stream) {
+    if (!W_f16 || !qweight || !scales_f16) return W4A16_ERR_NULL;
+    if (group != W4A16_GROUP || !good_nk(N, K)) return W4A16_ERR_SHAPE;
+    if (!aligned16(W_f16) || !aligned16(qweight) || !aligned16(scales_f16)) return W4A16_ERR_ALIGN;
+    DeviceCtx ctx;
+    if (int rc = device_ctx(&ctx)) return rc;
+    return from_cuda(launch_quantize(W_f16, N, K, qweight, scales_f16,
+                                     static_cast<cudaStream_t>(stream), ctx));
+}
+
+int64_t w4a16_repacked_bytes(int64_t N, int64_t K) {
+    if (!good_nk(N, K)) return -1;
+    return (N + kBlockRows - 1) / kBlockRows * kBlockRows * (K / 2);
+}
+
+int w4a16_repack(const void* qweight, int64_t N, int64_t K, void* repacked, void* stream) {
+    if (!qweight || !repacked) return W4A16_ERR_NULL;
+    if (!good_nk(N, K)) return W4A16_ERR_SHAPE;
+    if (!aligned16(qweight) || !aligned16(repacked)) return W4A16_ERR_ALIGN;
+    DeviceCtx ctx;
+    if (int rc = device_ctx(&ctx)) return rc;
+    return from_cuda(
+        launch_repack(qweight, N, K, repacked, static_cast<cudaStream_t>(stream), ctx));
+}
+
+int w4a16_unrepack(const void* repacked, int64_t N, int64_t K, void* qweight, void* stream) {
+    if (!qweight || !repacked) return W4A16_ERR_NULL;
+    if (!good_nk(N, K)) return W4A16_ERR_SHAPE;
+    if (!aligned16(qweight) || !aligned16(repacked)) return W4A16_ERR_ALIGN;
+    DeviceCtx ctx;
+    if (int rc = device_ctx(&ctx)) return rc;
+    return from_cuda(
+        launch_unrepack(repacked, N, K, qweight, static_cast<cudaStream_t>(stream), ctx));
+}
+
+int w4a16_gemm(const void* x_f16, const void* repacked, const void* scales_f16, void* y_f16,
+               int64_t M, int64_t N, int64_t K, void* stream) {
+    if (!x_f16 || !repacked || !scales_f16 || !y_f16) return W4A16_ERR_NULL;
+    if (M < 1 || M > (int64_t)1 << 24 || !good_nk(N, K) || N > (int64_t)1 << 28)
+        return W4A16_ERR_SHAPE;
+    if (!aligned16(x_f16) || !aligned16(repacked) || !aligned16(scales_f16) || !aligned16(y_f16))
+        return W4A16_ERR_ALIGN;
+    DeviceCtx ctx;
+    if (int rc = device_ctx(&ctx)) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (M <= 16) return from_cuda(launch_gemv(x_f16, repacked, scales_f16, y_f16, (int)M, N, K, s, ctx));
+    return from_cuda(launch_gemm_tc(x_f16, repacked, scales_f16, y_f16, M, N, K, s, ctx));
+}
+
+int w4a16_device_status(int* status) {
+    if (!status) return W4A16_ERR_NULL;
+    DeviceCtx ctx;
+    if (int rc = device_ctx(&ctx)) return rc;
+    if (cudaDeviceSynchronize() != cudaSuccess) return W4A16_ERR_CUDA;
+    unsigned word = 0;
+    if (cudaMemcpy(&word, ctx.status, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return W4A16_ERR_CUDA;
+    const unsigned zero = 0;
+    if (cudaMemcpy(ctx.status, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+        return W4A16_ERR_CUDA;
+    *status = (word & kDevTimeout) ? W4A16_ERR_TIMEOUT
+              : (word & kDevBadLaunch) ? W4A16_ERR_SHAPE
+                                       : W4A16_OK;
+    return W4A16_OK;
+}
+
+void w4a16_set_wait_timeout_ns(uint64_t timeout_ns) {
+    g_timeout_ns = timeout_ns == 0 ? 1 : timeout_ns;
+}
+
+int w4a16_selftest_wait_timeout(uint64_t timeout_ns, void* stream) {
+    DeviceCtx ctx;
+    if (int rc = device_ctx(&ctx)) return rc;
+    return from_cuda(launch_selftest_wait(timeout_ns, static_cast<cudaStream_t>(stream), ctx));
+}
+
+}  // extern "C"

@@ -1,0 +1,36 @@
+// kernels.h -- host-side launchers of the W4A16 kernels (internal to the
+// library; the public C ABI is include/w4a16.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace w4a16 {
+
+// Per-device facts and the device status word, resolved once per device.
+struct DeviceCtx {
+    unsigned* status;       // device address of the status word
+    uint64_t timeout_ns;    // bound on every in-kernel wait
+    int num_sms;
+    int max_smem_optin;     // bytes of dynamic shared memory a block may opt into
+};
+
+// Rows per repacked block and chunk width of the kernel layout.
+constexpr int kBlockRows = 128;
+constexpr int kChunkK = 64;
+constexpr int kGroup = 128;
+
+cudaError_t launch_quantize(const void* W, int64_t N, int64_t K, void* qweight, void* scales,
+                            cudaStream_t stream, const DeviceCtx& ctx);
+cudaError_t launch_repack(const void* qweight, int64_t N, int64_t K, void* repacked,
+                          cudaStream_t stream, const DeviceCtx& ctx);
+cudaError_t launch_unrepack(const void* repacked, int64_t N, int64_t K, void* qweight,
+                            cudaStream_t stream, const DeviceCtx& ctx);
+cudaError_t launch_gemv(const void* x, const void* repacked, const void* scales, void* y, int M,
+                        int64_t N, int64_t K, cudaStream_t stream, const DeviceCtx& ctx);
+cudaError_t launch_gemm_tc(const void* x, const void* repacked, const void* scales, void* y,
+                           int64_t M, int64_t N, int64_t K, cudaStream_t stream,
+                           const DeviceCtx& ctx);
+cudaError_t launch_selftest_wait(uint64_t timeout_ns, cudaStream_t stream, const DeviceCtx& ctx);
+
+}  // namespace w4a16

@@ -1,0 +1,123 @@
+"""Python entry points over the C ABI, for torch tensors.
+
+Each function validates shapes/dtypes, allocates outputs with torch (device
+memory is torch's), and calls the library on the current CUDA stream.  No
+arithmetic of the method happens here.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _native
+
+GROUP = 128
+
+
+def _stream_ptr(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, dtype, name: str) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def quantize(W: torch.Tensor, group: int = GROUP, stream=None):
+    """W fp16 [N, K] -> (qweight uint8 [N, K/2], scales fp16 [N, K/128])."""
+    _need(W, torch.float16, "W")
+    N, K = W.shape
+    q = torch.empty((N, K // 2), dtype=torch.uint8, device=W.device)
+    s = torch.empty((N, K // GROUP), dtype=torch.float16, device=W.device)
+    rc = _native.lib().w4a16_quantize(W.data_ptr(), N, K, group, q.data_ptr(), s.data_ptr(),
+                                      _stream_ptr(stream))
+    _native.check(rc, "w4a16_quantize")
+    return q, s
+
+
+def repacked_bytes(N: int, K: int) -> int:
+    n = _native.lib().w4a16_repacked_bytes(N, K)
+    if n < 0:
+        raise ValueError(f"unsupported shape N={N} K={K}")
+    return int(n)
+
+
+def repack(qweight: torch.Tensor, stream=None) -> torch.Tensor:
+    """Canonical [N, K/2] packed bytes -> kernel-layout bytes (1-D uint8)."""
+    _need(qweight, torch.uint8, "qweight")
+    N, K2 = qweight.shape
+    out = torch.empty(repacked_bytes(N, 2 * K2), dtype=torch.uint8, device=qweight.device)
+    rc = _native.lib().w4a16_repack(qweight.data_ptr(), N, 2 * K2, out.data_ptr(),
+                                    _stream_ptr(stream))
+    _native.check(rc, "w4a16_repack")
+    return out
+
+
+def unrepack(repacked: torch.Tensor, N: int, K: int, stream=None) -> torch.Tensor:
+    """Kernel-layout bytes -> canonical [N, K/2] packed bytes."""
+    _need(repacked, torch.uint8, "repacked")
+    if repacked.numel() != repacked_bytes(N, K):
+        raise ValueError("repacked buffer size does not match N, K")
+    q = torch.empty((N, K // 2), dtype=torch.uint8, device=repacked.device)
+    rc = _native.lib().w4a16_unrepack(repacked.data_ptr(), N, K, q.data_ptr(),
+                                      _stream_ptr(stream))
+    _native.check(rc, "w4a16_unrepack")
+    return q
+
+
+def gemm(x: torch.Tensor, repacked: torch.Tensor, scales: torch.Tensor,
+         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y[M, N] = x[M, K] @ dequant(W)^T; W given as kernel-layout bytes + scales [N, K/128]."""
+    _need(x, torch.float16, "x")
+    _need(repacked, torch.uint8, "repacked")
+    _need(scales, torch.float16, "scales")
+    M, K = x.shape
+    N = scales.shape[0]
+    if scales.shape[1] * GROUP != K:
+        raise ValueError("scales and x disagree on K")
+    if repacked.numel() != repacked_bytes(N, K):
+        raise ValueError("repacked buffer size does not match N, K")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    else:
+        _need(out, torch.float16, "out")
+        if tuple(out.shape) != (M, N):
+            raise ValueError("out has the wrong shape")
+    rc = _native.lib().w4a16_gemm(x.data_ptr(), repacked.data_ptr(), scales.data_ptr(),
+                                  out.data_ptr(), M, N, K, _stream_ptr(stream))
+    _native.check(rc, "w4a16_gemm")
+    return out
+
+
+def device_status() -> int:
+    """Synchronise and return (and clear) the kernels' recorded status code."""
+    st = ctypes.c_int(0)
+    _native.check(_native.lib().w4a16_device_status(ctypes.byref(st)), "w4a16_device_status")
+    return st.value
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    _native.lib().w4a16_set_wait_timeout_ns(int(ns))
+
+
+def selftest_wait_timeout(timeout_ns: int, stream=None) -> None:
+    rc = _native.lib().w4a16_selftest_wait_timeout(int(timeout_ns), _stream_ptr(stream))
+    _native.check(rc, "w4a16_selftest_wait_timeout")
+
+
+class W4A16Linear:
+    """A quantized linear layer y = x W^T held as kernel-layout weights + scales."""
+
+    def __init__(self, W: torch.Tensor):
+        self.N, self.K = W.shape
+        q, self.scales = quantize(W)
+        self.repacked = repack(q)
+
+    def __call__(self, x: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+        return gemm(x, self.repacked, self.scales, out=out)
