@@ -283,7 +283,8 @@ def run_ours(args, rank, world):
         "frac": round(per_rank_gbs / peaks.get("hbm_gbs", 6800.0), 3),
         "peak_source": "measured" if "hbm_gbs" in peaks else "fallback",
         "kernel": "gemv_kernel<1> (all launches of the step)",
-        "traffic": None,
+        "bytes_per_launch": step_bytes / len(layers),
+        "traffic": recorded_traffic(),
     }
     result["e2e"] = e2e_eager(layers, args, world)
     if rank == 0 and not args.skip_extras:
@@ -391,6 +392,31 @@ def quantizer_throughput():
     del Ws, qs, ss, rt
     return {"us": round(t * 1e6, 2), "gbs": round(b / t / 1e9, 1), "bytes": b,
             "repack_us_wall": round(trep * 1e6, 1)}
+
+
+def kernel_sha1() -> str:
+    import hashlib
+    h = hashlib.sha1()
+    for name in ("gemv.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "w4a16_weight_only_gemm_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """dram read + write bytes per launch of the GEMV kernel from the committed
+    ncu summary, or None if the kernel sources changed since that capture."""
+    import re
+    path = os.path.join(ROOT, "profiles", "gemv_kernel_llama3_8b_decode_m1.md")
+    try:
+        text = open(path, encoding="utf-8").read()
+    except OSError:
+        return None
+    sha = re.search(r"kernel_sha1: ([0-9a-f]+)", text)
+    tr = re.search(r"traffic_bytes_per_step: (\d+)", text)
+    if not sha or not tr or sha.group(1) != kernel_sha1():
+        return None
+    return int(tr.group(1)) / len(workloads.LLAMA3_8B)
 
 
 def load_peaks() -> dict:

@@ -1,31 +1,41 @@
-// gemv.cu -- W4A16 decode GEMV/skinny GEMM for M = 1..16.
+// gemv.cu -- W4A16 decode GEMV / skinny GEMM for M = 1..16.
 //
 // y[m, n] = sum_k x[m, k] * (nib[n, k] - 8) * scale[n, k / 128]
 // (mhpq.cn W4A16 report §二/§五: the packed weights stay packed in memory and
 // are unpacked in registers; the qaqbuyan.com tutorial §3 dequantizer fixes
 // the arithmetic).
 //
-// Design (one thread block = one 128-row block of W times a K range):
-//  * a producer warp streams the block's weights -- 4 KB per 64-wide chunk,
-//    contiguous in the kernel layout -- into a ring of shared-memory stages
-//    with bulk async copies (TMA engine) completing on mbarriers, L2 policy
-//    evict-first; the x slice of the K range arrives the same way;
-//  * 8 consumer warps own 16 rows each.  Per 64-wide chunk a lane reads 16
-//    bytes of its tile, expands each 32-bit word into an mma.m16n8k16 A
-//    fragment with lop3 + one f16x2 op per nibble pair (exact q), and
-//    multiplies it with x fragments read from shared memory.  M <= 8 uses
-//    one n8 MMA per 16 k, M <= 16 two.  Each 128-wide group accumulates in a
-//    fresh FP32 fragment that is scaled once by its fp16 scale and added to
-//    the FP32 running sum -- products q * x are exact, only FP32 sums round;
-//  * narrow N: the K range is split over the CTAs of a thread-block cluster
-//    (up to 8), whose FP32 partials are reduced through distributed shared
-//    memory in a fixed order -- no global workspace and no atomics;
-//  * programmatic dependent launch: the block prefetches its first stages
-//    into L2 before waiting on the previous kernel of the stream, and
-//    releases its dependents once its main loop is done.
-// Every wait is bounded (see common.cuh); on a time-out the block records it
-// in the status word, stops issuing copies, drains the ones in flight and
-// exits.
+// One thread block = 8 consumer warps (16 weight rows each: one 128-row
+// block of the kernel layout) + 1 producer warp.
+//  * The producer streams weights -- 4 KB per 64-wide chunk of a block,
+//    contiguous in the kernel layout -- into a ring of 16 KB shared-memory
+//    stages with bulk async copies (TMA engine) that complete on mbarriers,
+//    L2 policy evict-first.  Each block's fp16 scale slab (128 rows x K/128,
+//    contiguous in the canonical layout) arrives the same way into one of two
+//    buffers, and the x slice of the block's K range once per thread block.
+//  * Consumers: per 64-wide chunk a lane reads 16 bytes of its tile, expands
+//    each 32-bit word into an mma.m16n8k16 A fragment with lop3 + one f16x2
+//    op per nibble pair (exact q), and multiplies it with x fragments read
+//    from shared memory.  M <= 8 uses one n8 MMA per 16 k, M <= 16 two.
+//    Every 128-wide group accumulates in a fresh FP32 fragment that is scaled
+//    once by its fp16 scale and added to the FP32 running sum: q * x products
+//    are exact and only FP32 sums round.
+//  * Work split: when there are fewer 128-row blocks than SM slots, the K
+//    range is split over the CTAs of a thread-block cluster (up to 8) whose
+//    FP32 partials are reduced through distributed shared memory in a fixed
+//    order (no global workspace, no atomics).  Otherwise the grid is
+//    persistent: each CTA walks blocks y, y + gridDim.y, ... while the
+//    producer keeps the ring full across block boundaries.
+//  * Programmatic dependent launch: the CTA releases its dependents at once,
+//    prefetches its first weights and scales into L2 (safe before the
+//    dependency wait: L2 is the coherence point), then waits for the
+//    previous kernel before any copy into shared memory or write of y.
+// Every wait is bounded (common.cuh); on a time-out the CTA records it in the
+// status word, stops issuing copies, drains those in flight and exits.
+#include <mutex>
+#include <utility>
+#include <vector>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -33,12 +43,23 @@ namespace w4a16 {
 namespace {
 
 constexpr int kConsumerWarps = 8;                      // 8 x 16 rows = one block
-constexpr int kGemvThreads = (kConsumerWarps + 1) * 32;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kGemvThreads = kConsumers + 32;
 constexpr int kChunkBytes = kBlockRows * kChunkK / 2;  // 4096 B per block-chunk
-constexpr int kStages = 4;
-constexpr int kChunksPerStage = 4;                     // even: whole groups
+constexpr int kStages = 3;
+constexpr int kChunksPerStage = 4;                     // two whole groups
+constexpr int kGroupsPerStage = kChunksPerStage / 2;
 constexpr int kStageBytes = kChunksPerStage * kChunkBytes;
 constexpr int kMaxSplits = 8;
+
+// Barrier area at the start of shared memory.
+constexpr int kBarFull = 0;                    // [kStages]
+constexpr int kBarEmpty = kBarFull + 8 * kStages;
+constexpr int kBarX = kBarEmpty + 8 * kStages;
+constexpr int kBarSFull = kBarX + 8;           // [2]
+constexpr int kBarSEmpty = kBarSFull + 16;     // [2]
+constexpr int kAbortFlag = kBarSEmpty + 16;
+constexpr int kBarAreaBytes = 1024;
 
 struct GemvArgs {
     const uint8_t* wq;       // kernel-layout weights
@@ -48,8 +69,10 @@ struct GemvArgs {
     unsigned* status;
     uint64_t timeout_ns;
     int M, N, K, G;
+    int NB;                  // 128-row blocks
     int xs_stride;           // bytes between x rows in shared memory
-    int ng_max;              // groups per split, rounded up
+    int slab_bytes;          // bytes of one scale buffer (128 * G * 2, rounded)
+    int n_sbuf;              // scale buffers: 2 when a CTA walks several blocks
     uint32_t off_ring, off_x, off_s, off_red;
 };
 
@@ -57,206 +80,269 @@ __device__ __forceinline__ int split_group_begin(int split, int S, int G) {
     return (int)(((long long)split * G) / S);
 }
 
+// One 128-wide group (two chunks) of one consumer lane: 8 MMAs into a fresh
+// FP32 fragment, then scaled into acc.
 template <int MT>
-__global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_constant__ GemvArgs a) {
+__device__ __forceinline__ void mma_group(uint32_t w_addr, uint32_t x0_addr, uint32_t x1_addr,
+                                          float s0, float s1, float (&acc)[MT][4]) {
+    float g[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) g[mt][e] = 0.0f;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        const uint4 wv = lds128(w_addr + c * kChunkBytes);
+        const uint4 xa = lds128(x0_addr + c * 128);
+        const uint4 xb = lds128(x0_addr + c * 128 + 16);
+        uint4 xa1 = xa, xb1 = xb;
+        if (MT == 2) {
+            xa1 = lds128(x1_addr + c * 128);
+            xb1 = lds128(x1_addr + c * 128 + 16);
+        }
+        const uint32_t wrd[4] = {wv.x, wv.y, wv.z, wv.w};
+        const uint32_t b0[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+        const uint32_t b1[8] = {xa1.x, xa1.y, xa1.z, xa1.w, xb1.x, xb1.y, xb1.z, xb1.w};
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+            uint32_t af[4];
+            dequant8(wrd[s], af);
+            mma_16816(g[0], af, b0[2 * s], b0[2 * s + 1], g[0]);
+            if (MT == 2) mma_16816(g[MT - 1], af, b1[2 * s], b1[2 * s + 1], g[MT - 1]);
+        }
+    }
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+        acc[mt][0] = fmaf(s0, g[mt][0], acc[mt][0]);
+        acc[mt][1] = fmaf(s0, g[mt][1], acc[mt][1]);
+        acc[mt][2] = fmaf(s1, g[mt][2], acc[mt][2]);
+        acc[mt][3] = fmaf(s1, g[mt][3], acc[mt][3]);
+    }
+}
+
+template <int MT>
+__global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2) gemv_kernel(const __grid_constant__ GemvArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int S = (int)gridDim.x;  // cluster spans the whole x dimension
+    const int S = (int)gridDim.x;  // the cluster spans the whole x dimension
     const int split = (int)blockIdx.x;
-    const int rb = (int)blockIdx.y;
     const int C = a.K / kChunkK;
     const int g0 = split_group_begin(split, S, a.G);
-    const int g1 = split_group_begin(split + 1, S, a.G);
-    const int ng = g1 - g0;
+    const int ng = split_group_begin(split + 1, S, a.G) - g0;
     const int nck = 2 * ng;
-    const int iters = (nck + kChunksPerStage - 1) / kChunksPerStage;
+    const int nstg = (nck + kChunksPerStage - 1) / kChunksPerStage;
+    const int nblk = (a.NB - (int)blockIdx.y + (int)gridDim.y - 1) / (int)gridDim.y;
 
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t bar_full = sbase;
-    const uint32_t bar_empty = sbase + 8 * kStages;
-    const uint32_t bar_x = sbase + 16 * kStages;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 16 * kStages + 8);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortFlag);
     const uint32_t ring = sbase + a.off_ring;
-    const uint32_t xs = sbase + a.off_x;
-    __half* ss = reinterpret_cast<__half*>(smem + a.off_s);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, kConsumerWarps);
+            mbar_init(sbase + kBarFull + 8 * s, 1);
+            mbar_init(sbase + kBarEmpty + 8 * s, kConsumerWarps);
         }
-        mbar_init(bar_x, 1);
+        mbar_init(sbase + kBarX, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(sbase + kBarSFull + 8 * b, 1);
+            mbar_init(sbase + kBarSEmpty + 8 * b, kConsumerWarps);
+        }
         *abort_flag = 0;
         fence_barrier_init();
     }
     __syncthreads();
-
-    const uint8_t* wsrc = a.wq + ((size_t)rb * C + 2 * (size_t)g0) * kChunkBytes;
+    // Dependents may start their own prologue (and L2 prefetch) right away;
+    // their griddepcontrol.wait still waits for this grid to complete.
+    grid_launch_dependents();
 
     if (warp == kConsumerWarps) {
-        // ------------------------------ producer ------------------------------
+        // =============================== producer ===============================
         if (lane == 0) {
-            const int pre = iters < kStages ? iters : kStages;
-            for (int i = 0; i < pre; ++i) {
-                const int nc = min(kChunksPerStage, nck - i * kChunksPerStage);
-                bulk_prefetch_l2(wsrc + (size_t)i * kStageBytes, nc * kChunkBytes);
+            const uint64_t pol = l2_policy_evict_first();
+            const size_t block_stride = (size_t)C * kChunkBytes;
+            {   // L2 prefetch of the first block (weights of this split, scale slab).
+                const int rb = (int)blockIdx.y;
+                const uint8_t* w = a.wq + (size_t)rb * block_stride + 2 * (size_t)g0 * kChunkBytes;
+                const int pre = nstg < 2 * kStages ? nstg : 2 * kStages;
+                for (int i = 0; i < pre; ++i)
+                    bulk_prefetch_l2(w + (size_t)i * kStageBytes,
+                                     min(kChunksPerStage, nck - i * kChunksPerStage) * kChunkBytes);
+                const int rows = min(kBlockRows, a.N - rb * kBlockRows);
+                const uint32_t sb = ((uint32_t)(rows * a.G * 2)) & ~15u;
+                if (sb) bulk_prefetch_l2(a.scales + (size_t)rb * kBlockRows * a.G, sb);
             }
             grid_dependency_wait();
-            const uint64_t pol = l2_policy_evict_first();
             const uint32_t xbytes = (uint32_t)nck * (kChunkK * 2);
-            mbar_arrive_expect_tx(bar_x, xbytes * a.M);
+            mbar_arrive_expect_tx(sbase + kBarX, xbytes * a.M);
             for (int m = 0; m < a.M; ++m)
-                bulk_g2s(xs + m * a.xs_stride, a.x + (size_t)m * a.K + (size_t)g0 * kGroup, xbytes,
-                         bar_x);
-            int issued = 0;
-            for (int i = 0; i < iters; ++i) {
-                const int slot = i % kStages;
-                if (i >= kStages) {
-                    if (!mbar_wait(bar_empty + 8 * slot, ((i / kStages) - 1) & 1, a.timeout_ns,
-                                   a.status)) {
-                        *abort_flag = 1;
+                bulk_g2s(sbase + a.off_x + m * a.xs_stride,
+                         a.x + (size_t)m * a.K + (size_t)g0 * kGroup, xbytes, sbase + kBarX);
+            int it = 0;
+            bool ok = true;
+            int sb_issued = 0;
+            for (int j = 0; ok && j < nblk; ++j) {
+                const int rb = (int)blockIdx.y + j * (int)gridDim.y;
+                // --- scale slab of block rb ---
+                const int sbuf = j % a.n_sbuf;
+                if (j >= a.n_sbuf &&
+                    !mbar_wait(sbase + kBarSEmpty + 8 * sbuf, ((j / a.n_sbuf) - 1) & 1,
+                               a.timeout_ns, a.status)) {
+                    ok = false;
+                    break;
+                }
+                {
+                    const int rows = min(kBlockRows, a.N - rb * kBlockRows);
+                    const uint32_t bytes = (uint32_t)(rows * a.G * 2);
+                    const uint32_t bulk = bytes & ~15u;
+                    const __half* src = a.scales + (size_t)rb * kBlockRows * a.G;
+                    __half* dst = reinterpret_cast<__half*>(smem + a.off_s + sbuf * a.slab_bytes);
+                    for (uint32_t e = bulk / 2; e < bytes / 2; ++e) dst[e] = src[e];  // ragged tail
+                    mbar_arrive_expect_tx(sbase + kBarSFull + 8 * sbuf, bulk);
+                    if (bulk)
+                        bulk_g2s(sbase + a.off_s + sbuf * a.slab_bytes, src, bulk,
+                                 sbase + kBarSFull + 8 * sbuf);
+                    sb_issued = j + 1;
+                }
+                // --- weight stages of block rb ---
+                const uint8_t* w = a.wq + (size_t)rb * block_stride + 2 * (size_t)g0 * kChunkBytes;
+                for (int st = 0; st < nstg; ++st, ++it) {
+                    const int slot = it % kStages;
+                    if (it >= kStages &&
+                        !mbar_wait(sbase + kBarEmpty + 8 * slot, ((it / kStages) - 1) & 1,
+                                   a.timeout_ns, a.status)) {
+                        ok = false;
                         break;
                     }
+                    if (*abort_flag) {
+                        ok = false;
+                        break;
+                    }
+                    const int nc = min(kChunksPerStage, nck - st * kChunksPerStage);
+                    mbar_arrive_expect_tx(sbase + kBarFull + 8 * slot, nc * kChunkBytes);
+                    bulk_g2s_hint(ring + slot * kStageBytes, w + (size_t)st * kStageBytes,
+                                  nc * kChunkBytes, sbase + kBarFull + 8 * slot, pol);
                 }
-                if (*abort_flag) break;
-                const int nc = min(kChunksPerStage, nck - i * kChunksPerStage);
-                mbar_arrive_expect_tx(bar_full + 8 * slot, nc * kChunkBytes);
-                bulk_g2s_hint(ring + slot * kStageBytes, wsrc + (size_t)i * kStageBytes,
-                              nc * kChunkBytes, bar_full + 8 * slot, pol);
-                issued = i + 1;
             }
-            // Drain: every issued copy must land before the block may exit.
-            mbar_wait(bar_x, 0, a.timeout_ns, a.status);
-            for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
-                mbar_wait(bar_full + 8 * (i % kStages), (i / kStages) & 1, a.timeout_ns, a.status);
+            if (!ok) *abort_flag = 1;
+            // Drain: every issued copy must land before the CTA may exit.
+            mbar_wait(sbase + kBarX, 0, a.timeout_ns, a.status);
+            for (int i = (it > kStages ? it - kStages : 0); i < it; ++i)
+                mbar_wait(sbase + kBarFull + 8 * (i % kStages), (i / kStages) & 1, a.timeout_ns,
+                          a.status);
+            for (int j = (sb_issued > a.n_sbuf ? sb_issued - a.n_sbuf : 0); j < sb_issued; ++j)
+                mbar_wait(sbase + kBarSFull + 8 * (j % a.n_sbuf), (j / a.n_sbuf) & 1, a.timeout_ns,
+                          a.status);
         }
         __syncwarp();
     } else {
-        // ------------------------------ consumers -----------------------------
+        // =============================== consumers ==============================
         grid_dependency_wait();
-        // Scales of this block's 128 rows and groups [g0, g1) -> smem [row][ng_max].
-        {
-            const int rows_here = min(kBlockRows, a.N - rb * kBlockRows);
-            for (int idx = threadIdx.x; idx < kBlockRows * ng; idx += kConsumerWarps * 32) {
-                const int r = idx / ng, gg = idx - r * ng;
-                __half v = __ushort_as_half(0);
-                if (r < rows_here) v = a.scales[(size_t)(rb * kBlockRows + r) * a.G + g0 + gg];
-                ss[r * a.ng_max + gg] = v;
-            }
-            asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-        }
-
         const int g = lane >> 2, t = lane & 3;
-        const int row0 = warp * 16 + g;  // local rows of this lane's fragments
+        const int row0 = warp * 16 + g;  // rows of this lane's fragments in the block
         const int row1 = row0 + 8;
-        const bool xl0 = g < a.M;
-        const bool xl1 = (g + 8) < a.M;
-        const uint32_t xa0 = xs + g * a.xs_stride + t * 32;
-        const uint32_t xa1 = xs + (g + 8) * a.xs_stride + t * 32;
+        // x rows: lanes beyond M read row M-1; their MMA columns are discarded.
+        const int xr0 = g < a.M ? g : a.M - 1;
+        const int xr1 = g + 8 < a.M ? g + 8 : a.M - 1;
+        const uint32_t x0 = sbase + a.off_x + xr0 * a.xs_stride + t * 32;
+        const uint32_t x1 = sbase + a.off_x + xr1 * a.xs_stride + t * 32;
         const uint32_t wl = ring + warp * 512 + lane * 16;
+        const int nfull = nck / kChunksPerStage;       // stages holding two groups
+        const bool tail = (nck % kChunksPerStage) != 0;  // one group left
 
-        float acc[MT][4];
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) acc[mt][j] = 0.0f;
-
-        bool ok = mbar_wait(bar_x, 0, a.timeout_ns, a.status);
-        for (int i = 0; ok && i < iters; ++i) {
-            const int slot = i % kStages;
-            if (!mbar_wait(bar_full + 8 * slot, (i / kStages) & 1, a.timeout_ns, a.status)) {
+        bool ok = mbar_wait(sbase + kBarX, 0, a.timeout_ns, a.status);
+        int it = 0;
+        for (int j = 0; ok && j < nblk; ++j) {
+            const int rb = (int)blockIdx.y + j * (int)gridDim.y;
+            const int sbuf = j % a.n_sbuf;
+            if (!mbar_wait(sbase + kBarSFull + 8 * sbuf, (j / a.n_sbuf) & 1, a.timeout_ns,
+                           a.status)) {
                 ok = false;
                 break;
             }
-            const int nc = min(kChunksPerStage, nck - i * kChunksPerStage);
+            const __half* sc0 = reinterpret_cast<const __half*>(smem + a.off_s + sbuf * a.slab_bytes) +
+                                row0 * a.G + g0;
+            const __half* sc1 = sc0 + 8 * a.G;
+            float acc[MT][4];
 #pragma unroll
-            for (int j = 0; j < kChunksPerStage; j += 2) {
-                if (j < nc) {
-                    float gacc[MT][4];
+            for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-                    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) gacc[mt][e] = 0.0f;
-#pragma unroll
-                    for (int jj = 0; jj < 2; ++jj) {
-                        const int cl = i * kChunksPerStage + j + jj;  // local chunk
-                        const uint4 wv = lds128(wl + slot * kStageBytes + (j + jj) * kChunkBytes);
-                        uint4 xv0a = make_uint4(0, 0, 0, 0), xv0b = xv0a, xv1a = xv0a, xv1b = xv0a;
-                        if (xl0) {
-                            xv0a = lds128(xa0 + cl * 128);
-                            xv0b = lds128(xa0 + cl * 128 + 16);
-                        }
-                        if (MT == 2 && xl1) {
-                            xv1a = lds128(xa1 + cl * 128);
-                            xv1b = lds128(xa1 + cl * 128 + 16);
-                        }
-                        const uint32_t wrd[4] = {wv.x, wv.y, wv.z, wv.w};
-                        const uint32_t xb0[8] = {xv0a.x, xv0a.y, xv0a.z, xv0a.w,
-                                                 xv0b.x, xv0b.y, xv0b.z, xv0b.w};
-                        const uint32_t xb1[8] = {xv1a.x, xv1a.y, xv1a.z, xv1a.w,
-                                                 xv1b.x, xv1b.y, xv1b.z, xv1b.w};
-#pragma unroll
-                        for (int s = 0; s < 4; ++s) {
-                            uint32_t af[4];
-                            dequant8(wrd[s], af);
-                            mma_16816(gacc[0], af, xb0[2 * s], xb0[2 * s + 1], gacc[0]);
-                            if (MT == 2)
-                                mma_16816(gacc[MT - 1], af, xb1[2 * s], xb1[2 * s + 1],
-                                          gacc[MT - 1]);
-                        }
-                    }
-                    const int gl = (i * kChunksPerStage + j) >> 1;  // local group
-                    const float s0 = __half2float(ss[row0 * a.ng_max + gl]);
-                    const float s1 = __half2float(ss[row1 * a.ng_max + gl]);
-#pragma unroll
-                    for (int mt = 0; mt < MT; ++mt) {
-                        acc[mt][0] = fmaf(s0, gacc[mt][0], acc[mt][0]);
-                        acc[mt][1] = fmaf(s0, gacc[mt][1], acc[mt][1]);
-                        acc[mt][2] = fmaf(s1, gacc[mt][2], acc[mt][2]);
-                        acc[mt][3] = fmaf(s1, gacc[mt][3], acc[mt][3]);
-                    }
+                for (int e = 0; e < 4; ++e) acc[mt][e] = 0.0f;
+
+            uint32_t xs_off = 0;
+            for (int st = 0; st < nfull; ++st, ++it, xs_off += kChunksPerStage * 128) {
+                const int slot = it % kStages;
+                if (!mbar_wait(sbase + kBarFull + 8 * slot, (it / kStages) & 1, a.timeout_ns,
+                               a.status)) {
+                    ok = false;
+                    break;
                 }
+                const uint32_t wa = wl + slot * kStageBytes;
+#pragma unroll
+                for (int gi = 0; gi < kGroupsPerStage; ++gi) {
+                    const int gl = st * kGroupsPerStage + gi;
+                    mma_group<MT>(wa + gi * 2 * kChunkBytes, x0 + xs_off + gi * 256,
+                                  x1 + xs_off + gi * 256, __half2float(sc0[gl]),
+                                  __half2float(sc1[gl]), acc);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sbase + kBarEmpty + 8 * slot);
+            }
+            if (ok && tail) {
+                const int slot = it % kStages;
+                if (!mbar_wait(sbase + kBarFull + 8 * slot, (it / kStages) & 1, a.timeout_ns,
+                               a.status)) {
+                    ok = false;
+                } else {
+                    const int gl = nfull * kGroupsPerStage;
+                    mma_group<MT>(wl + slot * kStageBytes, x0 + xs_off, x1 + xs_off,
+                                  __half2float(sc0[gl]), __half2float(sc1[gl]), acc);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(sbase + kBarEmpty + 8 * slot);
+                }
+                ++it;
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
+            if (lane == 0) mbar_arrive(sbase + kBarSEmpty + 8 * sbuf);
+            if (!ok) break;
+
+            const int R0 = rb * kBlockRows + row0;
+            const int R1 = rb * kBlockRows + row1;
+            if (S == 1) {
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    const int m0 = mt * 8 + 2 * t, m1 = m0 + 1;
+                    if (m0 < a.M) {
+                        if (R0 < a.N) a.y[(size_t)m0 * a.N + R0] = __float2half_rn(acc[mt][0]);
+                        if (R1 < a.N) a.y[(size_t)m0 * a.N + R1] = __float2half_rn(acc[mt][2]);
+                    }
+                    if (m1 < a.M) {
+                        if (R0 < a.N) a.y[(size_t)m1 * a.N + R0] = __float2half_rn(acc[mt][1]);
+                        if (R1 < a.N) a.y[(size_t)m1 * a.N + R1] = __float2half_rn(acc[mt][3]);
+                    }
+                }
+            } else {
+                // One block per CTA in split mode: park the partials for the
+                // cluster reduction below.
+                float* red = reinterpret_cast<float*>(smem + a.off_red);  // [128][16]
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    const int m0 = mt * 8 + 2 * t;
+                    red[row0 * 16 + m0] = acc[mt][0];
+                    red[row0 * 16 + m0 + 1] = acc[mt][1];
+                    red[row1 * 16 + m0] = acc[mt][2];
+                    red[row1 * 16 + m0 + 1] = acc[mt][3];
+                }
+            }
         }
         if (!ok) *abort_flag = 1;
-
-        grid_launch_dependents();
-
-        const int R0 = rb * kBlockRows + row0;
-        const int R1 = rb * kBlockRows + row1;
-        if (S == 1) {
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-                const int m0 = mt * 8 + 2 * t, m1 = m0 + 1;
-                if (m0 < a.M) {
-                    if (R0 < a.N) a.y[(size_t)m0 * a.N + R0] = __float2half_rn(acc[mt][0]);
-                    if (R1 < a.N) a.y[(size_t)m0 * a.N + R1] = __float2half_rn(acc[mt][2]);
-                }
-                if (m1 < a.M) {
-                    if (R0 < a.N) a.y[(size_t)m1 * a.N + R0] = __float2half_rn(acc[mt][1]);
-                    if (R1 < a.N) a.y[(size_t)m1 * a.N + R1] = __float2half_rn(acc[mt][3]);
-                }
-            }
-        } else {
-            float* red = reinterpret_cast<float*>(smem + a.off_red);  // [128][16]
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-                const int m0 = mt * 8 + 2 * t;
-                red[row0 * 16 + m0] = acc[mt][0];
-                red[row0 * 16 + m0 + 1] = acc[mt][1];
-                red[row1 * 16 + m0] = acc[mt][2];
-                red[row1 * 16 + m0 + 1] = acc[mt][3];
-            }
-        }
     }
 
     if (S > 1) {
         // Fixed-order reduction of the cluster's partials through DSMEM: CTA
-        // `split` finalises rows split, split + S, ... of the block.
+        // `split` finalises rows split, split + S, ... of its block.
         cluster_sync_all();
+        const int rb = (int)blockIdx.y;
         const uint32_t red_base = sbase + a.off_red;
         const int M = a.M;
         for (int idx = threadIdx.x; idx < kBlockRows * M; idx += kGemvThreads) {
@@ -274,52 +360,133 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
 }
 
 struct GemvPlan {
-    int S;
-    int xs_stride;
-    int ng_max;
-    uint32_t off_ring, off_x, off_s, off_red, smem;
+    int S = 0;
+    int grid_y = 0;
+    int n_sbuf = 1;
+    int xs_stride = 0;
+    int slab_bytes = 0;
+    uint32_t off_ring = 0, off_x = 0, off_s = 0, off_red = 0, smem = 0;
+    double eff = 0.0;
 };
 
+template <int MT>
+int occupancy(uint32_t smem) {
+    int blocks = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, gemv_kernel<MT>, kGemvThreads,
+                                                      smem) != cudaSuccess)
+        return 0;
+    return blocks;
+}
+
+template <int MT>
+cudaError_t ensure_smem_attr() {
+    static bool done[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(gemv_kernel<MT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+    return e;
+}
+
+// Shared-memory layout of a launch with K split S and `nsb` scale buffers.
+template <int MT>
+bool layout(GemvPlan& p, int M, int G, int S, int nsb, const DeviceCtx& ctx) {
+    p.S = S;
+    p.n_sbuf = nsb;
+    const int ng_max = (G + S - 1) / S;
+    p.xs_stride = ng_max * kGroup * 2 + 16;  // +16 B keeps x rows conflict-free
+    p.slab_bytes = ((kBlockRows * G * 2 + 127) / 128) * 128;
+    p.off_ring = kBarAreaBytes;
+    p.off_x = p.off_ring + kStages * kStageBytes;
+    p.off_s = p.off_x + ((M * p.xs_stride + 127) / 128) * 128;
+    p.off_red = p.off_s + nsb * p.slab_bytes;
+    p.smem = p.off_red + (S > 1 ? kBlockRows * 16 * 4 : 0);
+    return (int)p.smem <= ctx.max_smem_optin;
+}
+
+// Chooses the K split S (cluster size).  With more 128-row blocks than CTA
+// slots the grid is persistent (S = 1, one CTA per slot walking blocks).
+// Otherwise every CTA handles one block's K range 1/S and S is chosen so the
+// heaviest SM carries as little as possible; near-ties go to the larger S
+// (more, shorter CTAs hide latency better).
+template <int MT>
 GemvPlan plan_gemv(int M, int N, int K, const DeviceCtx& ctx) {
     const int G = K / kGroup;
     const int NB = (N + kBlockRows - 1) / kBlockRows;
-    GemvPlan best{};
-    best.S = 0;
+    GemvPlan best;
+    {
+        GemvPlan p;
+        if (layout<MT>(p, M, G, 1, 2, ctx)) {
+            const int occ = occupancy<MT>(p.smem);
+            if (occ > 0 && NB > ctx.num_sms * occ) {
+                p.grid_y = ctx.num_sms * occ;
+                p.eff = 1.0;
+                return p;
+            }
+        }
+    }
+    const double per_sm = (double)NB / ctx.num_sms;
     const int max_s = G < kMaxSplits ? G : kMaxSplits;
     for (int S = 1; S <= max_s; ++S) {
-        GemvPlan p{};
-        p.S = S;
-        p.ng_max = (G + S - 1) / S;
-        p.xs_stride = p.ng_max * kGroup * 2 + 16;  // +16 B: conflict-free x rows
-        p.off_ring = 1024;
-        p.off_x = p.off_ring + kStages * kStageBytes;
-        p.off_s = p.off_x + ((M * p.xs_stride + 127) / 128) * 128;
-        p.off_red = p.off_s + ((kBlockRows * p.ng_max * 2 + 127) / 128) * 128;
-        p.smem = p.off_red + (S > 1 ? kBlockRows * 16 * 4 : 0);
-        if ((int)p.smem > ctx.max_smem_optin) continue;
-        if (best.S == 0) best = p;
-        // Enough blocks to cover every SM at least once; stop at the first
-        // split count that does, keeping clusters small.
-        best = p;
-        if ((long long)NB * S >= ctx.num_sms) break;
+        GemvPlan p;
+        if (!layout<MT>(p, M, G, S, 1, ctx)) continue;
+        const int occ = occupancy<MT>(p.smem);
+        if (occ == 0) continue;
+        const long long units = (long long)NB * S;
+        const long long slots = (long long)ctx.num_sms * occ;
+        const long long heaviest = (units + ctx.num_sms - 1) / ctx.num_sms;
+        double eff = per_sm / ((double)heaviest / S);
+        if (units > slots) eff *= 0.85;  // more than one wave of CTAs
+        eff += 0.001 * S;
+        p.grid_y = NB;
+        p.eff = eff;
+        if (eff > best.eff) best = p;
     }
     return best;
 }
 
+struct PlanKey {
+    int dev, M, N, K;
+    bool operator==(const PlanKey& o) const {
+        return dev == o.dev && M == o.M && N == o.N && K == o.K;
+    }
+};
+
 template <int MT>
-cudaError_t launch_gemv_mt(const GemvArgs& args, const GemvPlan& p, int NB, cudaStream_t stream) {
-    static bool attr_done[64] = {};
+GemvPlan cached_plan(int M, int N, int K, const DeviceCtx& ctx) {
+    static std::mutex mu;
+    static std::vector<std::pair<PlanKey, GemvPlan>> cache;
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 64 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(gemv_kernel<MT>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             227 * 1024);
-        if (e != cudaSuccess) return e;
-        attr_done[dev] = true;
+    const PlanKey key{dev, M, N, K};
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (const auto& e : cache)
+            if (e.first == key) return e.second;
     }
+    const GemvPlan p = plan_gemv<MT>(M, N, K, ctx);
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache.size() < 4096) cache.emplace_back(key, p);
+    return p;
+}
+
+template <int MT>
+cudaError_t launch_gemv_mt(GemvArgs args, int M, cudaStream_t stream, const DeviceCtx& ctx) {
+    cudaError_t e = ensure_smem_attr<MT>();
+    if (e != cudaSuccess) return e;
+    const GemvPlan p = cached_plan<MT>(M, args.N, args.K, ctx);
+    if (p.S == 0) return cudaErrorInvalidValue;
+    args.xs_stride = p.xs_stride;
+    args.slab_bytes = p.slab_bytes;
+    args.n_sbuf = p.n_sbuf;
+    args.off_ring = p.off_ring;
+    args.off_x = p.off_x;
+    args.off_s = p.off_s;
+    args.off_red = p.off_red;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)p.S, (unsigned)NB, 1);
+    cfg.gridDim = dim3((unsigned)p.S, (unsigned)p.grid_y, 1);
     cfg.blockDim = dim3(kGemvThreads, 1, 1);
     cfg.dynamicSmemBytes = p.smem;
     cfg.stream = stream;
@@ -344,8 +511,6 @@ cudaError_t launch_gemv_mt(const GemvArgs& args, const GemvPlan& p, int NB, cuda
 
 cudaError_t launch_gemv(const void* x, const void* repacked, const void* scales, void* y, int M,
                         int64_t N, int64_t K, cudaStream_t stream, const DeviceCtx& ctx) {
-    const GemvPlan p = plan_gemv(M, (int)N, (int)K, ctx);
-    if (p.S == 0) return cudaErrorInvalidValue;
     GemvArgs a{};
     a.wq = static_cast<const uint8_t*>(repacked);
     a.scales = static_cast<const __half*>(scales);
@@ -357,15 +522,9 @@ cudaError_t launch_gemv(const void* x, const void* repacked, const void* scales,
     a.N = (int)N;
     a.K = (int)K;
     a.G = (int)(K / kGroup);
-    a.xs_stride = p.xs_stride;
-    a.ng_max = p.ng_max;
-    a.off_ring = p.off_ring;
-    a.off_x = p.off_x;
-    a.off_s = p.off_s;
-    a.off_red = p.off_red;
-    const int NB = (int)((N + kBlockRows - 1) / kBlockRows);
-    if (M <= 8) return launch_gemv_mt<1>(a, p, NB, stream);
-    return launch_gemv_mt<2>(a, p, NB, stream);
+    a.NB = (int)((N + kBlockRows - 1) / kBlockRows);
+    if (M <= 8) return launch_gemv_mt<1>(a, M, stream, ctx);
+    return launch_gemv_mt<2>(a, M, stream, ctx);
 }
 
 }  // namespace w4a16
