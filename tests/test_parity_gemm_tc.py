@@ -1,0 +1,82 @@
+"""Prefill GEMM (M > 16, tcgen05 tensor cores) vs the binary64 oracle.
+
+The kernel stages fp16(q * scale) -- the tutorial's own fp16 dequantized
+weight, one rounding of at most 2^-11 relative -- and accumulates in FP32 in
+tensor memory; together with the final fp16 rounding of y that stays inside
+the same bar as the GEMV: max|y - y_ref| <= 2e-3 max|y_ref| and
+||y - y_ref|| <= 1e-3 ||y_ref||."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import assert_close, from_bits16
+from parity_data import acts, as_device, quantized, sample_rows
+import w4a16_weight_only_gemm_gb300 as w4
+from w4a16_weight_only_gemm_gb300 import synthetic, workloads
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gemm(x16, q, s):
+    qt, st = as_device(q, s)
+    y = w4.gemm(from_bits16(x16), w4.repack(qt), st)
+    torch.cuda.synchronize()
+    assert w4.device_status() == 0
+    return y.float().cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("M", [17, 31, 64, 128, 130, 256, 300])
+def test_m_values(w4lib, M):
+    N, K = 256, 512
+    w16, q, s = quantized(N, K, 61)
+    x16 = acts(M, K, 62 + M)
+    assert_close(run_gemm(x16, q, s), oracle.gemm(x16, q, s), f"M={M}")
+
+
+@pytest.mark.parametrize("N,K", [(128, 128), (200, 384), (1000, 1152), (4168, 640), (136, 18944)])
+@pytest.mark.parametrize("M", [20, 144])
+def test_shapes_and_tails(w4lib, M, N, K):
+    w16, q, s = quantized(N, K, 71)
+    x16 = acts(M, K, 72)
+    assert_close(run_gemm(x16, q, s), oracle.gemm(x16, q, s), f"M={M} N={N} K={K}")
+
+
+def test_every_nibble_value(w4lib):
+    rng = np.random.default_rng(81)
+    N, K, M = 384, 1024, 96
+    q = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    s = (rng.uniform(0.5, 2.0, size=(N, K // 128)) * 2.0 ** rng.integers(-12, 2, size=(N, K // 128))
+         ).astype(np.float16).view(np.uint16)
+    x16 = acts(M, K, 82)
+    assert_close(run_gemm(x16, q, s), oracle.gemm(x16, q, s), "nibbles")
+
+
+def test_guard_bands(w4lib):
+    N, K, M = 200, 256, 70
+    w16, q, s = quantized(N, K, 91)
+    x = from_bits16(acts(M, K, 92))
+    qt, st = as_device(q, s)
+    r = w4.repack(qt)
+    pad = 64
+    buf = torch.full((M * N + 2 * pad,), float("nan"), dtype=torch.float16, device="cuda")
+    y = buf[pad:pad + M * N].view(M, N)
+    w4.gemm(x, r, st, out=y)
+    torch.cuda.synchronize()
+    assert torch.isnan(buf[:pad]).all() and torch.isnan(buf[pad + M * N:]).all()
+    x16 = x.cpu().view(torch.int16).numpy().view(np.uint16)
+    assert_close(y.float().cpu().numpy(), oracle.gemm(x16, q, s), "guard")
+
+
+@pytest.mark.parametrize("idx", range(len(workloads.PREFILL)))
+def test_prefill_full_size(w4lib, idx):
+    """M = 512 prompt pass on the two prefill shapes; oracle on sampled rows."""
+    lin = workloads.PREFILL[idx]
+    sw, sx = synthetic.seeds("prefill", idx)
+    w16, q, s = quantized(lin.N, lin.K, sw)
+    x16 = acts(workloads.PREFILL_M, lin.K, sx)
+    y = run_gemm(x16, q, s)
+    rows = sample_rows(lin.N, 96, sw)
+    assert_close(y[:, rows], oracle.gemm_rows(x16, q, s, rows), lin.name)

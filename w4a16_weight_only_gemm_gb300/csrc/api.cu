@@ -57,7 +57,12 @@ bool good_nk(int64_t N, int64_t K) {
            K <= (int64_t)1 << 20 && N * K <= (int64_t)1 << 40;
 }
 
-int from_cuda(cudaError_t e) { return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA; }
+// Launchers report an unsupported configuration (no shared-memory layout
+// fits) as cudaErrorInvalidValue before launching anything.
+int from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return W4A16_OK;
+    return e == cudaErrorInvalidValue ? W4A16_ERR_SHAPE : W4A16_ERR_CUDA;
+}
 
 __global__ void selftest_wait_kernel(unsigned* status, uint64_t timeout_ns) {
     __shared__ __align__(8) uint64_t bar;
@@ -137,7 +142,8 @@ int w4a16_unrepack(const void* repacked, int64_t N, int64_t K, void* qweight, vo
 int w4a16_gemm(const void* x_f16, const void* repacked, const void* scales_f16, void* y_f16,
                int64_t M, int64_t N, int64_t K, void* stream) {
     if (!x_f16 || !repacked || !scales_f16 || !y_f16) return W4A16_ERR_NULL;
-    if (M < 1 || M > (int64_t)1 << 24 || !good_nk(N, K) || N > (int64_t)1 << 28)
+    if (M < 1 || M > (int64_t)1 << 22 || !good_nk(N, K) || N > (int64_t)1 << 28 ||
+        K > (int64_t)1 << 15)
         return W4A16_ERR_SHAPE;
     if (!aligned16(x_f16) || !aligned16(repacked) || !aligned16(scales_f16) || !aligned16(y_f16))
         return W4A16_ERR_ALIGN;
