@@ -342,6 +342,32 @@ def extras(layers):
             sweep[f"{fam}_{lin.name}_m{M}"] = per_shape_us(lin, "decode_sweep", i, M=M, reps=10)
     out["decode_sweep"] = sweep
     out["quantizer"] = quantizer_throughput()
+    out["prefill_m512"] = prefill()
+    return out
+
+
+def prefill():
+    """M = 512 prompt pass on the two prefill shapes (tcgen05 path), with a
+    cuBLAS fp16 GEMM on pre-dequantised weights of the same shape as the
+    practical ceiling (context only)."""
+    import w4a16_weight_only_gemm_gb300 as w4
+    out = {}
+    peaks = load_peaks()
+    for i, lin in enumerate(workloads.PREFILL):
+        layer = make_layer(lin, "prefill", i, M=workloads.PREFILL_M)
+        stream = torch.cuda.Stream()
+        g = capture(lambda: gemm_call(layer), stream)
+        t = time_graph(g, stream, 20, 3)
+        flops = 2.0 * workloads.PREFILL_M * lin.N * lin.K
+        wd = torch.randn(lin.N, lin.K, device="cuda", dtype=torch.float16)
+        gc = capture(lambda: torch.matmul(layer["x"], wd.t()), stream)
+        tc = time_graph(gc, stream, 20, 3)
+        tf = flops / t / 1e12
+        out[lin.name] = {"us": round(t * 1e6, 2), "tflops": round(tf, 1),
+                         "frac_of_measured_bf16_peak": round(tf / peaks.get("bf16_tflops", 1900.0), 3),
+                         "cublas_fp16_us": round(tc * 1e6, 2),
+                         "cublas_fp16_tflops": round(flops / tc / 1e12, 1)}
+        del layer, wd, g, gc
     return out
 
 
