@@ -136,9 +136,14 @@ int w4a16_unrepack(const void *repacked, int64_t N, int64_t K, void *qweight, vo
  *   N, K       N >= 1; K >= 128 and K % 128 == 0.
  * Accuracy against the exact result: max|y - y_ref| <= 2e-3 * max|y_ref|
  * and ||y - y_ref||_2 <= 1e-3 * ||y_ref||_2 for the library's test inputs.
- * The call is graph-capturable; launches use programmatic dependent launch,
- * and only L2 prefetches of the weights run before the previous kernel on
- * the stream completes.
+ * The call is graph-capturable and uses programmatic dependent launch.
+ * Weights and scales are read as constants of the call: their first tiles
+ * may be loaded while the kernel enqueued before it on the stream is still
+ * running (x is read and y written only after that kernel completes).  So
+ * the weights and scales must not be written by work that is still pending
+ * on the stream when w4a16_gemm is enqueued -- synchronise (or wait on an
+ * event) after writing them -- except by w4a16_quantize and w4a16_repack,
+ * which make their results visible before they finish.
  * Errors: NULL -> W4A16_ERR_NULL; bad M, N, K -> W4A16_ERR_SHAPE;
  *         misaligned pointer -> W4A16_ERR_ALIGN; launch failure ->
  *         W4A16_ERR_CUDA.

@@ -21,15 +21,17 @@
 //    once by its fp16 scale and added to the FP32 running sum: q * x products
 //    are exact and only FP32 sums round.
 //  * Work split: when there are fewer 128-row blocks than SM slots, the K
-//    range is split over the CTAs of a thread-block cluster (up to 8) whose
-//    FP32 partials are reduced through distributed shared memory in a fixed
-//    order (no global workspace, no atomics).  Otherwise the grid is
+//    range is split over the CTAs of a thread-block cluster (up to 8).  Each
+//    CTA pushes its FP32 partials into the shared memory of the CTA that owns
+//    the row (distributed shared memory), one cluster barrier later the owner
+//    sums them in a fixed order (no global workspace, no atomics).  Otherwise the grid is
 //    persistent: each CTA walks blocks y, y + gridDim.y, ... while the
 //    producer keeps the ring full across block boundaries.
-//  * Programmatic dependent launch: the CTA releases its dependents at once,
-//    prefetches its first weights and scales into L2 (safe before the
-//    dependency wait: L2 is the coherence point), then waits for the
-//    previous kernel before any copy into shared memory or write of y.
+//  * Programmatic dependent launch: the CTA releases its dependents at once
+//    and loads its first ring stages and scale slab -- constants of the call
+//    -- while the previous kernel on the stream is still running; x (which
+//    that kernel may produce) is copied, and y written, only after the
+//    grid-dependency wait.
 // Every wait is bounded (common.cuh); on a time-out the CTA records it in the
 // status word, stops issuing copies, drains those in flight and exits.
 #include <mutex>
@@ -73,6 +75,7 @@ struct GemvArgs {
     int xs_stride;           // bytes between x rows in shared memory
     int slab_bytes;          // bytes of one scale buffer (128 * G * 2, rounded)
     int n_sbuf;              // scale buffers: 2 when a CTA walks several blocks
+    int rpo;                 // rows owned per CTA in the split reduction
     uint32_t off_ring, off_x, off_s, off_red;
 };
 
@@ -85,11 +88,17 @@ __device__ __forceinline__ int split_group_begin(int split, int S, int G) {
 template <int MT>
 __device__ __forceinline__ void mma_group(uint32_t w_addr, uint32_t x0_addr, uint32_t x1_addr,
                                           float s0, float s1, float (&acc)[MT][4]) {
-    float g[MT][4];
+    // M <= 8: one FP32 fragment per chunk -- two independent MMA chains per
+    // group halve the dependent-latency path of a lane (M <= 16 has two
+    // chains already, one per n8 tile, and no registers to spare).
+    constexpr int NCH = MT == 1 ? 2 : 1;
+    float g[NCH][MT][4];
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
+    for (int c = 0; c < NCH; ++c)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) g[mt][e] = 0.0f;
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) g[c][mt][e] = 0.0f;
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
         const uint4 wv = lds128(w_addr + c * kChunkBytes);
@@ -107,16 +116,20 @@ __device__ __forceinline__ void mma_group(uint32_t w_addr, uint32_t x0_addr, uin
         for (int s = 0; s < 4; ++s) {
             uint32_t af[4];
             dequant8(wrd[s], af);
-            mma_16816(g[0], af, b0[2 * s], b0[2 * s + 1], g[0]);
-            if (MT == 2) mma_16816(g[MT - 1], af, b1[2 * s], b1[2 * s + 1], g[MT - 1]);
+            mma_16816(g[c % NCH][0], af, b0[2 * s], b0[2 * s + 1], g[c % NCH][0]);
+            if (MT == 2)
+                mma_16816(g[c % NCH][MT - 1], af, b1[2 * s], b1[2 * s + 1], g[c % NCH][MT - 1]);
         }
     }
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
-        acc[mt][0] = fmaf(s0, g[mt][0], acc[mt][0]);
-        acc[mt][1] = fmaf(s0, g[mt][1], acc[mt][1]);
-        acc[mt][2] = fmaf(s1, g[mt][2], acc[mt][2]);
-        acc[mt][3] = fmaf(s1, g[mt][3], acc[mt][3]);
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = NCH == 2 ? g[0][mt][e] + g[NCH - 1][mt][e] : g[0][mt][e];
+        acc[mt][0] = fmaf(s0, v[0], acc[mt][0]);
+        acc[mt][1] = fmaf(s0, v[1], acc[mt][1]);
+        acc[mt][2] = fmaf(s1, v[2], acc[mt][2]);
+        acc[mt][3] = fmaf(s1, v[3], acc[mt][3]);
     }
 }
 
@@ -172,12 +185,19 @@ __global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2) gemv_kernel(con
                 const uint32_t sb = ((uint32_t)(rows * a.G * 2)) & ~15u;
                 if (sb) bulk_prefetch_l2(a.scales + (size_t)rb * kBlockRows * a.G, sb);
             }
-            grid_dependency_wait();
-            const uint32_t xbytes = (uint32_t)nck * (kChunkK * 2);
-            mbar_arrive_expect_tx(sbase + kBarX, xbytes * a.M);
-            for (int m = 0; m < a.M; ++m)
-                bulk_g2s(sbase + a.off_x + m * a.xs_stride,
-                         a.x + (size_t)m * a.K + (size_t)g0 * kGroup, xbytes, sbase + kBarX);
+            // Weights and scales are constants of the call: the first ring
+            // stages and scale slab load while the previous kernel is still
+            // running.  x (its output, possibly) loads only after the wait.
+            bool x_issued = false;
+            auto issue_x = [&]() {
+                grid_dependency_wait();
+                const uint32_t xbytes = (uint32_t)nck * (kChunkK * 2);
+                mbar_arrive_expect_tx(sbase + kBarX, xbytes * a.M);
+                for (int m = 0; m < a.M; ++m)
+                    bulk_g2s(sbase + a.off_x + m * a.xs_stride,
+                             a.x + (size_t)m * a.K + (size_t)g0 * kGroup, xbytes, sbase + kBarX);
+                x_issued = true;
+            };
             int it = 0;
             bool ok = true;
             int sb_issued = 0;
@@ -208,6 +228,7 @@ __global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2) gemv_kernel(con
                 const uint8_t* w = a.wq + (size_t)rb * block_stride + 2 * (size_t)g0 * kChunkBytes;
                 for (int st = 0; st < nstg; ++st, ++it) {
                     const int slot = it % kStages;
+                    if (it >= kStages && !x_issued) issue_x();
                     if (it >= kStages &&
                         !mbar_wait(sbase + kBarEmpty + 8 * slot, ((it / kStages) - 1) & 1,
                                    a.timeout_ns, a.status)) {
@@ -224,6 +245,7 @@ __global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2) gemv_kernel(con
                                   nc * kChunkBytes, sbase + kBarFull + 8 * slot, pol);
                 }
             }
+            if (!x_issued) issue_x();
             if (!ok) *abort_flag = 1;
             // Drain: every issued copy must land before the CTA may exit.
             mbar_wait(sbase + kBarX, 0, a.timeout_ns, a.status);
@@ -322,16 +344,16 @@ __global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2) gemv_kernel(con
                     }
                 }
             } else {
-                // One block per CTA in split mode: park the partials for the
-                // cluster reduction below.
-                float* red = reinterpret_cast<float*>(smem + a.off_red);  // [128][16]
+                // One block per CTA in split mode: push the partials straight
+                // into the owner of each row (CTA row % S), slot [split][row / S].
+                const uint32_t red = sbase + a.off_red;  // [S][rpo][16] floats
+                const uint32_t d0 = red + (uint32_t)((split * a.rpo + row0 / S) * 64);
+                const uint32_t d1 = red + (uint32_t)((split * a.rpo + row1 / S) * 64);
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt) {
-                    const int m0 = mt * 8 + 2 * t;
-                    red[row0 * 16 + m0] = acc[mt][0];
-                    red[row0 * 16 + m0 + 1] = acc[mt][1];
-                    red[row1 * 16 + m0] = acc[mt][2];
-                    red[row1 * 16 + m0 + 1] = acc[mt][3];
+                    const uint32_t c = (uint32_t)((mt * 8 + 2 * t) * 4);
+                    st_cluster_v2f(map_to_cta(d0 + c, (uint32_t)(row0 % S)), acc[mt][0], acc[mt][1]);
+                    st_cluster_v2f(map_to_cta(d1 + c, (uint32_t)(row1 % S)), acc[mt][2], acc[mt][3]);
                 }
             }
         }
@@ -339,23 +361,23 @@ __global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2) gemv_kernel(con
     }
 
     if (S > 1) {
-        // Fixed-order reduction of the cluster's partials through DSMEM: CTA
-        // `split` finalises rows split, split + S, ... of its block.
+        // One cluster barrier: every CTA has pushed its partials into the
+        // owners' shared memory (release/acquire), and nobody touches a
+        // peer's shared memory afterwards.  CTA `split` then sums, in a
+        // fixed order, the S slices of the rows split, split + S, ...
         cluster_sync_all();
         const int rb = (int)blockIdx.y;
-        const uint32_t red_base = sbase + a.off_red;
+        const float* red = reinterpret_cast<const float*>(smem + a.off_red);
         const int M = a.M;
-        for (int idx = threadIdx.x; idx < kBlockRows * M; idx += kGemvThreads) {
-            const int r = idx / M, m = idx - r * M;
-            if (r % S != split) continue;
-            const int R = rb * kBlockRows + r;
+        const int rows_owned = (kBlockRows - split + S - 1) / S;
+        for (int idx = threadIdx.x; idx < rows_owned * M; idx += kGemvThreads) {
+            const int li = idx / M, m = idx - li * M;
+            const int R = rb * kBlockRows + split + li * S;
             if (R >= a.N) continue;
             float sum = 0.0f;
-            for (int q = 0; q < S; ++q)
-                sum += ld_cluster_f32(map_to_cta(red_base + (uint32_t)(r * 16 + m) * 4, q));
+            for (int q = 0; q < S; ++q) sum += red[(q * a.rpo + li) * 16 + m];
             a.y[(size_t)m * a.N + R] = __float2half_rn(sum);
         }
-        cluster_sync_all();
     }
 }
 
@@ -365,6 +387,7 @@ struct GemvPlan {
     int n_sbuf = 1;
     int xs_stride = 0;
     int slab_bytes = 0;
+    int rpo = 0;
     uint32_t off_ring = 0, off_x = 0, off_s = 0, off_red = 0, smem = 0;
     double eff = 0.0;
 };
@@ -376,6 +399,24 @@ int occupancy(uint32_t smem) {
                                                       smem) != cudaSuccess)
         return 0;
     return blocks;
+}
+
+template <int MT>
+int max_active_clusters(int S, uint32_t smem) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)S, 1, 1);
+    cfg.blockDim = dim3(kGemvThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = (unsigned)S;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemv_kernel<MT>, &cfg) != cudaSuccess) return 0;
+    return n;
 }
 
 template <int MT>
@@ -402,7 +443,8 @@ bool layout(GemvPlan& p, int M, int G, int S, int nsb, const DeviceCtx& ctx) {
     p.off_x = p.off_ring + kStages * kStageBytes;
     p.off_s = p.off_x + ((M * p.xs_stride + 127) / 128) * 128;
     p.off_red = p.off_s + nsb * p.slab_bytes;
-    p.smem = p.off_red + (S > 1 ? kBlockRows * 16 * 4 : 0);
+    p.rpo = (kBlockRows + S - 1) / S;
+    p.smem = p.off_red + (S > 1 ? S * p.rpo * 16 * 4 : 0);
     return (int)p.smem <= ctx.max_smem_optin;
 }
 
@@ -435,7 +477,9 @@ GemvPlan plan_gemv(int M, int N, int K, const DeviceCtx& ctx) {
         const int occ = occupancy<MT>(p.smem);
         if (occ == 0) continue;
         const long long units = (long long)NB * S;
-        const long long slots = (long long)ctx.num_sms * occ;
+        // Clusters live inside one GPC: count co-resident clusters, not SM slots.
+        const long long slots =
+            S == 1 ? (long long)ctx.num_sms * occ : (long long)max_active_clusters<MT>(S, p.smem) * S;
         const long long heaviest = (units + ctx.num_sms - 1) / ctx.num_sms;
         double eff = per_sm / ((double)heaviest / S);
         if (units > slots) eff *= 0.85;  // more than one wave of CTAs
@@ -485,6 +529,7 @@ cudaError_t launch_gemv_mt(GemvArgs args, int M, cudaStream_t stream, const Devi
     args.off_x = p.off_x;
     args.off_s = p.off_s;
     args.off_red = p.off_red;
+    args.rpo = p.rpo;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.S, (unsigned)p.grid_y, 1);
     cfg.blockDim = dim3(kGemvThreads, 1, 1);

@@ -58,6 +58,10 @@ __global__ void __launch_bounds__(kQuantThreads)
         qweight[grp * 16 + lane16] = packed;
         if (lane16 == 0) scales[grp] = __float2half_rn(s);
     }
+    // Publish the packed weights and scales device-wide before this block
+    // ends: a GEMM launched next on the stream may read them before the
+    // grid-completion flush (it treats them as constants).
+    __threadfence();
 }
 
 }  // namespace

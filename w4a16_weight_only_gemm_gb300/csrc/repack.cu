@@ -77,6 +77,9 @@ __global__ void __launch_bounds__(kRepackThreads)
         w.w = interleave_word(a.y >> 16, b.y >> 16);
         out[o] = w;
     }
+    // Publish before the block ends: the GEMM that reads these weights may
+    // start before the grid-completion flush (see w4a16_gemm).
+    __threadfence();
 }
 
 __global__ void __launch_bounds__(kRepackThreads)
