@@ -76,7 +76,7 @@ struct GemvArgs {
     int slab_bytes;          // bytes of one scale buffer (128 * G * 2, rounded)
     int n_sbuf;              // scale buffers: 2 when a CTA walks several blocks
     int rpo;                 // rows owned per CTA in the split reduction
-    uint32_t off_ring, off_x, off_s, off_red;
+    uint32_t off_ring, off_x, off_s, off_red, off_sx;
 };
 
 __device__ __forceinline__ int split_group_begin(int split, int S, int G) {
@@ -87,7 +87,8 @@ __device__ __forceinline__ int split_group_begin(int split, int S, int G) {
 // FP32 fragment, then scaled into acc.
 template <int MT>
 __device__ __forceinline__ void mma_group(uint32_t w_addr, uint32_t x0_addr, uint32_t x1_addr,
-                                          float s0, float s1, float (&acc)[MT][4]) {
+                                          uint32_t sx_addr, float s0, float s1,
+                                          float (&acc)[MT][4]) {
     // M <= 8: one FP32 fragment per chunk -- two independent MMA chains per
     // group halve the dependent-latency path of a lane (M <= 16 has two
     // chains already, one per n8 tile, and no registers to spare).
@@ -115,7 +116,7 @@ __device__ __forceinline__ void mma_group(uint32_t w_addr, uint32_t x0_addr, uin
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
             uint32_t af[4];
-            dequant8(wrd[s], af);
+            dequant8_bias72(wrd[s], af);
             mma_16816(g[c % NCH][0], af, b0[2 * s], b0[2 * s + 1], g[c % NCH][0]);
             if (MT == 2)
                 mma_16816(g[c % NCH][MT - 1], af, b1[2 * s], b1[2 * s + 1], g[c % NCH][MT - 1]);
@@ -126,10 +127,13 @@ __device__ __forceinline__ void mma_group(uint32_t w_addr, uint32_t x0_addr, uin
         float v[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) v[e] = NCH == 2 ? g[0][mt][e] + g[NCH - 1][mt][e] : g[0][mt][e];
+        // rows r1 carry 72 * sum_k x[m, k] over the group (dequant8_bias72)
+        const float2 sx = lds64f(sx_addr + mt * 32);
+        const float c1 = -72.0f * s1;
         acc[mt][0] = fmaf(s0, v[0], acc[mt][0]);
         acc[mt][1] = fmaf(s0, v[1], acc[mt][1]);
-        acc[mt][2] = fmaf(s1, v[2], acc[mt][2]);
-        acc[mt][3] = fmaf(s1, v[3], acc[mt][3]);
+        acc[mt][2] = fmaf(c1, sx.x, fmaf(s1, v[2], acc[mt][2]));
+        acc[mt][3] = fmaf(c1, sx.y, fmaf(s1, v[3], acc[mt][3]));
     }
 }
 
@@ -273,6 +277,37 @@ __global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2) gemv_kernel(con
         const bool tail = (nck % kChunksPerStage) != 0;  // one group left
 
         bool ok = mbar_wait(sbase + kBarX, 0, a.timeout_ns, a.status);
+        // Activation sums per group and row, Sx[gl][m] in FP32, for the bias
+        // correction of dequant8_bias72: 8 threads per (group, row), 16
+        // values each, combined with xor-shuffles in a fixed order.
+        {
+            float* sxw = reinterpret_cast<float*>(smem + a.off_sx);
+            const int total = ng * a.M * 8;
+            for (int base = 0; base < total; base += kConsumers) {
+                const int task = base + (int)threadIdx.x;
+                const int e = task >> 3, gl = e / a.M, m = e - gl * a.M;
+                float sum = 0.0f;
+                if (ok && task < total) {
+                    const uint32_t src = sbase + a.off_x + m * a.xs_stride + gl * 256 + (task & 7) * 32;
+                    const uint4 p[2] = {lds128(src), lds128(src + 16)};
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t wv[4] = {p[h].x, p[h].y, p[h].z, p[h].w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[i]));
+                            sum += f.x + f.y;
+                        }
+                    }
+                }
+                sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+                sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+                sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+                if (task < total && (task & 7) == 0) sxw[gl * 16 + m] = sum;
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+        }
+        const uint32_t sxl = sbase + a.off_sx + t * 8;  // this lane's columns 2t, 2t + 1
         int it = 0;
         for (int j = 0; ok && j < nblk; ++j) {
             const int rb = (int)blockIdx.y + j * (int)gridDim.y;
@@ -304,7 +339,7 @@ __global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2) gemv_kernel(con
                 for (int gi = 0; gi < kGroupsPerStage; ++gi) {
                     const int gl = st * kGroupsPerStage + gi;
                     mma_group<MT>(wa + gi * 2 * kChunkBytes, x0 + xs_off + gi * 256,
-                                  x1 + xs_off + gi * 256, __half2float(sc0[gl]),
+                                  x1 + xs_off + gi * 256, sxl + gl * 64, __half2float(sc0[gl]),
                                   __half2float(sc1[gl]), acc);
                 }
                 __syncwarp();
@@ -317,7 +352,7 @@ __global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2) gemv_kernel(con
                     ok = false;
                 } else {
                     const int gl = nfull * kGroupsPerStage;
-                    mma_group<MT>(wl + slot * kStageBytes, x0 + xs_off, x1 + xs_off,
+                    mma_group<MT>(wl + slot * kStageBytes, x0 + xs_off, x1 + xs_off, sxl + gl * 64,
                                   __half2float(sc0[gl]), __half2float(sc1[gl]), acc);
                     __syncwarp();
                     if (lane == 0) mbar_arrive(sbase + kBarEmpty + 8 * slot);
@@ -388,7 +423,7 @@ struct GemvPlan {
     int xs_stride = 0;
     int slab_bytes = 0;
     int rpo = 0;
-    uint32_t off_ring = 0, off_x = 0, off_s = 0, off_red = 0, smem = 0;
+    uint32_t off_ring = 0, off_x = 0, off_s = 0, off_red = 0, off_sx = 0, smem = 0;
     double eff = 0.0;
 };
 
@@ -444,7 +479,8 @@ bool layout(GemvPlan& p, int M, int G, int S, int nsb, const DeviceCtx& ctx) {
     p.off_s = p.off_x + ((M * p.xs_stride + 127) / 128) * 128;
     p.off_red = p.off_s + nsb * p.slab_bytes;
     p.rpo = (kBlockRows + S - 1) / S;
-    p.smem = p.off_red + (S > 1 ? S * p.rpo * 16 * 4 : 0);
+    p.off_sx = p.off_red + (S > 1 ? S * p.rpo * 16 * 4 : 0);
+    p.smem = p.off_sx + ng_max * 16 * 4;
     return (int)p.smem <= ctx.max_smem_optin;
 }
 
@@ -529,6 +565,7 @@ cudaError_t launch_gemv_mt(GemvArgs args, int M, cudaStream_t stream, const Devi
     args.off_x = p.off_x;
     args.off_s = p.off_s;
     args.off_red = p.off_red;
+    args.off_sx = p.off_sx;
     args.rpo = p.rpo;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.S, (unsigned)p.grid_y, 1);
