@@ -55,6 +55,10 @@ def parse_args():
                    help="headline step only (no per-shape, stack, sweep, quantizer sections)")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="budget of the CPU oracle baseline sample")
+    p.add_argument("--section", choices=("prefill", "quantizer", "stack", "per_shape"),
+                   default=None,
+                   help="run one section alone and print its JSON (profiling aid; not the "
+                        "benchmark line)")
     return p.parse_args()
 
 
@@ -533,6 +537,14 @@ def run_reference(args, rank, world):
 
 def main():
     args = parse_args()
+    if args.section is not None:
+        from w4a16_weight_only_gemm_gb300 import build
+        build.build()
+        run = {"prefill": prefill, "quantizer": quantizer_throughput, "stack": stack_8b,
+               "per_shape": lambda: {lin.name: per_shape_us(lin, "llama3_8b_decode", i)
+                                     for i, lin in enumerate(workloads.LLAMA3_8B)}}
+        print(json.dumps({"section": args.section, "result": run[args.section]()}), flush=True)
+        return
     if args.impl == "reference":
         # Only rank 0 times the CPU oracle; other ranks exit without work.
         rank = int(os.environ.get("RANK", "0"))

@@ -61,6 +61,48 @@ def test_random_fp16_bit_patterns(w4lib):
     _check(bits)
 
 
+def _all_below(amax: float) -> np.ndarray:
+    """Every finite fp16 bit pattern with |value| <= amax, in groups of 127
+    that each get amax itself as element 0 (so every group has that scale)."""
+    vals = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = vals[(vals & 0x7C00) != 0x7C00]                      # finite patterns only
+    vals = vals[np.abs(vals.view(np.float16).astype(np.float64)) <= amax]
+    pad = (-len(vals)) % 127
+    vals = np.concatenate([vals, np.zeros(pad, np.uint16)]).reshape(-1, 127)
+    head = np.full((vals.shape[0], 1), np.float16(amax).view(np.uint16), np.uint16)
+    return np.concatenate([head, vals], axis=1)
+
+
+# 0.2002, 0.024566650390625 and 3.14453125 are scales at which rounding
+# w * fl(1 / s) instead of fl(w / s) changes some codes (found by scanning
+# fp16 absmax values on the CPU); the others are plain and boundary scales.
+@pytest.mark.parametrize("amax", [1.0, 0.0123, 3.7, 0.2002, 0.024566650390625, 3.14453125,
+                                  65504.0, 2.0 ** -14, 7.0 * 2.0 ** -10])
+def test_every_fp16_value_per_scale(w4lib, amax):
+    """Each rounding decision w / s for all fp16 w of one scale: exact ties
+    and values a few ulps either side of a half-integer included."""
+    groups = _all_below(amax)
+    K = 128 * 8
+    rows = -(-groups.shape[0] // 8)
+    full = np.zeros((rows * 8, 128), np.uint16)
+    full[: groups.shape[0]] = groups
+    _check(full.reshape(rows, K))
+
+
+def test_every_fp16_absmax(w4lib):
+    """One group per finite fp16 absmax a (both signs of it), the other 127
+    weights spread over [-a, a]: every scale RN(a / 7) the quantizer can
+    produce, and codes at each of those scales."""
+    bits = np.arange(0x7C00, dtype=np.uint32).astype(np.uint16)
+    a = bits.view(np.float16).astype(np.float64)
+    frac = np.linspace(-1.0, 1.0, 127)
+    body = (a[:, None] * frac[None, :]).astype(np.float16).view(np.uint16)
+    sign = np.where(np.arange(len(bits)) % 2 == 1, 0x8000, 0).astype(np.uint16)
+    groups = np.concatenate([(bits | sign)[:, None], body], axis=1)
+    groups = groups[: len(groups) // 8 * 8]
+    _check(groups.reshape(-1, 128 * 8))
+
+
 @pytest.mark.parametrize("N,K", [(14336, 4096), (128256, 4096), (4096, 14336)])
 def test_full_size(w4lib, N, K):
     """The quantizer workload [14336, 4096] plus the largest decode shapes."""

@@ -7,23 +7,26 @@
 // prompt pass).  Unlike decode, the prompt pass is a dense contraction, so it
 // runs on the tensor cores:
 //
-// One thread block computes a 128 (weight rows = MMA M) x 128 (activation
-// rows = MMA N) tile of y^T with FP32 accumulators in tensor memory.
+// One thread block computes a 128 (activation rows = MMA M) x 128 (weight
+// rows = MMA N) tile of y with FP32 accumulators in tensor memory.
 //  * warp 0 (one thread): TMA producer.  Per 64-wide k-block it loads the x
-//    tile [128 x 64] fp16 with a 2-D tensor-map copy in the 128-byte swizzled
-//    K-major layout and the block's 4 KB of packed weights with a bulk copy,
-//    both completing on one mbarrier; the 128-row scale slab arrives once.
-//  * warps 4-7 (128 threads): dequantise the packed chunk in registers (lop3
-//    magic-number expansion, exact q), multiply by the fp16 group scale
-//    (one RNE rounding, as the tutorial's dequantizer), and store the fp16
-//    A tile [128 x 64] into shared memory in the same 128-byte swizzled
-//    K-major layout; then fence the generic->async proxy and arrive.
+//    tile [128 x 64] fp16 (operand A) with a 2-D tensor-map copy in the
+//    128-byte swizzled K-major layout and the block's 4 KB of packed weights
+//    with a bulk copy, both completing on one mbarrier; the 128-row scale
+//    slab arrives once.
+//  * warps 4-19, two sets of 8 taking alternate k-blocks (one 16-byte lane
+//    chunk of packed weights per thread): dequantise in registers (lop3
+//    magic-number expansion, exact q), multiply by the fp16 group scale (one
+//    RNE rounding, as the tutorial's dequantizer) and store the fp16 weight
+//    tile [128 x 64] (operand B) in the same 128-byte swizzled K-major
+//    layout; then fence the generic->async proxy and arrive.
 //  * warp 1 (one thread): issues 4 tcgen05.mma (M=128, N=128, K=16) per
-//    k-block reading A and x from shared memory through matrix descriptors,
-//    and commits to the stage's mbarrier, which frees the stage for both
-//    the producer and the dequantisers.  A last commit releases the epilogue.
-//  * warps 4-7 then read the accumulators with tcgen05.ld (warp w owns TMEM
-//    lanes 32 (w % 4) ..+31 = weight rows), round to fp16 and store y.
+//    k-block from the shared-memory matrix descriptors and commits to the
+//    stage's mbarrier, which frees the stage for the producer and the
+//    dequantisers.  A last commit releases the epilogue.
+//  * epilogue, warps 4-19: warp w reads TMEM lanes 32 (w % 4) .. +31 (rows
+//    of y) and 32 accumulator columns (weight rows) with tcgen05.ld, rounds
+//    to fp16 and writes 64 contiguous bytes of a y row per thread.
 // Every wait is bounded; tensor memory is freed on every path.
 #include <cudaTypedefs.h>
 
@@ -36,27 +39,28 @@
 namespace w4a16 {
 namespace {
 
-constexpr int kTcThreads = 256;
-constexpr int kTileW = kBlockRows;              // weight rows per tile (MMA M)
-constexpr int kTileX = 128;                     // activation rows per tile (MMA N)
+constexpr int kTcThreads = 640;                 // 20 warps
+constexpr int kDequantWarps = 16;               // warps 4 .. 19, two sets of 8
+constexpr int kTileW = kBlockRows;              // weight rows per tile (MMA N)
+constexpr int kTileX = 128;                     // activation rows per tile (MMA M)
 constexpr int kBK = kChunkK;                    // 64: one kernel-layout chunk
-constexpr int kTcStages = 4;
+constexpr int kStages = 4;                      // ring: x tile, packed and dequantised weights
 constexpr int kAStageBytes = kTileW * kBK * 2;  // 16 KB fp16, 128B-swizzled
 constexpr int kXStageBytes = kTileX * kBK * 2;  // 16 KB
 constexpr int kWStageBytes = kTileW * kBK / 2;  // 4 KB packed
-constexpr uint32_t kTmemCols = kTileX;          // fp32 accumulator columns
+constexpr uint32_t kTmemCols = kTileW;          // fp32 accumulator columns
 
-constexpr int kBarLoadFull = 0;
-constexpr int kBarAFull = kBarLoadFull + 8 * kTcStages;
-constexpr int kBarMmaDone = kBarAFull + 8 * kTcStages;
-constexpr int kBarAcc = kBarMmaDone + 8 * kTcStages;
+constexpr int kBarLoadFull = 0;                      // [stages] x + packed weights landed
+constexpr int kBarAFull = kBarLoadFull + 8 * kStages;  // [stages] dequantised tile written
+constexpr int kBarFree = kBarAFull + 8 * kStages;      // [stages] MMAs done: stage reusable
+constexpr int kBarAcc = kBarFree + 8 * kStages;
 constexpr int kBarSlab = kBarAcc + 8;
 constexpr int kTmemSlot = kBarSlab + 8;
 constexpr int kAbortFlag = kTmemSlot + 8;
-constexpr int kOffA = 1024;
-constexpr int kOffX = kOffA + kTcStages * kAStageBytes;
-constexpr int kOffW = kOffX + kTcStages * kXStageBytes;
-constexpr int kOffSlab = kOffW + kTcStages * kWStageBytes;
+constexpr int kOffA = 1024;                              // dequantised tiles
+constexpr int kOffX = kOffA + kStages * kAStageBytes;    // x tiles
+constexpr int kOffW = kOffX + kStages * kXStageBytes;    // packed weights
+constexpr int kOffSlab = kOffW + kStages * kWStageBytes; // scale slab
 
 struct TcArgs {
     const uint8_t* wq;
@@ -101,10 +105,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int nkb = a.K / kBK;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kTcStages; ++s) {
+        for (int s = 0; s < kStages; ++s) {
             mbar_init(base + kBarLoadFull + 8 * s, 1);
-            mbar_init(base + kBarAFull + 8 * s, 128);
-            mbar_init(base + kBarMmaDone + 8 * s, 1);
+            mbar_init(base + kBarAFull + 8 * s, kDequantWarps / 2 * 32);
+            mbar_init(base + kBarFree + 8 * s, 1);
         }
         mbar_init(base + kBarAcc, 1);
         mbar_init(base + kBarSlab, 1);
@@ -126,7 +130,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
             tma_prefetch_map(&xmap);
             const uint8_t* w = a.wq + (size_t)rb * nkb * kWStageBytes;
-            for (int i = 0; i < kTcStages && i < nkb; ++i)
+            for (int i = 0; i < kStages && i < nkb; ++i)
                 bulk_prefetch_l2(w + (size_t)i * kWStageBytes, kWStageBytes);
             grid_dependency_wait();
             {   // the block's scale slab (rows x G fp16, contiguous)
@@ -141,10 +145,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             int issued = 0;
             bool ok = true;
-            for (int i = 0; i < nkb; ++i) {
-                const int s = i % kTcStages;
-                if (i >= kTcStages &&
-                    !mbar_wait(base + kBarMmaDone + 8 * s, ((i / kTcStages) - 1) & 1, a.timeout_ns,
+            for (int i = 0, ts = 0, round = 0; i < nkb; ++i) {
+                if (i >= kStages &&
+                    !mbar_wait(base + kBarFree + 8 * ts, (round - 1) & 1, a.timeout_ns,
                                a.status)) {
                     ok = false;
                     break;
@@ -153,41 +156,48 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(base + kBarLoadFull + 8 * s, kXStageBytes + kWStageBytes);
-                tma_load_2d(base + kOffX + s * kXStageBytes, &xmap, i * kBK, m0,
-                            base + kBarLoadFull + 8 * s);
-                bulk_g2s(base + kOffW + s * kWStageBytes, w + (size_t)i * kWStageBytes,
-                         kWStageBytes, base + kBarLoadFull + 8 * s);
+                mbar_arrive_expect_tx(base + kBarLoadFull + 8 * ts, kXStageBytes + kWStageBytes);
+                tma_load_2d(base + kOffX + ts * kXStageBytes, &xmap, i * kBK, m0,
+                            base + kBarLoadFull + 8 * ts);
+                bulk_g2s(base + kOffW + ts * kWStageBytes, w + (size_t)i * kWStageBytes,
+                         kWStageBytes, base + kBarLoadFull + 8 * ts);
                 issued = i + 1;
+                if (++ts == kStages) {
+                    ts = 0;
+                    ++round;
+                }
             }
             if (!ok) *abort_flag = 1;
             // Drain the copies in flight before the block may exit.
             mbar_wait(base + kBarSlab, 0, a.timeout_ns, a.status);
-            for (int i = (issued > kTcStages ? issued - kTcStages : 0); i < issued; ++i)
-                mbar_wait(base + kBarLoadFull + 8 * (i % kTcStages), (i / kTcStages) & 1,
-                          a.timeout_ns, a.status);
+            for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
+                mbar_wait(base + kBarLoadFull + 8 * (i % kStages), (i / kStages) & 1, a.timeout_ns,
+                          a.status);
         }
         __syncwarp();
     } else if (warp == 1) {
         // ============================= MMA issuer =============================
         if (lane == 0) {
-            const uint32_t idesc = umma_idesc_f16_f32(kTileW, kTileX);
+            const uint32_t idesc = umma_idesc_f16_f32(kTileX, kTileW);
             bool ok = true;
-            for (int i = 0; i < nkb; ++i) {
-                const int s = i % kTcStages;
-                if (!mbar_wait(base + kBarAFull + 8 * s, (i / kTcStages) & 1, a.timeout_ns,
-                               a.status)) {
+            for (int i = 0, ts = 0, tr = 0; i < nkb; ++i) {
+                // the dequantisers waited for the stage's copies: A full implies x landed
+                if (!mbar_wait(base + kBarAFull + 8 * ts, tr & 1, a.timeout_ns, a.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t aa = base + kOffA + s * kAStageBytes;
-                const uint32_t xa = base + kOffX + s * kXStageBytes;
+                const uint32_t xa = base + kOffX + ts * kXStageBytes;
+                const uint32_t wa = base + kOffA + ts * kAStageBytes;
 #pragma unroll
-                for (int j = 0; j < kBK / 16; ++j)
-                    tc_mma_f16(tmem, umma_desc_sw128(aa + 32 * j), umma_desc_sw128(xa + 32 * j),
+                for (int j = 0; j < kBK / 16; ++j)  // A = x rows, B = weight rows
+                    tc_mma_f16(tmem, umma_desc_sw128(xa + 32 * j), umma_desc_sw128(wa + 32 * j),
                                idesc, (i | j) != 0);
-                tc_commit(base + kBarMmaDone + 8 * s);
+                tc_commit(base + kBarFree + 8 * ts);  // stage reusable once these MMAs finish
+                if (++ts == kStages) {
+                    ts = 0;
+                    ++tr;
+                }
             }
             tc_commit(base + kBarAcc);  // completes once every issued MMA has
             if (!ok) *abort_flag = 1;
@@ -196,65 +206,75 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else if (warp >= 4) {
         // ===================== dequantisers, then epilogue ====================
         grid_dependency_wait();
-        const int wq = warp - 4;  // 0..3; also the TMEM lane quarter of this warp
+        const int dw = (warp - 4) & 7;    // tile (16 weight rows) of this warp
+        const int set = (warp - 4) >> 3;  // k-blocks set, set + 2, ...
         const int g = lane >> 2, tq = lane & 3;
+        const int r0 = dw * 16 + g, r1 = r0 + 8;
         const __half* slab = reinterpret_cast<const __half*>(smem + kOffSlab);
         bool ok = mbar_wait(base + kBarSlab, 0, a.timeout_ns, a.status);
-        for (int i = 0; ok && i < nkb; ++i) {
-            const int s = i % kTcStages;
-            if (!mbar_wait(base + kBarLoadFull + 8 * s, (i / kTcStages) & 1, a.timeout_ns,
+        for (int i = set; ok && i < nkb; i += 2) {
+            // The stage's copies were issued after its previous MMAs finished,
+            // so their arrival also means the dequantised slot is free.
+            const int ts = i % kStages;
+            if (!mbar_wait(base + kBarLoadFull + 8 * ts, (i / kStages) & 1, a.timeout_ns,
                            a.status)) {
                 ok = false;
                 break;
             }
             const int grp = i >> 1;  // two 64-wide k-blocks per scale group
-            const uint32_t wst = base + kOffW + s * kWStageBytes;
-            const uint32_t ast = base + kOffA + s * kAStageBytes;
+            const uint32_t wst = base + kOffW + ts * kWStageBytes;
+            const uint32_t ast = base + kOffA + ts * kAStageBytes;
+            const uint4 pk = lds128(wst + (dw * 32 + lane) * 16);
+            const __half2 s0 = __half2half2(slab[r0 * a.G + grp]);
+            const __half2 s1 = __half2half2(slab[r1 * a.G + grp]);
+            const uint32_t wrd[4] = {pk.x, pk.y, pk.z, pk.w};
+            uint32_t o0[8], o1[8];  // rows r0 / r1, k = 16 tq .. 16 tq + 15
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int tile = wq + 4 * h;
-                const int r0 = tile * 16 + g, r1 = r0 + 8;
-                const uint4 pk = lds128(wst + (tile * 32 + lane) * 16);
-                const __half2 s0 = __half2half2(slab[r0 * a.G + grp]);
-                const __half2 s1 = __half2half2(slab[r1 * a.G + grp]);
-                const uint32_t wrd[4] = {pk.x, pk.y, pk.z, pk.w};
-                uint32_t o0[8], o1[8];  // rows r0 / r1, k = 16 tq .. 16 tq + 15
-#pragma unroll
-                for (int ws = 0; ws < 4; ++ws) {
-                    uint32_t af[4];
-                    dequant8(wrd[ws], af);
-                    o0[2 * ws] = hmul2_u32(af[0], s0);
-                    o0[2 * ws + 1] = hmul2_u32(af[2], s0);
-                    o1[2 * ws] = hmul2_u32(af[1], s1);
-                    o1[2 * ws + 1] = hmul2_u32(af[3], s1);
-                }
-                sts128(ast + swz128(r0, 2 * tq), o0[0], o0[1], o0[2], o0[3]);
-                sts128(ast + swz128(r0, 2 * tq + 1), o0[4], o0[5], o0[6], o0[7]);
-                sts128(ast + swz128(r1, 2 * tq), o1[0], o1[1], o1[2], o1[3]);
-                sts128(ast + swz128(r1, 2 * tq + 1), o1[4], o1[5], o1[6], o1[7]);
+            for (int ws = 0; ws < 4; ++ws) {
+                uint32_t af[4];
+                dequant8(wrd[ws], af);
+                o0[2 * ws] = hmul2_u32(af[0], s0);
+                o0[2 * ws + 1] = hmul2_u32(af[2], s0);
+                o1[2 * ws] = hmul2_u32(af[1], s1);
+                o1[2 * ws + 1] = hmul2_u32(af[3], s1);
             }
+            sts128(ast + swz128(r0, 2 * tq), o0[0], o0[1], o0[2], o0[3]);
+            sts128(ast + swz128(r0, 2 * tq + 1), o0[4], o0[5], o0[6], o0[7]);
+            sts128(ast + swz128(r1, 2 * tq), o1[0], o1[1], o1[2], o1[3]);
+            sts128(ast + swz128(r1, 2 * tq + 1), o1[4], o1[5], o1[6], o1[7]);
             fence_proxy_async_smem();  // generic stores -> visible to the tensor core
-            mbar_arrive(base + kBarAFull + 8 * s);
+            mbar_arrive(base + kBarAFull + 8 * ts);
         }
         if (!ok) *abort_flag = 1;
 
         // ------------------------------ epilogue ------------------------------
         if (mbar_wait(base + kBarAcc, 0, a.timeout_ns, a.status)) {
             tc_fence_after_sync();
-            const int row = wq * 32 + lane;  // TMEM lane = weight row in the block
-            const int n = rb * kTileW + row;
-            const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
-#pragma unroll 1
-            for (int cc = 0; cc < kTileX / 32; ++cc) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(lane_addr + cc * 32, v);
-                tmem_ld_wait();
-                if (n < a.N) {
+            const int q = warp & 3;           // TMEM lane quarter = rows of y
+            const int cc = (warp - 4) >> 2;   // 32-column chunk = weight rows
+            const int m = m0 + q * 32 + lane;
+            const int n = rb * kTileW + cc * 32;
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(cc * 32), v);
+            tmem_ld_wait();
+            if (m < a.M) {
+                __half* yrow = a.y + (size_t)m * a.N;
+                if (n + 32 <= a.N && (a.N & 7) == 0) {
+                    uint32_t h[16];
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        const int m = m0 + cc * 32 + c;
-                        if (m < a.M) a.y[(size_t)m * a.N + n] = __float2half_rn(__uint_as_float(v[c]));
+                    for (int c = 0; c < 16; ++c) {
+                        __half2 p = __floats2half2_rn(__uint_as_float(v[2 * c]),
+                                                      __uint_as_float(v[2 * c + 1]));
+                        h[c] = *reinterpret_cast<uint32_t*>(&p);
                     }
+                    uint4* dst = reinterpret_cast<uint4*>(yrow + n);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        dst[c] = make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        if (n + c < a.N) yrow[n + c] = __float2half_rn(__uint_as_float(v[c]));
                 }
             }
         }
@@ -288,6 +308,7 @@ cudaError_t launch_gemm_tc(const void* x, const void* repacked, const void* scal
                            int64_t M, int64_t N, int64_t K, cudaStream_t stream,
                            const DeviceCtx& ctx) {
     const int G = (int)(K / kGroup);
+    // +1 KB: slack for aligning the window to 1024 bytes
     const uint32_t smem = kOffSlab + ((kTileW * G * 2 + 127) / 128) * 128 + 1024;
     if ((int)smem > ctx.max_smem_optin) return cudaErrorInvalidValue;
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();

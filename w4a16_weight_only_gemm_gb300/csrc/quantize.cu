@@ -4,14 +4,17 @@
 // "LLM quantization from IEEE 754 to GPTQ/AWQ/GGUF", chapter "量化的数学基石",
 // §2 symmetric formula and §3 per_group_symmetric_quantize):
 //   s32 = max(max|w| / 7, 1e-8) in binary32 with a correctly rounded divide,
-//   q   = clamp(round_half_even(w / s32), -8, 7),
+//   q   = clamp(round_half_even(fl(w / s32)), -8, 7)  (fl: IEEE division),
 //   scale = fp16(s32) rounded to nearest even, byte = (q_odd+8)<<4 | (q_even+8).
 //
 // One half-warp per group: each of the 16 lanes loads 8 fp16 values with a
 // single 16-byte load, the absmax is reduced with xor-shuffles inside the
 // half-warp, and each lane writes its 4 packed bytes (the group's 64 bytes
-// are one coalesced segment).  HBM-bound: 256 B read and 66 B written per
-// group.
+// are one coalesced segment).  Each half-warp issues the loads of four
+// groups before quantizing them, and the grid is one resident wave.  256 B
+// are read and 66 B written per group; the per-element work is four
+// floating-point instructions (fma-rounding, its residual, the tie test),
+// which keeps the issue rate near the HBM rate.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -19,44 +22,111 @@ namespace w4a16 {
 namespace {
 
 constexpr int kQuantThreads = 256;
+constexpr int kQuantUnroll = 4;  // groups per half-warp per iteration, loads issued together
+
+// s32 = RN(a / 7) for an fp16 absmax a, by Markstein's theorem on FMA
+// division (P. Markstein, IBM J. Res. Dev. 34(1), 1990): with y = RN(1/7)
+// and q = RN(a * y) within an ulp of a / 7, the residual a - 7q is exact and
+// RN(q + (a - 7q) y) = RN(a / 7).  a is never subnormal in binary32 here; the
+// identity was also checked for every finite fp16 a against IEEE division.
+__device__ __forceinline__ float div7_rn(float a) {
+    constexpr float y = 1.0f / 7.0f;
+    const float q = __fmul_rn(a, y);
+    const float r = __fmaf_rn(-q, 7.0f, a);
+    return __fmaf_rn(r, y, q);
+}
+
+// 1/s to within 2^-23 relative: hardware approximation plus one
+// Newton-Raphson step (e = 1 - s y0, y = y0 + y0 e).  s >= 1e-8 is normal.
+__device__ __forceinline__ float rcp_nr(float s) {
+    float y0;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y0) : "f"(s));
+    return __fmaf_rn(y0, __fmaf_rn(-s, y0, 1.0f), y0);
+}
+
+// Adding kRound = 1.5 * 2^23 + 8 to a binary32 |r| < 8 rounds r to the
+// nearest integer, ties to even (kRound is even and the sum's ulp is 1), and
+// leaves q + 8 in the low 4 bits of the sum.
+constexpr float kRound = 12582920.0f;
+
+// Quantizes one group held as 8 fp16 values per lane of a half-warp.
+//
+// q = round_half_even(fl(w / s)) is formed from the exact product w * y of
+// the refined reciprocal, rounded by the fma with kRound: |w y - w / s| <=
+// 7 * 2^-23 and |fl(w / s) - w / s| <= 7 * 2^-24, so the two sit within
+// 1.3e-6 of each other and round to the same integer unless the product's
+// distance to its integer exceeds 1/2 - 1e-5.  When any lane of the warp
+// sees that (exact ties included) the warp takes the correctly rounded
+// divide for all its elements.  No clamp is needed: s >= (max|w| / 7)(1 -
+// 2^-24) bounds |w / s| below 7.5, so q already lies in [-7, 7].
+__device__ __forceinline__ void quantize_group(const uint4 raw, uint32_t& packed, float& scale) {
+    const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+    __half2 m2 = __habs2(h2[0]);
+#pragma unroll
+    for (int i = 1; i < 4; ++i) m2 = __hmax2(m2, __habs2(h2[i]));
+    float amax = fmaxf(__low2float(m2), __high2float(m2));
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1)
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+
+    float s = div7_rn(amax);
+    if (s < 1e-8f) s = 1e-8f;
+    const float y = rcp_nr(s);
+
+    float w[8], t[8];
+    float dmax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __half22float2(h2[i]);
+        w[2 * i] = f.x;
+        w[2 * i + 1] = f.y;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        t[i] = __fmaf_rn(w[i], y, kRound);
+        const float d = __fmaf_rn(w[i], y, -__fsub_rn(t[i], kRound));  // w y - q
+        dmax = fmaxf(dmax, fabsf(d));
+    }
+    if (__any_sync(0xffffffffu, dmax > 0.5f - 1.0e-5f)) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t[i] = __fadd_rn(__fdiv_rn(w[i], s), kRound);
+    }
+    packed = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) packed |= (__float_as_uint(t[i]) & 0xFu) << (4 * i);
+    scale = s;
+}
 
 __global__ void __launch_bounds__(kQuantThreads)
     quantize_kernel(const uint4* __restrict__ W, int64_t groups_total,
                     uint32_t* __restrict__ qweight, __half* __restrict__ scales) {
     const int lane16 = threadIdx.x & 15;
-    const int64_t step = (int64_t)gridDim.x * (kQuantThreads / 16);
-    for (int64_t grp = (int64_t)blockIdx.x * (kQuantThreads / 16) + (threadIdx.x >> 4);
-         grp < groups_total; grp += step) {
-        // group `grp` = row grp / G, group grp % G; its 128 halves are
-        // contiguous at element offset grp * 128 of the row-major matrix.
-        const uint4 raw = __ldg(W + grp * 16 + lane16);
-        const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
-        float w[8];
+    const int64_t stride = (int64_t)gridDim.x * (kQuantThreads / 16);
+    // group `grp` = row grp / G, group grp % G; its 128 halves are contiguous
+    // at element offset grp * 128 of the row-major matrix.  The two
+    // half-warps of a warp differ only in bit 0 of g0 (stride is a multiple
+    // of 16), so the loop test on g0 with that bit cleared is warp-uniform
+    // and the full-warp shuffles always see every lane; groups past the end
+    // load nothing and store nothing.
+    for (int64_t g0 = (int64_t)blockIdx.x * (kQuantThreads / 16) + (threadIdx.x >> 4);
+         (g0 & ~(int64_t)1) < groups_total; g0 += kQuantUnroll * stride) {
+        uint4 raw[kQuantUnroll];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 f = __half22float2(h2[i]);
-            w[2 * i] = f.x;
-            w[2 * i + 1] = f.y;
+        for (int u = 0; u < kQuantUnroll; ++u) {
+            const int64_t grp = g0 + u * stride;
+            raw[u] = grp < groups_total ? __ldcs(W + grp * 16 + lane16) : make_uint4(0, 0, 0, 0);
         }
-        float amax = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(w[i]));
-#pragma unroll
-        for (int off = 8; off > 0; off >>= 1)
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-
-        float s = __fdiv_rn(amax, 7.0f);
-        if (s < 1e-8f) s = 1e-8f;
-
-        uint32_t packed = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            int q = __float2int_rn(__fdiv_rn(w[i], s));
-            q = q < -8 ? -8 : (q > 7 ? 7 : q);
-            packed |= (uint32_t)(q + 8) << (4 * i);
+        for (int u = 0; u < kQuantUnroll; ++u) {
+            const int64_t grp = g0 + u * stride;
+            uint32_t packed;
+            float sc;
+            quantize_group(raw[u], packed, sc);
+            if (grp < groups_total) {
+                qweight[grp * 16 + lane16] = packed;
+                if (lane16 == 0) scales[grp] = __float2half_rn(sc);
+            }
         }
-        qweight[grp * 16 + lane16] = packed;
-        if (lane16 == 0) scales[grp] = __float2half_rn(s);
     }
     // Publish the packed weights and scales device-wide before this block
     // ends: a GEMM launched next on the stream may read them before the
@@ -72,7 +142,7 @@ cudaError_t launch_quantize(const void* W, int64_t N, int64_t K, void* qweight, 
     const int64_t groups = N * G;
     const int64_t per_block = kQuantThreads / 16;
     int64_t blocks = (groups + per_block - 1) / per_block;
-    const int64_t cap = (int64_t)ctx.num_sms * 16;
+    const int64_t cap = (int64_t)ctx.num_sms * (2048 / kQuantThreads);  // one resident wave
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     quantize_kernel<<<(unsigned)blocks, kQuantThreads, 0, stream>>>(
