@@ -151,6 +151,24 @@ int w4a16_unrepack(const void *repacked, int64_t N, int64_t K, void *qweight, vo
 int w4a16_gemm(const void *x_f16, const void *repacked, const void *scales_f16, void *y_f16,
                int64_t M, int64_t N, int64_t K, void *stream);
 
+/* Paths reported by w4a16_gemm_plan. */
+enum { W4A16_PATH_GEMV = 1, W4A16_PATH_TENSOR_CORE = 2 };
+
+/*
+ * w4a16_gemm_plan -- the launch w4a16_gemm makes for (M, N, K) on the current
+ * device, without launching anything (introspection for tests and tuning).
+ *
+ *   *path            W4A16_PATH_GEMV (M <= 16) or W4A16_PATH_TENSOR_CORE.
+ *   *splits          CTAs sharing the K range of one 128-row block (the
+ *                    thread-block cluster size; 1 = no split).
+ *   *ctas            CTAs launched.
+ *   *blocks_per_cta  most 128-row blocks one CTA walks (> 1: persistent).
+ * Errors: NULL output -> W4A16_ERR_NULL; bad M, N, K -> W4A16_ERR_SHAPE;
+ *         no supported device -> W4A16_ERR_DEVICE / W4A16_ERR_CUDA.
+ */
+int w4a16_gemm_plan(int64_t M, int64_t N, int64_t K, int *path, int *splits, int *ctas,
+                    int *blocks_per_cta);
+
 /*
  * w4a16_device_status -- synchronises the current device, returns in
  * *status the OR of the W4A16_ERR_* conditions recorded by kernels since

@@ -36,7 +36,8 @@ def test_m_values(w4lib, M):
     assert_close(run_gemm(x16, q, s), oracle.gemm(x16, q, s), f"M={M}")
 
 
-@pytest.mark.parametrize("N,K", [(128, 128), (200, 384), (1000, 1152), (4168, 640), (136, 18944)])
+@pytest.mark.parametrize("N,K", [(128, 128), (200, 384), (1000, 1152), (4168, 640), (136, 18944),
+                                 (136, 32768)])
 @pytest.mark.parametrize("M", [20, 144])
 def test_shapes_and_tails(w4lib, M, N, K):
     w16, q, s = quantized(N, K, 71)

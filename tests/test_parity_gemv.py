@@ -81,6 +81,18 @@ def test_single_gemv_4096(w4lib):
     assert_close(run_gemm(x16, q, s), oracle.gemm(x16, q, s), "gemv_4096")
 
 
+@pytest.mark.parametrize("M", [1, 5, 9, 16])
+@pytest.mark.parametrize("N,K", [(70001, 1152), (50000, 4096)])
+def test_persistent_path_all_rows(w4lib, M, N, K):
+    """More 128-row blocks than CTA slots: each CTA walks several blocks with
+    its ring running across block boundaries; every row checked."""
+    plan = w4.gemm_plan(M, N, K)
+    assert plan["path"] == "gemv" and plan["blocks_per_cta"] > 1, plan
+    w16, q, s = quantized(N, K, 51)
+    x16 = acts(M, K, 52)
+    assert_close(run_gemm(x16, q, s), oracle.gemm(x16, q, s), f"M={M} N={N} K={K} {plan}")
+
+
 def _sampled(lin, M, workload, idx):
     sw, sx = synthetic.seeds(workload, idx)
     w16, q, s = quantized(lin.N, lin.K, sw)

@@ -154,6 +154,27 @@ int w4a16_gemm(const void* x_f16, const void* repacked, const void* scales_f16, 
     return from_cuda(launch_gemm_tc(x_f16, repacked, scales_f16, y_f16, M, N, K, s, ctx));
 }
 
+int w4a16_gemm_plan(int64_t M, int64_t N, int64_t K, int* path, int* splits, int* ctas,
+                    int* blocks_per_cta) {
+    if (!path || !splits || !ctas || !blocks_per_cta) return W4A16_ERR_NULL;
+    if (M < 1 || M > (int64_t)1 << 22 || !good_nk(N, K) || N > (int64_t)1 << 28 ||
+        K > (int64_t)1 << 15)
+        return W4A16_ERR_SHAPE;
+    DeviceCtx ctx;
+    if (int rc = device_ctx(&ctx)) return rc;
+    if (M > 16) {
+        *path = W4A16_PATH_TENSOR_CORE;
+        *splits = 1;
+        *ctas = (int)(((N + kBlockRows - 1) / kBlockRows) * ((M + 127) / 128));
+        *blocks_per_cta = 1;
+        return W4A16_OK;
+    }
+    if (int rc = from_cuda(gemv_plan_info((int)M, N, K, ctx, splits, ctas, blocks_per_cta)))
+        return rc;
+    *path = W4A16_PATH_GEMV;
+    return W4A16_OK;
+}
+
 int w4a16_device_status(int* status) {
     if (!status) return W4A16_ERR_NULL;
     DeviceCtx ctx;

@@ -591,6 +591,20 @@ cudaError_t launch_gemv_mt(GemvArgs args, int M, cudaStream_t stream, const Devi
 
 }  // namespace
 
+cudaError_t gemv_plan_info(int M, int64_t N, int64_t K, const DeviceCtx& ctx, int* splits,
+                           int* ctas, int* blocks_per_cta) {
+    cudaError_t e = M <= 8 ? ensure_smem_attr<1>() : ensure_smem_attr<2>();
+    if (e != cudaSuccess) return e;
+    const GemvPlan p = M <= 8 ? cached_plan<1>(M, (int)N, (int)K, ctx)
+                              : cached_plan<2>(M, (int)N, (int)K, ctx);
+    if (p.S == 0) return cudaErrorInvalidValue;
+    const int NB = (int)((N + kBlockRows - 1) / kBlockRows);
+    *splits = p.S;
+    *ctas = p.S * p.grid_y;
+    *blocks_per_cta = (NB + p.grid_y - 1) / p.grid_y;
+    return cudaSuccess;
+}
+
 cudaError_t launch_gemv(const void* x, const void* repacked, const void* scales, void* y, int M,
                         int64_t N, int64_t K, cudaStream_t stream, const DeviceCtx& ctx) {
     GemvArgs a{};

@@ -28,6 +28,10 @@ cudaError_t launch_unrepack(const void* repacked, int64_t N, int64_t K, void* qw
                             cudaStream_t stream, const DeviceCtx& ctx);
 cudaError_t launch_gemv(const void* x, const void* repacked, const void* scales, void* y, int M,
                         int64_t N, int64_t K, cudaStream_t stream, const DeviceCtx& ctx);
+// The launch the decode GEMV would make: K split (cluster size), CTAs and
+// the most 128-row blocks one CTA walks.
+cudaError_t gemv_plan_info(int M, int64_t N, int64_t K, const DeviceCtx& ctx, int* splits,
+                           int* ctas, int* blocks_per_cta);
 cudaError_t launch_gemm_tc(const void* x, const void* repacked, const void* scales, void* y,
                            int64_t M, int64_t N, int64_t K, cudaStream_t stream,
                            const DeviceCtx& ctx);

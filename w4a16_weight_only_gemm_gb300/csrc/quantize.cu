@@ -74,26 +74,34 @@ __device__ __forceinline__ void quantize_group(const uint4 raw, uint32_t& packed
     const float y = rcp_nr(s);
 
     float w[8], t[8];
-    float dmax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const float2 f = __half22float2(h2[i]);
         w[2 * i] = f.x;
         w[2 * i + 1] = f.y;
     }
+    // e = kTieSq - d^2 with d = w y - q is negative exactly when |d| >
+    // sqrt(kTieSq) ~ 1/2 - 1e-5 (the fma rounds once, so its sign is exact):
+    // OR-ing the sign bits flags a near tie without min/max instructions.
+    constexpr float kTieSq = 0.25f - 1.0e-5f;
+    uint32_t tie_bits = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         t[i] = __fmaf_rn(w[i], y, kRound);
         const float d = __fmaf_rn(w[i], y, -__fsub_rn(t[i], kRound));  // w y - q
-        dmax = fmaxf(dmax, fabsf(d));
+        tie_bits |= __float_as_uint(__fmaf_rn(-d, d, kTieSq));
     }
-    if (__any_sync(0xffffffffu, dmax > 0.5f - 1.0e-5f)) {
+    if (__any_sync(0xffffffffu, (tie_bits >> 31) != 0)) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) t[i] = __fadd_rn(__fdiv_rn(w[i], s), kRound);
     }
-    packed = 0;
+    // Each t holds 0x4B400000 + (q + 8): sum t_i 16^i (Horner, integer
+    // multiply-adds) and remove the constant part once; the nibbles q + 8
+    // occupy disjoint bits, so no carries cross between them.
+    uint32_t acc = __float_as_uint(t[7]);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) packed |= (__float_as_uint(t[i]) & 0xFu) << (4 * i);
+    for (int i = 6; i >= 0; --i) acc = acc * 16u + __float_as_uint(t[i]);
+    packed = acc - 0x4B400000u * 0x11111111u;
     scale = s;
 }
 
@@ -142,7 +150,18 @@ cudaError_t launch_quantize(const void* W, int64_t N, int64_t K, void* qweight, 
     const int64_t groups = N * G;
     const int64_t per_block = kQuantThreads / 16;
     int64_t blocks = (groups + per_block - 1) / per_block;
-    const int64_t cap = (int64_t)ctx.num_sms * (2048 / kQuantThreads);  // one resident wave
+    static int occ[64] = {};  // resident blocks per SM, per device (one resident wave)
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int per_sm = (dev >= 0 && dev < 64) ? occ[dev] : 0;
+    if (per_sm == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quantize_kernel, kQuantThreads,
+                                                          0) != cudaSuccess ||
+            per_sm < 1)
+            per_sm = 1;
+        if (dev >= 0 && dev < 64) occ[dev] = per_sm;
+    }
+    const int64_t cap = (int64_t)ctx.num_sms * per_sm;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     quantize_kernel<<<(unsigned)blocks, kQuantThreads, 0, stream>>>(

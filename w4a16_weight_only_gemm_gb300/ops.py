@@ -95,6 +95,18 @@ def gemm(x: torch.Tensor, repacked: torch.Tensor, scales: torch.Tensor,
     return out
 
 
+def gemm_plan(M: int, N: int, K: int) -> dict:
+    """The launch gemm() makes for (M, N, K) on the current device:
+    {"path": "gemv" | "tensor_core", "splits", "ctas", "blocks_per_cta"}."""
+    out = [ctypes.c_int(0) for _ in range(4)]
+    _native.check(_native.lib().w4a16_gemm_plan(int(M), int(N), int(K),
+                                                *[ctypes.byref(o) for o in out]),
+                  "w4a16_gemm_plan")
+    path = {1: "gemv", 2: "tensor_core"}[out[0].value]
+    return {"path": path, "splits": out[1].value, "ctas": out[2].value,
+            "blocks_per_cta": out[3].value}
+
+
 def device_status() -> int:
     """Synchronise and return (and clear) the kernels' recorded status code."""
     st = ctypes.c_int(0)
