@@ -48,16 +48,17 @@ constexpr int kConsumerWarps = 8;                      // 8 x 16 rows = one bloc
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kGemvThreads = kConsumers + 32;
 constexpr int kChunkBytes = kBlockRows * kChunkK / 2;  // 4096 B per block-chunk
-constexpr int kStages = 3;
+constexpr int kStages = 3;                             // ring depth of split launches
+constexpr int kMaxStages = 6;                          // deepest ring (persistent launches)
 constexpr int kChunksPerStage = 4;                     // two whole groups
 constexpr int kGroupsPerStage = kChunksPerStage / 2;
 constexpr int kStageBytes = kChunksPerStage * kChunkBytes;
 constexpr int kMaxSplits = 8;
 
 // Barrier area at the start of shared memory.
-constexpr int kBarFull = 0;                    // [kStages]
-constexpr int kBarEmpty = kBarFull + 8 * kStages;
-constexpr int kBarX = kBarEmpty + 8 * kStages;
+constexpr int kBarFull = 0;                    // [kMaxStages]
+constexpr int kBarEmpty = kBarFull + 8 * kMaxStages;
+constexpr int kBarX = kBarEmpty + 8 * kMaxStages;
 constexpr int kBarSFull = kBarX + 8;           // [2]
 constexpr int kBarSEmpty = kBarSFull + 16;     // [2]
 constexpr int kAbortFlag = kBarSEmpty + 16;
@@ -75,6 +76,7 @@ struct GemvArgs {
     int xs_stride;           // bytes between x rows in shared memory
     int slab_bytes;          // bytes of one scale buffer (128 * G * 2, rounded)
     int n_sbuf;              // scale buffers: 2 when a CTA walks several blocks
+    int nstages;             // ring stages (<= kMaxStages)
     int rpo;                 // rows owned per CTA in the split reduction
     uint32_t off_ring, off_x, off_s, off_red, off_sx;
 };
@@ -156,7 +158,7 @@ __global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2) gemv_kernel(con
     const uint32_t ring = sbase + a.off_ring;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < a.nstages; ++s) {
             mbar_init(sbase + kBarFull + 8 * s, 1);
             mbar_init(sbase + kBarEmpty + 8 * s, kConsumerWarps);
         }
@@ -181,7 +183,7 @@ __global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2) gemv_kernel(con
             {   // L2 prefetch of the first block (weights of this split, scale slab).
                 const int rb = (int)blockIdx.y;
                 const uint8_t* w = a.wq + (size_t)rb * block_stride + 2 * (size_t)g0 * kChunkBytes;
-                const int pre = nstg < 2 * kStages ? nstg : 2 * kStages;
+                const int pre = nstg < 2 * a.nstages ? nstg : 2 * a.nstages;
                 for (int i = 0; i < pre; ++i)
                     bulk_prefetch_l2(w + (size_t)i * kStageBytes,
                                      min(kChunksPerStage, nck - i * kChunksPerStage) * kChunkBytes);
@@ -202,7 +204,8 @@ __global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2) gemv_kernel(con
                              a.x + (size_t)m * a.K + (size_t)g0 * kGroup, xbytes, sbase + kBarX);
                 x_issued = true;
             };
-            int it = 0;
+            const int NS = a.nstages;
+            int it = 0, slot = 0, round = 0;  // slot = it % NS, round = it / NS
             bool ok = true;
             int sb_issued = 0;
             for (int j = 0; ok && j < nblk; ++j) {
@@ -230,12 +233,11 @@ __global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2) gemv_kernel(con
                 }
                 // --- weight stages of block rb ---
                 const uint8_t* w = a.wq + (size_t)rb * block_stride + 2 * (size_t)g0 * kChunkBytes;
-                for (int st = 0; st < nstg; ++st, ++it) {
-                    const int slot = it % kStages;
-                    if (it >= kStages && !x_issued) issue_x();
-                    if (it >= kStages &&
-                        !mbar_wait(sbase + kBarEmpty + 8 * slot, ((it / kStages) - 1) & 1,
-                                   a.timeout_ns, a.status)) {
+                for (int st = 0; st < nstg; ++st) {
+                    if (it >= NS && !x_issued) issue_x();
+                    if (it >= NS &&
+                        !mbar_wait(sbase + kBarEmpty + 8 * slot, (round - 1) & 1, a.timeout_ns,
+                                   a.status)) {
                         ok = false;
                         break;
                     }
@@ -247,15 +249,19 @@ __global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2) gemv_kernel(con
                     mbar_arrive_expect_tx(sbase + kBarFull + 8 * slot, nc * kChunkBytes);
                     bulk_g2s_hint(ring + slot * kStageBytes, w + (size_t)st * kStageBytes,
                                   nc * kChunkBytes, sbase + kBarFull + 8 * slot, pol);
+                    ++it;
+                    if (++slot == NS) {
+                        slot = 0;
+                        ++round;
+                    }
                 }
             }
             if (!x_issued) issue_x();
             if (!ok) *abort_flag = 1;
             // Drain: every issued copy must land before the CTA may exit.
             mbar_wait(sbase + kBarX, 0, a.timeout_ns, a.status);
-            for (int i = (it > kStages ? it - kStages : 0); i < it; ++i)
-                mbar_wait(sbase + kBarFull + 8 * (i % kStages), (i / kStages) & 1, a.timeout_ns,
-                          a.status);
+            for (int i = (it > NS ? it - NS : 0); i < it; ++i)
+                mbar_wait(sbase + kBarFull + 8 * (i % NS), (i / NS) & 1, a.timeout_ns, a.status);
             for (int j = (sb_issued > a.n_sbuf ? sb_issued - a.n_sbuf : 0); j < sb_issued; ++j)
                 mbar_wait(sbase + kBarSFull + 8 * (j % a.n_sbuf), (j / a.n_sbuf) & 1, a.timeout_ns,
                           a.status);
@@ -308,7 +314,9 @@ __global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2) gemv_kernel(con
             asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
         }
         const uint32_t sxl = sbase + a.off_sx + t * 8;  // this lane's columns 2t, 2t + 1
-        int it = 0;
+        const int NS = a.nstages;
+        int slot = 0;
+        uint32_t phase = 0;  // parity of the ring's current pass
         for (int j = 0; ok && j < nblk; ++j) {
             const int rb = (int)blockIdx.y + j * (int)gridDim.y;
             const int sbuf = j % a.n_sbuf;
@@ -327,10 +335,8 @@ __global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2) gemv_kernel(con
                 for (int e = 0; e < 4; ++e) acc[mt][e] = 0.0f;
 
             uint32_t xs_off = 0;
-            for (int st = 0; st < nfull; ++st, ++it, xs_off += kChunksPerStage * 128) {
-                const int slot = it % kStages;
-                if (!mbar_wait(sbase + kBarFull + 8 * slot, (it / kStages) & 1, a.timeout_ns,
-                               a.status)) {
+            for (int st = 0; st < nfull; ++st, xs_off += kChunksPerStage * 128) {
+                if (!mbar_wait(sbase + kBarFull + 8 * slot, phase, a.timeout_ns, a.status)) {
                     ok = false;
                     break;
                 }
@@ -344,11 +350,13 @@ __global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2) gemv_kernel(con
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(sbase + kBarEmpty + 8 * slot);
+                if (++slot == NS) {
+                    slot = 0;
+                    phase ^= 1u;
+                }
             }
             if (ok && tail) {
-                const int slot = it % kStages;
-                if (!mbar_wait(sbase + kBarFull + 8 * slot, (it / kStages) & 1, a.timeout_ns,
-                               a.status)) {
+                if (!mbar_wait(sbase + kBarFull + 8 * slot, phase, a.timeout_ns, a.status)) {
                     ok = false;
                 } else {
                     const int gl = nfull * kGroupsPerStage;
@@ -357,7 +365,10 @@ __global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2) gemv_kernel(con
                     __syncwarp();
                     if (lane == 0) mbar_arrive(sbase + kBarEmpty + 8 * slot);
                 }
-                ++it;
+                if (++slot == NS) {
+                    slot = 0;
+                    phase ^= 1u;
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(sbase + kBarSEmpty + 8 * sbuf);
@@ -420,6 +431,7 @@ struct GemvPlan {
     int S = 0;
     int grid_y = 0;
     int n_sbuf = 1;
+    int nstages = kStages;
     int xs_stride = 0;
     int slab_bytes = 0;
     int rpo = 0;
@@ -468,14 +480,15 @@ cudaError_t ensure_smem_attr() {
 
 // Shared-memory layout of a launch with K split S and `nsb` scale buffers.
 template <int MT>
-bool layout(GemvPlan& p, int M, int G, int S, int nsb, const DeviceCtx& ctx) {
+bool layout(GemvPlan& p, int M, int G, int S, int nsb, const DeviceCtx& ctx, int nst = kStages) {
     p.S = S;
     p.n_sbuf = nsb;
+    p.nstages = nst;
     const int ng_max = (G + S - 1) / S;
     p.xs_stride = ng_max * kGroup * 2 + 16;  // +16 B keeps x rows conflict-free
     p.slab_bytes = ((kBlockRows * G * 2 + 127) / 128) * 128;
     p.off_ring = kBarAreaBytes;
-    p.off_x = p.off_ring + kStages * kStageBytes;
+    p.off_x = p.off_ring + p.nstages * kStageBytes;
     p.off_s = p.off_x + ((M * p.xs_stride + 127) / 128) * 128;
     p.off_red = p.off_s + nsb * p.slab_bytes;
     p.rpo = (kBlockRows + S - 1) / S;
@@ -499,6 +512,15 @@ GemvPlan plan_gemv(int M, int N, int K, const DeviceCtx& ctx) {
         if (layout<MT>(p, M, G, 1, 2, ctx)) {
             const int occ = occupancy<MT>(p.smem);
             if (occ > 0 && NB > ctx.num_sms * occ) {
+                // The deepest ring that keeps the same CTAs per SM: more bytes
+                // in flight per CTA, for the same number of streams.
+                for (int nst = kMaxStages; nst > kStages; --nst) {
+                    GemvPlan q;
+                    if (layout<MT>(q, M, G, 1, 2, ctx, nst) && occupancy<MT>(q.smem) == occ) {
+                        p = q;
+                        break;
+                    }
+                }
                 p.grid_y = ctx.num_sms * occ;
                 p.eff = 1.0;
                 return p;
@@ -561,6 +583,7 @@ cudaError_t launch_gemv_mt(GemvArgs args, int M, cudaStream_t stream, const Devi
     args.xs_stride = p.xs_stride;
     args.slab_bytes = p.slab_bytes;
     args.n_sbuf = p.n_sbuf;
+    args.nstages = p.nstages;
     args.off_ring = p.off_ring;
     args.off_x = p.off_x;
     args.off_s = p.off_s;
