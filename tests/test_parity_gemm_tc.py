@@ -71,6 +71,18 @@ def test_guard_bands(w4lib):
     assert_close(y.float().cpu().numpy(), oracle.gemm(x16, q, s), "guard")
 
 
+@pytest.mark.parametrize("M,N,K", [(300, 19000, 384), (200, 40000, 256), (512, 38400, 128)])
+def test_cta_pair_path(w4lib, M, N, K):
+    """256 x 256 tiles on CTA pairs (2-CTA MMAs): an odd number of 128-row
+    weight blocks (the last pair's odd CTA holds none), ragged M; every
+    output compared."""
+    plan = w4.gemm_plan(M, N, K)
+    assert plan["path"] == "tensor_core" and plan["splits"] == 2, plan
+    w16, q, s = quantized(N, K, 81)
+    x16 = acts(M, K, 82)
+    assert_close(run_gemm(x16, q, s), oracle.gemm(x16, q, s), f"M={M} N={N} K={K} {plan}")
+
+
 @pytest.mark.parametrize("idx", range(len(workloads.PREFILL)))
 def test_prefill_full_size(w4lib, idx):
     """M = 512 prompt pass on the two prefill shapes; oracle on sampled rows."""

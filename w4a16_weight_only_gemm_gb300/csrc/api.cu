@@ -164,8 +164,7 @@ int w4a16_gemm_plan(int64_t M, int64_t N, int64_t K, int* path, int* splits, int
     if (int rc = device_ctx(&ctx)) return rc;
     if (M > 16) {
         *path = W4A16_PATH_TENSOR_CORE;
-        *splits = 1;
-        *ctas = (int)(((N + kBlockRows - 1) / kBlockRows) * ((M + 127) / 128));
+        gemm_tc_plan_info(M, N, ctx, splits, ctas);
         *blocks_per_cta = 1;
         return W4A16_OK;
     }

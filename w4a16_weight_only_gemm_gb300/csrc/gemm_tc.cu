@@ -7,8 +7,11 @@
 // prompt pass).  Unlike decode, the prompt pass is a dense contraction, so it
 // runs on the tensor cores:
 //
-// One thread block computes a 128 (activation rows = MMA M) x 128 (weight
-// rows = MMA N) tile of y with FP32 accumulators in tensor memory.
+// A thread block computes a 128 (activation rows = MMA M) x 128 (weight rows
+// = MMA N) tile of y with FP32 accumulators in tensor memory; once M > 128 a
+// cluster of two blocks computes a 256 x 256 tile with 2-CTA MMAs (see
+// gemm_tc_kernel<true, XT>), which cuts the shared-memory operand traffic per
+// FLOP and puts more MMA work behind every stage hand-off.
 //  * warp 0 (one thread): TMA producer.  Per 64-wide k-block it loads the x
 //    tile [128 x 64] fp16 (operand A) with a 2-D tensor-map copy in the
 //    128-byte swizzled K-major layout and the block's 4 KB of packed weights
@@ -44,23 +47,21 @@ constexpr int kDequantWarps = 16;               // warps 4 .. 19, two sets of 8
 constexpr int kTileW = kBlockRows;              // weight rows per tile (MMA N)
 constexpr int kTileX = 128;                     // activation rows per tile (MMA M)
 constexpr int kBK = kChunkK;                    // 64: one kernel-layout chunk
-constexpr int kStages = 4;                      // ring: x tile, packed and dequantised weights
+constexpr int kMaxStages = 6;                   // ring: x tile, packed and dequantised weights
+constexpr int kSingleStages = 4;                // ring of the single-CTA tile
 constexpr int kAStageBytes = kTileW * kBK * 2;  // 16 KB fp16, 128B-swizzled
 constexpr int kXStageBytes = kTileX * kBK * 2;  // 16 KB
 constexpr int kWStageBytes = kTileW * kBK / 2;  // 4 KB packed
-constexpr uint32_t kTmemCols = kTileW;          // fp32 accumulator columns
 
 constexpr int kBarLoadFull = 0;                      // [stages] x + packed weights landed
-constexpr int kBarAFull = kBarLoadFull + 8 * kStages;  // [stages] dequantised tile written
-constexpr int kBarFree = kBarAFull + 8 * kStages;      // [stages] MMAs done: stage reusable
-constexpr int kBarAcc = kBarFree + 8 * kStages;
+constexpr int kBarAFull = kBarLoadFull + 8 * kMaxStages;  // [stages] dequantised tile written
+constexpr int kBarFree = kBarAFull + 8 * kMaxStages;      // [stages] MMAs done: stage reusable
+constexpr int kBarAcc = kBarFree + 8 * kMaxStages;
 constexpr int kBarSlab = kBarAcc + 8;
 constexpr int kTmemSlot = kBarSlab + 8;
 constexpr int kAbortFlag = kTmemSlot + 8;
 constexpr int kOffA = 1024;                              // dequantised tiles
-constexpr int kOffX = kOffA + kStages * kAStageBytes;    // x tiles
-constexpr int kOffW = kOffX + kStages * kXStageBytes;    // packed weights
-constexpr int kOffSlab = kOffW + kStages * kWStageBytes; // scale slab
+// then x tiles, packed weights and the scale slab at offsets set per launch
 
 struct TcArgs {
     const uint8_t* wq;
@@ -69,6 +70,8 @@ struct TcArgs {
     unsigned* status;
     uint64_t timeout_ns;
     int M, N, K, G;
+    int nst;                           // ring stages (<= kMaxStages)
+    uint32_t off_x, off_w, off_slab;   // shared-memory offsets after the window base
 };
 
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -89,6 +92,17 @@ __device__ __forceinline__ uint32_t swz128(int r, int c) {
     return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
+// PAIR = false: one CTA computes a 128 x 128 tile of y with its own MMAs.
+// PAIR = true: a cluster of two CTAs computes a (256 XT) (x rows) x 256
+// (weight rows) tile with 2-CTA MMAs (tcgen05 cta_group::2): CTA r of the
+// pair dequantises weight rows n0 + 128 r (its half of B) and stages XT x
+// tiles, rows m0 + 256 t + 128 r (its half of A for MMA t); the even CTA
+// issues XT MMAs per 16-wide k-step, which read both CTAs' shared memory and
+// leave in each CTA's tensor memory its 128 rows of the 256 XT x 256 D
+// (MMA t in columns 256 t ..).  Each SM reads (16 XT + 16) KB of operands per
+// 64-wide k-block for 2 XT times the FLOPs of the single-CTA tile, and every
+// stage hand-off covers XT times more MMA work.
+template <bool PAIR, int XT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -98,16 +112,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint8_t* smem = smem_raw + (base - raw);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortFlag);
 
+    static_assert(XT == 1 || (PAIR && XT == 2), "two x tiles per stage need CTA pairs");
+    constexpr uint32_t kCols = PAIR ? 2 * kTileW * XT : kTileW;  // accumulator columns
+    constexpr int kXBytes = XT * kXStageBytes;                     // x bytes per stage
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int rb = (int)blockIdx.x;             // 128-row weight block
-    const int m0 = (int)blockIdx.y * kTileX;    // first activation row
+    const int rank = PAIR ? (int)(cluster_cta_rank() & 1) : 0;
+    const bool leader = rank == 0;
+    // This CTA's 128-row weight block and first x row; y columns start at n_out.
+    const int rb = PAIR ? (int)blockIdx.x : (int)blockIdx.x;
+    const int n_out = PAIR ? ((int)blockIdx.x >> 1) * 2 * kTileW : (int)blockIdx.x * kTileW;
+    const int m0 = PAIR ? (int)blockIdx.y * 2 * kTileX * XT + rank * kTileX : (int)blockIdx.y * kTileX;
+    const int NB = (a.N + kTileW - 1) / kTileW;
+    const bool wvalid = rb < NB;  // the odd CTA of the last pair may hold no weights
     const int nkb = a.K / kBK;
+    // The single-CTA tile always runs kSingleStages stages at fixed offsets
+    // (compile-time constants there); pairs size their ring per launch.
+    const int NS = PAIR ? a.nst : kSingleStages;
+    const uint32_t kOffX = PAIR ? a.off_x : kOffA + kSingleStages * kAStageBytes;
+    const uint32_t kOffW = PAIR ? a.off_w : kOffX + kSingleStages * kXStageBytes;
+    const uint32_t kOffSlab = PAIR ? a.off_slab : kOffW + kSingleStages * kWStageBytes;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < NS; ++s) {
             mbar_init(base + kBarLoadFull + 8 * s, 1);
-            mbar_init(base + kBarAFull + 8 * s, kDequantWarps / 2 * 32);
+            // pair: one elected arrival per dequantising warp of a set in
+            // both CTAs (the peer's are remote); single: every dequantiser
+            mbar_init(base + kBarAFull + 8 * s, PAIR ? kDequantWarps : kDequantWarps / 2 * 32);
             mbar_init(base + kBarFree + 8 * s, 1);
         }
         mbar_init(base + kBarAcc, 1);
@@ -116,13 +147,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         fence_barrier_init();
     }
     if (warp == 1) {
-        tmem_alloc(base + kTmemSlot, kTmemCols);
-        tmem_relinquish();
+        if (PAIR) {
+            tmem_alloc_pair(base + kTmemSlot, kCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(base + kTmemSlot, kCols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kTmemSlot);
+    // Pair: the peer's barriers must be initialised before the first remote
+    // arrival or multicast commit.  Every thread arrives now and waits once,
+    // before its first remote operation or at the end.
+    bool cl_waited = !PAIR;
+    if (PAIR) cluster_arrive();
     grid_launch_dependents();
 
     if (warp == 0) {
@@ -130,11 +171,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
             tma_prefetch_map(&xmap);
             const uint8_t* w = a.wq + (size_t)rb * nkb * kWStageBytes;
-            for (int i = 0; i < kStages && i < nkb; ++i)
-                bulk_prefetch_l2(w + (size_t)i * kWStageBytes, kWStageBytes);
+            if (wvalid)
+                for (int i = 0; i < NS && i < nkb; ++i)
+                    bulk_prefetch_l2(w + (size_t)i * kWStageBytes, kWStageBytes);
             grid_dependency_wait();
             {   // the block's scale slab (rows x G fp16, contiguous)
-                const int rows = min(kTileW, a.N - rb * kTileW);
+                const int rows = max(0, min(kTileW, a.N - rb * kTileW));
                 const uint32_t bytes = (uint32_t)(rows * a.G * 2);
                 const uint32_t bulk = bytes & ~15u;
                 const __half* src = a.scales + (size_t)rb * kTileW * a.G;
@@ -146,7 +188,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             int issued = 0;
             bool ok = true;
             for (int i = 0, ts = 0, round = 0; i < nkb; ++i) {
-                if (i >= kStages &&
+                if (i >= NS &&
                     !mbar_wait(base + kBarFree + 8 * ts, (round - 1) & 1, a.timeout_ns,
                                a.status)) {
                     ok = false;
@@ -156,13 +198,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(base + kBarLoadFull + 8 * ts, kXStageBytes + kWStageBytes);
-                tma_load_2d(base + kOffX + ts * kXStageBytes, &xmap, i * kBK, m0,
-                            base + kBarLoadFull + 8 * ts);
-                bulk_g2s(base + kOffW + ts * kWStageBytes, w + (size_t)i * kWStageBytes,
-                         kWStageBytes, base + kBarLoadFull + 8 * ts);
+                mbar_arrive_expect_tx(base + kBarLoadFull + 8 * ts,
+                                      kXBytes + (wvalid ? kWStageBytes : 0));
+#pragma unroll
+                for (int xt = 0; xt < XT; ++xt)
+                    tma_load_2d(base + kOffX + ts * kXBytes + xt * kXStageBytes, &xmap, i * kBK,
+                                m0 + xt * 2 * kTileX, base + kBarLoadFull + 8 * ts);
+                if (wvalid)
+                    bulk_g2s(base + kOffW + ts * kWStageBytes, w + (size_t)i * kWStageBytes,
+                             kWStageBytes, base + kBarLoadFull + 8 * ts);
                 issued = i + 1;
-                if (++ts == kStages) {
+                if (++ts == NS) {
                     ts = 0;
                     ++round;
                 }
@@ -170,36 +216,57 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (!ok) *abort_flag = 1;
             // Drain the copies in flight before the block may exit.
             mbar_wait(base + kBarSlab, 0, a.timeout_ns, a.status);
-            for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
-                mbar_wait(base + kBarLoadFull + 8 * (i % kStages), (i / kStages) & 1, a.timeout_ns,
+            for (int i = (issued > NS ? issued - NS : 0); i < issued; ++i)
+                mbar_wait(base + kBarLoadFull + 8 * (i % NS), (i / NS) & 1, a.timeout_ns,
                           a.status);
         }
         __syncwarp();
     } else if (warp == 1) {
         // ============================= MMA issuer =============================
-        if (lane == 0) {
-            const uint32_t idesc = umma_idesc_f16_f32(kTileX, kTileW);
+        if (lane == 0 && leader) {
+            // A = x rows (M), B = weight rows (N), both K-major.
+            const uint32_t idesc = umma_idesc_f16_f32(PAIR ? 2 * kTileX : kTileX, PAIR ? 2 * kTileW : kTileW);
             bool ok = true;
             for (int i = 0, ts = 0, tr = 0; i < nkb; ++i) {
                 // the dequantisers waited for the stage's copies: A full implies x landed
-                if (!mbar_wait(base + kBarAFull + 8 * ts, tr & 1, a.timeout_ns, a.status)) {
+                const bool got = PAIR ? mbar_wait_cluster(base + kBarAFull + 8 * ts, tr & 1,
+                                                          a.timeout_ns, a.status)
+                                      : mbar_wait(base + kBarAFull + 8 * ts, tr & 1, a.timeout_ns,
+                                                  a.status);
+                if (!got) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t xa = base + kOffX + ts * kXStageBytes;
+                const uint32_t xa = base + kOffX + ts * kXBytes;
                 const uint32_t wa = base + kOffA + ts * kAStageBytes;
 #pragma unroll
-                for (int j = 0; j < kBK / 16; ++j)  // A = x rows, B = weight rows
-                    tc_mma_f16(tmem, umma_desc_sw128(xa + 32 * j), umma_desc_sw128(wa + 32 * j),
-                               idesc, (i | j) != 0);
-                tc_commit(base + kBarFree + 8 * ts);  // stage reusable once these MMAs finish
-                if (++ts == kStages) {
+                for (int j = 0; j < kBK / 16; ++j) {
+                    if (PAIR) {
+#pragma unroll
+                        for (int xt = 0; xt < XT; ++xt)
+                            tc_mma_f16_pair(tmem + (uint32_t)(xt * 2 * kTileW),
+                                            umma_desc_sw128(xa + xt * kXStageBytes + 32 * j),
+                                            umma_desc_sw128(wa + 32 * j), idesc, (i | j) != 0);
+                    } else
+                        tc_mma_f16(tmem, umma_desc_sw128(xa + 32 * j), umma_desc_sw128(wa + 32 * j),
+                                   idesc, (i | j) != 0);
+                }
+                // stage reusable (in both CTAs of a pair) once these MMAs finish
+                if (PAIR)
+                    tc_commit_pair_multicast(base + kBarFree + 8 * ts, 0x3);
+                else
+                    tc_commit(base + kBarFree + 8 * ts);
+                if (++ts == NS) {
                     ts = 0;
                     ++tr;
                 }
             }
-            tc_commit(base + kBarAcc);  // completes once every issued MMA has
+            // completes once every issued MMA has
+            if (PAIR)
+                tc_commit_pair_multicast(base + kBarAcc, 0x3);
+            else
+                tc_commit(base + kBarAcc);
             if (!ok) *abort_flag = 1;
         }
         __syncwarp();
@@ -211,39 +278,63 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int g = lane >> 2, tq = lane & 3;
         const int r0 = dw * 16 + g, r1 = r0 + 8;
         const __half* slab = reinterpret_cast<const __half*>(smem + kOffSlab);
+        // the stage barrier lives in the even CTA of a pair
+        const uint32_t afull0 = PAIR ? map_to_cta(base + kBarAFull, 0) : base + kBarAFull;
+        if (PAIR && !leader) {
+            cluster_wait();
+            cl_waited = true;
+        }
         bool ok = mbar_wait(base + kBarSlab, 0, a.timeout_ns, a.status);
+        // stage ts = i % NS and its pass parity, advanced by two k-blocks a step
+        int ts = set % NS;
+        uint32_t tph = (uint32_t)((set / NS) & 1);
         for (int i = set; ok && i < nkb; i += 2) {
             // The stage's copies were issued after its previous MMAs finished,
             // so their arrival also means the dequantised slot is free.
-            const int ts = i % kStages;
-            if (!mbar_wait(base + kBarLoadFull + 8 * ts, (i / kStages) & 1, a.timeout_ns,
-                           a.status)) {
+            if (!mbar_wait(base + kBarLoadFull + 8 * ts, tph, a.timeout_ns, a.status)) {
                 ok = false;
                 break;
             }
-            const int grp = i >> 1;  // two 64-wide k-blocks per scale group
-            const uint32_t wst = base + kOffW + ts * kWStageBytes;
-            const uint32_t ast = base + kOffA + ts * kAStageBytes;
-            const uint4 pk = lds128(wst + (dw * 32 + lane) * 16);
-            const __half2 s0 = __half2half2(slab[r0 * a.G + grp]);
-            const __half2 s1 = __half2half2(slab[r1 * a.G + grp]);
-            const uint32_t wrd[4] = {pk.x, pk.y, pk.z, pk.w};
-            uint32_t o0[8], o1[8];  // rows r0 / r1, k = 16 tq .. 16 tq + 15
+            if (wvalid) {
+                const int grp = i >> 1;  // two 64-wide k-blocks per scale group
+                const uint32_t wst = base + kOffW + ts * kWStageBytes;
+                const uint32_t ast = base + kOffA + ts * kAStageBytes;
+                const uint4 pk = lds128(wst + (dw * 32 + lane) * 16);
+                const __half2 s0 = __half2half2(slab[r0 * a.G + grp]);
+                const __half2 s1 = __half2half2(slab[r1 * a.G + grp]);
+                const uint32_t wrd[4] = {pk.x, pk.y, pk.z, pk.w};
+                uint32_t o0[8], o1[8];  // rows r0 / r1, k = 16 tq .. 16 tq + 15
 #pragma unroll
-            for (int ws = 0; ws < 4; ++ws) {
-                uint32_t af[4];
-                dequant8(wrd[ws], af);
-                o0[2 * ws] = hmul2_u32(af[0], s0);
-                o0[2 * ws + 1] = hmul2_u32(af[2], s0);
-                o1[2 * ws] = hmul2_u32(af[1], s1);
-                o1[2 * ws + 1] = hmul2_u32(af[3], s1);
+                for (int ws = 0; ws < 4; ++ws) {
+                    uint32_t af[4];
+                    dequant8(wrd[ws], af);
+                    o0[2 * ws] = hmul2_u32(af[0], s0);
+                    o0[2 * ws + 1] = hmul2_u32(af[2], s0);
+                    o1[2 * ws] = hmul2_u32(af[1], s1);
+                    o1[2 * ws + 1] = hmul2_u32(af[3], s1);
+                }
+                sts128(ast + swz128(r0, 2 * tq), o0[0], o0[1], o0[2], o0[3]);
+                sts128(ast + swz128(r0, 2 * tq + 1), o0[4], o0[5], o0[6], o0[7]);
+                sts128(ast + swz128(r1, 2 * tq), o1[0], o1[1], o1[2], o1[3]);
+                sts128(ast + swz128(r1, 2 * tq + 1), o1[4], o1[5], o1[6], o1[7]);
+                fence_proxy_async_smem();  // generic stores -> visible to the tensor core
             }
-            sts128(ast + swz128(r0, 2 * tq), o0[0], o0[1], o0[2], o0[3]);
-            sts128(ast + swz128(r0, 2 * tq + 1), o0[4], o0[5], o0[6], o0[7]);
-            sts128(ast + swz128(r1, 2 * tq), o1[0], o1[1], o1[2], o1[3]);
-            sts128(ast + swz128(r1, 2 * tq + 1), o1[4], o1[5], o1[6], o1[7]);
-            fence_proxy_async_smem();  // generic stores -> visible to the tensor core
-            mbar_arrive(base + kBarAFull + 8 * ts);
+            if (PAIR) {
+                __syncwarp();
+                if (lane == 0) {
+                    if (leader)
+                        mbar_arrive(base + kBarAFull + 8 * ts);
+                    else
+                        mbar_arrive_remote(afull0 + 8 * ts);
+                }
+            } else {
+                mbar_arrive(base + kBarAFull + 8 * ts);
+            }
+            ts += 2;
+            if (ts >= NS) {
+                ts -= NS;
+                tph ^= 1u;
+            }
         }
         if (!ok) *abort_flag = 1;
 
@@ -251,30 +342,37 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (mbar_wait(base + kBarAcc, 0, a.timeout_ns, a.status)) {
             tc_fence_after_sync();
             const int q = warp & 3;           // TMEM lane quarter = rows of y
-            const int cc = (warp - 4) >> 2;   // 32-column chunk = weight rows
-            const int m = m0 + q * 32 + lane;
-            const int n = rb * kTileW + cc * 32;
-            uint32_t v[32];
-            tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(cc * 32), v);
-            tmem_ld_wait();
-            if (m < a.M) {
-                __half* yrow = a.y + (size_t)m * a.N;
-                if (n + 32 <= a.N && (a.N & 7) == 0) {
-                    uint32_t h[16];
+            const int cc = (warp - 4) >> 2;   // column chunk = weight rows
+            constexpr int kChunkCols = (int)kCols / 4;  // 32 (single), 64 or 128 (pair)
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        __half2 p = __floats2half2_rn(__uint_as_float(v[2 * c]),
-                                                      __uint_as_float(v[2 * c + 1]));
-                        h[c] = *reinterpret_cast<uint32_t*>(&p);
+            for (int half = 0; half < kChunkCols / 32; ++half) {
+                const int col = cc * kChunkCols + half * 32;
+                // pair: columns 256 t .. belong to MMA t, i.e. x rows m0 + 256 t
+                const int xt = PAIR ? col / (2 * kTileW) : 0;
+                const int n = n_out + (PAIR ? col % (2 * kTileW) : col);
+                const int m = m0 + xt * 2 * kTileX + q * 32 + lane;
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)col, v);
+                tmem_ld_wait();
+                if (m < a.M) {
+                    __half* yrow = a.y + (size_t)m * a.N;
+                    if (n + 32 <= a.N && (a.N & 7) == 0) {
+                        uint32_t h[16];
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            __half2 p2 = __floats2half2_rn(__uint_as_float(v[2 * c]),
+                                                           __uint_as_float(v[2 * c + 1]));
+                            h[c] = *reinterpret_cast<uint32_t*>(&p2);
+                        }
+                        uint4* dst = reinterpret_cast<uint4*>(yrow + n);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            dst[c] = make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            if (n + c < a.N) yrow[n + c] = __float2half_rn(__uint_as_float(v[c]));
                     }
-                    uint4* dst = reinterpret_cast<uint4*>(yrow + n);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        dst[c] = make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        if (n + c < a.N) yrow[n + c] = __float2half_rn(__uint_as_float(v[c]));
                 }
             }
         }
@@ -282,9 +380,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     tc_fence_before_sync();
     __syncthreads();
+    if (PAIR) {
+        // Neither CTA frees its tensor memory or leaves while the pair's
+        // MMAs or the peer's arrivals may still touch it.
+        if (!cl_waited) cluster_wait();
+        cluster_sync_all();
+    }
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem, kTmemCols);
+        if (PAIR)
+            tmem_dealloc_pair(tmem, kCols);
+        else
+            tmem_dealloc(tmem, kCols);
     }
 }
 
@@ -302,14 +409,72 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
+// Launch shape of the tensor-core GEMM for (M, N):
+//  * xt = 2: CTA pairs with two x tiles per CTA, 512 x rows x 256 weight rows
+//    per pair -- the most MMA work per stage hand-off -- when M > 256 and the
+//    pairs still occupy at least half of the SMs;
+//  * xt = 1: CTA pairs with 256 x 256 tiles when M > 128 and they cover
+//    every SM;
+//  * otherwise one CTA per 128 x 128 tile (cluster 1).
+struct TcPlan {
+    int cluster = 1, xt = 1;
+    unsigned gx = 0, gy = 0;
+    long long ctas = 0;
+};
+
+TcPlan tc_plan(int64_t M, int64_t N, const DeviceCtx& ctx) {
+    TcPlan p;
+    const int NB = (int)((N + kTileW - 1) / kTileW);
+    const long long pairs = (NB + 1) / 2;
+    if (NB >= 2) {
+        const long long c2 = 2 * pairs * ((M + 4 * kTileX - 1) / (4 * kTileX));
+        const long long c1 = 2 * pairs * ((M + 2 * kTileX - 1) / (2 * kTileX));
+        if (M > 2 * kTileX && 2 * c2 >= ctx.num_sms) {
+            p.cluster = 2;
+            p.xt = 2;
+            p.gx = (unsigned)(2 * pairs);
+            p.gy = (unsigned)((M + 4 * kTileX - 1) / (4 * kTileX));
+            p.ctas = c2;
+            return p;
+        }
+        if (M > kTileX && c1 >= ctx.num_sms) {
+            p.cluster = 2;
+            p.gx = (unsigned)(2 * pairs);
+            p.gy = (unsigned)((M + 2 * kTileX - 1) / (2 * kTileX));
+            p.ctas = c1;
+            return p;
+        }
+    }
+    p.gx = (unsigned)NB;
+    p.gy = (unsigned)((M + kTileX - 1) / kTileX);
+    p.ctas = (long long)p.gx * p.gy;
+    return p;
+}
+
 }  // namespace
+
+void gemm_tc_plan_info(int64_t M, int64_t N, const DeviceCtx& ctx, int* cluster, int* ctas) {
+    const TcPlan p = tc_plan(M, N, ctx);
+    *cluster = p.cluster;
+    *ctas = (int)p.ctas;
+}
 
 cudaError_t launch_gemm_tc(const void* x, const void* repacked, const void* scales, void* y,
                            int64_t M, int64_t N, int64_t K, cudaStream_t stream,
                            const DeviceCtx& ctx) {
     const int G = (int)(K / kGroup);
-    // +1 KB: slack for aligning the window to 1024 bytes
-    const uint32_t smem = kOffSlab + ((kTileW * G * 2 + 127) / 128) * 128 + 1024;
+    const TcPlan plan = tc_plan(M, N, ctx);
+    // Ring stages next to the scale slab (+1 KB slack for aligning the window
+    // to 1024 bytes).  Pairs take as many as fit: a deeper ring hides more of
+    // the copy -> dequantise -> MMA -> release round trip.  The single-CTA
+    // tile keeps 4 (deeper measured slower there).
+    const uint32_t slab = ((kTileW * G * 2 + 127) / 128) * 128;
+    const uint32_t stage = (uint32_t)(kAStageBytes + plan.xt * kXStageBytes + kWStageBytes);
+    int nst = plan.cluster == 2 ? kMaxStages : kSingleStages;
+    while (plan.cluster == 2 && nst > 2 &&
+           kOffA + (uint32_t)nst * stage + slab + 1024 > (uint32_t)ctx.max_smem_optin)
+        --nst;
+    const uint32_t smem = kOffA + (uint32_t)nst * stage + slab + 1024;
     if ((int)smem > ctx.max_smem_optin) return cudaErrorInvalidValue;
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
@@ -327,10 +492,11 @@ cudaError_t launch_gemm_tc(const void* x, const void* repacked, const void* scal
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             ctx.max_smem_optin);
-        if (e != cudaSuccess) return e;
+        for (auto fn : {gemm_tc_kernel<false, 1>, gemm_tc_kernel<true, 1>, gemm_tc_kernel<true, 2>}) {
+            cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 ctx.max_smem_optin);
+            if (e != cudaSuccess) return e;
+        }
         attr_done[dev] = true;
     }
     TcArgs args{};
@@ -343,18 +509,28 @@ cudaError_t launch_gemm_tc(const void* x, const void* repacked, const void* scal
     args.N = (int)N;
     args.K = (int)K;
     args.G = G;
+    args.nst = nst;
+    args.off_x = kOffA + (uint32_t)nst * kAStageBytes;
+    args.off_w = args.off_x + (uint32_t)nst * plan.xt * kXStageBytes;
+    args.off_slab = args.off_w + (uint32_t)nst * kWStageBytes;
 
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((N + kTileW - 1) / kTileW), (unsigned)((M + kTileX - 1) / kTileX), 1);
+    cfg.gridDim = dim3(plan.gx, plan.gy, 1);
     cfg.blockDim = dim3(kTcThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr.val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, map, args);
+    cudaLaunchAttribute attrs[2];
+    attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[0].val.programmaticStreamSerializationAllowed = 1;
+    attrs[1].id = cudaLaunchAttributeClusterDimension;
+    attrs[1].val.clusterDim.x = 2;
+    attrs[1].val.clusterDim.y = 1;
+    attrs[1].val.clusterDim.z = 1;
+    cfg.attrs = attrs;
+    cfg.numAttrs = plan.cluster == 2 ? 2 : 1;
+    if (plan.cluster == 1) return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<false, 1>, map, args);
+    if (plan.xt == 1) return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true, 1>, map, args);
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true, 2>, map, args);
 }
 
 }  // namespace w4a16
