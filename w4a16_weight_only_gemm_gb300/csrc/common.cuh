@@ -61,7 +61,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Same wait with cluster-scope acquire: for barriers completed by remote
-// CTAs (st.async complete-tx, remote arrives) whose data this thread reads.
+// CTAs (remote arrivals) after which this thread reads their data.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -114,12 +114,6 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
-
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
     return pol;
 }
 
@@ -181,13 +175,6 @@ __device__ __forceinline__ uint32_t map_to_cta(uint32_t smem_addr, uint32_t rank
     return r;
 }
 
-// Load a float from another CTA's shared memory (cluster window address).
-__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
-}
-
 // Store two floats into another CTA's shared memory (cluster window address).
 __device__ __forceinline__ void st_cluster_v2f(uint32_t addr, float a, float b) {
     asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b)
@@ -201,42 +188,6 @@ __device__ __forceinline__ void cluster_arrive() {
 
 __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Asynchronous store of two floats into another CTA's shared memory; the
-// 8 bytes complete-tx on the mbarrier `remote_bar` of that CTA.
-__device__ __forceinline__ void st_async_v2(uint32_t remote_addr, float a, float b,
-                                            uint32_t remote_bar) {
-    asm volatile(
-        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
-            remote_addr),
-        "f"(a), "f"(b), "r"(remote_bar)
-        : "memory");
-}
-
-// Bulk copy from this CTA's shared memory into another CTA's shared memory
-// (addresses of the cluster window), completing on that CTA's mbarrier.
-__device__ __forceinline__ void bulk_s2s_cluster(uint32_t remote_dst, uint32_t local_src,
-                                                 uint32_t bytes, uint32_t remote_bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
-        "[%3];" ::"r"(remote_dst),
-        "r"(local_src), "r"(bytes), "r"(remote_bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit_group() {
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-// Wait until at most N committed bulk groups still read their source.
-template <int N>
-__device__ __forceinline__ void bulk_wait_group_read() {
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ void sts_v2f(uint32_t addr, float a, float b) {
-    asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
 }
 
 // Arrive (release, cluster scope) on an mbarrier of another CTA.
