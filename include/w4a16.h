@@ -161,8 +161,10 @@ enum { W4A16_PATH_GEMV = 1, W4A16_PATH_TENSOR_CORE = 2 };
  *   *path            W4A16_PATH_GEMV (M <= 16) or W4A16_PATH_TENSOR_CORE.
  *   *splits          the thread-block cluster size: for the GEMV, the CTAs
  *                    sharing the K range of one 128-row block (1 = no
- *                    split); for the tensor-core GEMM, 2 when CTA pairs
- *                    compute 256 x 256 tiles with 2-CTA MMAs, else 1.
+ *                    split); for the tensor-core GEMM, 1 (a CTA per
+ *                    128 x 128 tile), 2 (CTA pairs with 2-CTA MMAs) or 4 / 8
+ *                    (CTA pairs splitting K 2 / 4 ways, reduced through the
+ *                    cluster's shared memory).
  *   *ctas            CTAs launched.
  *   *blocks_per_cta  most 128-row blocks one CTA walks (> 1: persistent).
  * Errors: NULL output -> W4A16_ERR_NULL; bad M, N, K -> W4A16_ERR_SHAPE;

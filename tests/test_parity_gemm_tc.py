@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import assert_close, from_bits16
+from gpu_util import assert_close, bits16, from_bits16
 from parity_data import acts, as_device, quantized, sample_rows
 import w4a16_weight_only_gemm_gb300 as w4
 from w4a16_weight_only_gemm_gb300 import synthetic, workloads
@@ -71,16 +71,39 @@ def test_guard_bands(w4lib):
     assert_close(y.float().cpu().numpy(), oracle.gemm(x16, q, s), "guard")
 
 
-@pytest.mark.parametrize("M,N,K", [(300, 19000, 384), (200, 40000, 256), (512, 38400, 128)])
+@pytest.mark.parametrize("M,N,K", [(300, 19000, 384), (200, 19300, 256), (512, 38400, 128)])
 def test_cta_pair_path(w4lib, M, N, K):
-    """256 x 256 tiles on CTA pairs (2-CTA MMAs): an odd number of 128-row
-    weight blocks (the last pair's odd CTA holds none), ragged M; every
-    output compared."""
+    """Tiles on CTA pairs (2-CTA MMAs): 512 x 256 and 256 x 256, an odd
+    number of 128-row weight blocks (the last pair's odd CTA holds none),
+    ragged M; every output compared."""
     plan = w4.gemm_plan(M, N, K)
     assert plan["path"] == "tensor_core" and plan["splits"] == 2, plan
     w16, q, s = quantized(N, K, 81)
     x16 = acts(M, K, 82)
     assert_close(run_gemm(x16, q, s), oracle.gemm(x16, q, s), f"M={M} N={N} K={K} {plan}")
+
+
+@pytest.mark.parametrize("M,N,K,cluster", [(300, 8000, 1920, 4), (300, 1000, 18944, 8),
+                                           (300, 136, 18944, 8)])
+def test_split_k_path(w4lib, M, N, K, cluster):
+    """CTA pairs splitting K two or four ways, the splits of a tile reducing
+    through the cluster's shared memory (ragged M; a pair whose odd CTA holds
+    no weights): every output compared, and two calls give the same bits
+    (the reduction order is fixed)."""
+    plan = w4.gemm_plan(M, N, K)
+    assert plan["path"] == "tensor_core" and plan["splits"] == cluster, plan
+    w16, q, s = quantized(N, K, 91)
+    x16 = acts(M, K, 92)
+    qt, st = as_device(q, s)
+    r = w4.repack(qt)
+    x = from_bits16(x16)
+    y1 = w4.gemm(x, r, st)
+    y2 = w4.gemm(x, r, st)
+    torch.cuda.synchronize()
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    assert_close(y1.float().cpu().numpy().astype(np.float64), oracle.gemm(x16, q, s),
+                 f"M={M} N={N} K={K} {plan}")
+    assert w4.device_status() == 0
 
 
 @pytest.mark.parametrize("idx", range(len(workloads.PREFILL)))

@@ -181,6 +181,15 @@ __device__ __forceinline__ void st_cluster_v2f(uint32_t addr, float a, float b) 
                  : "memory");
 }
 
+// Store four 32-bit words into another CTA's shared memory (16-byte aligned
+// cluster window address).
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                              uint32_t d) {
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b),
+                 "r"(c), "r"(d)
+                 : "memory");
+}
+
 // Split cluster barrier: every thread of every CTA arrives, later waits.
 __device__ __forceinline__ void cluster_arrive() {
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");

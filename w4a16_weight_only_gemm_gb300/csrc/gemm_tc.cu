@@ -33,6 +33,7 @@
 // Every wait is bounded; tensor memory is freed on every path.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -60,6 +61,10 @@ constexpr int kBarAcc = kBarFree + 8 * kMaxStages;
 constexpr int kBarSlab = kBarAcc + 8;
 constexpr int kTmemSlot = kBarSlab + 8;
 constexpr int kAbortFlag = kTmemSlot + 8;
+// Split-K reduction: per source split, 128 rows of 64 FP32 columns padded to
+// 68 (16-byte accesses of 8 consecutive rows hit distinct banks).
+constexpr int kRedRow = 68;
+constexpr int kRedSlotFloats = 128 * kRedRow;
 constexpr int kOffA = 1024;                              // dequantised tiles
 // then x tiles, packed weights and the scale slab at offsets set per launch
 
@@ -72,6 +77,11 @@ struct TcArgs {
     int M, N, K, G;
     int nst;                           // ring stages (<= kMaxStages)
     uint32_t off_x, off_w, off_slab;   // shared-memory offsets after the window base
+    // Split K (pairs only, splits > 1): blockIdx.z takes k-blocks
+    // [z nkb / splits, (z + 1) nkb / splits); the splits of a tile form one
+    // thread-block cluster (2 x splits CTAs) and reduce their accumulators
+    // through distributed shared memory.
+    int splits;
 };
 
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -84,6 +94,28 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, __half2 s) {
     __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&a), s);
     return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Rounds 32 FP32 accumulators to fp16 and stores them at y[m, n .. n + 31]
+// (64 contiguous bytes when N allows, else element by element up to N).
+__device__ __forceinline__ void store_y32(const TcArgs& a, int m, int n, const uint32_t (&v)[32]) {
+    if (m >= a.M) return;
+    __half* yrow = a.y + (size_t)m * a.N;
+    if (n + 32 <= a.N && (a.N & 7) == 0) {
+        uint32_t h[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            __half2 p2 = __floats2half2_rn(__uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1]));
+            h[c] = *reinterpret_cast<uint32_t*>(&p2);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(yrow + n);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) dst[c] = make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+    } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+            if (n + c < a.N) yrow[n + c] = __float2half_rn(__uint_as_float(v[c]));
+    }
 }
 
 // Byte offset of the 16-byte chunk `c` of row `r` in a 128-byte swizzled,
@@ -117,15 +149,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     constexpr int kXBytes = XT * kXStageBytes;                     // x bytes per stage
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int rank = PAIR ? (int)(cluster_cta_rank() & 1) : 0;
+    // Cluster rank: CTA pairs are ranks (2 j, 2 j + 1); with split K the
+    // cluster holds the pairs of all splits of one tile (split = rank / 2).
+    const uint32_t crank = PAIR ? cluster_cta_rank() : 0u;
+    const int rank = (int)(crank & 1u);
+    const uint32_t lead = crank & ~1u;  // the pair's even CTA: issues its MMAs
     const bool leader = rank == 0;
+    const uint16_t pair_mask = (uint16_t)(3u << lead);
     // This CTA's 128-row weight block and first x row; y columns start at n_out.
     const int rb = PAIR ? (int)blockIdx.x : (int)blockIdx.x;
     const int n_out = PAIR ? ((int)blockIdx.x >> 1) * 2 * kTileW : (int)blockIdx.x * kTileW;
     const int m0 = PAIR ? (int)blockIdx.y * 2 * kTileX * XT + rank * kTileX : (int)blockIdx.y * kTileX;
     const int NB = (a.N + kTileW - 1) / kTileW;
     const bool wvalid = rb < NB;  // the odd CTA of the last pair may hold no weights
-    const int nkb = a.K / kBK;
+    // this CTA's k-blocks: kb0 .. kb0 + nkb - 1 (all of K unless split)
+    const int kb0 = (int)(((long long)blockIdx.z * (a.K / kBK)) / a.splits);
+    const int nkb = (int)((((long long)blockIdx.z + 1) * (a.K / kBK)) / a.splits) - kb0;
     // The single-CTA tile always runs kSingleStages stages at fixed offsets
     // (compile-time constants there); pairs size their ring per launch.
     const int NS = PAIR ? a.nst : kSingleStages;
@@ -170,7 +209,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ============================ TMA producer ============================
         if (lane == 0) {
             tma_prefetch_map(&xmap);
-            const uint8_t* w = a.wq + (size_t)rb * nkb * kWStageBytes;
+            const uint8_t* w = a.wq + ((size_t)rb * (a.K / kBK) + kb0) * kWStageBytes;
             if (wvalid)
                 for (int i = 0; i < NS && i < nkb; ++i)
                     bulk_prefetch_l2(w + (size_t)i * kWStageBytes, kWStageBytes);
@@ -202,7 +241,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                       kXBytes + (wvalid ? kWStageBytes : 0));
 #pragma unroll
                 for (int xt = 0; xt < XT; ++xt)
-                    tma_load_2d(base + kOffX + ts * kXBytes + xt * kXStageBytes, &xmap, i * kBK,
+                    tma_load_2d(base + kOffX + ts * kXBytes + xt * kXStageBytes, &xmap, (kb0 + i) * kBK,
                                 m0 + xt * 2 * kTileX, base + kBarLoadFull + 8 * ts);
                 if (wvalid)
                     bulk_g2s(base + kOffW + ts * kWStageBytes, w + (size_t)i * kWStageBytes,
@@ -254,7 +293,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 // stage reusable (in both CTAs of a pair) once these MMAs finish
                 if (PAIR)
-                    tc_commit_pair_multicast(base + kBarFree + 8 * ts, 0x3);
+                    tc_commit_pair_multicast(base + kBarFree + 8 * ts, pair_mask);
                 else
                     tc_commit(base + kBarFree + 8 * ts);
                 if (++ts == NS) {
@@ -264,7 +303,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             // completes once every issued MMA has
             if (PAIR)
-                tc_commit_pair_multicast(base + kBarAcc, 0x3);
+                tc_commit_pair_multicast(base + kBarAcc, pair_mask);
             else
                 tc_commit(base + kBarAcc);
             if (!ok) *abort_flag = 1;
@@ -279,7 +318,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int r0 = dw * 16 + g, r1 = r0 + 8;
         const __half* slab = reinterpret_cast<const __half*>(smem + kOffSlab);
         // the stage barrier lives in the even CTA of a pair
-        const uint32_t afull0 = PAIR ? map_to_cta(base + kBarAFull, 0) : base + kBarAFull;
+        const uint32_t afull0 = PAIR ? map_to_cta(base + kBarAFull, lead) : base + kBarAFull;
         if (PAIR && !leader) {
             cluster_wait();
             cl_waited = true;
@@ -296,7 +335,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 break;
             }
             if (wvalid) {
-                const int grp = i >> 1;  // two 64-wide k-blocks per scale group
+                const int grp = (kb0 + i) >> 1;  // two 64-wide k-blocks per scale group
                 const uint32_t wst = base + kOffW + ts * kWStageBytes;
                 const uint32_t ast = base + kOffA + ts * kAStageBytes;
                 const uint4 pk = lds128(wst + (dw * 32 + lane) * 16);
@@ -339,40 +378,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!ok) *abort_flag = 1;
 
         // ------------------------------ epilogue ------------------------------
-        if (mbar_wait(base + kBarAcc, 0, a.timeout_ns, a.status)) {
-            tc_fence_after_sync();
-            const int q = warp & 3;           // TMEM lane quarter = rows of y
-            const int cc = (warp - 4) >> 2;   // column chunk = weight rows
-            constexpr int kChunkCols = (int)kCols / 4;  // 32 (single), 64 or 128 (pair)
+        const bool acc_ok = mbar_wait(base + kBarAcc, 0, a.timeout_ns, a.status);
+        if (acc_ok) tc_fence_after_sync();
+        const int q = warp & 3;           // TMEM lane quarter = rows of y
+        const int cc = (warp - 4) >> 2;   // column chunk = weight rows
+        constexpr int kChunkCols = (int)kCols / 4;  // 32 (single), 64 or 128 (pair)
+        const int row = q * 32 + lane;    // accumulator row (TMEM lane)
+        if (a.splits == 1) {  // split K: reduced over the cluster below
+            if (acc_ok) {
 #pragma unroll
-            for (int half = 0; half < kChunkCols / 32; ++half) {
-                const int col = cc * kChunkCols + half * 32;
-                // pair: columns 256 t .. belong to MMA t, i.e. x rows m0 + 256 t
-                const int xt = PAIR ? col / (2 * kTileW) : 0;
-                const int n = n_out + (PAIR ? col % (2 * kTileW) : col);
-                const int m = m0 + xt * 2 * kTileX + q * 32 + lane;
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)col, v);
-                tmem_ld_wait();
-                if (m < a.M) {
-                    __half* yrow = a.y + (size_t)m * a.N;
-                    if (n + 32 <= a.N && (a.N & 7) == 0) {
-                        uint32_t h[16];
-#pragma unroll
-                        for (int c = 0; c < 16; ++c) {
-                            __half2 p2 = __floats2half2_rn(__uint_as_float(v[2 * c]),
-                                                           __uint_as_float(v[2 * c + 1]));
-                            h[c] = *reinterpret_cast<uint32_t*>(&p2);
-                        }
-                        uint4* dst = reinterpret_cast<uint4*>(yrow + n);
-#pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            dst[c] = make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < 32; ++c)
-                            if (n + c < a.N) yrow[n + c] = __float2half_rn(__uint_as_float(v[c]));
-                    }
+                for (int half = 0; half < kChunkCols / 32; ++half) {
+                    const int col = cc * kChunkCols + half * 32;
+                    // pair: columns 256 t .. belong to MMA t, i.e. x rows m0 + 256 t
+                    const int xt = PAIR ? col / (2 * kTileW) : 0;
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)col, v);
+                    tmem_ld_wait();
+                    store_y32(a, m0 + xt * 2 * kTileX + row, n_out + (PAIR ? col % (2 * kTileW) : col),
+                              v);
                 }
             }
         }
@@ -381,9 +404,72 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_before_sync();
     __syncthreads();
     if (PAIR) {
-        // Neither CTA frees its tensor memory or leaves while the pair's
-        // MMAs or the peer's arrivals may still touch it.
         if (!cl_waited) cluster_wait();
+        if (a.splits > 1) {
+            // Split-K reduction over the cluster.  Split z owns columns
+            // [z part, (z + 1) part) of the tile; in rounds of 64 columns every
+            // CTA pushes its partial of each split's columns (its own
+            // included) into slot z of that split's ring memory (free now:
+            // all MMAs of the cluster are done), and each owner sums its S
+            // slots in split order and writes y.  Every thread joins the
+            // cluster barriers; warps 4..19 move the data, each reading only
+            // its own TMEM lane quarter.
+            tc_fence_after_sync();
+            const int S = a.splits, z = (int)blockIdx.z;
+            const int part = (int)kCols / S;
+            float* recv = reinterpret_cast<float*>(smem + kOffA);
+            const uint32_t recv_u32 = base + kOffA;
+            const int q = warp & 3, wq = (warp - 4) >> 2;  // quarter; warp index within it
+            const int row = q * 32 + lane;
+#pragma unroll 1
+            for (int r = 0; r < part / 64; ++r) {
+                cluster_sync_all();  // mainloops done / previous round's slices read
+                if (warp >= 4) {
+#pragma unroll 1
+                    for (int task = wq; task < 2 * S; task += 4) {
+                        const int d = task >> 1, c = task & 1;  // destination split, 32-column half
+                        const int col = d * part + r * 64 + c * 32;
+                        uint32_t v[32];
+                        tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)col, v);
+                        tmem_ld_wait();
+                        const uint32_t dst = map_to_cta(
+                            recv_u32 + (uint32_t)((z * kRedSlotFloats + row * kRedRow + c * 32) * 4),
+                            (uint32_t)(2 * d + rank));
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            st_cluster_v4(dst + 16 * e, v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+                    }
+                }
+                cluster_sync_all();  // every slice of this round has landed
+                if (warp >= 4 && wq < 2) {
+                    const int col = z * part + r * 64 + wq * 32;
+                    float sum[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) sum[e] = 0.0f;
+#pragma unroll 1
+                    for (int zz = 0; zz < S; ++zz) {
+                        const float4* src = reinterpret_cast<const float4*>(
+                            recv + zz * kRedSlotFloats + row * kRedRow + wq * 32);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float4 f = src[e];
+                            sum[4 * e] += f.x;
+                            sum[4 * e + 1] += f.y;
+                            sum[4 * e + 2] += f.z;
+                            sum[4 * e + 3] += f.w;
+                        }
+                    }
+                    uint32_t v[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(sum[e]);
+                    const int xt = col / (2 * kTileW);
+                    store_y32(a, m0 + xt * 2 * kTileX + row, n_out + col % (2 * kTileW), v);
+                }
+            }
+            tc_fence_before_sync();
+        }
+        // Neither CTA frees its tensor memory or leaves while the pair's
+        // MMAs, the peer's arrivals or the cluster's pushes may still touch it.
         cluster_sync_all();
     }
     if (warp == 1) {
@@ -417,44 +503,145 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 //    every SM;
 //  * otherwise one CTA per 128 x 128 tile (cluster 1).
 struct TcPlan {
-    int cluster = 1, xt = 1;
+    int cluster = 1, xt = 1, splits = 1;
     unsigned gx = 0, gy = 0;
     long long ctas = 0;
 };
 
-TcPlan tc_plan(int64_t M, int64_t N, const DeviceCtx& ctx) {
-    TcPlan p;
+int max_active_clusters(const void* fn, int cluster_z, uint32_t smem) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, (unsigned)cluster_z);
+    cfg.blockDim = dim3(kTcThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = (unsigned)cluster_z;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) return 0;
+    return n;
+}
+
+// Shared memory of a launch: `nst` ring stages with xt x tiles each, next to
+// the scale slab, +1 KB slack for aligning the window to 1024 bytes.
+uint32_t tc_smem(int nst, int xt, int G) {
+    const uint32_t slab = ((kTileW * G * 2 + 127) / 128) * 128;
+    const uint32_t stage = (uint32_t)(kAStageBytes + xt * kXStageBytes + kWStageBytes);
+    return kOffA + (uint32_t)nst * stage + slab + 1024;
+}
+
+// Pairs take as many ring stages as fit: a deeper ring hides more of the
+// copy -> dequantise -> MMA -> release round trip.  The single-CTA tile keeps
+// kSingleStages (deeper measured slower there).
+int tc_stages(const TcPlan& p, int G, const DeviceCtx& ctx) {
+    if (p.cluster == 1) return kSingleStages;
+    int nst = kMaxStages;
+    while (nst > 2 && tc_smem(nst, p.xt, G) > (uint32_t)ctx.max_smem_optin) --nst;
+    return nst;
+}
+
+// Launch shape of the tensor-core GEMM for (M, N, K), the cheapest of:
+//  * one CTA per 128 x 128 tile (cluster 1);
+//  * CTA pairs with 256 x 256 tiles (xt = 1, cluster 2), M > 128;
+//  * CTA pairs with 512 x-row x 256 weight-row tiles (xt = 2), M > 256 --
+//    the most MMA work per stage hand-off;
+//  * the latter splitting K two or four ways (every k-range >= 8 k-blocks),
+//    the splits of a tile forming one cluster (4 or 8 CTAs) that reduces
+//    through distributed shared memory; only when the whole grid is
+//    co-resident.
+// Cost = waves x k-blocks per CTA x the measured time of one k-block of the
+// tile on a busy GPU (about 0.36, 0.63 and 0.84 us at M = 512), plus about a
+// microsecond per 64-column round of a split reduction.
+TcPlan tc_plan(int64_t M, int64_t N, int64_t K, const DeviceCtx& ctx) {
+    constexpr double kSingleKb = 0.36, kPairKb = 0.63, kPair2Kb = 0.84, kRound = 1.0;
     const int NB = (int)((N + kTileW - 1) / kTileW);
     const long long pairs = (NB + 1) / 2;
-    if (NB >= 2) {
-        const long long c2 = 2 * pairs * ((M + 4 * kTileX - 1) / (4 * kTileX));
-        const long long c1 = 2 * pairs * ((M + 2 * kTileX - 1) / (2 * kTileX));
-        if (M > 2 * kTileX && 2 * c2 >= ctx.num_sms) {
-            p.cluster = 2;
-            p.xt = 2;
-            p.gx = (unsigned)(2 * pairs);
-            p.gy = (unsigned)((M + 4 * kTileX - 1) / (4 * kTileX));
-            p.ctas = c2;
-            return p;
-        }
-        if (M > kTileX && c1 >= ctx.num_sms) {
-            p.cluster = 2;
-            p.gx = (unsigned)(2 * pairs);
-            p.gy = (unsigned)((M + 2 * kTileX - 1) / (2 * kTileX));
-            p.ctas = c1;
-            return p;
+    const long long nkb = K / kBK;
+    const int G = (int)(K / kGroup);
+    auto waves = [&](long long ctas) { return (double)((ctas + ctx.num_sms - 1) / ctx.num_sms); };
+
+    TcPlan best;  // single-CTA tiles
+    best.gx = (unsigned)NB;
+    best.gy = (unsigned)((M + kTileX - 1) / kTileX);
+    best.ctas = (long long)best.gx * best.gy;
+    double t_best = waves(best.ctas) * nkb * kSingleKb;
+    if (NB < 2) return best;
+
+    if (M > kTileX) {
+        TcPlan p;
+        p.cluster = 2;
+        p.gx = (unsigned)(2 * pairs);
+        p.gy = (unsigned)((M + 2 * kTileX - 1) / (2 * kTileX));
+        p.ctas = (long long)p.gx * p.gy;
+        const double t = waves(p.ctas) * nkb * kPairKb;
+        if (t < t_best) {
+            t_best = t;
+            best = p;
         }
     }
-    p.gx = (unsigned)NB;
-    p.gy = (unsigned)((M + kTileX - 1) / kTileX);
-    p.ctas = (long long)p.gx * p.gy;
-    return p;
+    if (M > 2 * kTileX) {
+        TcPlan p;
+        p.cluster = 2;
+        p.xt = 2;
+        p.gx = (unsigned)(2 * pairs);
+        p.gy = (unsigned)((M + 4 * kTileX - 1) / (4 * kTileX));
+        p.ctas = (long long)p.gx * p.gy;
+        double t = waves(p.ctas) * nkb * kPair2Kb;
+        if (t < t_best) {
+            t_best = t;
+            best = p;
+        }
+        const int nst = tc_stages(p, G, ctx);
+        const uint32_t smem = tc_smem(nst, 2, G);
+        const uint32_t ring = (uint32_t)nst * (kAStageBytes + 2 * kXStageBytes + kWStageBytes);
+        for (int S = 2; S <= 4; S *= 2) {
+            const long long ctas = p.ctas * S;
+            if (ctas > ctx.num_sms || nkb < 8 * S) continue;
+            // the S receive slots of the reduction live in the ring
+            if ((uint32_t)S * kRedSlotFloats * 4 > ring) continue;
+            const long long fit =
+                (long long)max_active_clusters((const void*)gemm_tc_kernel<true, 2>, S, smem);
+            if (fit * 2 * S < ctas) continue;  // not one co-resident wave
+            t = (double)((nkb + S - 1) / S) * kPair2Kb + kRound * (4 * kTileW / S / 64 + 1);
+            if (t < t_best) {
+                t_best = t;
+                best = p;
+                best.splits = S;
+                best.cluster = 2 * S;
+                best.ctas = ctas;
+            }
+        }
+    }
+    return best;
+}
+
+cudaError_t ensure_tc_attrs(const DeviceCtx& ctx) {
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && attr_done[dev]) return cudaSuccess;
+    for (auto fn : {gemm_tc_kernel<false, 1>, gemm_tc_kernel<true, 1>, gemm_tc_kernel<true, 2>}) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             ctx.max_smem_optin);
+        if (e != cudaSuccess) return e;
+    }
+    if (dev >= 0 && dev < 64) attr_done[dev] = true;
+    return cudaSuccess;
 }
 
 }  // namespace
 
-void gemm_tc_plan_info(int64_t M, int64_t N, const DeviceCtx& ctx, int* cluster, int* ctas) {
-    const TcPlan p = tc_plan(M, N, ctx);
+void gemm_tc_plan_info(int64_t M, int64_t N, int64_t K, const DeviceCtx& ctx, int* cluster,
+                       int* ctas) {
+    if (ensure_tc_attrs(ctx) != cudaSuccess) {
+        *cluster = 0;
+        *ctas = 0;
+        return;
+    }
+    const TcPlan p = tc_plan(M, N, K, ctx);
     *cluster = p.cluster;
     *ctas = (int)p.ctas;
 }
@@ -463,18 +650,11 @@ cudaError_t launch_gemm_tc(const void* x, const void* repacked, const void* scal
                            int64_t M, int64_t N, int64_t K, cudaStream_t stream,
                            const DeviceCtx& ctx) {
     const int G = (int)(K / kGroup);
-    const TcPlan plan = tc_plan(M, N, ctx);
-    // Ring stages next to the scale slab (+1 KB slack for aligning the window
-    // to 1024 bytes).  Pairs take as many as fit: a deeper ring hides more of
-    // the copy -> dequantise -> MMA -> release round trip.  The single-CTA
-    // tile keeps 4 (deeper measured slower there).
-    const uint32_t slab = ((kTileW * G * 2 + 127) / 128) * 128;
-    const uint32_t stage = (uint32_t)(kAStageBytes + plan.xt * kXStageBytes + kWStageBytes);
-    int nst = plan.cluster == 2 ? kMaxStages : kSingleStages;
-    while (plan.cluster == 2 && nst > 2 &&
-           kOffA + (uint32_t)nst * stage + slab + 1024 > (uint32_t)ctx.max_smem_optin)
-        --nst;
-    const uint32_t smem = kOffA + (uint32_t)nst * stage + slab + 1024;
+    cudaError_t e = ensure_tc_attrs(ctx);
+    if (e != cudaSuccess) return e;
+    const TcPlan plan = tc_plan(M, N, K, ctx);
+    const int nst = tc_stages(plan, G, ctx);
+    const uint32_t smem = tc_smem(nst, plan.xt, G);
     if ((int)smem > ctx.max_smem_optin) return cudaErrorInvalidValue;
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
@@ -488,17 +668,6 @@ cudaError_t launch_gemm_tc(const void* x, const void* repacked, const void* scal
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
 
-    static bool attr_done[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        for (auto fn : {gemm_tc_kernel<false, 1>, gemm_tc_kernel<true, 1>, gemm_tc_kernel<true, 2>}) {
-            cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 ctx.max_smem_optin);
-            if (e != cudaSuccess) return e;
-        }
-        attr_done[dev] = true;
-    }
     TcArgs args{};
     args.wq = static_cast<const uint8_t*>(repacked);
     args.scales = static_cast<const __half*>(scales);
@@ -513,9 +682,10 @@ cudaError_t launch_gemm_tc(const void* x, const void* repacked, const void* scal
     args.off_x = kOffA + (uint32_t)nst * kAStageBytes;
     args.off_w = args.off_x + (uint32_t)nst * plan.xt * kXStageBytes;
     args.off_slab = args.off_w + (uint32_t)nst * kWStageBytes;
+    args.splits = plan.splits;
 
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(plan.gx, plan.gy, 1);
+    cfg.gridDim = dim3(plan.gx, plan.gy, (unsigned)plan.splits);
     cfg.blockDim = dim3(kTcThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
@@ -525,9 +695,9 @@ cudaError_t launch_gemm_tc(const void* x, const void* repacked, const void* scal
     attrs[1].id = cudaLaunchAttributeClusterDimension;
     attrs[1].val.clusterDim.x = 2;
     attrs[1].val.clusterDim.y = 1;
-    attrs[1].val.clusterDim.z = 1;
+    attrs[1].val.clusterDim.z = (unsigned)plan.splits;
     cfg.attrs = attrs;
-    cfg.numAttrs = plan.cluster == 2 ? 2 : 1;
+    cfg.numAttrs = plan.cluster > 1 ? 2 : 1;
     if (plan.cluster == 1) return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<false, 1>, map, args);
     if (plan.xt == 1) return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true, 1>, map, args);
     return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true, 2>, map, args);
