@@ -540,7 +540,9 @@ GemvPlan plan_gemv(int M, int N, int K, const DeviceCtx& ctx) {
             S == 1 ? (long long)ctx.num_sms * occ : (long long)max_active_clusters<MT>(S, p.smem) * S;
         const long long heaviest = (units + ctx.num_sms - 1) / ctx.num_sms;
         double eff = per_sm / ((double)heaviest / S);
-        if (units > slots) eff *= 0.85;  // more than one wave of CTAs
+        // more than one wave of CTAs: each wave pays its own start-up and
+        // x / reduction latency, so count every wave as a whole pass
+        if (units > slots) eff /= (double)((units + slots - 1) / slots);
         eff += 0.001 * S;
         p.grid_y = NB;
         p.eff = eff;
