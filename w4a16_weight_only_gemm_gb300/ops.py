@@ -7,6 +7,7 @@ arithmetic of the method happens here.
 from __future__ import annotations
 
 import ctypes
+import functools
 
 import torch
 
@@ -41,6 +42,7 @@ def quantize(W: torch.Tensor, group: int = GROUP, stream=None):
     return q, s
 
 
+@functools.lru_cache(maxsize=1024)
 def repacked_bytes(N: int, K: int) -> int:
     n = _native.lib().w4a16_repacked_bytes(N, K)
     if n < 0:
@@ -71,18 +73,23 @@ def unrepack(repacked: torch.Tensor, N: int, K: int, stream=None) -> torch.Tenso
     return q
 
 
-def gemm(x: torch.Tensor, repacked: torch.Tensor, scales: torch.Tensor,
-         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """y[M, N] = x[M, K] @ dequant(W)^T; W given as kernel-layout bytes + scales [N, K/128]."""
-    _need(x, torch.float16, "x")
+def _check_weights(repacked: torch.Tensor, scales: torch.Tensor) -> tuple[int, int]:
     _need(repacked, torch.uint8, "repacked")
     _need(scales, torch.float16, "scales")
-    M, K = x.shape
-    N = scales.shape[0]
-    if scales.shape[1] * GROUP != K:
-        raise ValueError("scales and x disagree on K")
-    if repacked.numel() != repacked_bytes(N, K):
-        raise ValueError("repacked buffer size does not match N, K")
+    N, G = scales.shape
+    if repacked.numel() != repacked_bytes(N, G * GROUP):
+        raise ValueError("repacked buffer size does not match the scales' N, K")
+    return N, G * GROUP
+
+
+def _gemm(x: torch.Tensor, repacked: torch.Tensor, scales: torch.Tensor, N: int, K: int,
+          out: torch.Tensor | None, stream) -> torch.Tensor:
+    _need(x, torch.float16, "x")
+    if x.dim() != 2 or x.shape[1] != K:
+        raise ValueError(f"x must be [M, {K}]")
+    if x.device != scales.device:
+        raise ValueError("x and the weights are on different devices")
+    M = x.shape[0]
     if out is None:
         out = torch.empty((M, N), dtype=torch.float16, device=x.device)
     else:
@@ -91,8 +98,16 @@ def gemm(x: torch.Tensor, repacked: torch.Tensor, scales: torch.Tensor,
             raise ValueError("out has the wrong shape")
     rc = _native.lib().w4a16_gemm(x.data_ptr(), repacked.data_ptr(), scales.data_ptr(),
                                   out.data_ptr(), M, N, K, _stream_ptr(stream))
-    _native.check(rc, "w4a16_gemm")
+    if rc:
+        _native.check(rc, "w4a16_gemm")
     return out
+
+
+def gemm(x: torch.Tensor, repacked: torch.Tensor, scales: torch.Tensor,
+         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y[M, N] = x[M, K] @ dequant(W)^T; W given as kernel-layout bytes + scales [N, K/128]."""
+    N, K = _check_weights(repacked, scales)
+    return _gemm(x, repacked, scales, N, K, out, stream)
 
 
 def gemm_plan(M: int, N: int, K: int) -> dict:
@@ -131,5 +146,7 @@ class W4A16Linear:
         q, self.scales = quantize(W)
         self.repacked = repack(q)
 
-    def __call__(self, x: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
-        return gemm(x, self.repacked, self.scales, out=out)
+    def __call__(self, x: torch.Tensor, out: torch.Tensor | None = None,
+                 stream=None) -> torch.Tensor:
+        # the weights were checked when they were made: only x / out here
+        return _gemm(x, self.repacked, self.scales, self.N, self.K, out, stream)
