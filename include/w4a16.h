@@ -162,8 +162,8 @@ enum { W4A16_PATH_GEMV = 1, W4A16_PATH_TENSOR_CORE = 2 };
  *   *splits          the thread-block cluster size: for the GEMV, the CTAs
  *                    sharing the K range of one 128-row block (1 = no
  *                    split); for the tensor-core GEMM, 1 (a CTA per
- *                    128 x 128 tile), 2 (CTA pairs with 2-CTA MMAs) or 4 / 8
- *                    (CTA pairs splitting K 2 / 4 ways, reduced through the
+ *                    128 x 128 tile), 2 (CTA pairs with 2-CTA MMAs) or 4, 6, 8
+ *                    (CTA pairs splitting K 2, 3, 4 ways, reduced through the
  *                    cluster's shared memory).
  *   *ctas            CTAs launched.
  *   *blocks_per_cta  most 128-row blocks one CTA walks (> 1: persistent).

@@ -83,10 +83,10 @@ def test_cta_pair_path(w4lib, M, N, K):
     assert_close(run_gemm(x16, q, s), oracle.gemm(x16, q, s), f"M={M} N={N} K={K} {plan}")
 
 
-@pytest.mark.parametrize("M,N,K,cluster", [(300, 8000, 1920, 4), (300, 1000, 18944, 8),
-                                           (300, 136, 18944, 8)])
+@pytest.mark.parametrize("M,N,K,cluster", [(300, 8000, 1920, 4), (300, 4000, 16384, 6),
+                                           (300, 1000, 18944, 8), (300, 136, 18944, 8)])
 def test_split_k_path(w4lib, M, N, K, cluster):
-    """CTA pairs splitting K two or four ways, the splits of a tile reducing
+    """CTA pairs splitting K two, three or four ways, the splits of a tile reducing
     through the cluster's shared memory (ragged M; a pair whose odd CTA holds
     no weights): every output compared, and two calls give the same bits
     (the reduction order is fixed)."""

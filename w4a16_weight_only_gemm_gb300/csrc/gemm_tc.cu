@@ -82,6 +82,11 @@ struct TcArgs {
     // thread-block cluster (2 x splits CTAs) and reduce their accumulators
     // through distributed shared memory.
     int splits;
+    // Scale slab: slab_ld groups per row.  slab_tma = 1: a 2-D tensor-map copy
+    // of the 128 rows x slab_ld groups starting at this CTA's first group
+    // rounded down to 8 (a split's own groups only); else the whole
+    // [128][G] slab by bulk copy (slab_ld = G).
+    int slab_ld, slab_tma;
 };
 
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -136,7 +141,8 @@ __device__ __forceinline__ uint32_t swz128(int r, int c) {
 // stage hand-off covers XT times more MMA work.
 template <bool PAIR, int XT>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ TcArgs a) {
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap smap,
+                   const __grid_constant__ TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     // Swizzled tiles need 1024-byte alignment: align the window by hand.
     const uint32_t raw = smem_u32(smem_raw);
@@ -165,6 +171,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // this CTA's k-blocks: kb0 .. kb0 + nkb - 1 (all of K unless split)
     const int kb0 = (int)(((long long)blockIdx.z * (a.K / kBK)) / a.splits);
     const int nkb = (int)((((long long)blockIdx.z + 1) * (a.K / kBK)) / a.splits) - kb0;
+    const int slab_g0 = a.slab_tma ? ((kb0 >> 1) & ~7) : 0;  // first group held in the slab
     // The single-CTA tile always runs kSingleStages stages at fixed offsets
     // (compile-time constants there); pairs size their ring per launch.
     const int NS = PAIR ? a.nst : kSingleStages;
@@ -214,7 +221,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int i = 0; i < NS && i < nkb; ++i)
                     bulk_prefetch_l2(w + (size_t)i * kWStageBytes, kWStageBytes);
             grid_dependency_wait();
-            {   // the block's scale slab (rows x G fp16, contiguous)
+            if (a.slab_tma) {  // this split's groups of the block's 128 rows
+                mbar_arrive_expect_tx(base + kBarSlab, (uint32_t)(kTileW * a.slab_ld * 2));
+                tma_load_2d(base + kOffSlab, &smap, slab_g0, rb * kTileW, base + kBarSlab);
+            } else {  // the block's scale slab (rows x G fp16, contiguous)
                 const int rows = max(0, min(kTileW, a.N - rb * kTileW));
                 const uint32_t bytes = (uint32_t)(rows * a.G * 2);
                 const uint32_t bulk = bytes & ~15u;
@@ -339,8 +349,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const uint32_t wst = base + kOffW + ts * kWStageBytes;
                 const uint32_t ast = base + kOffA + ts * kAStageBytes;
                 const uint4 pk = lds128(wst + (dw * 32 + lane) * 16);
-                const __half2 s0 = __half2half2(slab[r0 * a.G + grp]);
-                const __half2 s1 = __half2half2(slab[r1 * a.G + grp]);
+                const __half2 s0 = __half2half2(slab[r0 * a.slab_ld + grp - slab_g0]);
+                const __half2 s1 = __half2half2(slab[r1 * a.slab_ld + grp - slab_g0]);
                 const uint32_t wrd[4] = {pk.x, pk.y, pk.z, pk.w};
                 uint32_t o0[8], o1[8];  // rows r0 / r1, k = 16 tq .. 16 tq + 15
 #pragma unroll
@@ -416,7 +426,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // its own TMEM lane quarter.
             tc_fence_after_sync();
             const int S = a.splits, z = (int)blockIdx.z;
-            const int part = (int)kCols / S;
+            // owner z: columns [z part, min((z + 1) part, kCols)), part a
+            // multiple of 64 (S = 3 owns 192 / 192 / 128 of 512)
+            const int part = (((int)kCols / S + 63) / 64) * 64;
             float* recv = reinterpret_cast<float*>(smem + kOffA);
             const uint32_t recv_u32 = base + kOffA;
             const int q = warp & 3, wq = (warp - 4) >> 2;  // quarter; warp index within it
@@ -429,6 +441,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     for (int task = wq; task < 2 * S; task += 4) {
                         const int d = task >> 1, c = task & 1;  // destination split, 32-column half
                         const int col = d * part + r * 64 + c * 32;
+                        if (col >= (int)kCols) continue;  // d owns fewer rounds
                         uint32_t v[32];
                         tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)col, v);
                         tmem_ld_wait();
@@ -441,7 +454,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 }
                 cluster_sync_all();  // every slice of this round has landed
-                if (warp >= 4 && wq < 2) {
+                if (warp >= 4 && wq < 2 && z * part + r * 64 + wq * 32 < (int)kCols) {
                     const int col = z * part + r * 64 + wq * 32;
                     float sum[32];
 #pragma unroll
@@ -504,6 +517,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 //  * otherwise one CTA per 128 x 128 tile (cluster 1).
 struct TcPlan {
     int cluster = 1, xt = 1, splits = 1;
+    int slab_ld = 0;  // > 0: split slab of this many groups per row (tensor-map copy)
     unsigned gx = 0, gy = 0;
     long long ctas = 0;
 };
@@ -526,20 +540,36 @@ int max_active_clusters(const void* fn, int cluster_z, uint32_t smem) {
 }
 
 // Shared memory of a launch: `nst` ring stages with xt x tiles each, next to
-// the scale slab, +1 KB slack for aligning the window to 1024 bytes.
-uint32_t tc_smem(int nst, int xt, int G) {
-    const uint32_t slab = ((kTileW * G * 2 + 127) / 128) * 128;
+// a scale slab of `ld` groups per row, +1 KB slack for aligning the window to
+// 1024 bytes.
+uint32_t tc_smem(int nst, int xt, int ld) {
+    const uint32_t slab = ((kTileW * ld * 2 + 127) / 128) * 128;
     const uint32_t stage = (uint32_t)(kAStageBytes + xt * kXStageBytes + kWStageBytes);
     return kOffA + (uint32_t)nst * stage + slab + 1024;
+}
+
+// Groups per slab row when K is split S ways: the widest span from a
+// split's first group rounded down to 8 to its last group, rounded up to 8
+// (the tensor-map copy needs 16-byte rows and a 16-byte aligned start).
+// 0 when G is not a multiple of 8 or the span exceeds a copy's 256 limit.
+int split_slab_ld(long long nkb, int S, int G) {
+    if (G % 8 != 0) return 0;
+    int w = 0;
+    for (int z = 0; z < S; ++z) {
+        const long long kb0 = z * nkb / S, kb1 = (z + 1) * nkb / S;
+        const int g0 = (int)(kb0 >> 1) & ~7, g1 = (int)((kb1 - 1) >> 1);
+        w = std::max(w, ((g1 - g0 + 1 + 7) / 8) * 8);
+    }
+    return w <= 256 ? w : 0;
 }
 
 // Pairs take as many ring stages as fit: a deeper ring hides more of the
 // copy -> dequantise -> MMA -> release round trip.  The single-CTA tile keeps
 // kSingleStages (deeper measured slower there).
-int tc_stages(const TcPlan& p, int G, const DeviceCtx& ctx) {
+int tc_stages(const TcPlan& p, int ld, const DeviceCtx& ctx) {
     if (p.cluster == 1) return kSingleStages;
     int nst = kMaxStages;
-    while (nst > 2 && tc_smem(nst, p.xt, G) > (uint32_t)ctx.max_smem_optin) --nst;
+    while (nst > 2 && tc_smem(nst, p.xt, ld) > (uint32_t)ctx.max_smem_optin) --nst;
     return nst;
 }
 
@@ -548,8 +578,8 @@ int tc_stages(const TcPlan& p, int G, const DeviceCtx& ctx) {
 //  * CTA pairs with 256 x 256 tiles (xt = 1, cluster 2), M > 128;
 //  * CTA pairs with 512 x-row x 256 weight-row tiles (xt = 2), M > 256 --
 //    the most MMA work per stage hand-off;
-//  * the latter splitting K two or four ways (every k-range >= 8 k-blocks),
-//    the splits of a tile forming one cluster (4 or 8 CTAs) that reduces
+//  * the latter splitting K two to four ways (every k-range >= 8 k-blocks),
+//    the splits of a tile forming one cluster (4, 6 or 8 CTAs) that reduces
 //    through distributed shared memory; only when the whole grid is
 //    co-resident.
 // Cost = waves x k-blocks per CTA x the measured time of one k-block of the
@@ -589,29 +619,34 @@ TcPlan tc_plan(int64_t M, int64_t N, int64_t K, const DeviceCtx& ctx) {
         p.gx = (unsigned)(2 * pairs);
         p.gy = (unsigned)((M + 4 * kTileX - 1) / (4 * kTileX));
         p.ctas = (long long)p.gx * p.gy;
-        double t = waves(p.ctas) * nkb * kPair2Kb;
+        double t = waves(p.ctas) * nkb * kPair2Kb * (tc_stages(p, G, ctx) >= 4 ? 1.0 : 1.25);
         if (t < t_best) {
             t_best = t;
             best = p;
         }
-        const int nst = tc_stages(p, G, ctx);
-        const uint32_t smem = tc_smem(nst, 2, G);
-        const uint32_t ring = (uint32_t)nst * (kAStageBytes + 2 * kXStageBytes + kWStageBytes);
-        for (int S = 2; S <= 4; S *= 2) {
+        for (int S = 2; S <= 4; ++S) {
             const long long ctas = p.ctas * S;
             if (ctas > ctx.num_sms || nkb < 8 * S) continue;
+            // a split holds only its own groups' scales, leaving room for a
+            // deeper ring (3 stages run a k-block about 25 % slower than 4)
+            const int ld = split_slab_ld(nkb, S, G);
+            const int nst = tc_stages(p, ld ? ld : G, ctx);
+            const uint32_t smem = tc_smem(nst, 2, ld ? ld : G);
+            const uint32_t ring = (uint32_t)nst * (kAStageBytes + 2 * kXStageBytes + kWStageBytes);
             // the S receive slots of the reduction live in the ring
             if ((uint32_t)S * kRedSlotFloats * 4 > ring) continue;
             const long long fit =
                 (long long)max_active_clusters((const void*)gemm_tc_kernel<true, 2>, S, smem);
             if (fit * 2 * S < ctas) continue;  // not one co-resident wave
-            t = (double)((nkb + S - 1) / S) * kPair2Kb + kRound * (4 * kTileW / S / 64 + 1);
+            t = (double)((nkb + S - 1) / S) * kPair2Kb * (nst >= 4 ? 1.0 : 1.25) +
+                kRound * ((4 * kTileW / S + 63) / 64 + 1);
             if (t < t_best) {
                 t_best = t;
                 best = p;
                 best.splits = S;
                 best.cluster = 2 * S;
                 best.ctas = ctas;
+                best.slab_ld = ld;
             }
         }
     }
@@ -653,8 +688,9 @@ cudaError_t launch_gemm_tc(const void* x, const void* repacked, const void* scal
     cudaError_t e = ensure_tc_attrs(ctx);
     if (e != cudaSuccess) return e;
     const TcPlan plan = tc_plan(M, N, K, ctx);
-    const int nst = tc_stages(plan, G, ctx);
-    const uint32_t smem = tc_smem(nst, plan.xt, G);
+    const int ld = plan.slab_ld ? plan.slab_ld : G;
+    const int nst = tc_stages(plan, ld, ctx);
+    const uint32_t smem = tc_smem(nst, plan.xt, ld);
     if ((int)smem > ctx.max_smem_optin) return cudaErrorInvalidValue;
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
@@ -667,6 +703,16 @@ cudaError_t launch_gemm_tc(const void* x, const void* repacked, const void* scal
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
+    CUtensorMap smap = map;  // unused unless the slab is copied per split
+    if (plan.slab_ld) {
+        const cuuint64_t sdims[2] = {(cuuint64_t)G, (cuuint64_t)N};
+        const cuuint64_t sstrides[1] = {(cuuint64_t)G * 2};
+        const cuuint32_t sbox[2] = {(cuuint32_t)plan.slab_ld, (cuuint32_t)kTileW};
+        if (encode(&smap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(scales), sdims,
+                   sstrides, sbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
 
     TcArgs args{};
     args.wq = static_cast<const uint8_t*>(repacked);
@@ -683,6 +729,8 @@ cudaError_t launch_gemm_tc(const void* x, const void* repacked, const void* scal
     args.off_w = args.off_x + (uint32_t)nst * plan.xt * kXStageBytes;
     args.off_slab = args.off_w + (uint32_t)nst * kWStageBytes;
     args.splits = plan.splits;
+    args.slab_ld = ld;
+    args.slab_tma = plan.slab_ld ? 1 : 0;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(plan.gx, plan.gy, (unsigned)plan.splits);
@@ -698,9 +746,9 @@ cudaError_t launch_gemm_tc(const void* x, const void* repacked, const void* scal
     attrs[1].val.clusterDim.z = (unsigned)plan.splits;
     cfg.attrs = attrs;
     cfg.numAttrs = plan.cluster > 1 ? 2 : 1;
-    if (plan.cluster == 1) return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<false, 1>, map, args);
-    if (plan.xt == 1) return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true, 1>, map, args);
-    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true, 2>, map, args);
+    if (plan.cluster == 1) return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<false, 1>, map, smap, args);
+    if (plan.xt == 1) return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true, 1>, map, smap, args);
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true, 2>, map, smap, args);
 }
 
 }  // namespace w4a16

@@ -33,8 +33,8 @@ cudaError_t launch_gemv(const void* x, const void* repacked, const void* scales,
 cudaError_t gemv_plan_info(int M, int64_t N, int64_t K, const DeviceCtx& ctx, int* splits,
                            int* ctas, int* blocks_per_cta);
 // The launch the tensor-core GEMM would make: cluster size (1: one CTA per
-// 128 x 128 tile; 2: CTA pairs with 2-CTA MMAs; 4 or 8: CTA pairs splitting
-// K two or four ways, reduced over the cluster) and CTAs.
+// 128 x 128 tile; 2: CTA pairs with 2-CTA MMAs; 4, 6 or 8: CTA pairs
+// splitting K two, three or four ways, reduced over the cluster) and CTAs.
 void gemm_tc_plan_info(int64_t M, int64_t N, int64_t K, const DeviceCtx& ctx, int* cluster,
                        int* ctas);
 cudaError_t launch_gemm_tc(const void* x, const void* repacked, const void* scales, void* y,
