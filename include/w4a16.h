@@ -167,11 +167,16 @@ enum { W4A16_PATH_GEMV = 1, W4A16_PATH_TENSOR_CORE = 2 };
  *                    cluster's shared memory).
  *   *ctas            CTAs launched.
  *   *blocks_per_cta  most 128-row blocks one CTA walks (> 1: persistent).
+ *   *rows_per_cta    weight rows one CTA computes of each block it handles:
+ *                    128 (a whole block; the tensor-core GEMM always), or for
+ *                    the GEMV 16, 32 or 64 (1, 2 or 4 of a block's 16-row
+ *                    tiles over the whole K range, the CTA's warps splitting
+ *                    K and reducing in its own shared memory).
  * Errors: NULL output -> W4A16_ERR_NULL; bad M, N, K -> W4A16_ERR_SHAPE;
  *         no supported device -> W4A16_ERR_DEVICE / W4A16_ERR_CUDA.
  */
 int w4a16_gemm_plan(int64_t M, int64_t N, int64_t K, int *path, int *splits, int *ctas,
-                    int *blocks_per_cta);
+                    int *blocks_per_cta, int *rows_per_cta);
 
 /*
  * w4a16_device_status -- synchronises the current device, returns in

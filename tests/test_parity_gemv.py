@@ -93,6 +93,46 @@ def test_persistent_path_all_rows(w4lib, M, N, K):
     assert_close(run_gemm(x16, q, s), oracle.gemm(x16, q, s), f"M={M} N={N} K={K} {plan}")
 
 
+# Launches made of sub-block units (16, 32 or 64 weight rows per CTA over the
+# whole K range): ragged row tails inside a tile, and K ranges that end in a
+# partial ring stage (K = 11008: 172 chunks; K = 1920: 30).
+SUB_BLOCK_CASES = [(1000, 2048, 1), (1000, 2048, 4), (4096, 4096, 1),
+                   (4096, 4096, 2), (6144, 4096, 1), (4136, 11008, 1), (8000, 1920, 1),
+                   (8000, 1920, 4), (24000, 1024, 1), (24000, 1024, 3), (16384, 2048, 2)]
+
+
+@pytest.mark.parametrize("N,K,M", SUB_BLOCK_CASES)
+def test_sub_block_units_all_rows(w4lib, N, K, M):
+    """Every row of launches whose CTAs own 1, 2 or 4 tiles and split K over
+    their warps, reducing in shared memory."""
+    plan = w4.gemm_plan(M, N, K)
+    assert plan["path"] == "gemv" and plan["splits"] == 1 and plan["rows_per_cta"] < 128, plan
+    w16, q, s = quantized(N, K, 61)
+    x16 = acts(M, K, 62 + M)
+    y = run_gemm(x16, q, s)
+    assert_close(y, oracle.gemm(x16, q, s), f"M={M} N={N} K={K} {plan}")
+    # the in-CTA reduction runs in a fixed order: a repeat call is bit-identical
+    assert np.array_equal(run_gemm(x16, q, s), y)
+
+
+def test_sub_block_unit_sizes_covered(w4lib):
+    """The cases above exercise all three unit sizes."""
+    rows = {w4.gemm_plan(M, N, K)["rows_per_cta"] for N, K, M in SUB_BLOCK_CASES}
+    assert {16, 32, 64} <= rows, rows
+
+
+def test_sub_block_units_two_n8_tiles(w4lib):
+    """Sub-block units with M > 8 (two n8 tiles per MMA step): the launches
+    among these shapes that the planner makes of units, every row."""
+    cands = [(16384, 2048, 12), (8000, 1920, 9), (16384, 2048, 9), (12000, 1536, 10)]
+    picked = [(N, K, M) for N, K, M in cands if w4.gemm_plan(M, N, K)["rows_per_cta"] < 128]
+    assert picked, [w4.gemm_plan(M, N, K) for N, K, M in cands]
+    for N, K, M in picked[:2]:
+        w16, q, s = quantized(N, K, 63)
+        x16 = acts(M, K, 64)
+        assert_close(run_gemm(x16, q, s), oracle.gemm(x16, q, s), f"M={M} N={N} K={K}")
+
+
 def _sampled(lin, M, workload, idx):
     sw, sx = synthetic.seeds(workload, idx)
     w16, q, s = quantized(lin.N, lin.K, sw)

@@ -77,6 +77,20 @@ __global__ void selftest_wait_kernel(unsigned* status, uint64_t timeout_ns) {
 
 }  // namespace
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, []() {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
 cudaError_t launch_selftest_wait(uint64_t timeout_ns, cudaStream_t stream, const DeviceCtx& ctx) {
     selftest_wait_kernel<<<1, 32, 0, stream>>>(ctx.status, timeout_ns);
     return cudaGetLastError();
@@ -155,8 +169,8 @@ int w4a16_gemm(const void* x_f16, const void* repacked, const void* scales_f16, 
 }
 
 int w4a16_gemm_plan(int64_t M, int64_t N, int64_t K, int* path, int* splits, int* ctas,
-                    int* blocks_per_cta) {
-    if (!path || !splits || !ctas || !blocks_per_cta) return W4A16_ERR_NULL;
+                    int* blocks_per_cta, int* rows_per_cta) {
+    if (!path || !splits || !ctas || !blocks_per_cta || !rows_per_cta) return W4A16_ERR_NULL;
     if (M < 1 || M > (int64_t)1 << 22 || !good_nk(N, K) || N > (int64_t)1 << 28 ||
         K > (int64_t)1 << 15)
         return W4A16_ERR_SHAPE;
@@ -167,9 +181,11 @@ int w4a16_gemm_plan(int64_t M, int64_t N, int64_t K, int* path, int* splits, int
         gemm_tc_plan_info(M, N, K, ctx, splits, ctas);
         if (*splits == 0) return W4A16_ERR_CUDA;
         *blocks_per_cta = 1;
+        *rows_per_cta = 128;
         return W4A16_OK;
     }
-    if (int rc = from_cuda(gemv_plan_info((int)M, N, K, ctx, splits, ctas, blocks_per_cta)))
+    if (int rc = from_cuda(
+            gemv_plan_info((int)M, N, K, ctx, splits, ctas, blocks_per_cta, rows_per_cta)))
         return rc;
     *path = W4A16_PATH_GEMV;
     return W4A16_OK;

@@ -494,20 +494,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, []() {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
 // Launch shape of the tensor-core GEMM for (M, N):
 //  * xt = 2: CTA pairs with two x tiles per CTA, 512 x rows x 256 weight rows
 //    per pair -- the most MMA work per stage hand-off -- when M > 256 and the

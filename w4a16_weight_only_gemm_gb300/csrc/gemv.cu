@@ -5,14 +5,17 @@
 // are unpacked in registers; the qaqbuyan.com tutorial §3 dequantizer fixes
 // the arithmetic).
 //
-// One thread block = 8 consumer warps (16 weight rows each: one 128-row
-// block of the kernel layout) + 1 producer warp.
-//  * The producer streams weights -- 4 KB per 64-wide chunk of a block,
-//    contiguous in the kernel layout -- into a ring of 16 KB shared-memory
-//    stages with bulk async copies (TMA engine) that complete on mbarriers,
-//    L2 policy evict-first.  Each block's fp16 scale slab (128 rows x K/128,
-//    contiguous in the canonical layout) arrives the same way into one of two
-//    buffers, and the x slice of the block's K range once per thread block.
+// One thread block = 8 consumer warps + 1 producer warp.  A CTA computes
+// either whole 128-row blocks of the kernel layout (one 16-row tile per
+// warp) or a sub-block unit of T = 1, 2 or 4 tiles over the whole K range,
+// the 8 / T warps of a tile sharing out the groups of every stage.
+//  * The producer streams weights into a ring of 16 KB shared-memory stages
+//    with async copies (TMA engine) that complete on mbarriers, L2 policy
+//    evict-first: a whole block's 64-wide chunks are 4 KB contiguous (one
+//    bulk copy per stage); a unit's T tiles of 32 / T consecutive chunks are
+//    one tensor-map box.  The fp16 scale slab of the CTA's rows (contiguous
+//    in the canonical layout) arrives the same way into one of two buffers,
+//    and the x slice of the CTA's K range once per thread block.
 //  * Consumers: per 64-wide chunk a lane reads 16 bytes of its tile, expands
 //    each 32-bit word into an mma.m16n8k16 A fragment with lop3 + one f16x2
 //    op per nibble pair (exact q), and multiplies it with x fragments read
@@ -20,13 +23,15 @@
 //    Every 128-wide group accumulates in a fresh FP32 fragment that is scaled
 //    once by its fp16 scale and added to the FP32 running sum: q * x products
 //    are exact and only FP32 sums round.
-//  * Work split: when there are fewer 128-row blocks than SM slots, the K
-//    range is split over the CTAs of a thread-block cluster (up to 8).  Each
-//    CTA pushes its FP32 partials into the shared memory of the CTA that owns
-//    the row (distributed shared memory), one cluster barrier later the owner
-//    sums them in a fixed order (no global workspace, no atomics).  Otherwise the grid is
-//    persistent: each CTA walks blocks y, y + gridDim.y, ... while the
-//    producer keeps the ring full across block boundaries.
+//  * Work split, chosen per shape by a launch-time model: sub-block units
+//    (the warps of a tile add their partial sums in shared memory, in a
+//    fixed order); or whole blocks with the K range split over the S CTAs of
+//    a thread-block cluster (up to 8), each CTA pushing its FP32 partials
+//    into the shared memory of the CTA that owns the row (distributed shared
+//    memory) and the owner summing them in a fixed order one cluster barrier
+//    later (no global workspace, no atomics); or, with more blocks than CTA
+//    slots, a persistent grid where each CTA walks blocks y, y + gridDim.y,
+//    ... while the producer keeps the ring full across block boundaries.
 //  * Programmatic dependent launch: the CTA releases its dependents at once
 //    and loads its first ring stages and scale slab -- constants of the call
 //    -- while the previous kernel on the stream is still running; x (which
@@ -47,12 +52,12 @@ namespace {
 constexpr int kConsumerWarps = 8;                      // 8 x 16 rows = one block
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kGemvThreads = kConsumers + 32;
+constexpr int kTileBytes = 16 * kChunkK / 2;           // 512 B: one 16-row tile, one chunk
 constexpr int kChunkBytes = kBlockRows * kChunkK / 2;  // 4096 B per block-chunk
-constexpr int kStages = 3;                             // ring depth of split launches
+constexpr int kStages = 3;                             // ring depth of non-persistent launches
 constexpr int kMaxStages = 6;                          // deepest ring (persistent launches)
-constexpr int kChunksPerStage = 4;                     // two whole groups
-constexpr int kGroupsPerStage = kChunksPerStage / 2;
-constexpr int kStageBytes = kChunksPerStage * kChunkBytes;
+constexpr int kStageBytes = 16384;                     // every ring stage
+constexpr int kGroupsPerWarpStage = 2;                 // groups a warp takes from one stage
 constexpr int kMaxSplits = 8;
 
 // Barrier area at the start of shared memory.
@@ -73,8 +78,9 @@ struct GemvArgs {
     uint64_t timeout_ns;
     int M, N, K, G;
     int NB;                  // 128-row blocks
+    int T;                   // 16-row tiles per CTA: 8 = whole blocks; 1, 2, 4 = sub-block units
     int xs_stride;           // bytes between x rows in shared memory
-    int slab_bytes;          // bytes of one scale buffer (128 * G * 2, rounded)
+    int slab_bytes;          // bytes of one scale buffer (16 T rows x G, rounded)
     int n_sbuf;              // scale buffers: 2 when a CTA walks several blocks
     int nstages;             // ring stages (<= kMaxStages)
     int rpo;                 // rows owned per CTA in the split reduction
@@ -88,8 +94,8 @@ __device__ __forceinline__ int split_group_begin(int split, int S, int G) {
 // One 128-wide group (two chunks) of one consumer lane: 8 MMAs into a fresh
 // FP32 fragment, then scaled into acc.
 template <int MT>
-__device__ __forceinline__ void mma_group(uint32_t w_addr, uint32_t x0_addr, uint32_t x1_addr,
-                                          uint32_t sx_addr, float s0, float s1,
+__device__ __forceinline__ void mma_group(uint32_t w_addr, uint32_t cs, uint32_t x0_addr,
+                                          uint32_t x1_addr, uint32_t sx_addr, float s0, float s1,
                                           float (&acc)[MT][4]) {
     // M <= 8: one FP32 fragment per chunk -- two independent MMA chains per
     // group halve the dependent-latency path of a lane (M <= 16 has two
@@ -104,7 +110,7 @@ __device__ __forceinline__ void mma_group(uint32_t w_addr, uint32_t x0_addr, uin
             for (int e = 0; e < 4; ++e) g[c][mt][e] = 0.0f;
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
-        const uint4 wv = lds128(w_addr + c * kChunkBytes);
+        const uint4 wv = lds128(w_addr + c * cs);
         const uint4 xa = lds128(x0_addr + c * 128);
         const uint4 xb = lds128(x0_addr + c * 128 + 16);
         uint4 xa1 = xa, xb1 = xb;
@@ -139,19 +145,55 @@ __device__ __forceinline__ void mma_group(uint32_t w_addr, uint32_t x0_addr, uin
     }
 }
 
+// Stores the FP32 results of a lane's fragments (rows R0, R1; columns
+// 2t, 2t + 1 of each n8 tile) as fp16.
 template <int MT>
-__global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2) gemv_kernel(const __grid_constant__ GemvArgs a) {
+__device__ __forceinline__ void store_y(const GemvArgs& a, int R0, int R1, int t,
+                                        const float (&acc)[MT][4]) {
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+        const int m0 = mt * 8 + 2 * t, m1 = m0 + 1;
+        if (m0 < a.M) {
+            if (R0 < a.N) a.y[(size_t)m0 * a.N + R0] = __float2half_rn(acc[mt][0]);
+            if (R1 < a.N) a.y[(size_t)m0 * a.N + R1] = __float2half_rn(acc[mt][2]);
+        }
+        if (m1 < a.M) {
+            if (R0 < a.N) a.y[(size_t)m1 * a.N + R0] = __float2half_rn(acc[mt][1]);
+            if (R1 < a.N) a.y[(size_t)m1 * a.N + R1] = __float2half_rn(acc[mt][3]);
+        }
+    }
+}
+
+// WHOLE: the CTA computes whole 128-row blocks (T = 8, stage geometry fixed
+// at compile time); otherwise sub-block units of a.T tiles.  The weight map
+// (`wmap`) views the kernel layout as rows of 4 KB chunks (512 eight-byte
+// elements, one row per block-chunk); sub-block launches copy a box of T
+// tiles x 32 / T chunks per ring stage through it.
+template <int MT, bool WHOLE>
+__device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const GemvArgs& a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int S = (int)gridDim.x;  // the cluster spans the whole x dimension
     const int split = (int)blockIdx.x;
     const int C = a.K / kChunkK;
+    const int T = WHOLE ? kConsumerWarps : a.T;
+    constexpr bool whole = WHOLE;
+    const int W = kConsumerWarps / T;        // warps per tile, sharing out its groups
+    const int CPS = kStageBytes / (T * kTileBytes);  // chunks per stage
+    const int GPS = CPS / 2;                         // groups per stage
     const int g0 = split_group_begin(split, S, a.G);
     const int ng = split_group_begin(split + 1, S, a.G) - g0;
     const int nck = 2 * ng;
-    const int nstg = (nck + kChunksPerStage - 1) / kChunksPerStage;
-    const int nblk = (a.NB - (int)blockIdx.y + (int)gridDim.y - 1) / (int)gridDim.y;
+    const int nstg = (nck + CPS - 1) / CPS;
+    // Whole blocks: the CTA walks blocks y, y + gridDim.y, ...  Sub-block
+    // units: CTA y owns rows [16 T y, 16 T (y + 1)), tiles t0 .. t0 + T - 1
+    // of block 16 T y / 128.
+    const int nblk = whole ? (a.NB - (int)blockIdx.y + (int)gridDim.y - 1) / (int)gridDim.y : 1;
+    const int t0 = whole ? 0 : ((int)blockIdx.y * T) & (kConsumerWarps - 1);
+    auto block_of = [&](int j) {
+        return whole ? (int)blockIdx.y + j * (int)gridDim.y : ((int)blockIdx.y * T) / kConsumerWarps;
+    };
 
     const uint32_t sbase = smem_u32(smem);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortFlag);
@@ -177,67 +219,140 @@ __global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2) gemv_kernel(con
 
     if (warp == kConsumerWarps) {
         // =============================== producer ===============================
-        if (lane == 0) {
-            const uint64_t pol = l2_policy_evict_first();
-            const size_t block_stride = (size_t)C * kChunkBytes;
-            {   // L2 prefetch of the first block (weights of this split, scale slab).
-                const int rb = (int)blockIdx.y;
-                const uint8_t* w = a.wq + (size_t)rb * block_stride + 2 * (size_t)g0 * kChunkBytes;
-                const int pre = nstg < 2 * a.nstages ? nstg : 2 * a.nstages;
-                for (int i = 0; i < pre; ++i)
-                    bulk_prefetch_l2(w + (size_t)i * kStageBytes,
-                                     min(kChunksPerStage, nck - i * kChunksPerStage) * kChunkBytes);
-                const int rows = min(kBlockRows, a.N - rb * kBlockRows);
-                const uint32_t sb = ((uint32_t)(rows * a.G * 2)) & ~15u;
-                if (sb) bulk_prefetch_l2(a.scales + (size_t)rb * kBlockRows * a.G, sb);
-            }
-            // Weights and scales are constants of the call: the first ring
-            // stages and scale slab load while the previous kernel is still
-            // running.  x (its output, possibly) loads only after the wait.
-            bool x_issued = false;
-            auto issue_x = [&]() {
-                grid_dependency_wait();
-                const uint32_t xbytes = (uint32_t)nck * (kChunkK * 2);
-                mbar_arrive_expect_tx(sbase + kBarX, xbytes * a.M);
-                for (int m = 0; m < a.M; ++m)
-                    bulk_g2s(sbase + a.off_x + m * a.xs_stride,
-                             a.x + (size_t)m * a.K + (size_t)g0 * kGroup, xbytes, sbase + kBarX);
-                x_issued = true;
-            };
-            const int NS = a.nstages;
-            int it = 0, slot = 0, round = 0;  // slot = it % NS, round = it / NS
-            bool ok = true;
-            int sb_issued = 0;
-            for (int j = 0; ok && j < nblk; ++j) {
-                const int rb = (int)blockIdx.y + j * (int)gridDim.y;
-                // --- scale slab of block rb ---
-                const int sbuf = j % a.n_sbuf;
-                if (j >= a.n_sbuf &&
-                    !mbar_wait(sbase + kBarSEmpty + 8 * sbuf, ((j / a.n_sbuf) - 1) & 1,
-                               a.timeout_ns, a.status)) {
-                    ok = false;
-                    break;
-                }
-                {
+        if constexpr (WHOLE) {
+            // Whole blocks: one bulk copy of CPS contiguous 4 KB chunks per stage.
+            if (lane == 0) {
+                const uint64_t pol = l2_policy_evict_first();
+                const size_t block_stride = (size_t)C * kChunkBytes;
+                {   // L2 prefetch of the first block (weights of this split, scale slab).
+                    const int rb = (int)blockIdx.y;
+                    const uint8_t* w = a.wq + (size_t)rb * block_stride + 2 * (size_t)g0 * kChunkBytes;
+                    const int pre = nstg < 2 * a.nstages ? nstg : 2 * a.nstages;
+                    for (int i = 0; i < pre; ++i)
+                        bulk_prefetch_l2(w + (size_t)i * kStageBytes,
+                                         min(CPS, nck - i * CPS) * kChunkBytes);
                     const int rows = min(kBlockRows, a.N - rb * kBlockRows);
+                    const uint32_t sb = ((uint32_t)(rows * a.G * 2)) & ~15u;
+                    if (sb) bulk_prefetch_l2(a.scales + (size_t)rb * kBlockRows * a.G, sb);
+                }
+                // Weights and scales are constants of the call: the first ring
+                // stages and scale slab load while the previous kernel is still
+                // running.  x (its output, possibly) loads only after the wait.
+                bool x_issued = false;
+                auto issue_x = [&]() {
+                    grid_dependency_wait();
+                    const uint32_t xbytes = (uint32_t)nck * (kChunkK * 2);
+                    mbar_arrive_expect_tx(sbase + kBarX, xbytes * a.M);
+                    for (int m = 0; m < a.M; ++m)
+                        bulk_g2s(sbase + a.off_x + m * a.xs_stride,
+                                 a.x + (size_t)m * a.K + (size_t)g0 * kGroup, xbytes, sbase + kBarX);
+                    x_issued = true;
+                };
+                const int NS = a.nstages;
+                int it = 0, slot = 0, round = 0;  // slot = it % NS, round = it / NS
+                bool ok = true;
+                int sb_issued = 0;
+                for (int j = 0; ok && j < nblk; ++j) {
+                    const int rb = (int)blockIdx.y + j * (int)gridDim.y;
+                    // --- scale slab of block rb ---
+                    const int sbuf = j % a.n_sbuf;
+                    if (j >= a.n_sbuf &&
+                        !mbar_wait(sbase + kBarSEmpty + 8 * sbuf, ((j / a.n_sbuf) - 1) & 1,
+                                   a.timeout_ns, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    {
+                        const int rows = min(kBlockRows, a.N - rb * kBlockRows);
+                        const uint32_t bytes = (uint32_t)(rows * a.G * 2);
+                        const uint32_t bulk = bytes & ~15u;
+                        const __half* src = a.scales + (size_t)rb * kBlockRows * a.G;
+                        __half* dst = reinterpret_cast<__half*>(smem + a.off_s + sbuf * a.slab_bytes);
+                        for (uint32_t e = bulk / 2; e < bytes / 2; ++e) dst[e] = src[e];  // ragged tail
+                        mbar_arrive_expect_tx(sbase + kBarSFull + 8 * sbuf, bulk);
+                        if (bulk)
+                            bulk_g2s(sbase + a.off_s + sbuf * a.slab_bytes, src, bulk,
+                                     sbase + kBarSFull + 8 * sbuf);
+                        sb_issued = j + 1;
+                    }
+                    // --- weight stages of block rb ---
+                    const uint8_t* w = a.wq + (size_t)rb * block_stride + 2 * (size_t)g0 * kChunkBytes;
+                    for (int st = 0; st < nstg; ++st) {
+                        if (it >= NS && !x_issued) issue_x();
+                        if (it >= NS &&
+                            !mbar_wait(sbase + kBarEmpty + 8 * slot, (round - 1) & 1, a.timeout_ns,
+                                       a.status)) {
+                            ok = false;
+                            break;
+                        }
+                        if (*abort_flag) {
+                            ok = false;
+                            break;
+                        }
+                        const int nc = min(CPS, nck - st * CPS);
+                        mbar_arrive_expect_tx(sbase + kBarFull + 8 * slot, nc * kChunkBytes);
+                        bulk_g2s_hint(ring + slot * kStageBytes, w + (size_t)st * kStageBytes,
+                                      nc * kChunkBytes, sbase + kBarFull + 8 * slot, pol);
+                        ++it;
+                        if (++slot == NS) {
+                            slot = 0;
+                            ++round;
+                        }
+                    }
+                }
+                if (!x_issued) issue_x();
+                if (!ok) *abort_flag = 1;
+                // Drain: every issued copy must land before the CTA may exit.
+                mbar_wait(sbase + kBarX, 0, a.timeout_ns, a.status);
+                for (int i = (it > NS ? it - NS : 0); i < it; ++i)
+                    mbar_wait(sbase + kBarFull + 8 * (i % NS), (i / NS) & 1, a.timeout_ns, a.status);
+                for (int j = (sb_issued > a.n_sbuf ? sb_issued - a.n_sbuf : 0); j < sb_issued; ++j)
+                    mbar_wait(sbase + kBarSFull + 8 * (j % a.n_sbuf), (j / a.n_sbuf) & 1, a.timeout_ns,
+                              a.status);
+            }
+        } else {
+            // Sub-block units (one block, one scale buffer): a tensor-map box of
+            // T tiles x CPS chunks per stage, the K tail chunk by chunk.
+            if (lane == 0) {
+                const uint64_t pol = l2_policy_evict_first();
+                const int NS = a.nstages;
+                const int rb = block_of(0);
+                const int r0 = rb * kBlockRows + t0 * 16;    // first weight row of the unit
+                const int box_x = t0 * (kTileBytes / 8);     // map x coordinate of its tiles
+                const int cy0 = rb * C + 2 * g0;             // map row of its first chunk
+                tma_prefetch_map(wmap);
+                // L2 prefetch of the stages beyond the first ring pass (those
+                // inside it load now)
+                for (int i = NS; i < nstg && i < 2 * NS; ++i)
+                    if ((i + 1) * CPS <= nck) tma_prefetch_2d(wmap, box_x, cy0 + i * CPS);
+                {   // scale slab of the unit's rows
+                    const int rows = min(16 * T, a.N - r0);
                     const uint32_t bytes = (uint32_t)(rows * a.G * 2);
                     const uint32_t bulk = bytes & ~15u;
-                    const __half* src = a.scales + (size_t)rb * kBlockRows * a.G;
-                    __half* dst = reinterpret_cast<__half*>(smem + a.off_s + sbuf * a.slab_bytes);
+                    const __half* src = a.scales + (size_t)r0 * a.G;
+                    __half* dst = reinterpret_cast<__half*>(smem + a.off_s);
                     for (uint32_t e = bulk / 2; e < bytes / 2; ++e) dst[e] = src[e];  // ragged tail
-                    mbar_arrive_expect_tx(sbase + kBarSFull + 8 * sbuf, bulk);
-                    if (bulk)
-                        bulk_g2s(sbase + a.off_s + sbuf * a.slab_bytes, src, bulk,
-                                 sbase + kBarSFull + 8 * sbuf);
-                    sb_issued = j + 1;
+                    mbar_arrive_expect_tx(sbase + kBarSFull, bulk);
+                    if (bulk) bulk_g2s(sbase + a.off_s, src, bulk, sbase + kBarSFull);
                 }
-                // --- weight stages of block rb ---
-                const uint8_t* w = a.wq + (size_t)rb * block_stride + 2 * (size_t)g0 * kChunkBytes;
-                for (int st = 0; st < nstg; ++st) {
+                // Weights and scales are constants of the call and load before
+                // the grid-dependency wait; x loads after it.
+                bool x_issued = false;
+                auto issue_x = [&]() {
+                    grid_dependency_wait();
+                    const uint32_t xbytes = (uint32_t)nck * (kChunkK * 2);
+                    mbar_arrive_expect_tx(sbase + kBarX, xbytes * a.M);
+                    for (int m = 0; m < a.M; ++m)
+                        bulk_g2s(sbase + a.off_x + m * a.xs_stride,
+                                 a.x + (size_t)m * a.K + (size_t)g0 * kGroup, xbytes, sbase + kBarX);
+                    x_issued = true;
+                };
+                int it = 0, slot = 0, round = 0;  // slot = it % NS, round = it / NS
+                bool ok = true;
+                for (; it < nstg; ++it) {
                     if (it >= NS && !x_issued) issue_x();
-                    if (it >= NS &&
-                        !mbar_wait(sbase + kBarEmpty + 8 * slot, (round - 1) & 1, a.timeout_ns,
-                                   a.status)) {
+                    if (it >= NS && !mbar_wait(sbase + kBarEmpty + 8 * slot, (round - 1) & 1,
+                                               a.timeout_ns, a.status)) {
                         ok = false;
                         break;
                     }
@@ -245,42 +360,52 @@ __global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2) gemv_kernel(con
                         ok = false;
                         break;
                     }
-                    const int nc = min(kChunksPerStage, nck - st * kChunksPerStage);
-                    mbar_arrive_expect_tx(sbase + kBarFull + 8 * slot, nc * kChunkBytes);
-                    bulk_g2s_hint(ring + slot * kStageBytes, w + (size_t)st * kStageBytes,
-                                  nc * kChunkBytes, sbase + kBarFull + 8 * slot, pol);
-                    ++it;
+                    const int nc = min(CPS, nck - it * CPS);
+                    const uint32_t dst = ring + slot * kStageBytes;
+                    const uint32_t bar = sbase + kBarFull + 8 * slot;
+                    if (nc == CPS) {
+                        mbar_arrive_expect_tx(bar, kStageBytes);
+                        tma_load_2d_hint(dst, wmap, box_x, cy0 + it * CPS, bar, pol);
+                    } else {
+                        // the K tail: one copy of T tiles per chunk
+                        const uint32_t rowb = (uint32_t)(T * kTileBytes);
+                        const uint8_t* src = a.wq + (size_t)(cy0 + it * CPS) * kChunkBytes +
+                                             (size_t)t0 * kTileBytes;
+                        mbar_arrive_expect_tx(bar, nc * rowb);
+                        for (int c = 0; c < nc; ++c)
+                            bulk_g2s_hint(dst + c * rowb, src + (size_t)c * kChunkBytes, rowb, bar,
+                                          pol);
+                    }
                     if (++slot == NS) {
                         slot = 0;
                         ++round;
                     }
                 }
+                if (!x_issued) issue_x();
+                if (!ok) *abort_flag = 1;
+                // Drain: every issued copy must land before the CTA may exit.
+                mbar_wait(sbase + kBarX, 0, a.timeout_ns, a.status);
+                for (int i = (it > NS ? it - NS : 0); i < it; ++i)
+                    mbar_wait(sbase + kBarFull + 8 * (i % NS), (i / NS) & 1, a.timeout_ns, a.status);
+                mbar_wait(sbase + kBarSFull, 0, a.timeout_ns, a.status);
             }
-            if (!x_issued) issue_x();
-            if (!ok) *abort_flag = 1;
-            // Drain: every issued copy must land before the CTA may exit.
-            mbar_wait(sbase + kBarX, 0, a.timeout_ns, a.status);
-            for (int i = (it > NS ? it - NS : 0); i < it; ++i)
-                mbar_wait(sbase + kBarFull + 8 * (i % NS), (i / NS) & 1, a.timeout_ns, a.status);
-            for (int j = (sb_issued > a.n_sbuf ? sb_issued - a.n_sbuf : 0); j < sb_issued; ++j)
-                mbar_wait(sbase + kBarSFull + 8 * (j % a.n_sbuf), (j / a.n_sbuf) & 1, a.timeout_ns,
-                          a.status);
         }
         __syncwarp();
     } else {
         // =============================== consumers ==============================
         grid_dependency_wait();
         const int g = lane >> 2, t = lane & 3;
-        const int row0 = warp * 16 + g;  // rows of this lane's fragments in the block
+        const int ti = warp / W;         // tile of this warp within the CTA's rows
+        const int ks = warp - ti * W;    // its share of every stage's groups
+        const int row0 = ti * 16 + g;    // rows of this lane's fragments among the CTA's rows
         const int row1 = row0 + 8;
         // x rows: lanes beyond M read row M-1; their MMA columns are discarded.
         const int xr0 = g < a.M ? g : a.M - 1;
         const int xr1 = g + 8 < a.M ? g + 8 : a.M - 1;
         const uint32_t x0 = sbase + a.off_x + xr0 * a.xs_stride + t * 32;
         const uint32_t x1 = sbase + a.off_x + xr1 * a.xs_stride + t * 32;
-        const uint32_t wl = ring + warp * 512 + lane * 16;
-        const int nfull = nck / kChunksPerStage;       // stages holding two groups
-        const bool tail = (nck % kChunksPerStage) != 0;  // one group left
+        const uint32_t cs = (uint32_t)(T * kTileBytes);  // bytes between chunks in a stage
+        const uint32_t wl = ring + ti * kTileBytes + lane * 16;
 
         bool ok = mbar_wait(sbase + kBarX, 0, a.timeout_ns, a.status);
         // Activation sums per group and row, Sx[gl][m] in FP32, for the bias
@@ -317,8 +442,9 @@ __global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2) gemv_kernel(con
         const int NS = a.nstages;
         int slot = 0;
         uint32_t phase = 0;  // parity of the ring's current pass
+        float part[MT][4] = {};  // sub-block units: this warp's sums, for the in-CTA reduction
         for (int j = 0; ok && j < nblk; ++j) {
-            const int rb = (int)blockIdx.y + j * (int)gridDim.y;
+            const int rb = block_of(j);
             const int sbuf = j % a.n_sbuf;
             if (!mbar_wait(sbase + kBarSFull + 8 * sbuf, (j / a.n_sbuf) & 1, a.timeout_ns,
                            a.status)) {
@@ -334,61 +460,97 @@ __global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2) gemv_kernel(con
 #pragma unroll
                 for (int e = 0; e < 4; ++e) acc[mt][e] = 0.0f;
 
-            uint32_t xs_off = 0;
-            for (int st = 0; st < nfull; ++st, xs_off += kChunksPerStage * 128) {
-                if (!mbar_wait(sbase + kBarFull + 8 * slot, phase, a.timeout_ns, a.status)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t wa = wl + slot * kStageBytes;
+            if constexpr (WHOLE) {
+                // Whole blocks: every stage holds two groups of the warp's
+                // tile, except a one-group tail when the K range has an odd
+                // number of groups.
+                const int nfull = nck / 4;
+                uint32_t xs_off = 0;
+                for (int st = 0; st < nfull; ++st, xs_off += 4 * 128) {
+                    if (!mbar_wait(sbase + kBarFull + 8 * slot, phase, a.timeout_ns, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t wa = wl + slot * kStageBytes;
 #pragma unroll
-                for (int gi = 0; gi < kGroupsPerStage; ++gi) {
-                    const int gl = st * kGroupsPerStage + gi;
-                    mma_group<MT>(wa + gi * 2 * kChunkBytes, x0 + xs_off + gi * 256,
-                                  x1 + xs_off + gi * 256, sxl + gl * 64, __half2float(sc0[gl]),
-                                  __half2float(sc1[gl]), acc);
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(sbase + kBarEmpty + 8 * slot);
-                if (++slot == NS) {
-                    slot = 0;
-                    phase ^= 1u;
-                }
-            }
-            if (ok && tail) {
-                if (!mbar_wait(sbase + kBarFull + 8 * slot, phase, a.timeout_ns, a.status)) {
-                    ok = false;
-                } else {
-                    const int gl = nfull * kGroupsPerStage;
-                    mma_group<MT>(wl + slot * kStageBytes, x0 + xs_off, x1 + xs_off, sxl + gl * 64,
-                                  __half2float(sc0[gl]), __half2float(sc1[gl]), acc);
+                    for (int gi = 0; gi < 2; ++gi) {
+                        const int gl = st * 2 + gi;
+                        mma_group<MT>(wa + gi * 2 * kChunkBytes, kChunkBytes, x0 + xs_off + gi * 256,
+                                      x1 + xs_off + gi * 256, sxl + gl * 64, __half2float(sc0[gl]),
+                                      __half2float(sc1[gl]), acc);
+                    }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(sbase + kBarEmpty + 8 * slot);
+                    if (++slot == NS) {
+                        slot = 0;
+                        phase ^= 1u;
+                    }
                 }
-                if (++slot == NS) {
-                    slot = 0;
-                    phase ^= 1u;
+                if (ok && (nck & 3)) {
+                    if (!mbar_wait(sbase + kBarFull + 8 * slot, phase, a.timeout_ns, a.status)) {
+                        ok = false;
+                    } else {
+                        const int gl = nfull * 2;
+                        mma_group<MT>(wl + slot * kStageBytes, kChunkBytes, x0 + xs_off, x1 + xs_off,
+                                      sxl + gl * 64, __half2float(sc0[gl]), __half2float(sc1[gl]),
+                                      acc);
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(sbase + kBarEmpty + 8 * slot);
+                    }
+                    if (++slot == NS) {
+                        slot = 0;
+                        phase ^= 1u;
+                    }
+                }
+            } else {
+                // Sub-block units: a stage holds GPS groups of T tiles; the W
+                // warps of a tile take two groups each.
+                for (int st = 0; st < nstg; ++st) {
+                    if (!mbar_wait(sbase + kBarFull + 8 * slot, phase, a.timeout_ns, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    const int gs = min(GPS, ng - st * GPS);     // groups in this stage
+                    const int gsl0 = ks * kGroupsPerWarpStage;  // this warp's first group in it
+                    const int gl0 = st * GPS + gsl0;
+                    const uint32_t wa = wl + slot * kStageBytes + gsl0 * 2 * cs;
+                    if (gs == GPS) {
+#pragma unroll
+                        for (int gi = 0; gi < kGroupsPerWarpStage; ++gi)
+                            mma_group<MT>(wa + gi * 2 * cs, cs, x0 + (gl0 + gi) * 256,
+                                          x1 + (gl0 + gi) * 256, sxl + (gl0 + gi) * 64,
+                                          __half2float(sc0[gl0 + gi]), __half2float(sc1[gl0 + gi]),
+                                          acc);
+                    } else {
+                        for (int gi = 0; gi < kGroupsPerWarpStage && gsl0 + gi < gs; ++gi)
+                            mma_group<MT>(wa + gi * 2 * cs, cs, x0 + (gl0 + gi) * 256,
+                                          x1 + (gl0 + gi) * 256, sxl + (gl0 + gi) * 64,
+                                          __half2float(sc0[gl0 + gi]), __half2float(sc1[gl0 + gi]),
+                                          acc);
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(sbase + kBarEmpty + 8 * slot);
+                    if (++slot == NS) {
+                        slot = 0;
+                        phase ^= 1u;
+                    }
                 }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(sbase + kBarSEmpty + 8 * sbuf);
+            if constexpr (!WHOLE) {
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) part[mt][e] = acc[mt][e];
+                break;  // one unit per CTA
+            }
             if (!ok) break;
 
             const int R0 = rb * kBlockRows + row0;
             const int R1 = rb * kBlockRows + row1;
             if (S == 1) {
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    const int m0 = mt * 8 + 2 * t, m1 = m0 + 1;
-                    if (m0 < a.M) {
-                        if (R0 < a.N) a.y[(size_t)m0 * a.N + R0] = __float2half_rn(acc[mt][0]);
-                        if (R1 < a.N) a.y[(size_t)m0 * a.N + R1] = __float2half_rn(acc[mt][2]);
-                    }
-                    if (m1 < a.M) {
-                        if (R0 < a.N) a.y[(size_t)m1 * a.N + R0] = __float2half_rn(acc[mt][1]);
-                        if (R1 < a.N) a.y[(size_t)m1 * a.N + R1] = __float2half_rn(acc[mt][3]);
-                    }
-                }
+                store_y<MT>(a, R0, R1, t, acc);
             } else {
                 // One block per CTA in split mode: push the partials straight
                 // into the owner of each row (CTA row % S), slot [split][row / S].
@@ -401,6 +563,33 @@ __global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2) gemv_kernel(con
                     st_cluster_v2f(map_to_cta(d0 + c, (uint32_t)(row0 % S)), acc[mt][0], acc[mt][1]);
                     st_cluster_v2f(map_to_cta(d1 + c, (uint32_t)(row1 % S)), acc[mt][2], acc[mt][3]);
                 }
+            }
+        }
+        if constexpr (!WHOLE) {
+            // The W warps of a tile hold sums over disjoint groups of its
+            // rows: the first adds the others' in warp order (fixed, so
+            // repeated calls agree bit for bit) and writes the rows.
+            float4* red = reinterpret_cast<float4*>(smem + a.off_red);  // [warp][MT][lane]
+            if (ks > 0) {
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt)
+                    red[(warp * MT + mt) * 32 + lane] =
+                        make_float4(part[mt][0], part[mt][1], part[mt][2], part[mt][3]);
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+            if (ks == 0 && ok) {
+                for (int w2 = 1; w2 < W; ++w2) {
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt) {
+                        const float4 v = red[((warp + w2) * MT + mt) * 32 + lane];
+                        part[mt][0] += v.x;
+                        part[mt][1] += v.y;
+                        part[mt][2] += v.z;
+                        part[mt][3] += v.w;
+                    }
+                }
+                const int rbase = block_of(0) * kBlockRows + t0 * 16;
+                store_y<MT>(a, rbase + row0, rbase + row1, t, part);
             }
         }
         if (!ok) *abort_flag = 1;
@@ -427,8 +616,23 @@ __global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2) gemv_kernel(con
     }
 }
 
+// Whole 128-row blocks per CTA (split or persistent launches).
+template <int MT>
+__global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2)
+    gemv_kernel(const __grid_constant__ GemvArgs a) {
+    gemv_body<MT, true>(nullptr, a);
+}
+
+// Sub-block units of a.T tiles, weights copied through the tensor map.
+template <int MT>
+__global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2)
+    gemv_unit_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ GemvArgs a) {
+    gemv_body<MT, false>(&wmap, a);
+}
+
 struct GemvPlan {
     int S = 0;
+    int T = kConsumerWarps;
     int grid_y = 0;
     int n_sbuf = 1;
     int nstages = kStages;
@@ -436,16 +640,18 @@ struct GemvPlan {
     int slab_bytes = 0;
     int rpo = 0;
     uint32_t off_ring = 0, off_x = 0, off_s = 0, off_red = 0, off_sx = 0, smem = 0;
-    double eff = 0.0;
+    double cost = 0.0;
 };
 
-template <int MT>
+template <int MT, bool WHOLE = true>
 int occupancy(uint32_t smem) {
     int blocks = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, gemv_kernel<MT>, kGemvThreads,
-                                                      smem) != cudaSuccess)
-        return 0;
-    return blocks;
+    const cudaError_t e =
+        WHOLE ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, gemv_kernel<MT>, kGemvThreads,
+                                                              smem)
+              : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, gemv_unit_kernel<MT>,
+                                                              kGemvThreads, smem);
+    return e == cudaSuccess ? blocks : 0;
 }
 
 template <int MT>
@@ -474,79 +680,137 @@ cudaError_t ensure_smem_attr() {
     if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(gemv_kernel<MT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemv_unit_kernel<MT>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
     return e;
 }
 
-// Shared-memory layout of a launch with K split S and `nsb` scale buffers.
+// Shared-memory layout of a launch with K split S, T tiles per CTA and
+// `nsb` scale buffers.
 template <int MT>
-bool layout(GemvPlan& p, int M, int G, int S, int nsb, const DeviceCtx& ctx, int nst = kStages) {
+bool layout(GemvPlan& p, int M, int G, int S, int T, int nsb, const DeviceCtx& ctx,
+            int nst = kStages) {
     p.S = S;
+    p.T = T;
     p.n_sbuf = nsb;
-    p.nstages = nst;
     const int ng_max = (G + S - 1) / S;
+    // a CTA that sees only one block needs no more stages than it fills
+    const int fill = (2 * ng_max * T * kTileBytes + kStageBytes - 1) / kStageBytes;
+    p.nstages = nsb == 1 && fill < nst ? fill : nst;
     p.xs_stride = ng_max * kGroup * 2 + 16;  // +16 B keeps x rows conflict-free
-    p.slab_bytes = ((kBlockRows * G * 2 + 127) / 128) * 128;
+    p.slab_bytes = ((16 * T * G * 2 + 127) / 128) * 128;
     p.off_ring = kBarAreaBytes;
     p.off_x = p.off_ring + p.nstages * kStageBytes;
     p.off_s = p.off_x + ((M * p.xs_stride + 127) / 128) * 128;
     p.off_red = p.off_s + nsb * p.slab_bytes;
     p.rpo = (kBlockRows + S - 1) / S;
-    p.off_sx = p.off_red + (S > 1 ? S * p.rpo * 16 * 4 : 0);
+    const int red_bytes = S > 1 ? S * p.rpo * 16 * 4
+                          : T < kConsumerWarps ? kConsumerWarps * MT * 32 * 16
+                                               : 0;
+    p.off_sx = p.off_red + red_bytes;
     p.smem = p.off_sx + ng_max * 16 * 4;
     return (int)p.smem <= ctx.max_smem_optin;
 }
 
-// Chooses the K split S (cluster size).  With more 128-row blocks than CTA
-// slots the grid is persistent (S = 1, one CTA per slot walking blocks).
-// Otherwise every CTA handles one block's K range 1/S and S is chosen so the
-// heaviest SM carries as little as possible; near-ties go to the larger S
-// (more, shorter CTAs hide latency better).
+// Launch-time model (microseconds) used to rank the candidate launches,
+// fitted to GB300 timings of every candidate on the Llama-3-8B and
+// Qwen2.5-7B decode shapes at M = 1..16.  A CTA wave costs a fixed start-up
+// plus the longer of (a) the heaviest SM streaming its CTAs' weights at the
+// per-SM rate seen when every SM streams, and (b) one CTA streaming its own
+// weights, which its 8 consumer warps cap (at half the rate with two n8
+// tiles, M > 8); copying and summing the CTA's activation slice (M x its K
+// range) adds to both.  A K split adds the cluster barrier and the exchange
+// of partial sums through distributed shared memory.
+constexpr double kWaveUs = 1.5;
+constexpr double kSmBytesPerUs = 36.0e3;
+constexpr double kCtaBytesPerUs = 14.0e3;
+constexpr double kXBytesPerUs = 16.0e3;
+constexpr double kSplitReduceUs = 1.6;
+
+template <int MT>
+double launch_cost(long long units, long long slots, double w_bytes, double x_bytes, int S,
+                   const DeviceCtx& ctx) {
+    const long long waves = (units + slots - 1) / slots;
+    const long long per_wave = units < slots ? units : slots;
+    const long long heaviest = (per_wave + ctx.num_sms - 1) / ctx.num_sms;
+    const double x_us = x_bytes / kXBytesPerUs;
+    const double sm_us = (double)heaviest * (w_bytes / kSmBytesPerUs + x_us);
+    const double cta_us = w_bytes * MT / kCtaBytesPerUs + x_us;
+    return (double)waves * (kWaveUs + (sm_us > cta_us ? sm_us : cta_us)) +
+           (S > 1 ? kSplitReduceUs : 0.0);
+}
+
+// Chooses the launch.  With more 128-row blocks than CTA slots the grid is
+// persistent (whole blocks, one CTA per slot walking blocks).  Otherwise the
+// cheapest under launch_cost of
+//  * whole blocks with K split S ways over a cluster of S CTAs (S = 1..8),
+//  * sub-block units of T = 1, 2 or 4 tiles (16 T rows) over the whole K
+//    range, the 8 warps splitting K and reducing inside the CTA, each with
+//    the deepest ring that keeps the CTAs per SM its units need.
 template <int MT>
 GemvPlan plan_gemv(int M, int N, int K, const DeviceCtx& ctx) {
     const int G = K / kGroup;
     const int NB = (N + kBlockRows - 1) / kBlockRows;
-    GemvPlan best;
     {
         GemvPlan p;
-        if (layout<MT>(p, M, G, 1, 2, ctx)) {
+        if (layout<MT>(p, M, G, 1, kConsumerWarps, 2, ctx)) {
             const int occ = occupancy<MT>(p.smem);
             if (occ > 0 && NB > ctx.num_sms * occ) {
                 // The deepest ring that keeps the same CTAs per SM: more bytes
                 // in flight per CTA, for the same number of streams.
                 for (int nst = kMaxStages; nst > kStages; --nst) {
                     GemvPlan q;
-                    if (layout<MT>(q, M, G, 1, 2, ctx, nst) && occupancy<MT>(q.smem) == occ) {
+                    if (layout<MT>(q, M, G, 1, kConsumerWarps, 2, ctx, nst) &&
+                        occupancy<MT>(q.smem) == occ) {
                         p = q;
                         break;
                     }
                 }
                 p.grid_y = ctx.num_sms * occ;
-                p.eff = 1.0;
+                p.cost = 0.0;
                 return p;
             }
         }
     }
-    const double per_sm = (double)NB / ctx.num_sms;
+    GemvPlan best;
     const int max_s = G < kMaxSplits ? G : kMaxSplits;
     for (int S = 1; S <= max_s; ++S) {
         GemvPlan p;
-        if (!layout<MT>(p, M, G, S, 1, ctx)) continue;
+        if (!layout<MT>(p, M, G, S, kConsumerWarps, 1, ctx)) continue;
         const int occ = occupancy<MT>(p.smem);
         if (occ == 0) continue;
-        const long long units = (long long)NB * S;
         // Clusters live inside one GPC: count co-resident clusters, not SM slots.
         const long long slots =
             S == 1 ? (long long)ctx.num_sms * occ : (long long)max_active_clusters<MT>(S, p.smem) * S;
-        const long long heaviest = (units + ctx.num_sms - 1) / ctx.num_sms;
-        double eff = per_sm / ((double)heaviest / S);
-        // more than one wave of CTAs: each wave pays its own start-up and
-        // x / reduction latency, so count every wave as a whole pass
-        if (units > slots) eff /= (double)((units + slots - 1) / slots);
-        eff += 0.001 * S;
+        if (slots == 0) continue;
+        const int ng = (G + S - 1) / S;
         p.grid_y = NB;
-        p.eff = eff;
-        if (eff > best.eff) best = p;
+        p.cost = launch_cost<MT>((long long)NB * S, slots, (double)ng * kBlockRows * kGroup / 2,
+                                 (double)M * ng * kGroup * 2, S, ctx);
+        if (best.S == 0 || p.cost < best.cost) best = p;
+    }
+    for (int T = 1; T < kConsumerWarps; T *= 2) {
+        GemvPlan p;
+        if (!layout<MT>(p, M, G, 1, T, 1, ctx)) continue;
+        const int occ = occupancy<MT, false>(p.smem);
+        if (occ == 0) continue;
+        const long long units = ((long long)N + 16 * T - 1) / (16 * T);
+        const long long fit = (units + ctx.num_sms - 1) / ctx.num_sms;
+        const int need = fit < occ ? (int)fit : occ;
+        for (int nst = kMaxStages; nst > p.nstages; --nst) {
+            GemvPlan q;
+            if (layout<MT>(q, M, G, 1, T, 1, ctx, nst) && q.nstages == nst &&
+                occupancy<MT, false>(q.smem) >= need) {
+                p = q;
+                break;
+            }
+        }
+        p.grid_y = (int)units;
+        p.cost = launch_cost<MT>(units, (long long)ctx.num_sms * occ,
+                                 (double)G * 16 * T * kGroup / 2, (double)M * G * kGroup * 2, 1, ctx);
+        if (best.S == 0 || p.cost < best.cost) best = p;
     }
     return best;
 }
@@ -576,6 +840,46 @@ GemvPlan cached_plan(int M, int N, int K, const DeviceCtx& ctx) {
     return p;
 }
 
+// The tensor map of a sub-block launch: the kernel layout as [NB * C chunk
+// rows] x [512 eight-byte words]; a box is T tiles (64 T words) of 32 / T
+// consecutive chunks, 16 KB.  Encoded once per (weights, shape, T) and
+// reused: a decode step calls the same weights every token.
+cudaError_t weight_map(const uint8_t* wq, int NB, int K, int T, CUtensorMap* out) {
+    struct Entry {
+        const uint8_t* wq;
+        int NB, K, T;
+        CUtensorMap map;
+    };
+    static std::mutex mu;
+    static std::vector<Entry> cache;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (const Entry& e : cache)
+            if (e.wq == wq && e.NB == NB && e.K == K && e.T == T) {
+                *out = e.map;
+                return cudaSuccess;
+            }
+    }
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode) return cudaErrorNotSupported;
+    Entry e{wq, NB, K, T, {}};
+    const cuuint64_t dims[2] = {(cuuint64_t)(kChunkBytes / 8),
+                                (cuuint64_t)NB * (cuuint64_t)(K / kChunkK)};
+    const cuuint64_t strides[1] = {(cuuint64_t)kChunkBytes};
+    const cuuint32_t box[2] = {(cuuint32_t)(T * kTileBytes / 8),
+                               (cuuint32_t)(kStageBytes / (T * kTileBytes))};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&e.map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint8_t*>(wq), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    *out = e.map;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache.size() >= 4096) cache.clear();
+    cache.push_back(e);
+    return cudaSuccess;
+}
+
 template <int MT>
 cudaError_t launch_gemv_mt(GemvArgs args, int M, cudaStream_t stream, const DeviceCtx& ctx) {
     cudaError_t e = ensure_smem_attr<MT>();
@@ -592,6 +896,12 @@ cudaError_t launch_gemv_mt(GemvArgs args, int M, cudaStream_t stream, const Devi
     args.off_red = p.off_red;
     args.off_sx = p.off_sx;
     args.rpo = p.rpo;
+    args.T = p.T;
+    CUtensorMap wmap;
+    if (p.T < kConsumerWarps) {
+        const cudaError_t me = weight_map(args.wq, args.NB, args.K, p.T, &wmap);
+        if (me != cudaSuccess) return me;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.S, (unsigned)p.grid_y, 1);
     cfg.blockDim = dim3(kGemvThreads, 1, 1);
@@ -611,13 +921,14 @@ cudaError_t launch_gemv_mt(GemvArgs args, int M, cudaStream_t stream, const Devi
     }
     cfg.attrs = attrs;
     cfg.numAttrs = na;
+    if (p.T < kConsumerWarps) return cudaLaunchKernelEx(&cfg, gemv_unit_kernel<MT>, wmap, args);
     return cudaLaunchKernelEx(&cfg, gemv_kernel<MT>, args);
 }
 
 }  // namespace
 
 cudaError_t gemv_plan_info(int M, int64_t N, int64_t K, const DeviceCtx& ctx, int* splits,
-                           int* ctas, int* blocks_per_cta) {
+                           int* ctas, int* blocks_per_cta, int* rows_per_cta) {
     cudaError_t e = M <= 8 ? ensure_smem_attr<1>() : ensure_smem_attr<2>();
     if (e != cudaSuccess) return e;
     const GemvPlan p = M <= 8 ? cached_plan<1>(M, (int)N, (int)K, ctx)
@@ -626,7 +937,8 @@ cudaError_t gemv_plan_info(int M, int64_t N, int64_t K, const DeviceCtx& ctx, in
     const int NB = (int)((N + kBlockRows - 1) / kBlockRows);
     *splits = p.S;
     *ctas = p.S * p.grid_y;
-    *blocks_per_cta = (NB + p.grid_y - 1) / p.grid_y;
+    *blocks_per_cta = p.T == kConsumerWarps ? (NB + p.grid_y - 1) / p.grid_y : 1;
+    *rows_per_cta = 16 * p.T;
     return cudaSuccess;
 }
 

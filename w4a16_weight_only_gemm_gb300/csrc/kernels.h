@@ -2,6 +2,7 @@
 // library; the public C ABI is include/w4a16.h).
 #pragma once
 
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -20,6 +21,9 @@ constexpr int kBlockRows = 128;
 constexpr int kChunkK = 64;
 constexpr int kGroup = 128;
 
+// The driver's cuTensorMapEncodeTiled, resolved once (null if unavailable).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+
 cudaError_t launch_quantize(const void* W, int64_t N, int64_t K, void* qweight, void* scales,
                             cudaStream_t stream, const DeviceCtx& ctx);
 cudaError_t launch_repack(const void* qweight, int64_t N, int64_t K, void* repacked,
@@ -28,10 +32,10 @@ cudaError_t launch_unrepack(const void* repacked, int64_t N, int64_t K, void* qw
                             cudaStream_t stream, const DeviceCtx& ctx);
 cudaError_t launch_gemv(const void* x, const void* repacked, const void* scales, void* y, int M,
                         int64_t N, int64_t K, cudaStream_t stream, const DeviceCtx& ctx);
-// The launch the decode GEMV would make: K split (cluster size), CTAs and
-// the most 128-row blocks one CTA walks.
+// The launch the decode GEMV would make: K split (cluster size), CTAs, the
+// most 128-row blocks one CTA walks and the weight rows of one CTA's unit.
 cudaError_t gemv_plan_info(int M, int64_t N, int64_t K, const DeviceCtx& ctx, int* splits,
-                           int* ctas, int* blocks_per_cta);
+                           int* ctas, int* blocks_per_cta, int* rows_per_cta);
 // The launch the tensor-core GEMM would make: cluster size (1: one CTA per
 // 128 x 128 tile; 2: CTA pairs with 2-CTA MMAs; 4, 6 or 8: CTA pairs
 // splitting K two, three or four ways, reduced over the cluster) and CTAs.

@@ -1,5 +1,5 @@
-// tcgen05.cuh -- 5th-generation tensor core (tcgen05) and tensor-map TMA
-// helpers for sm_103a, written as inline PTX.
+// tcgen05.cuh -- 5th-generation tensor core (tcgen05) helpers for sm_103a,
+// written as inline PTX.
 //
 // Shared-memory matrix descriptor (64 bit) for tcgen05.mma operands:
 //   bits  0-13  start address >> 4
@@ -128,21 +128,6 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
 
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// --- tensor-map TMA --------------------------------------------------------
-__device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-
-// 2-D tiled load; c0 is the innermost coordinate (elements).
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
-        : "memory");
 }
 
 }  // namespace w4a16

@@ -112,14 +112,14 @@ def gemm(x: torch.Tensor, repacked: torch.Tensor, scales: torch.Tensor,
 
 def gemm_plan(M: int, N: int, K: int) -> dict:
     """The launch gemm() makes for (M, N, K) on the current device:
-    {"path": "gemv" | "tensor_core", "splits", "ctas", "blocks_per_cta"}."""
-    out = [ctypes.c_int(0) for _ in range(4)]
+    {"path": "gemv" | "tensor_core", "splits", "ctas", "blocks_per_cta", "rows_per_cta"}."""
+    out = [ctypes.c_int(0) for _ in range(5)]
     _native.check(_native.lib().w4a16_gemm_plan(int(M), int(N), int(K),
                                                 *[ctypes.byref(o) for o in out]),
                   "w4a16_gemm_plan")
     path = {1: "gemv", 2: "tensor_core"}[out[0].value]
     return {"path": path, "splits": out[1].value, "ctas": out[2].value,
-            "blocks_per_cta": out[3].value}
+            "blocks_per_cta": out[3].value, "rows_per_cta": out[4].value}
 
 
 def device_status() -> int:
