@@ -286,7 +286,7 @@ def run_ours(args, rank, world):
         "peak": peaks.get("hbm_gbs", 6800.0), "unit": "GB/s",
         "frac": round(per_rank_gbs / peaks.get("hbm_gbs", 6800.0), 3),
         "peak_source": "measured" if "hbm_gbs" in peaks else "fallback",
-        "kernel": "gemv_kernel<1> (all launches of the step)",
+        "kernel": "gemv_unit_kernel<1> + gemv_kernel<1> (all launches of the step)",
         "bytes_per_launch": step_bytes / len(layers),
         "traffic": recorded_traffic(),
     }
