@@ -13,7 +13,9 @@ section:
 
 * "LLM quantization from IEEE 754 to GPTQ/AWQ/GGUF" tutorial (qaqbuyan.com
   article 126), chapter "量化的数学基石": §1 FP16 bit layout, §2 symmetric
-  quantization formula, §3 per-group quantizer/dequantizer functions.
+  and asymmetric quantization formulas, §3 quantization granularity
+  (per-channel, per-group with group 128 or 32) and the per-group
+  quantizer/dequantizer functions.
 * "W4A16 量化算子解码性能基准跑分与端侧大模型推理显存实测报告" (mhpq.cn):
   §一 format (group 128, symmetric INT4, fp16 scales), §二/§五 the decode
   product y = x W^T from the packed weights.
@@ -77,13 +79,15 @@ def _bind(lib):
     lib.orc_float_to_half_n.argtypes = [p, i64, p]
     lib.orc_quantize.argtypes = [p, i64, i64, i64, p, p]
     lib.orc_quantize.restype = ctypes.c_int
-    lib.orc_dequantize.argtypes = [p, p, i64, i64, i64, p]
+    lib.orc_quantize_asym.argtypes = [p, i64, i64, i64, p, p, p]
+    lib.orc_quantize_asym.restype = ctypes.c_int
+    lib.orc_dequantize.argtypes = [p, p, p, i64, i64, i64, p]
     lib.orc_dequantize.restype = ctypes.c_int
-    lib.orc_dequantize_f16.argtypes = [p, p, i64, i64, i64, p]
+    lib.orc_dequantize_f16.argtypes = [p, p, p, i64, i64, i64, p]
     lib.orc_dequantize_f16.restype = ctypes.c_int
-    lib.orc_gemm.argtypes = [p, i64, i64, p, p, i64, i64, p]
+    lib.orc_gemm.argtypes = [p, i64, i64, p, p, p, i64, i64, p]
     lib.orc_gemm.restype = ctypes.c_int
-    lib.orc_gemm_rows.argtypes = [p, i64, i64, p, p, i64, i64, p, i64, p]
+    lib.orc_gemm_rows.argtypes = [p, i64, i64, p, p, p, i64, i64, p, i64, p]
     lib.orc_gemm_rows.restype = ctypes.c_int
     lib.orc_num_threads.restype = ctypes.c_int
     lib.orc_set_num_threads.argtypes = [ctypes.c_int]
@@ -96,6 +100,15 @@ def _c(a: np.ndarray, dtype) -> np.ndarray:
 
 def _ptr(a: np.ndarray) -> int:
     return a.ctypes.data
+
+
+def _zptr(zeros) -> int | None:
+    return None if zeros is None else zeros.ctypes.data
+
+
+def _group(group: int, K: int) -> int:
+    """group = -1 means per-channel: one group spanning the row."""
+    return K if group == -1 else group
 
 
 class Oracle:
@@ -139,12 +152,14 @@ class Oracle:
         """Group-wise symmetric RTN INT4 quantization of fp16 weights.
 
         ``W16``: uint16 fp16 bit patterns, shape [N, K] (rows = out_features).
+        ``group``: weights per scale along K; -1 = per-channel (one group per row).
         Returns ``(qweight uint8 [N, K/2], scales uint16 fp16 bits [N, K/group])``.
         """
         W16 = _c(W16, np.uint16)
         if W16.ndim != 2:
             raise ValueError("W must be 2-D [N, K]")
         N, K = W16.shape
+        group = _group(group, K)
         if group <= 0 or K % group:
             raise ValueError(f"K={K} is not a multiple of group={group}")
         q = np.empty((N, K // 2), dtype=np.uint8)
@@ -155,34 +170,67 @@ class Oracle:
         return q, s
 
     # ------------------------------------------------------------------
+    # Asymmetric quantizer (tutorial §2 asymmetric formula).  Pinned:
+    # integer-grid fixtures (min -> 0, max -> 15, z exact), constant and
+    # all-zero groups, nearest-level and nearest-zero-point brute force,
+    # round-trip bound, scale through numpy.
+    # ------------------------------------------------------------------
+    def quantize_asym(self, W16: np.ndarray, group: int = GROUP):
+        """Group-wise asymmetric RTN INT4 quantization of fp16 weights.
+
+        Returns ``(qweight uint8 [N, K/2] holding q in [0, 15],
+        scales uint16 fp16 bits [N, K/group], zeros uint8 [N, K/group])``."""
+        W16 = _c(W16, np.uint16)
+        if W16.ndim != 2:
+            raise ValueError("W must be 2-D [N, K]")
+        N, K = W16.shape
+        group = _group(group, K)
+        if group <= 0 or K % group:
+            raise ValueError(f"K={K} is not a multiple of group={group}")
+        q = np.empty((N, K // 2), dtype=np.uint8)
+        s = np.empty((N, K // group), dtype=np.uint16)
+        z = np.empty((N, K // group), dtype=np.uint8)
+        rc = self._lib.orc_quantize_asym(_ptr(W16), N, K, group, _ptr(q), _ptr(s), _ptr(z))
+        if rc != 0:
+            raise ValueError(f"oracle quantize_asym rejected shape N={N} K={K} group={group}")
+        return q, s, z
+
+    # ------------------------------------------------------------------
     # Dequantizer (tutorial §3 per_group_symmetric_dequantize).  Pinned:
     # closed forms and the round-trip bound against the master weights.
     # ------------------------------------------------------------------
     def dequantize(self, qweight: np.ndarray, scales: np.ndarray,
-                   group: int = GROUP) -> np.ndarray:
-        """Exact dequantized weights (nibble - 8) * scale16 in binary64, [N, K]."""
+                   group: int = GROUP, zeros: np.ndarray | None = None) -> np.ndarray:
+        """Exact dequantized weights (nibble - z) * scale16 in binary64, [N, K];
+        z = zeros[n, k / group] (asymmetric) or 8 (symmetric, zeros None)."""
         qweight = _c(qweight, np.uint8)
         scales = _c(scales, np.uint16)
+        zeros = None if zeros is None else _c(zeros, np.uint8)
         N, K2 = qweight.shape
         K = 2 * K2
+        group = _group(group, K)
         out = np.empty((N, K), dtype=np.float64)
-        rc = self._lib.orc_dequantize(_ptr(qweight), _ptr(scales), N, K, group, _ptr(out))
+        rc = self._lib.orc_dequantize(_ptr(qweight), _ptr(scales), _zptr(zeros), N, K, group,
+                                      _ptr(out))
         if rc != 0:
             raise ValueError("oracle dequantize rejected shape")
         return out
 
     def dequantize_f16(self, qweight: np.ndarray, scales: np.ndarray,
-                       group: int = GROUP) -> np.ndarray:
+                       group: int = GROUP, zeros: np.ndarray | None = None) -> np.ndarray:
         """The tutorial's own fp16 dequantized weight fp16(float(q) * float(s)).
 
         Returns uint16 fp16 bits [N, K].  Pinned: equals the single fp16
         rounding (numpy) of the exact dequantized value."""
         qweight = _c(qweight, np.uint8)
         scales = _c(scales, np.uint16)
+        zeros = None if zeros is None else _c(zeros, np.uint8)
         N, K2 = qweight.shape
         K = 2 * K2
+        group = _group(group, K)
         out = np.empty((N, K), dtype=np.uint16)
-        rc = self._lib.orc_dequantize_f16(_ptr(qweight), _ptr(scales), N, K, group, _ptr(out))
+        rc = self._lib.orc_dequantize_f16(_ptr(qweight), _ptr(scales), _zptr(zeros), N, K,
+                                          group, _ptr(out))
         if rc != 0:
             raise ValueError("oracle dequantize_f16 rejected shape")
         return out
@@ -193,36 +241,40 @@ class Oracle:
     # s = 1 gives y = sum_k x exactly.
     # ------------------------------------------------------------------
     def gemm(self, x16: np.ndarray, qweight: np.ndarray, scales: np.ndarray,
-             group: int = GROUP) -> np.ndarray:
+             group: int = GROUP, zeros: np.ndarray | None = None) -> np.ndarray:
         """y[m, n] = sum_k x[m, k] * Wd[n, k], binary64, unrounded.  x16: uint16 [M, K]."""
         x16 = _c(x16, np.uint16)
         qweight = _c(qweight, np.uint8)
         scales = _c(scales, np.uint16)
+        zeros = None if zeros is None else _c(zeros, np.uint8)
         M, K = x16.shape
         N = qweight.shape[0]
         if qweight.shape[1] * 2 != K:
             raise ValueError("x and qweight disagree on K")
+        group = _group(group, K)
         y = np.empty((M, N), dtype=np.float64)
-        rc = self._lib.orc_gemm(_ptr(x16), M, K, _ptr(qweight), _ptr(scales), N, group,
-                                _ptr(y))
+        rc = self._lib.orc_gemm(_ptr(x16), M, K, _ptr(qweight), _ptr(scales), _zptr(zeros), N,
+                                group, _ptr(y))
         if rc != 0:
             raise ValueError("oracle gemm rejected shape")
         return y
 
     def gemm_rows(self, x16: np.ndarray, qweight: np.ndarray, scales: np.ndarray,
-                  rows, group: int = GROUP) -> np.ndarray:
+                  rows, group: int = GROUP, zeros: np.ndarray | None = None) -> np.ndarray:
         """Columns ``rows`` of y only: returns [M, len(rows)] binary64."""
         x16 = _c(x16, np.uint16)
         qweight = _c(qweight, np.uint8)
         scales = _c(scales, np.uint16)
+        zeros = None if zeros is None else _c(zeros, np.uint8)
         rows = _c(np.asarray(rows), np.int64)
         M, K = x16.shape
         N = qweight.shape[0]
         if qweight.shape[1] * 2 != K:
             raise ValueError("x and qweight disagree on K")
+        group = _group(group, K)
         y = np.empty((M, rows.size), dtype=np.float64)
-        rc = self._lib.orc_gemm_rows(_ptr(x16), M, K, _ptr(qweight), _ptr(scales), N,
-                                     group, _ptr(rows), rows.size, _ptr(y))
+        rc = self._lib.orc_gemm_rows(_ptr(x16), M, K, _ptr(qweight), _ptr(scales), _zptr(zeros),
+                                     N, group, _ptr(rows), rows.size, _ptr(y))
         if rc != 0:
             raise ValueError("oracle gemm_rows rejected arguments")
         return y
@@ -249,20 +301,24 @@ def quantize(W16, group: int = GROUP):
     return default().quantize(W16, group)
 
 
-def dequantize(qweight, scales, group: int = GROUP):
-    return default().dequantize(qweight, scales, group)
+def quantize_asym(W16, group: int = GROUP):
+    return default().quantize_asym(W16, group)
 
 
-def dequantize_f16(qweight, scales, group: int = GROUP):
-    return default().dequantize_f16(qweight, scales, group)
+def dequantize(qweight, scales, group: int = GROUP, zeros=None):
+    return default().dequantize(qweight, scales, group, zeros)
 
 
-def gemm(x16, qweight, scales, group: int = GROUP):
-    return default().gemm(x16, qweight, scales, group)
+def dequantize_f16(qweight, scales, group: int = GROUP, zeros=None):
+    return default().dequantize_f16(qweight, scales, group, zeros)
 
 
-def gemm_rows(x16, qweight, scales, rows, group: int = GROUP):
-    return default().gemm_rows(x16, qweight, scales, rows, group)
+def gemm(x16, qweight, scales, group: int = GROUP, zeros=None):
+    return default().gemm(x16, qweight, scales, group, zeros)
+
+
+def gemm_rows(x16, qweight, scales, rows, group: int = GROUP, zeros=None):
+    return default().gemm_rows(x16, qweight, scales, rows, group, zeros)
 
 
 def num_threads() -> int:

@@ -11,7 +11,9 @@
  *        (qaqbuyan.com article 126), chapter "量化的数学基石":
  *          §1   FP16 bit layout  value = (-1)^S * 2^(E-15) * (1 + M/1024)
  *          §2   symmetric quantization  x_q = clamp(round(x/s), -8, 7),
- *               s = max|x| / 7
+ *               s = max|x| / 7; asymmetric quantization
+ *               x_q = clamp(round(x/s) + z, 0, 15), s = (max - min) / 15,
+ *               z = -round(min / s)
  *          §3   per-group granularity and the per_group_symmetric_quantize /
  *               per_group_symmetric_dequantize functions (groups along
  *               in_features, low nibble = even index, stored as q + 8,
@@ -27,6 +29,12 @@
  *     half_rne(s32);
  *   - round() is round-half-to-even (torch.round semantics);
  *   - the clamp(min=1e-8) is applied to s32 in binary32;
+ *   - asymmetric: min and max are taken over the group and 0 (the zero
+ *     point is the code of 0.0, so 0 lies in the quantized range and z is a
+ *     4-bit code in [0, 15]); the nibble stores q itself and the zero point
+ *     is stored as one byte per group; the same clamp(min=1e-8) guards s;
+ *   - per-channel quantization is one group spanning the whole row
+ *     (group = K);
  *   - the GEMM reference is the exact dequantized weight (nib-8)*scale16 in
  *     binary64, summed sequentially over k in binary64, never rounded to fp16.
  *
@@ -153,14 +161,14 @@ int orc_quantize(const uint16_t *W, int64_t N, int64_t K, int64_t group,
                  uint8_t *qweight, uint16_t *scales)
 {
     if (N < 0 || K <= 0 || group <= 0 || group % 2 != 0 || K % group != 0 ||
-        group > 4096)
+        group > 32768)
         return -1;
     int64_t ngroups = K / group;
 #ifdef _OPENMP
 #pragma omp parallel for schedule(static)
 #endif
     for (int64_t n = 0; n < N; ++n) {
-        int8_t q[4096];
+        int8_t q[32768];
         for (int64_t g = 0; g < ngroups; ++g) {
             const uint16_t *wg = W + n * K + g * group;
             scales[n * ngroups + g] = quantize_group(wg, group, q);
@@ -174,25 +182,85 @@ int orc_quantize(const uint16_t *W, int64_t N, int64_t K, int64_t group,
     return 0;
 }
 
+/* Quantize one group asymmetrically ([P4] §2 asymmetric formula).
+ * Returns the fp16 scale bits, writes q in [0, 15] and the zero point. */
+static uint16_t quantize_group_asym(const uint16_t *w16, int64_t group, uint8_t *q,
+                                    uint8_t *zero)
+{
+    /* min and max over the group and 0 */
+    float mn = 0.0f, mx = 0.0f;
+    for (int64_t i = 0; i < group; ++i) {
+        float v = (float)orc_half_to_double(w16[i]);
+        if (v < mn)
+            mn = v;
+        if (v > mx)
+            mx = v;
+    }
+    float s = (mx - mn) / 15.0f;  /* IEEE binary32 subtraction and division */
+    if (s < 1e-8f)
+        s = 1e-8f;
+    float z = -nearbyintf(mn / s); /* z = -round(min / s), in [0, 15] */
+
+    /* q = clamp(round(w / s) + z, 0, 15) with round-half-to-even */
+    for (int64_t i = 0; i < group; ++i) {
+        float w = (float)orc_half_to_double(w16[i]);
+        float rq = nearbyintf(w / s) + z;
+        if (rq < 0.0f)
+            rq = 0.0f;
+        if (rq > 15.0f)
+            rq = 15.0f;
+        q[i] = (uint8_t)rq;
+    }
+    *zero = (uint8_t)z;
+    return orc_float_to_half(s);
+}
+
+/* Asymmetric variant of orc_quantize: the nibbles hold q in [0, 15]
+ * (low nibble = even k), zeros: [N, K/group] bytes. */
+int orc_quantize_asym(const uint16_t *W, int64_t N, int64_t K, int64_t group,
+                      uint8_t *qweight, uint16_t *scales, uint8_t *zeros)
+{
+    if (N < 0 || K <= 0 || group <= 0 || group % 2 != 0 || K % group != 0 ||
+        group > 32768)
+        return -1;
+    int64_t ngroups = K / group;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+    for (int64_t n = 0; n < N; ++n) {
+        uint8_t q[32768];
+        for (int64_t g = 0; g < ngroups; ++g) {
+            const uint16_t *wg = W + n * K + g * group;
+            scales[n * ngroups + g] = quantize_group_asym(wg, group, q, &zeros[n * ngroups + g]);
+            for (int64_t i = 0; i < group; i += 2)
+                qweight[n * (K / 2) + (g * group + i) / 2] =
+                    (uint8_t)(((q[i + 1] & 0x0f) << 4) | (q[i] & 0x0f));
+        }
+    }
+    return 0;
+}
+
 /* ------------------------------------------------------------------ */
 /* Dequantizer: [P4] §3 per_group_symmetric_dequantize, kept exact.     */
 /* ------------------------------------------------------------------ */
 
-/* Exact dequantized weight of row n: (nibble - 8) * scale16, in binary64.
- * An fp16 scale times an integer of magnitude <= 8 needs at most 15
- * significant bits, so binary64 holds it exactly. */
-static void dequant_row(const uint8_t *qrow, const uint16_t *srow, int64_t K,
-                        int64_t group, double *out)
+/* Exact dequantized weight of row n: (nibble - z) * scale16 in binary64,
+ * z the group's zero point (asymmetric: zrow != NULL) or 8 (symmetric: the
+ * nibble holds q + 8).  An fp16 scale times an integer of magnitude <= 15
+ * needs at most 15 significant bits, so binary64 holds it exactly. */
+static void dequant_row(const uint8_t *qrow, const uint16_t *srow, const uint8_t *zrow,
+                        int64_t K, int64_t group, double *out)
 {
     for (int64_t k = 0; k < K; ++k) {
         uint8_t byte = qrow[k / 2];
         int nib = (k % 2 == 0) ? (byte & 0x0f) : ((byte >> 4) & 0x0f);
-        out[k] = (double)(nib - 8) * orc_half_to_double(srow[k / group]);
+        int z = zrow ? zrow[k / group] : 8;
+        out[k] = (double)(nib - z) * orc_half_to_double(srow[k / group]);
     }
 }
 
-int orc_dequantize(const uint8_t *qweight, const uint16_t *scales, int64_t N,
-                   int64_t K, int64_t group, double *out)
+int orc_dequantize(const uint8_t *qweight, const uint16_t *scales, const uint8_t *zeros,
+                   int64_t N, int64_t K, int64_t group, double *out)
 {
     if (N < 0 || K <= 0 || group <= 0 || K % group != 0 || K % 2 != 0)
         return -1;
@@ -200,16 +268,16 @@ int orc_dequantize(const uint8_t *qweight, const uint16_t *scales, int64_t N,
 #pragma omp parallel for schedule(static)
 #endif
     for (int64_t n = 0; n < N; ++n)
-        dequant_row(qweight + n * (K / 2), scales + n * (K / group), K, group,
-                    out + n * K);
+        dequant_row(qweight + n * (K / 2), scales + n * (K / group),
+                    zeros ? zeros + n * (K / group) : NULL, K, group, out + n * K);
     return 0;
 }
 
 /* The page's own fp16 dequantized weight: float(q) * float(scale) rounded
  * once to fp16 ([P4] §3 dequantize, "float32 intermediate").  Used by the
  * tests to bound the rounding a kernel adds when it stages fp16 q*scale. */
-int orc_dequantize_f16(const uint8_t *qweight, const uint16_t *scales, int64_t N,
-                       int64_t K, int64_t group, uint16_t *out)
+int orc_dequantize_f16(const uint8_t *qweight, const uint16_t *scales, const uint8_t *zeros,
+                       int64_t N, int64_t K, int64_t group, uint16_t *out)
 {
     if (N < 0 || K <= 0 || group <= 0 || K % group != 0 || K % 2 != 0)
         return -1;
@@ -218,7 +286,8 @@ int orc_dequantize_f16(const uint8_t *qweight, const uint16_t *scales, int64_t N
             uint8_t byte = qweight[n * (K / 2) + k / 2];
             int nib = (k % 2 == 0) ? (byte & 0x0f) : ((byte >> 4) & 0x0f);
             float s = (float)orc_half_to_double(scales[n * (K / group) + k / group]);
-            float v = (float)(nib - 8) * s;
+            int z = zeros ? zeros[n * (K / group) + k / group] : 8;
+            float v = (float)(nib - z) * s;
             out[n * K + k] = orc_float_to_half(v);
         }
     return 0;
@@ -231,7 +300,7 @@ int orc_dequantize_f16(const uint8_t *qweight, const uint16_t *scales, int64_t N
 /* Rows `rows[0..nrows)` of W only; y is [M, nrows] binary64, unrounded.
  * x: fp16 bits [M, K]. */
 int orc_gemm_rows(const uint16_t *x, int64_t M, int64_t K, const uint8_t *qweight,
-                  const uint16_t *scales, int64_t N, int64_t group,
+                  const uint16_t *scales, const uint8_t *zeros, int64_t N, int64_t group,
                   const int64_t *rows, int64_t nrows, double *y)
 {
     if (M < 0 || N < 0 || K <= 0 || group <= 0 || K % group != 0 || K % 2 != 0 ||
@@ -247,7 +316,8 @@ int orc_gemm_rows(const uint16_t *x, int64_t M, int64_t K, const uint8_t *qweigh
         int64_t n = rows[r];
         double wd[32768];
         double xv;
-        dequant_row(qweight + n * (K / 2), scales + n * (K / group), K, group, wd);
+        dequant_row(qweight + n * (K / 2), scales + n * (K / group),
+                    zeros ? zeros + n * (K / group) : NULL, K, group, wd);
         for (int64_t m = 0; m < M; ++m) {
             double acc = 0.0;
             for (int64_t k = 0; k < K; ++k) {
@@ -262,7 +332,7 @@ int orc_gemm_rows(const uint16_t *x, int64_t M, int64_t K, const uint8_t *qweigh
 
 /* All rows: y is [M, N]. */
 int orc_gemm(const uint16_t *x, int64_t M, int64_t K, const uint8_t *qweight,
-             const uint16_t *scales, int64_t N, int64_t group, double *y)
+             const uint16_t *scales, const uint8_t *zeros, int64_t N, int64_t group, double *y)
 {
     if (M < 0 || N < 0 || K <= 0 || group <= 0 || K % group != 0 || K % 2 != 0 ||
         K > 32768)
@@ -272,7 +342,8 @@ int orc_gemm(const uint16_t *x, int64_t M, int64_t K, const uint8_t *qweight,
 #endif
     for (int64_t n = 0; n < N; ++n) {
         double wd[32768];
-        dequant_row(qweight + n * (K / 2), scales + n * (K / group), K, group, wd);
+        dequant_row(qweight + n * (K / 2), scales + n * (K / group),
+                    zeros ? zeros + n * (K / group) : NULL, K, group, wd);
         for (int64_t m = 0; m < M; ++m) {
             double acc = 0.0;
             for (int64_t k = 0; k < K; ++k)

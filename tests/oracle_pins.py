@@ -8,9 +8,10 @@ a hand-derived fixture, a closed form, an invariant, a library routine
 brute-force enumeration on tiny inputs.
 
 Sources: qaqbuyan.com quantization tutorial, chapter "量化的数学基石"
-(§1 FP16 bit layout; §2 symmetric formula and the rounding-error model
-|error| <= s/2; §3 per-group quantizer and dequantizer); W4A16 benchmark
-report (mhpq.cn) §二/§五 for y = x W^T.
+(§1 FP16 bit layout; §2 symmetric and asymmetric formulas and the
+rounding-error model |error| <= s/2; §3 granularity -- per-channel,
+per-group 128 and 32 -- and the per-group quantizer and dequantizer); W4A16
+benchmark report (mhpq.cn) §二/§五 for y = x W^T.
 """
 from __future__ import annotations
 
@@ -271,6 +272,145 @@ def pin_gemm_closed_form(o) -> None:
             assert y[m, n] == expect, (m, n, y[m, n], expect)
 
 
+# --------------------------------------------------------------------------
+# Asymmetric quantizer (tutorial §2 asymmetric formula) and other group sizes
+# (tutorial §3: per-group 128 and 32, per-channel)
+# --------------------------------------------------------------------------
+
+def pin_asym_integer_grid(o) -> None:
+    """Weights on an integer grid from min = -5 to max = 10 (times 2^-4): the
+    step is exactly (10 + 5) / 15 = one grid unit, z = 5, and every weight v
+    quantizes to v + 5 -- the minimum to 0, the maximum to 15."""
+    rng = np.random.default_rng(21)
+    for group in (32, 64, 128):
+        v = rng.integers(-5, 11, size=(2, 4 * group))
+        v[:, ::group] = -5   # every group holds the minimum ...
+        v[:, 1::group] = 10  # ... and the maximum
+        q, s, z = o.quantize_asym(_f16_bits(v * 2.0 ** -4), group)
+        assert (z == 5).all(), z
+        assert (s == _f16_bits([2.0 ** -4])[0]).all()
+        assert np.array_equal(_nibbles(q), v + 5)
+
+
+def pin_asym_range_includes_zero(o) -> None:
+    """The zero point is the code of 0.0, so 0 is in every group's range: an
+    all-positive group 0.5 j (j = 1..15) gets step 0.5 and z = 0 (q = j); the
+    all-negative -0.5 j gets z = 15 (q = 15 - j)."""
+    j = np.concatenate([np.arange(1, 16), np.ones(GROUP - 15, dtype=np.int64)])
+    q, s, z = o.quantize_asym(_f16_bits(np.stack([0.5 * j, -0.5 * j])), GROUP)
+    assert z[:, 0].tolist() == [0, 15]
+    assert (s == _f16_bits([0.5])[0]).all()
+    nib = _nibbles(q)
+    assert np.array_equal(nib[0], j) and np.array_equal(nib[1], 15 - j)
+
+
+def pin_asym_constant_and_zero_groups(o) -> None:
+    """A constant group c > 0 stores q = 15, z = 0 and s = fp16(c / 15); c < 0
+    stores q = 0, z = 15; an all-zero group stores q = 0, z = 0 and comes back
+    as exact zeros."""
+    w = np.zeros((3, GROUP), dtype=np.uint16)
+    w[0] = _f16_bits([3.0])[0]
+    w[1] = _f16_bits([-0.75])[0]
+    q, s, z = o.quantize_asym(w, GROUP)
+    nib = _nibbles(q)
+    assert (nib[0] == 15).all() and z[0, 0] == 0 and s[0, 0] == _f16_bits([0.2])[0]
+    assert (nib[1] == 0).all() and z[1, 0] == 15 and s[1, 0] == _f16_bits([0.05])[0]
+    assert (nib[2] == 0).all() and z[2, 0] == 0
+    wd = o.dequantize(q, s, GROUP, zeros=z)
+    assert (wd[2] == 0).all()
+    assert np.allclose(wd[0], 3.0, rtol=2e-3) and np.allclose(wd[1], -0.75, rtol=2e-3)
+
+
+def pin_asym_nearest_level_brute_force(o) -> None:
+    """Tiny inputs, with s32 = max(fp32(max' - min') / 15, 1e-8) over the group
+    and 0 (a numpy float32 restatement of the step only): -z is the integer
+    nearest to min'/s32 and q is the level j in [0, 15] whose j - z is nearest
+    to fp32(w) / s32, ties to even, both found by enumerating all 16 codes."""
+    rng = np.random.default_rng(22)
+    codes = np.arange(16, dtype=np.float64)
+    for group in (32, 128):
+        w16 = _random_weights(rng, 4, 2 * group)
+        w16[0] = _f16_bits(np.abs(w16[0].view(np.float16).astype(np.float64)))  # all >= 0
+        q, _, z = o.quantize_asym(w16, group)
+        nib = _nibbles(q)
+        w32 = w16.view(np.float16).astype(np.float32)
+        for n in range(w32.shape[0]):
+            for g in range(w32.shape[1] // group):
+                blk = w32[n, g * group:(g + 1) * group]
+                mn = min(np.float32(blk.min()), np.float32(0.0))
+                mx = max(np.float32(blk.max()), np.float32(0.0))
+                s32 = max(np.float32(mx - mn) / np.float32(15.0), np.float32(1e-8))
+                r0 = float(np.float32(mn) / s32)
+                d0 = np.abs(-codes - r0)
+                cand = codes[d0 == d0.min()]
+                zb = cand[0] if cand.size == 1 else cand[np.fmod(cand, 2) == 0][0]
+                zz = int(z[n, g])
+                assert zz == zb, (n, g, zz, r0)
+                for i, wv in enumerate(blk):
+                    r = float(np.float32(wv) / s32)
+                    d = np.abs((codes - zz) - r)
+                    best = codes[d == d.min()]
+                    jb = best[0] if best.size == 1 else best[np.fmod(best - zz, 2) == 0][0]
+                    assert nib[n, g * group + i] == jb, (n, g, i, r, zz)
+
+
+def pin_asym_round_trip_bound(o) -> None:
+    """Every element comes back within one step (half a step of rounding, at
+    most half a step more where the rounded zero point pushes it to a clamped
+    end), and on average within a quarter step (uniform rounding noise)."""
+    rng = np.random.default_rng(23)
+    w16 = _random_weights(rng, 128, 4096)
+    w = w16.view(np.float16).astype(np.float64)
+    for group in (32, 128):
+        q, s, z = o.quantize_asym(w16, group)
+        s64 = np.repeat(o.half_to_double(s), group, axis=1)
+        err = np.abs(w - o.dequantize(q, s, group, zeros=z))
+        assert (err <= s64 * (1 + 2.0 ** -6)).all(), float((err / s64).max())
+        rel = (err / s64).mean()
+        assert 0.2 < rel < 0.3, rel
+
+
+def pin_asym_gemm_numpy_tiny(o) -> None:
+    """With zero points, y equals numpy's float64 x @ ((nibble - z) * s)^T,
+    nibbles, zero points and scales decoded by numpy."""
+    rng = np.random.default_rng(24)
+    for M, N, K, group in ((1, 1, 128, 128), (2, 3, 256, 64), (3, 5, 384, 32), (2, 2, 256, 256)):
+        q, s, z = o.quantize_asym(_random_weights(rng, N, K), group)
+        x16 = rng.standard_normal((M, K)).astype(np.float16).view(np.uint16)
+        wd = (_nibbles(q) - np.repeat(z.astype(np.int16), group, axis=1)) * np.repeat(
+            s.view(np.float16).astype(np.float64), group, axis=1)
+        np.testing.assert_array_equal(o.dequantize(q, s, group, zeros=z), wd)
+        y = o.gemm(x16, q, s, group, zeros=z)
+        np.testing.assert_allclose(y, x16.view(np.float16).astype(np.float64) @ wd.T,
+                                   rtol=1e-12, atol=1e-12)
+        rows = np.array([N - 1, 0])
+        np.testing.assert_array_equal(o.gemm_rows(x16, q, s, rows, group, zeros=z), y[:, rows])
+
+
+def pin_group_sizes_symmetric(o) -> None:
+    """Groups of 32 and 64 and one group per row (per-channel, rows up to
+    8192): every group's largest |w| maps to +-7, its scale is numpy's
+    fp16(max(fp32(amax) / 7, 1e-8)), and dequantization uses the group's own
+    scale."""
+    rng = np.random.default_rng(25)
+    for K, group in ((1024, 32), (1024, 64), (4096, -1), (8192, -1)):
+        g = K if group == -1 else group
+        w16 = _random_weights(rng, 16, K)
+        q, s = o.quantize(w16, group)
+        assert s.shape == (16, K // g)
+        w = w16.view(np.float16)
+        wg = w.astype(np.float64).reshape(16, -1, g)
+        qg = (_nibbles(q) - 8).reshape(16, -1, g)
+        idx = np.abs(wg).argmax(axis=-1)[..., None]
+        assert (np.take_along_axis(qg, idx, -1) == 7 * np.sign(np.take_along_axis(wg, idx, -1))).all()
+        a = np.abs(w.astype(np.float32)).reshape(16, -1, g).max(-1)
+        ref = np.maximum(a / np.float32(7.0), np.float32(1e-8)).astype(np.float16).view(np.uint16)
+        assert np.array_equal(s, ref)
+        wd = o.dequantize(q, s, group)
+        s64 = np.repeat(o.half_to_double(s), g, axis=1)
+        np.testing.assert_array_equal(wd, (_nibbles(q) - 8) * s64)
+
+
 ALL_PINS = (
     pin_half_to_double_exhaustive,
     pin_float_to_half_numpy,
@@ -286,4 +426,11 @@ ALL_PINS = (
     pin_dequant_closed_forms,
     pin_gemm_numpy_tiny,
     pin_gemm_closed_form,
+    pin_asym_integer_grid,
+    pin_asym_range_includes_zero,
+    pin_asym_constant_and_zero_groups,
+    pin_asym_nearest_level_brute_force,
+    pin_asym_round_trip_bound,
+    pin_asym_gemm_numpy_tiny,
+    pin_group_sizes_symmetric,
 )

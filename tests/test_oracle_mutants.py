@@ -2,7 +2,9 @@
 plausible error (a wrong rounding mode, swapped nibbles, a dropped clamp, a
 wrong divisor, an off-by-one offset, a reversed operand, a truncating
 conversion, a wrong exponent bias, a wrong group stride, a transposed scale
-store, a scale taken from the wrong group).  The pin suite must reject every
+store, a scale taken from the wrong group; for the asymmetric quantizer a
+range that leaves out 0, a wrong divisor, a wrong-signed or truncated zero
+point, the symmetric +8 offset, zero points ignored by the dequantizer).  The pin suite must reject every
 one of them; a mutant that passes all pins means the pins are too weak."""
 from __future__ import annotations
 
@@ -20,7 +22,7 @@ MUTANTS = {
     "swapped_nibbles": ("(uint8_t)((hi << 4) | lo)", "(uint8_t)((lo << 4) | hi)"),
     "dropped_clamp": ("if (s < 1e-8f)", "if (s < 0.0f)"),
     "divide_by_8": ("float s = amax / 7.0f;", "float s = amax / 8.0f;"),
-    "offset_7": ("out[k] = (double)(nib - 8)", "out[k] = (double)(nib - 7)"),
+    "offset_7": ("int z = zrow ? zrow[k / group] : 8;", "int z = zrow ? zrow[k / group] : 7;"),
     "reversed_x": ("acc += orc_half_to_double(x[m * K + k]) * wd[k];",
                    "acc += orc_half_to_double(x[m * K + (K - 1 - k)]) * wd[k];"),
     "truncating_f2h": ("double m = rint(ldexp(a, 10 - e)) - 1024.0;",
@@ -31,10 +33,18 @@ MUTANTS = {
                      "const uint16_t *wg = W + n * K + g;"),
     "scale_transposed": ("scales[n * ngroups + g] = quantize_group",
                          "scales[g * N + n] = quantize_group"),
-    "scale_group_zero": ("out[k] = (double)(nib - 8) * orc_half_to_double(srow[k / group]);",
-                         "out[k] = (double)(nib - 8) * orc_half_to_double(srow[0]);"),
+    "scale_group_zero": ("out[k] = (double)(nib - z) * orc_half_to_double(srow[k / group]);",
+                         "out[k] = (double)(nib - z) * orc_half_to_double(srow[0]);"),
     "amax_signed": ("float a = fabsf((float)orc_half_to_double(w16[i]));",
                     "float a = (float)orc_half_to_double(w16[i]);"),
+    "asym_range_without_zero": ("float mn = 0.0f, mx = 0.0f;",
+                                "float mn = INFINITY, mx = -INFINITY;"),
+    "asym_divide_by_16": ("float s = (mx - mn) / 15.0f;", "float s = (mx - mn) / 16.0f;"),
+    "asym_zero_sign": ("float z = -nearbyintf(mn / s);", "float z = nearbyintf(-mn / s) + 1.0f;"),
+    "asym_zero_truncated": ("float z = -nearbyintf(mn / s);", "float z = -truncf(mn / s);"),
+    "asym_stored_plus_8": ("(uint8_t)(((q[i + 1] & 0x0f) << 4) | (q[i] & 0x0f));",
+                           "(uint8_t)((((q[i + 1] + 8) & 0x0f) << 4) | ((q[i] + 8) & 0x0f));"),
+    "zeros_ignored": ("int z = zrow ? zrow[k / group] : 8;", "int z = 8;"),
 }
 
 
