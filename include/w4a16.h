@@ -84,6 +84,40 @@ int w4a16_version(void);
 int w4a16_quantize(const void *W_f16, int64_t N, int64_t K, int32_t group, void *qweight,
                    void *scales_f16, void *stream);
 
+/* group argument of the format variants: one group spanning each row. */
+#define W4A16_GROUP_PER_CHANNEL (-1)
+
+/*
+ * w4a16_quantize_ex -- format variants of the quantizer: other group sizes
+ * and asymmetric INT4 with a zero point per group.
+ *
+ * Source: the same tutorial chapter, §3 granularity (per-channel, per-group
+ * 128 and 32) and §2 asymmetric formula x_q = clamp(round(x / s) + z, 0, 15),
+ * s = (max - min) / 15, z = -round(min / s).
+ *
+ * Per row n and group g, in IEEE binary32 on the exactly upcast inputs:
+ *   symmetric   as w4a16_quantize with the given group; the nibble holds q + 8.
+ *   asymmetric  lo = min(0, min_k W), hi = max(0, max_k W) over the group
+ *               (0 is kept in range so that z, the code of 0.0, is a 4-bit
+ *               code); s32 = max((hi - lo) / 15, 1e-8);
+ *               z = -round_half_even(lo / s32), in [0, 15];
+ *               q = clamp(round_half_even(W / s32) + z, 0, 15);
+ *               the nibble holds q; zeros_u8[n, g] = z.
+ *   scales_f16[n, g] = fp16_round_nearest_even(s32).
+ *
+ *   group      32, 64, 128, or W4A16_GROUP_PER_CHANNEL (one group of K).
+ *   asymmetric 0 (symmetric) or 1.
+ *   qweight    [N, K/2] bytes (low nibble = even k), written.
+ *   scales_f16 [N, K/group] fp16, written.
+ *   zeros_u8   [N, K/group] bytes, written when asymmetric (may be NULL
+ *              otherwise).
+ * Group 128 symmetric is exactly w4a16_quantize.  The results are
+ * bit-identical to the library's CPU reference definition.
+ * Errors: as w4a16_quantize; a group other than the above -> W4A16_ERR_SHAPE.
+ */
+int w4a16_quantize_ex(const void *W_f16, int64_t N, int64_t K, int32_t group, int32_t asymmetric,
+                      void *qweight, void *scales_f16, void *zeros_u8, void *stream);
+
 /*
  * Bytes of the kernel layout produced by w4a16_repack for an [N, K] weight:
  * N rounded up to a multiple of 128, times K/2.  Returns -1 on a bad shape.

@@ -70,6 +70,16 @@ def test_quantize_argument_errors(lib):
     assert q(MISALIGNED, 8, 128, 128, FAKE, FAKE, None) == 3
 
 
+def test_quantize_ex_argument_errors(lib):
+    q = lib.w4a16_quantize_ex
+    assert q(FAKE, 8, 128, 128, 1, FAKE, FAKE, None, None) == 1   # asymmetric needs zeros
+    assert q(FAKE, 8, 128, 16, 0, FAKE, FAKE, None, None) == 2    # group 16
+    assert q(FAKE, 8, 256, 96, 0, FAKE, FAKE, None, None) == 2    # group 96
+    assert q(FAKE, 8, 128, 128, 2, FAKE, FAKE, FAKE, None) == 2   # asymmetric flag
+    assert q(FAKE, 8, 200, -1, 0, FAKE, FAKE, None, None) == 2    # K % 128
+    assert q(FAKE, 8, 128, 32, 1, FAKE, FAKE, MISALIGNED, None) == 3
+
+
 def test_repack_argument_errors(lib):
     assert lib.w4a16_repack(None, 8, 128, FAKE, None) == 1
     assert lib.w4a16_repack(FAKE, 8, 96, FAKE, None) == 2

@@ -118,3 +118,53 @@ def test_round_trip_on_device(w4lib):
     w = w16.view(np.float16).astype(np.float64)
     s64 = np.repeat(oracle.half_to_double(bits16(s)), 128, axis=1)
     assert (np.abs(w - wd) <= s64 * (1 + 2.0 ** -10) * (0.5 + 2.0 ** -21 + 8 * 2.0 ** -11)).all()
+
+
+# --------------------------------------------------------------------------
+# Format variants: groups of 32 / 64 / per-channel, asymmetric with zero points
+# --------------------------------------------------------------------------
+
+def _special_rows(K: int, rng: np.random.Generator) -> np.ndarray:
+    """Rows exercising the variant-specific edge cases: all-zero, constant
+    positive / negative, all-positive and all-negative, integer-grid ties,
+    subnormals, and random outlier weights."""
+    rows = [
+        np.zeros(K),
+        np.full(K, 3.0),
+        np.full(K, -0.75),
+        np.abs(rng.standard_normal(K)) * 0.02,
+        -np.abs(rng.standard_normal(K)) * 0.02,
+        (rng.integers(-5, 11, size=K) * 2.0 ** -4),
+        rng.integers(-3, 4, size=K) * 2.0 ** -20,
+        rng.standard_normal(K) * 0.02 * np.where(rng.random(K) < 0.001, 20.0, 1.0),
+    ]
+    return np.stack(rows).astype(np.float16).view(np.uint16)
+
+
+@pytest.mark.parametrize("asym", [False, True])
+@pytest.mark.parametrize("group,K", [(32, 1024), (64, 1152), (128, 640), (w4.PER_CHANNEL, 4096),
+                                     (w4.PER_CHANNEL, 4224), (w4.PER_CHANNEL, 14336)])
+def test_format_variants_bit_exact(w4lib, group, K, asym):
+    """Packed codes, fp16 scales and zero points identical to the oracle."""
+    rng = np.random.default_rng(200 + K)
+    w16 = np.concatenate([_special_rows(K, rng), quantized(130, K, 201)[0]])
+    if asym:
+        q_ref, s_ref, z_ref = oracle.quantize_asym(w16, group)
+    else:
+        q_ref, s_ref = oracle.quantize(w16, group)
+    q, s, z = w4.quantize_ex(from_bits16(w16), group, asymmetric=asym)
+    torch.cuda.synchronize()
+    assert np.array_equal(q.cpu().numpy(), q_ref), np.count_nonzero(q.cpu().numpy() != q_ref)
+    assert np.array_equal(bits16(s), s_ref)
+    if asym:
+        assert np.array_equal(z.cpu().numpy(), z_ref)
+    else:
+        assert z is None
+
+
+def test_variant_group128_symmetric_is_the_default_quantizer(w4lib):
+    w16 = quantized(64, 1024, 202)[0]
+    q0, s0 = w4.quantize(from_bits16(w16))
+    q1, s1, _ = w4.quantize_ex(from_bits16(w16), 128)
+    torch.cuda.synchronize()
+    assert torch.equal(q0, q1) and torch.equal(s0, s1)

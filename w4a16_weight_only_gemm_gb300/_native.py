@@ -27,6 +27,7 @@ SIGNATURES = {
     "w4a16_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "w4a16_version": (ctypes.c_int, []),
     "w4a16_quantize": (ctypes.c_int, [_P, _I64, _I64, _I32, _P, _P, _P]),
+    "w4a16_quantize_ex": (ctypes.c_int, [_P, _I64, _I64, _I32, _I32, _P, _P, _P, _P]),
     "w4a16_repacked_bytes": (_I64, [_I64, _I64]),
     "w4a16_repack": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),
     "w4a16_unrepack": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),

@@ -128,6 +128,24 @@ int w4a16_quantize(const void* W_f16, int64_t N, int64_t K, int32_t group, void*
                                      static_cast<cudaStream_t>(stream), ctx));
 }
 
+int w4a16_quantize_ex(const void* W_f16, int64_t N, int64_t K, int32_t group, int32_t asymmetric,
+                      void* qweight, void* scales_f16, void* zeros_u8, void* stream) {
+    if (!W_f16 || !qweight || !scales_f16 || (asymmetric && !zeros_u8)) return W4A16_ERR_NULL;
+    if (!good_nk(N, K) || (asymmetric != 0 && asymmetric != 1)) return W4A16_ERR_SHAPE;
+    if (group == W4A16_GROUP_PER_CHANNEL) group = (int32_t)K;
+    if (!(group == 32 || group == 64 || group == 128 || group == K)) return W4A16_ERR_SHAPE;
+    if (!aligned16(W_f16) || !aligned16(qweight) || !aligned16(scales_f16) ||
+        (asymmetric && !aligned16(zeros_u8)))
+        return W4A16_ERR_ALIGN;
+    DeviceCtx ctx;
+    if (int rc = device_ctx(&ctx)) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (group == W4A16_GROUP && !asymmetric)
+        return from_cuda(launch_quantize(W_f16, N, K, qweight, scales_f16, s, ctx));
+    return from_cuda(launch_quantize_fmt(W_f16, N, K, group, asymmetric != 0, qweight, scales_f16,
+                                         zeros_u8, s, ctx));
+}
+
 int64_t w4a16_repacked_bytes(int64_t N, int64_t K) {
     if (!good_nk(N, K)) return -1;
     return (N + kBlockRows - 1) / kBlockRows * kBlockRows * (K / 2);

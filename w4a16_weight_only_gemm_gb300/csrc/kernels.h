@@ -26,6 +26,11 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 cudaError_t launch_quantize(const void* W, int64_t N, int64_t K, void* qweight, void* scales,
                             cudaStream_t stream, const DeviceCtx& ctx);
+// Format variants of the quantizer: group = 32, 64, 128 or K (per-channel),
+// symmetric or asymmetric (zeros: [N, K/group] bytes).
+cudaError_t launch_quantize_fmt(const void* W, int64_t N, int64_t K, int group, bool asym,
+                                void* qweight, void* scales, void* zeros, cudaStream_t stream,
+                                const DeviceCtx& ctx);
 cudaError_t launch_repack(const void* qweight, int64_t N, int64_t K, void* repacked,
                           cudaStream_t stream, const DeviceCtx& ctx);
 cudaError_t launch_unrepack(const void* repacked, int64_t N, int64_t K, void* qweight,

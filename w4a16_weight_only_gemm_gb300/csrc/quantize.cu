@@ -142,6 +142,91 @@ __global__ void __launch_bounds__(kQuantThreads)
     __threadfence();
 }
 
+// ---------------------------------------------------------------------------
+// Format variants: groups of 32, 64 or 128 weights or one group per row
+// (per-channel), symmetric as above or asymmetric (tutorial §2 asymmetric
+// formula: s = (max - min) / 15 with min and max taken over the group and 0,
+// z = -round(min / s), q = clamp(round(w / s) + z, 0, 15); the nibble holds
+// q, the zero point one byte per group).  Every step is the binary32
+// operation of the formula with a correctly rounded divide, so the codes,
+// scales and zero points match the plain statement bit for bit.
+//
+// A team of L = min(32, group / 8) lanes owns a group; each lane loads 8
+// weights (16 bytes) per pass and packs their 8 nibbles into one 32-bit word.
+// Groups wider than 256 (per-channel) take several passes, reading the row
+// twice (reduce, then quantize).
+// ---------------------------------------------------------------------------
+constexpr int kFmtThreads = 256;
+
+template <bool ASYM>
+__global__ void __launch_bounds__(kFmtThreads)
+    quantize_fmt_kernel(const uint4* __restrict__ W, int64_t groups_total, int group, int L,
+                        uint32_t* __restrict__ qweight, __half* __restrict__ scales,
+                        uint8_t* __restrict__ zeros) {
+    const int lane = threadIdx.x & 31;
+    const int tl = lane % L;                 // lane within the team
+    const unsigned team_mask = L == 32 ? 0xffffffffu : (((1u << L) - 1u) << (lane - tl));
+    const int teams_per_block = kFmtThreads / L;
+    const int64_t stride = (int64_t)gridDim.x * teams_per_block;
+    const int passes = group / (8 * L);
+    // Whole warps iterate together (a warp's teams share the loop test), so
+    // every team's shuffles see all of its lanes.
+    const int64_t warp_first =
+        (int64_t)blockIdx.x * teams_per_block + (threadIdx.x / 32) * (32 / L);
+    for (int64_t base = warp_first; base < groups_total; base += stride) {
+        const int64_t grp = base + lane / L;
+        const bool live = grp < groups_total;
+        const uint4* src = W + (live ? grp : 0) * (group / 8);
+        // --- pass 1: max |w| (symmetric) or min / max with 0 (asymmetric) ---
+        float lo = 0.0f, hi = 0.0f;
+        for (int p = 0; p < passes; ++p) {
+            const uint4 raw = live ? __ldg(src + p * L + tl) : make_uint4(0, 0, 0, 0);
+            const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = __half22float2(h2[i]);
+                if (ASYM) {
+                    lo = fminf(lo, fminf(f.x, f.y));
+                    hi = fmaxf(hi, fmaxf(f.x, f.y));
+                } else {
+                    hi = fmaxf(hi, fmaxf(fabsf(f.x), fabsf(f.y)));
+                }
+            }
+        }
+        for (int off = L / 2; off > 0; off >>= 1) {
+            hi = fmaxf(hi, __shfl_xor_sync(team_mask, hi, off));
+            if (ASYM) lo = fminf(lo, __shfl_xor_sync(team_mask, lo, off));
+        }
+        float s = ASYM ? __fdiv_rn(__fsub_rn(hi, lo), 15.0f) : __fdiv_rn(hi, 7.0f);
+        if (s < 1e-8f) s = 1e-8f;
+        const float z = ASYM ? -rintf(__fdiv_rn(lo, s)) : 8.0f;  // nibble offset
+        // --- pass 2: codes ---
+        for (int p = 0; p < passes && live; ++p) {
+            const uint4 raw = __ldg(src + p * L + tl);
+            const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+            uint32_t word = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = __half22float2(h2[i]);
+                const float qa = fminf(fmaxf(rintf(__fdiv_rn(f.x, s)) + (ASYM ? z : 0.0f),
+                                             ASYM ? 0.0f : -8.0f), ASYM ? 15.0f : 7.0f);
+                const float qb = fminf(fmaxf(rintf(__fdiv_rn(f.y, s)) + (ASYM ? z : 0.0f),
+                                             ASYM ? 0.0f : -8.0f), ASYM ? 15.0f : 7.0f);
+                const uint32_t na = (uint32_t)(int)(ASYM ? qa : qa + 8.0f);
+                const uint32_t nb = (uint32_t)(int)(ASYM ? qb : qb + 8.0f);
+                word |= (na | (nb << 4)) << (8 * i);
+            }
+            qweight[grp * (group / 8) + p * L + tl] = word;
+        }
+        if (live && tl == 0) {
+            scales[grp] = __float2half_rn(s);
+            if (ASYM) zeros[grp] = (uint8_t)(int)z;
+        }
+    }
+    // as quantize_kernel: publish before a following GEMM reads them
+    __threadfence();
+}
+
 }  // namespace
 
 cudaError_t launch_quantize(const void* W, int64_t N, int64_t K, void* qweight, void* scales,
@@ -167,6 +252,34 @@ cudaError_t launch_quantize(const void* W, int64_t N, int64_t K, void* qweight, 
     quantize_kernel<<<(unsigned)blocks, kQuantThreads, 0, stream>>>(
         static_cast<const uint4*>(W), groups, static_cast<uint32_t*>(qweight),
         static_cast<__half*>(scales));
+    return cudaGetLastError();
+}
+
+}  // namespace w4a16
+
+namespace w4a16 {
+
+cudaError_t launch_quantize_fmt(const void* W, int64_t N, int64_t K, int group, bool asym,
+                                void* qweight, void* scales, void* zeros, cudaStream_t stream,
+                                const DeviceCtx& ctx) {
+    // team width: 8 weights per lane per pass, a power of two dividing the
+    // group's 16-byte pieces (groups are multiples of 32; per-channel rows of
+    // K % 256 == 128 take teams of 16)
+    const int L = group / 8 < 32 ? group / 8 : ((group / 8) % 32 == 0 ? 32 : 16);
+    const int64_t groups = N * (K / group);
+    const int64_t per_block = kFmtThreads / L;
+    int64_t blocks = (groups + per_block - 1) / per_block;
+    const int64_t cap = (int64_t)ctx.num_sms * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    if (asym)
+        quantize_fmt_kernel<true><<<(unsigned)blocks, kFmtThreads, 0, stream>>>(
+            static_cast<const uint4*>(W), groups, group, L, static_cast<uint32_t*>(qweight),
+            static_cast<__half*>(scales), static_cast<uint8_t*>(zeros));
+    else
+        quantize_fmt_kernel<false><<<(unsigned)blocks, kFmtThreads, 0, stream>>>(
+            static_cast<const uint4*>(W), groups, group, L, static_cast<uint32_t*>(qweight),
+            static_cast<__half*>(scales), nullptr);
     return cudaGetLastError();
 }
 

@@ -42,6 +42,28 @@ def quantize(W: torch.Tensor, group: int = GROUP, stream=None):
     return q, s
 
 
+PER_CHANNEL = -1
+
+
+def quantize_ex(W: torch.Tensor, group: int = GROUP, asymmetric: bool = False, stream=None):
+    """Format variants: W fp16 [N, K] -> (qweight uint8 [N, K/2], scales fp16
+    [N, K/g], zeros uint8 [N, K/g] or None), g = group (32, 64, 128) or K for
+    PER_CHANNEL; asymmetric codes hold q in [0, 15] with a zero point per group."""
+    _need(W, torch.float16, "W")
+    N, K = W.shape
+    g = K if group == PER_CHANNEL else group
+    if g <= 0 or K % g:
+        raise ValueError(f"K={K} is not a multiple of group={group}")
+    q = torch.empty((N, K // 2), dtype=torch.uint8, device=W.device)
+    s = torch.empty((N, K // g), dtype=torch.float16, device=W.device)
+    z = torch.empty((N, K // g), dtype=torch.uint8, device=W.device) if asymmetric else None
+    rc = _native.lib().w4a16_quantize_ex(W.data_ptr(), N, K, group, int(asymmetric), q.data_ptr(),
+                                         s.data_ptr(), z.data_ptr() if asymmetric else None,
+                                         _stream_ptr(stream))
+    _native.check(rc, "w4a16_quantize_ex")
+    return q, s, z
+
+
 @functools.lru_cache(maxsize=1024)
 def repacked_bytes(N: int, K: int) -> int:
     n = _native.lib().w4a16_repacked_bytes(N, K)
