@@ -96,6 +96,14 @@ def test_gemm_argument_errors(lib):
     assert g(FAKE, FAKE, FAKE, MISALIGNED, 1, 8, 128, None) == 3
 
 
+def test_gemm_ex_argument_errors(lib):
+    g = lib.w4a16_gemm_ex
+    assert g(FAKE, FAKE, None, None, FAKE, 1, 8, 128, 32, None) == 1
+    assert g(FAKE, FAKE, FAKE, None, FAKE, 1, 8, 128, 16, None) == 2     # group 16
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 17, 8, 128, 32, None) == 2    # variants: M <= 16
+    assert g(FAKE, FAKE, FAKE, MISALIGNED, FAKE, 1, 8, 128, 32, None) == 3
+
+
 def test_device_status_rejects_null(lib):
     assert lib.w4a16_device_status(None) == 1
 

@@ -1,0 +1,85 @@
+"""Format variants of the decode GEMV (w4a16_gemm_ex: groups of 32, 64, 128
+or per-channel, symmetric or asymmetric codes) vs the binary64 oracle, on the
+oracle's own codes, scales and zero points.
+
+Bar: the same as the default GEMV (max|dy| <= 2e-3 max|y_ref|, relative L2
+<= 1e-3).  The variants round (q - z) * scale once to fp16 per weight (the
+tutorial's own fp16 dequantised weight): about 2^-12 relative per weight,
+random in sign, well inside the L2 budget next to the final fp16 rounding."""
+from __future__ import annotations
+
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import assert_close, from_bits16, u8
+from parity_data import acts, sample_rows
+import w4a16_weight_only_gemm_gb300 as w4
+from w4a16_weight_only_gemm_gb300 import synthetic, workloads
+
+pytestmark = pytest.mark.gpu
+
+FORMATS = [(32, False), (32, True), (64, False), (64, True), (128, True), (w4.PER_CHANNEL, False),
+           (w4.PER_CHANNEL, True)]
+
+
+@functools.lru_cache(maxsize=32)
+def quantized_fmt(N: int, K: int, seed: int, group: int, asym: bool):
+    w16 = synthetic.master_weight(N, K, seed).contiguous().view(torch.int16).numpy().view(np.uint16)
+    if asym:
+        return oracle.quantize_asym(w16, group)
+    q, s = oracle.quantize(w16, group)
+    return q, s, None
+
+
+def run_fmt(x16, q, s, z, group):
+    r = w4.repack(u8(q))
+    st = from_bits16(s)
+    zt = u8(z) if z is not None else None
+    y = w4.gemm_ex(from_bits16(x16), r, st, zt, group)
+    torch.cuda.synchronize()
+    return y.float().cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("group,asym", FORMATS)
+@pytest.mark.parametrize("N,K", [(1000, 2048), (4136, 1152), (300, 4096)])
+@pytest.mark.parametrize("M", [1, 5, 16])
+def test_formats_every_row(w4lib, M, N, K, group, asym):
+    q, s, z = quantized_fmt(N, K, 300 + K, group, asym)
+    x16 = acts(M, K, 301 + M)
+    y = run_fmt(x16, q, s, z, group)
+    assert_close(y, oracle.gemm(x16, q, s, group, zeros=z), f"g={group} asym={asym} M={M}")
+    assert w4.device_status() == 0
+
+
+@pytest.mark.parametrize("group,asym", FORMATS)
+@pytest.mark.parametrize("idx", range(len(workloads.LLAMA3_8B)))
+def test_formats_llama3_8b_m1(w4lib, idx, group, asym):
+    """The Llama-3-8B decode shapes at M = 1, sampled rows."""
+    lin = workloads.LLAMA3_8B[idx]
+    sw, sx = synthetic.seeds("llama3_8b_decode", idx)
+    q, s, z = quantized_fmt(lin.N, lin.K, sw, group, asym)
+    x16 = acts(1, lin.K, sx)
+    y = run_fmt(x16, q, s, z, group)
+    rows = sample_rows(lin.N, 256, sw)
+    assert_close(y[:, rows], oracle.gemm_rows(x16, q, s, rows, group, zeros=z),
+                 f"{lin.name} g={group} asym={asym}")
+
+
+def test_group128_symmetric_is_the_default_gemm(w4lib):
+    q, s, _ = quantized_fmt(512, 1024, 310, 128, False)
+    x = from_bits16(acts(3, 1024, 311))
+    r = w4.repack(u8(q))
+    st = from_bits16(s)
+    assert torch.equal(w4.gemm_ex(x, r, st, None, 128), w4.gemm(x, r, st))
+
+
+def test_shape_that_does_not_fit_is_rejected(w4lib):
+    q, s, z = quantized_fmt(256, 14336, 312, 32, True)
+    x = from_bits16(acts(16, 14336, 313))
+    with pytest.raises(w4.ops._native.W4A16Error, match="SHAPE"):
+        w4.gemm_ex(x, w4.repack(u8(q)), from_bits16(s), u8(z), 32)
+    assert w4.device_status() == 0

@@ -5,10 +5,10 @@ The CUDA library is ``libw4a16.so`` (sources in ``csrc/``, ABI in
 package does not load the library; the first call does, and fails loudly if
 it has not been built.
 """
-from .ops import (GROUP, PER_CHANNEL, W4A16Linear, device_status, gemm, gemm_plan, quantize,
-                  quantize_ex, repack,
+from .ops import (GROUP, PER_CHANNEL, W4A16Linear, device_status, gemm, gemm_ex, gemm_plan,
+                  quantize, quantize_ex, repack,
                   repacked_bytes, selftest_wait_timeout, set_wait_timeout_ns, unrepack)
 
-__all__ = ["GROUP", "PER_CHANNEL", "W4A16Linear", "device_status", "gemm", "gemm_plan", "quantize",
-           "quantize_ex", "repack",
+__all__ = ["GROUP", "PER_CHANNEL", "W4A16Linear", "device_status", "gemm", "gemm_ex", "gemm_plan",
+           "quantize", "quantize_ex", "repack",
            "repacked_bytes", "selftest_wait_timeout", "set_wait_timeout_ns", "unrepack"]

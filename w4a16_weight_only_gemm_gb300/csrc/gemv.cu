@@ -927,6 +927,11 @@ cudaError_t launch_gemv_mt(GemvArgs args, int M, cudaStream_t stream, const Devi
 
 }  // namespace
 
+cudaError_t gemv_weight_map(const void* repacked, int64_t N, int64_t K, int T, CUtensorMap* out) {
+    return weight_map(static_cast<const uint8_t*>(repacked),
+                      (int)((N + kBlockRows - 1) / kBlockRows), (int)K, T, out);
+}
+
 cudaError_t gemv_plan_info(int M, int64_t N, int64_t K, const DeviceCtx& ctx, int* splits,
                            int* ctas, int* blocks_per_cta, int* rows_per_cta) {
     cudaError_t e = M <= 8 ? ensure_smem_attr<1>() : ensure_smem_attr<2>();

@@ -132,6 +132,41 @@ def gemm(x: torch.Tensor, repacked: torch.Tensor, scales: torch.Tensor,
     return _gemm(x, repacked, scales, N, K, out, stream)
 
 
+def gemm_ex(x: torch.Tensor, repacked: torch.Tensor, scales: torch.Tensor,
+            zeros: torch.Tensor | None = None, group: int = GROUP,
+            out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y = x @ dequant(W)^T for the format variants of quantize_ex: scales
+    [N, K/g] fp16, zeros [N, K/g] uint8 (asymmetric) or None, g = group or K
+    for PER_CHANNEL."""
+    _need(x, torch.float16, "x")
+    _need(repacked, torch.uint8, "repacked")
+    _need(scales, torch.float16, "scales")
+    if zeros is not None:
+        _need(zeros, torch.uint8, "zeros")
+        if zeros.shape != scales.shape:
+            raise ValueError("zeros and scales differ in shape")
+    if x.dim() != 2:
+        raise ValueError("x must be [M, K]")
+    M, K = x.shape
+    N = scales.shape[0]
+    g = K if group == PER_CHANNEL else group
+    if g <= 0 or K % g or scales.shape[1] != K // g:
+        raise ValueError(f"scales must be [N, {K}/{g}]")
+    if repacked.numel() != repacked_bytes(N, K):
+        raise ValueError("repacked buffer size does not match N, K")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    else:
+        _need(out, torch.float16, "out")
+        if tuple(out.shape) != (M, N):
+            raise ValueError("out has the wrong shape")
+    rc = _native.lib().w4a16_gemm_ex(x.data_ptr(), repacked.data_ptr(), scales.data_ptr(),
+                                     zeros.data_ptr() if zeros is not None else None,
+                                     out.data_ptr(), M, N, K, group, _stream_ptr(stream))
+    _native.check(rc, "w4a16_gemm_ex")
+    return out
+
+
 def gemm_plan(M: int, N: int, K: int) -> dict:
     """The launch gemm() makes for (M, N, K) on the current device:
     {"path": "gemv" | "tensor_core", "splits", "ctas", "blocks_per_cta", "rows_per_cta"}."""
