@@ -55,7 +55,7 @@ def parse_args():
                    help="headline step only (no per-shape, stack, sweep, quantizer sections)")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="budget of the CPU oracle baseline sample")
-    p.add_argument("--section", choices=("prefill", "quantizer", "stack", "per_shape"),
+    p.add_argument("--section", choices=("prefill", "quantizer", "stack", "per_shape", "formats"),
                    default=None,
                    help="run one section alone and print its JSON (profiling aid; not the "
                         "benchmark line)")
@@ -229,6 +229,46 @@ def per_shape_us(lin, workload, idx, M=1, reps=20):
     return {"us": round(t * 1e6, 3), "gbs": round(b / t / 1e9, 1), "bytes": b, "copies": copies}
 
 
+def formats_m1():
+    """The format variants (w4a16_gemm_ex) on the Llama-3-8B decode shapes at
+    M = 1: us per call over rotating weight copies (>= 4x L2), GB/s of the
+    variant's algorithmic bytes (its scales and zero points included)."""
+    import w4a16_weight_only_gemm_gb300 as w4
+    out = {}
+    formats = [(32, False), (32, True), (64, False), (128, True), (w4.PER_CHANNEL, False),
+               (w4.PER_CHANNEL, True)]
+    stream = torch.cuda.Stream()
+    for group, asym in formats:
+        name = ("g" + str(group) if group > 0 else "per_channel") + ("_asym" if asym else "_sym")
+        res = {}
+        for i, lin in enumerate(workloads.LLAMA3_8B):
+            sw, sx = synthetic.seeds("llama3_8b_decode", i)
+            W = synthetic.master_weight(lin.N, lin.K, sw, device="cuda")
+            q, s, z = w4.quantize_ex(W, group, asymmetric=asym)
+            r = w4.repack(q)
+            del W, q
+            x = synthetic.activations(1, lin.K, sx, device="cuda")
+            y = torch.empty((1, lin.N), dtype=torch.float16, device="cuda")
+            nbytes = r.numel() + s.numel() * 2 + (z.numel() if z is not None else 0)
+            copies = max(2, -(-4 * l2_bytes() // nbytes))
+            rs = [r] + [r.clone() for _ in range(copies - 1)]
+
+            def body():
+                for rr in rs:
+                    w4.gemm_ex(x, rr, s, z, group, out=y)
+            g = capture(body, stream)
+            t = time_graph(g, stream, 10, 3) / copies
+            b = workloads.algorithmic_bytes(1, lin.N, lin.K, group, asym)
+            res[lin.name] = {"us": round(t * 1e6, 3), "gbs": round(b / t / 1e9, 1)}
+            del rs, g, r, s, z
+        tot_t = sum(v["us"] for v in res.values())
+        tot_b = sum(workloads.algorithmic_bytes(1, l.N, l.K, group, asym) for l in workloads.LLAMA3_8B)
+        res["five_shapes"] = {"us": round(tot_t, 2), "gbs": round(tot_b / tot_t / 1e3, 1)}
+        out[name] = res
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, rank, world):
     import w4a16_weight_only_gemm_gb300 as w4
     from w4a16_weight_only_gemm_gb300 import build
@@ -355,6 +395,7 @@ def extras(layers):
     out["decode_sweep"] = sweep
     out["quantizer"] = quantizer_throughput()
     out["prefill_m512"] = prefill()
+    out["formats_m1"] = formats_m1()
     return out
 
 
@@ -549,6 +590,7 @@ def main():
         from w4a16_weight_only_gemm_gb300 import build
         build.build()
         run = {"prefill": prefill, "quantizer": quantizer_throughput, "stack": stack_8b,
+               "formats": formats_m1,
                "per_shape": lambda: {lin.name: per_shape_us(lin, "llama3_8b_decode", i)
                                      for i, lin in enumerate(workloads.LLAMA3_8B)}}
         print(json.dumps({"section": args.section, "result": run[args.section]()}), flush=True)

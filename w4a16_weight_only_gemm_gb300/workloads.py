@@ -54,6 +54,8 @@ def stack_8b() -> list[Linear]:
     return layers + [LLAMA3_8B[4]]
 
 
-def algorithmic_bytes(M: int, N: int, K: int, group: int = 128) -> int:
-    """Bytes one call must move: packed weights + fp16 scales + x + y."""
-    return N * K // 2 + 2 * N * (K // group) + 2 * M * K + 2 * M * N
+def algorithmic_bytes(M: int, N: int, K: int, group: int = 128, zero_points: bool = False) -> int:
+    """Bytes one call must move: packed weights + fp16 scales (+ one byte of
+    zero point per group) + x + y.  group = -1: one group per row."""
+    g = K if group == -1 else group
+    return N * K // 2 + (3 if zero_points else 2) * N * (K // g) + 2 * M * K + 2 * M * N
