@@ -236,10 +236,13 @@ def formats_m1():
     import w4a16_weight_only_gemm_gb300 as w4
     out = {}
     formats = [(32, False), (32, True), (64, False), (128, True), (w4.PER_CHANNEL, False),
-               (w4.PER_CHANNEL, True)]
+               (w4.PER_CHANNEL, True), (128, "awq")]
     stream = torch.cuda.Stream()
     for group, asym in formats:
+        awq = asym == "awq"  # group 128 symmetric codes with an AWQ activation scale
+        asym = False if awq else asym
         name = ("g" + str(group) if group > 0 else "per_channel") + ("_asym" if asym else "_sym")
+        name += "_awq" if awq else ""
         res = {}
         for i, lin in enumerate(workloads.LLAMA3_8B):
             sw, sx = synthetic.seeds("llama3_8b_decode", i)
@@ -248,6 +251,7 @@ def formats_m1():
             r = w4.repack(q)
             del W, q
             x = synthetic.activations(1, lin.K, sx, device="cuda")
+            alpha = (torch.rand(lin.K, device="cuda") * 1.5 + 0.5).half() if awq else None
             y = torch.empty((1, lin.N), dtype=torch.float16, device="cuda")
             nbytes = r.numel() + s.numel() * 2 + (z.numel() if z is not None else 0)
             copies = max(2, -(-4 * l2_bytes() // nbytes))
@@ -255,14 +259,15 @@ def formats_m1():
 
             def body():
                 for rr in rs:
-                    w4.gemm_ex(x, rr, s, z, group, out=y)
+                    w4.gemm_ex(x, rr, s, z, group, out=y, alpha=alpha)
             g = capture(body, stream)
             t = time_graph(g, stream, 10, 3) / copies
-            b = workloads.algorithmic_bytes(1, lin.N, lin.K, group, asym)
+            b = workloads.algorithmic_bytes(1, lin.N, lin.K, group, asym) + (2 * lin.K if awq else 0)
             res[lin.name] = {"us": round(t * 1e6, 3), "gbs": round(b / t / 1e9, 1)}
             del rs, g, r, s, z
         tot_t = sum(v["us"] for v in res.values())
-        tot_b = sum(workloads.algorithmic_bytes(1, l.N, l.K, group, asym) for l in workloads.LLAMA3_8B)
+        tot_b = sum(workloads.algorithmic_bytes(1, l.N, l.K, group, asym) + (2 * l.K if awq else 0)
+                    for l in workloads.LLAMA3_8B)
         res["five_shapes"] = {"us": round(tot_t, 2), "gbs": round(tot_b / tot_t / 1e3, 1)}
         out[name] = res
         torch.cuda.empty_cache()

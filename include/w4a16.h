@@ -186,12 +186,17 @@ int w4a16_gemm(const void *x_f16, const void *repacked, const void *scales_f16, 
                int64_t M, int64_t N, int64_t K, void *stream);
 
 /*
- * w4a16_gemm_ex -- w4a16_gemm for the format variants of w4a16_quantize_ex:
- *   y[m, n] = sum_k x[m, k] * (nib[n, k] - z[n, k/g]) * scale[n, k/g],
+ * w4a16_gemm_ex -- w4a16_gemm for the format variants of w4a16_quantize_ex,
+ * with an optional AWQ activation scale:
+ *   y[m, n] = sum_k x~[m, k] * (nib[n, k] - z[n, k/g]) * scale[n, k/g],
  * z = zeros_u8[n, k/g] for asymmetric codes, z = 8 for symmetric codes
- * (zeros_u8 NULL).  Source: tutorial §2 symmetric / asymmetric formulas and
- * §3 granularity; report §二/§五 for the decode product.
+ * (zeros_u8 NULL); x~ = x, or x~[m, k] = fp16_rne(x[m, k] * alpha[k]) when
+ * alpha_f16 is given.  Source: tutorial §2 symmetric / asymmetric formulas,
+ * §3 granularity and its AWQ section (x~_j = x_j alpha_j against weights
+ * quantized from W_{:,j} / alpha_j; the alpha search is the caller's);
+ * report §二/§五 for the decode product.
  *
+ *   alpha_f16  [K] fp16 per-input-channel scale, or NULL.
  *   repacked   w4a16_repack of the variant's packed codes (the layout does
  *              not depend on the format).
  *   scales_f16 [N, K/g] fp16; zeros_u8 [N, K/g] bytes or NULL.
@@ -200,16 +205,16 @@ int w4a16_gemm(const void *x_f16, const void *repacked, const void *scales_f16, 
  *              shared memory whole beside the weight ring: about
  *              2 * M * K <= 200 KB (M = 1: any K up to 32768; M = 16: K up to
  *              6144); a shape that does not fit -> W4A16_ERR_SHAPE.
- * Group 128 with symmetric codes runs w4a16_gemm's kernels (exact q * x
- * products, one FP32 rescale per group).  The other formats dequantise
+ * Group 128 with symmetric codes and no alpha runs w4a16_gemm's kernels
+ * (exact q * x products, one FP32 rescale per group).  The other calls dequantise
  * (nib - z) * scale once to fp16 per weight (the tutorial's own fp16
  * dequantised weight) and accumulate in FP32; the accuracy bar is the same.
  * Errors: as w4a16_gemm; a group other than the above, or M > 16 for a
- * format other than group 128 symmetric -> W4A16_ERR_SHAPE.
+ * format other than group 128 symmetric or with alpha -> W4A16_ERR_SHAPE.
  */
-int w4a16_gemm_ex(const void *x_f16, const void *repacked, const void *scales_f16,
-                  const void *zeros_u8, void *y_f16, int64_t M, int64_t N, int64_t K,
-                  int32_t group, void *stream);
+int w4a16_gemm_ex(const void *x_f16, const void *alpha_f16, const void *repacked,
+                  const void *scales_f16, const void *zeros_u8, void *y_f16, int64_t M,
+                  int64_t N, int64_t K, int32_t group, void *stream);
 
 /* Paths reported by w4a16_gemm_plan. */
 enum { W4A16_PATH_GEMV = 1, W4A16_PATH_TENSOR_CORE = 2 };

@@ -89,6 +89,7 @@ def _bind(lib):
     lib.orc_gemm.restype = ctypes.c_int
     lib.orc_gemm_rows.argtypes = [p, i64, i64, p, p, p, i64, i64, p, i64, p]
     lib.orc_gemm_rows.restype = ctypes.c_int
+    lib.orc_scale_activations.argtypes = [p, i64, i64, p, p]
     lib.orc_num_threads.restype = ctypes.c_int
     lib.orc_set_num_threads.argtypes = [ctypes.c_int]
     return lib
@@ -236,6 +237,22 @@ class Oracle:
         return out
 
     # ------------------------------------------------------------------
+    # AWQ activation scaling (tutorial AWQ section).  Pinned: numpy's exact
+    # binary32 product and IEEE fp16 conversion; alpha = 1 is the identity;
+    # alpha acts per input channel (one-hot alpha against numpy matmul).
+    # ------------------------------------------------------------------
+    def scale_activations(self, x16: np.ndarray, alpha16: np.ndarray) -> np.ndarray:
+        """x~[m, k] = fp16_rne(x[m, k] * alpha[k]); uint16 fp16 bits [M, K]."""
+        x16 = _c(x16, np.uint16)
+        alpha16 = _c(alpha16, np.uint16)
+        M, K = x16.shape
+        if alpha16.shape != (K,):
+            raise ValueError("alpha must be [K]")
+        out = np.empty((M, K), dtype=np.uint16)
+        self._lib.orc_scale_activations(_ptr(x16), M, K, _ptr(alpha16), _ptr(out))
+        return out
+
+    # ------------------------------------------------------------------
     # GEMM y = x W^T in binary64 (report §二/§五).  Pinned: numpy float64
     # matmul of the dequantized weights on tiny shapes; closed form q = 1,
     # s = 1 gives y = sum_k x exactly.
@@ -303,6 +320,10 @@ def quantize(W16, group: int = GROUP):
 
 def quantize_asym(W16, group: int = GROUP):
     return default().quantize_asym(W16, group)
+
+
+def scale_activations(x16, alpha16):
+    return default().scale_activations(x16, alpha16)
 
 
 def dequantize(qweight, scales, group: int = GROUP, zeros=None):

@@ -19,6 +19,9 @@
  *               in_features, low nibble = even index, stored as q + 8,
  *               scale clamp(min=1e-8), scales stored as fp16, dequant in
  *               fp32 intermediate).
+ *          AWQ section "AWQ 的数学原理": activation scaling per input
+ *               channel x~_j = x_j * alpha_j with W~_{:,j} = W_{:,j} / alpha_j
+ *               (the alpha search needs calibration data: not restated).
  *   [P1] "W4A16 量化算子解码性能基准跑分与端侧大模型推理显存实测报告"
  *        (mhpq.cn) §一: group size 128, symmetric INT4, fp16 scales;
  *        §二/§五: y = x * W^T computed from the packed weights.
@@ -35,6 +38,8 @@
  *     is stored as one byte per group; the same clamp(min=1e-8) guards s;
  *   - per-channel quantization is one group spanning the whole row
  *     (group = K);
+ *   - AWQ's scaled activation is rounded once to fp16: x~ = fp16_rne(x * alpha),
+ *     the product of two fp16 values being exact in binary32;
  *   - the GEMM reference is the exact dequantized weight (nib-8)*scale16 in
  *     binary64, summed sequentially over k in binary64, never rounded to fp16.
  *
@@ -291,6 +296,21 @@ int orc_dequantize_f16(const uint8_t *qweight, const uint16_t *scales, const uin
             out[n * K + k] = orc_float_to_half(v);
         }
     return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* AWQ activation scaling ([P4] AWQ section): x~[m, k] = x[m, k] * alpha[k] */
+/* ------------------------------------------------------------------ */
+
+void orc_scale_activations(const uint16_t *x, int64_t M, int64_t K, const uint16_t *alpha,
+                           uint16_t *out)
+{
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t k = 0; k < K; ++k) {
+            float p = (float)orc_half_to_double(x[m * K + k]) *
+                      (float)orc_half_to_double(alpha[k]);   /* exact in binary32 */
+            out[m * K + k] = orc_float_to_half(p);
+        }
 }
 
 /* ------------------------------------------------------------------ */

@@ -411,6 +411,45 @@ def pin_group_sizes_symmetric(o) -> None:
         np.testing.assert_array_equal(wd, (_nibbles(q) - 8) * s64)
 
 
+# --------------------------------------------------------------------------
+# AWQ activation scaling (tutorial AWQ section: x~_j = x_j * alpha_j)
+# --------------------------------------------------------------------------
+
+def pin_awq_scale_numpy(o) -> None:
+    """x~ is numpy's IEEE fp16 conversion of the exact binary32 product x * alpha
+    (subnormal, tie and overflow-free ranges included); alpha = 1 is the identity."""
+    rng = np.random.default_rng(31)
+    M, K = 5, 384
+    x = (rng.standard_normal((M, K)) * np.exp(rng.uniform(-12, 4, (M, K)))).astype(np.float16)
+    a = rng.uniform(0.5, 2.0, K).astype(np.float16)
+    a[:4] = [1.0, 2.0 ** -3, 1.0 + 2.0 ** -10, 1.5]
+    x[0, :4] = [1.0 + 2.0 ** -10, 3.0, 1.0 + 2.0 ** -10, 1.0 + 2.0 ** -10]
+    got = o.scale_activations(x.view(np.uint16), a.view(np.uint16))
+    ref = (x.astype(np.float32) * a.astype(np.float32)).astype(np.float16).view(np.uint16)
+    assert np.array_equal(got, ref)
+    # (1 + 2^-10)^2 rounds down to 1 + 2^-9; 1.5 (1 + 2^-10) is a tie -> even mantissa
+    assert got[0, 2] == 0x3C02 and got[0, 3] == 0x3E02
+    ones = np.full(K, 0x3C00, dtype=np.uint16)
+    assert np.array_equal(o.scale_activations(x.view(np.uint16), ones), x.view(np.uint16))
+
+
+def pin_awq_scale_per_input_channel(o) -> None:
+    """alpha acts on input channel k: a one-hot alpha (2 at channel j) changes y by
+    exactly x[:, j] * Wd[:, j], the dequantised column j (numpy)."""
+    rng = np.random.default_rng(32)
+    M, N, K = 3, 6, 256
+    q, s = o.quantize(_random_weights(rng, N, K), GROUP)
+    x16 = rng.standard_normal((M, K)).astype(np.float16).view(np.uint16)
+    j = 77
+    a = np.full(K, 0x3C00, dtype=np.uint16)
+    a[j] = 0x4000  # 2.0
+    y0 = o.gemm(x16, q, s, GROUP)
+    y1 = o.gemm(o.scale_activations(x16, a), q, s, GROUP)
+    wd = o.dequantize(q, s, GROUP)
+    np.testing.assert_allclose(y1 - y0, np.outer(x16.view(np.float16)[:, j].astype(np.float64), wd[:, j]),
+                               rtol=1e-12, atol=1e-12)
+
+
 ALL_PINS = (
     pin_half_to_double_exhaustive,
     pin_float_to_half_numpy,
@@ -433,4 +472,6 @@ ALL_PINS = (
     pin_asym_round_trip_bound,
     pin_asym_gemm_numpy_tiny,
     pin_group_sizes_symmetric,
+    pin_awq_scale_numpy,
+    pin_awq_scale_per_input_channel,
 )

@@ -98,10 +98,12 @@ def test_gemm_argument_errors(lib):
 
 def test_gemm_ex_argument_errors(lib):
     g = lib.w4a16_gemm_ex
-    assert g(FAKE, FAKE, None, None, FAKE, 1, 8, 128, 32, None) == 1
-    assert g(FAKE, FAKE, FAKE, None, FAKE, 1, 8, 128, 16, None) == 2     # group 16
-    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 17, 8, 128, 32, None) == 2    # variants: M <= 16
-    assert g(FAKE, FAKE, FAKE, MISALIGNED, FAKE, 1, 8, 128, 32, None) == 3
+    assert g(FAKE, None, FAKE, None, None, FAKE, 1, 8, 128, 32, None) == 1
+    assert g(FAKE, None, FAKE, FAKE, None, FAKE, 1, 8, 128, 16, None) == 2     # group 16
+    assert g(FAKE, None, FAKE, FAKE, FAKE, FAKE, 17, 8, 128, 32, None) == 2    # variants: M <= 16
+    assert g(FAKE, FAKE, FAKE, FAKE, None, FAKE, 17, 8, 128, 128, None) == 2   # alpha: M <= 16
+    assert g(FAKE, None, FAKE, FAKE, MISALIGNED, FAKE, 1, 8, 128, 32, None) == 3
+    assert g(FAKE, MISALIGNED, FAKE, FAKE, None, FAKE, 1, 8, 128, 32, None) == 3
 
 
 def test_device_status_rejects_null(lib):

@@ -45,6 +45,9 @@ MUTANTS = {
     "asym_stored_plus_8": ("(uint8_t)(((q[i + 1] & 0x0f) << 4) | (q[i] & 0x0f));",
                            "(uint8_t)((((q[i + 1] + 8) & 0x0f) << 4) | ((q[i] + 8) & 0x0f));"),
     "zeros_ignored": ("int z = zrow ? zrow[k / group] : 8;", "int z = 8;"),
+    "awq_alpha_by_row": ("(float)orc_half_to_double(alpha[k]);", "(float)orc_half_to_double(alpha[m]);"),
+    "awq_truncating": ("out[m * K + k] = orc_float_to_half(p);",
+                       "out[m * K + k] = orc_float_to_half(p * (1.0f - 1.0f / 4096.0f));"),
 }
 
 

@@ -83,3 +83,48 @@ def test_shape_that_does_not_fit_is_rejected(w4lib):
     with pytest.raises(w4.ops._native.W4A16Error, match="SHAPE"):
         w4.gemm_ex(x, w4.repack(u8(q)), from_bits16(s), u8(z), 32)
     assert w4.device_status() == 0
+
+
+# --------------------------------------------------------------------------
+# AWQ activation scale in the prologue: y = fp16(x * alpha) @ dequant(Q(W / alpha))^T
+# --------------------------------------------------------------------------
+
+def _awq_case(N, K, seed, group, asym):
+    """Weights divided by a per-input-channel alpha before quantization (the
+    AWQ transform, done here in numpy), alpha in [0.5, 2]."""
+    rng = np.random.default_rng(seed)
+    alpha = rng.uniform(0.5, 2.0, K).astype(np.float16)
+    w = synthetic.master_weight(N, K, seed).float().numpy()
+    w16 = (w / alpha.astype(np.float32)).astype(np.float16).view(np.uint16)
+    if asym:
+        q, s, z = oracle.quantize_asym(w16, group)
+    else:
+        (q, s), z = oracle.quantize(w16, group), None
+    return alpha.view(np.uint16), q, s, z
+
+
+@pytest.mark.parametrize("group,asym", [(128, False), (128, True), (32, True), (w4.PER_CHANNEL, False)])
+@pytest.mark.parametrize("M", [1, 7, 16])
+def test_awq_activation_scale(w4lib, M, group, asym):
+    N, K = 1000, 2048
+    alpha16, q, s, z = _awq_case(N, K, 400, group, asym)
+    x16 = acts(M, K, 401 + M)
+    r = w4.repack(u8(q))
+    y = w4.gemm_ex(from_bits16(x16), r, from_bits16(s), u8(z) if z is not None else None, group,
+                   alpha=from_bits16(alpha16))
+    torch.cuda.synchronize()
+    y_ref = oracle.gemm(oracle.scale_activations(x16, alpha16), q, s, group, zeros=z)
+    assert_close(y.float().cpu().numpy(), y_ref, f"awq g={group} asym={asym} M={M}")
+
+
+def test_awq_llama3_8b_gate_up_m1(w4lib):
+    lin = workloads.LLAMA3_8B[2]
+    sw, sx = synthetic.seeds("llama3_8b_decode", 2)
+    alpha16, q, s, z = _awq_case(lin.N, lin.K, sw, 128, False)
+    x16 = acts(1, lin.K, sx)
+    y = w4.gemm_ex(from_bits16(x16), w4.repack(u8(q)), from_bits16(s), None, 128,
+                   alpha=from_bits16(alpha16))
+    torch.cuda.synchronize()
+    rows = sample_rows(lin.N, 256, sw)
+    y_ref = oracle.gemm_rows(oracle.scale_activations(x16, alpha16), q, s, rows, 128)
+    assert_close(y[:, rows].float().cpu().numpy(), y_ref, "awq gate_up")

@@ -186,9 +186,9 @@ int w4a16_gemm(const void* x_f16, const void* repacked, const void* scales_f16, 
     return from_cuda(launch_gemm_tc(x_f16, repacked, scales_f16, y_f16, M, N, K, s, ctx));
 }
 
-int w4a16_gemm_ex(const void* x_f16, const void* repacked, const void* scales_f16,
-                  const void* zeros_u8, void* y_f16, int64_t M, int64_t N, int64_t K,
-                  int32_t group, void* stream) {
+int w4a16_gemm_ex(const void* x_f16, const void* alpha_f16, const void* repacked,
+                  const void* scales_f16, const void* zeros_u8, void* y_f16, int64_t M,
+                  int64_t N, int64_t K, int32_t group, void* stream) {
     if (!x_f16 || !repacked || !scales_f16 || !y_f16) return W4A16_ERR_NULL;
     if (M < 1 || M > (int64_t)1 << 22 || !good_nk(N, K) || N > (int64_t)1 << 28 ||
         K > (int64_t)1 << 15)
@@ -196,15 +196,15 @@ int w4a16_gemm_ex(const void* x_f16, const void* repacked, const void* scales_f1
     if (group == W4A16_GROUP_PER_CHANNEL) group = (int32_t)K;
     if (!(group == 32 || group == 64 || group == 128 || group == K)) return W4A16_ERR_SHAPE;
     if (!aligned16(x_f16) || !aligned16(repacked) || !aligned16(scales_f16) || !aligned16(y_f16) ||
-        (zeros_u8 && !aligned16(zeros_u8)))
+        (zeros_u8 && !aligned16(zeros_u8)) || (alpha_f16 && !aligned16(alpha_f16)))
         return W4A16_ERR_ALIGN;
-    if (group == W4A16_GROUP && !zeros_u8)
+    if (group == W4A16_GROUP && !zeros_u8 && !alpha_f16)
         return w4a16_gemm(x_f16, repacked, scales_f16, y_f16, M, N, K, stream);
     if (M > 16) return W4A16_ERR_SHAPE;
     DeviceCtx ctx;
     if (int rc = device_ctx(&ctx)) return rc;
-    return from_cuda(launch_gemv_fmt(x_f16, repacked, scales_f16, zeros_u8, y_f16, (int)M, N, K,
-                                     group, static_cast<cudaStream_t>(stream), ctx));
+    return from_cuda(launch_gemv_fmt(x_f16, alpha_f16, repacked, scales_f16, zeros_u8, y_f16,
+                                     (int)M, N, K, group, static_cast<cudaStream_t>(stream), ctx));
 }
 
 int w4a16_gemm_plan(int64_t M, int64_t N, int64_t K, int* path, int* splits, int* ctas,

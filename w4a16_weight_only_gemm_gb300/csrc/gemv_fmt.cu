@@ -5,7 +5,10 @@
 //   y[m, n] = sum_k x[m, k] * (nib[n, k] - z[n, k / g]) * scale[n, k / g],
 // z = 8 for symmetric codes (qaqbuyan.com tutorial, "量化的数学基石" §2
 // symmetric and asymmetric formulas, §3 granularity; mhpq.cn report §二/§五
-// for the decode product from packed weights).
+// for the decode product from packed weights).  With an AWQ activation scale
+// alpha [K] (tutorial AWQ section: x~_j = x_j alpha_j, the weights quantized
+// from W_{:,j} / alpha_j), x is replaced by x~ = fp16(x * alpha) in shared
+// memory before the products (one IEEE fp16 multiply per element).
 //
 // The structure is gemv_unit_kernel's (gemv.cu): one CTA per unit of T
 // 16-row tiles over the whole K range, 8 consumer warps + 1 producer warp,
@@ -51,6 +54,7 @@ struct FmtArgs {
     const uint8_t* wq;      // kernel-layout weights
     const __half* scales;   // [N, Gs]
     const uint8_t* zeros;   // [N, Gs] or null (symmetric: z = 8)
+    const __half* alpha;    // [K] AWQ activation scale, or null
     const __half* x;        // [M, K]
     __half* y;              // [M, N]
     unsigned* status;
@@ -259,6 +263,23 @@ __global__ void __launch_bounds__(kFThreads, MT == 1 ? 3 : 2)
     const uint8_t* zr1 = a.zeros ? zr0 + 8 * a.Gs : nullptr;
 
     bool ok = mbar_wait(sbase + kFBarX, 0, a.timeout_ns, a.status);
+    if (a.alpha) {
+        // AWQ: x~ = fp16(x * alpha) in place, 16 bytes per thread per step;
+        // every consumer thread takes part in the barrier below.
+        const int per_row = a.K / 8;
+        for (int q = (int)threadIdx.x; ok && q < a.M * per_row; q += kFConsumers) {
+            const int m = q / per_row, off = q - m * per_row;
+            const uint4 av = __ldg(reinterpret_cast<const uint4*>(a.alpha) + off);
+            uint4* xp = reinterpret_cast<uint4*>(smem + a.off_x + m * a.xs_stride + off * 16);
+            uint4 xv = *xp;
+            __half2* xh = reinterpret_cast<__half2*>(&xv);
+            const __half2* ah = reinterpret_cast<const __half2*>(&av);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) xh[i] = __hmul2(xh[i], ah[i]);
+            *xp = xv;
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kFConsumers) : "memory");
+    }
     if (ok) ok = mbar_wait(sbase + kFBarS, 0, a.timeout_ns, a.status);
     ok = __all_sync(0xffffffffu, ok);  // warp-uniform before the warp MMAs
     float acc[2][MT][4];
@@ -463,10 +484,11 @@ cudaError_t launch_fmt_mt(FmtArgs a, cudaStream_t stream, const DeviceCtx& ctx) 
 
 }  // namespace
 
-cudaError_t launch_gemv_fmt(const void* x, const void* repacked, const void* scales,
-                            const void* zeros, void* y, int M, int64_t N, int64_t K, int group,
-                            cudaStream_t stream, const DeviceCtx& ctx) {
+cudaError_t launch_gemv_fmt(const void* x, const void* alpha, const void* repacked,
+                            const void* scales, const void* zeros, void* y, int M, int64_t N,
+                            int64_t K, int group, cudaStream_t stream, const DeviceCtx& ctx) {
     FmtArgs a{};
+    a.alpha = static_cast<const __half*>(alpha);
     a.wq = static_cast<const uint8_t*>(repacked);
     a.scales = static_cast<const __half*>(scales);
     a.zeros = static_cast<const uint8_t*>(zeros);

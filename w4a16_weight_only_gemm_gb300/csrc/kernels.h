@@ -40,10 +40,10 @@ cudaError_t launch_unrepack(const void* repacked, int64_t N, int64_t K, void* qw
 // (T = 1, 2 or 4).
 cudaError_t gemv_weight_map(const void* repacked, int64_t N, int64_t K, int T, CUtensorMap* out);
 // Decode GEMV of the format variants (group = 32, 64, 128 or K; zeros NULL
-// for symmetric codes).
-cudaError_t launch_gemv_fmt(const void* x, const void* repacked, const void* scales,
-                            const void* zeros, void* y, int M, int64_t N, int64_t K, int group,
-                            cudaStream_t stream, const DeviceCtx& ctx);
+// for symmetric codes; alpha [K] an AWQ activation scale or NULL).
+cudaError_t launch_gemv_fmt(const void* x, const void* alpha, const void* repacked,
+                            const void* scales, const void* zeros, void* y, int M, int64_t N,
+                            int64_t K, int group, cudaStream_t stream, const DeviceCtx& ctx);
 cudaError_t launch_gemv(const void* x, const void* repacked, const void* scales, void* y, int M,
                         int64_t N, int64_t K, cudaStream_t stream, const DeviceCtx& ctx);
 // The launch the decode GEMV would make: K split (cluster size), CTAs, the

@@ -134,11 +134,17 @@ def gemm(x: torch.Tensor, repacked: torch.Tensor, scales: torch.Tensor,
 
 def gemm_ex(x: torch.Tensor, repacked: torch.Tensor, scales: torch.Tensor,
             zeros: torch.Tensor | None = None, group: int = GROUP,
-            out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """y = x @ dequant(W)^T for the format variants of quantize_ex: scales
+            out: torch.Tensor | None = None, stream=None,
+            alpha: torch.Tensor | None = None) -> torch.Tensor:
+    """y = x~ @ dequant(W)^T for the format variants of quantize_ex: scales
     [N, K/g] fp16, zeros [N, K/g] uint8 (asymmetric) or None, g = group or K
-    for PER_CHANNEL."""
+    for PER_CHANNEL; x~ = x, or fp16(x * alpha) with an AWQ activation scale
+    alpha [K] fp16."""
     _need(x, torch.float16, "x")
+    if alpha is not None:
+        _need(alpha, torch.float16, "alpha")
+        if alpha.shape != (x.shape[-1],):
+            raise ValueError("alpha must be [K]")
     _need(repacked, torch.uint8, "repacked")
     _need(scales, torch.float16, "scales")
     if zeros is not None:
@@ -160,7 +166,8 @@ def gemm_ex(x: torch.Tensor, repacked: torch.Tensor, scales: torch.Tensor,
         _need(out, torch.float16, "out")
         if tuple(out.shape) != (M, N):
             raise ValueError("out has the wrong shape")
-    rc = _native.lib().w4a16_gemm_ex(x.data_ptr(), repacked.data_ptr(), scales.data_ptr(),
+    rc = _native.lib().w4a16_gemm_ex(x.data_ptr(), alpha.data_ptr() if alpha is not None else None,
+                                     repacked.data_ptr(), scales.data_ptr(),
                                      zeros.data_ptr() if zeros is not None else None,
                                      out.data_ptr(), M, N, K, group, _stream_ptr(stream))
     _native.check(rc, "w4a16_gemm_ex")
