@@ -90,6 +90,12 @@ def _bind(lib):
     lib.orc_gemm_rows.argtypes = [p, i64, i64, p, p, p, i64, i64, p, i64, p]
     lib.orc_gemm_rows.restype = ctypes.c_int
     lib.orc_scale_activations.argtypes = [p, i64, i64, p, p]
+    lib.orc_quantize_w8.argtypes = [p, i64, i64, p, p]
+    lib.orc_quantize_w8.restype = ctypes.c_int
+    lib.orc_dequantize_w8.argtypes = [p, p, i64, i64, p]
+    lib.orc_dequantize_w8.restype = ctypes.c_int
+    lib.orc_gemm_rows_w8.argtypes = [p, i64, i64, p, p, i64, p, i64, p]
+    lib.orc_gemm_rows_w8.restype = ctypes.c_int
     lib.orc_num_threads.restype = ctypes.c_int
     lib.orc_set_num_threads.argtypes = [ctypes.c_int]
     return lib
@@ -237,6 +243,44 @@ class Oracle:
         return out
 
     # ------------------------------------------------------------------
+    # W8A16 per-channel INT8 (tutorial §2 formula with b = 8, INT8 section).
+    # Pinned: +-amax -> +-127, scale through numpy, nearest-level brute
+    # force, round-trip bound, numpy GEMM.
+    # ------------------------------------------------------------------
+    def quantize_w8(self, W16: np.ndarray):
+        """(q8 uint8 [N, K] holding q + 128, scales uint16 fp16 bits [N])."""
+        W16 = _c(W16, np.uint16)
+        N, K = W16.shape
+        q8 = np.empty((N, K), dtype=np.uint8)
+        s = np.empty((N,), dtype=np.uint16)
+        if self._lib.orc_quantize_w8(_ptr(W16), N, K, _ptr(q8), _ptr(s)) != 0:
+            raise ValueError("oracle quantize_w8 rejected shape")
+        return q8, s
+
+    def dequantize_w8(self, q8: np.ndarray, scales: np.ndarray) -> np.ndarray:
+        q8 = _c(q8, np.uint8)
+        scales = _c(scales, np.uint16)
+        N, K = q8.shape
+        out = np.empty((N, K), dtype=np.float64)
+        self._lib.orc_dequantize_w8(_ptr(q8), _ptr(scales), N, K, _ptr(out))
+        return out
+
+    def gemm_rows_w8(self, x16: np.ndarray, q8: np.ndarray, scales: np.ndarray,
+                     rows=None) -> np.ndarray:
+        """Columns ``rows`` (default all) of y = x Wd^T, binary64 [M, len(rows)]."""
+        x16 = _c(x16, np.uint16)
+        q8 = _c(q8, np.uint8)
+        scales = _c(scales, np.uint16)
+        M, K = x16.shape
+        N = q8.shape[0]
+        rows = _c(np.arange(N) if rows is None else np.asarray(rows), np.int64)
+        y = np.empty((M, rows.size), dtype=np.float64)
+        if self._lib.orc_gemm_rows_w8(_ptr(x16), M, K, _ptr(q8), _ptr(scales), N, _ptr(rows),
+                                      rows.size, _ptr(y)) != 0:
+            raise ValueError("oracle gemm_rows_w8 rejected arguments")
+        return y
+
+    # ------------------------------------------------------------------
     # AWQ activation scaling (tutorial AWQ section).  Pinned: numpy's exact
     # binary32 product and IEEE fp16 conversion; alpha = 1 is the identity;
     # alpha acts per input channel (one-hot alpha against numpy matmul).
@@ -320,6 +364,18 @@ def quantize(W16, group: int = GROUP):
 
 def quantize_asym(W16, group: int = GROUP):
     return default().quantize_asym(W16, group)
+
+
+def quantize_w8(W16):
+    return default().quantize_w8(W16)
+
+
+def dequantize_w8(q8, scales):
+    return default().dequantize_w8(q8, scales)
+
+
+def gemm_rows_w8(x16, q8, scales, rows=None):
+    return default().gemm_rows_w8(x16, q8, scales, rows)
 
 
 def scale_activations(x16, alpha16):

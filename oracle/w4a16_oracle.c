@@ -19,6 +19,9 @@
  *               in_features, low nibble = even index, stored as q + 8,
  *               scale clamp(min=1e-8), scales stored as fp16, dequant in
  *               fp32 intermediate).
+ *          "INT8 对称量化的精度实测": per-channel symmetric INT8 weights
+ *               (the §2 formula with b = 8: s = max|x| / 127,
+ *               x_q = clamp(round(x/s), -128, 127)), fp16 activations;
  *          AWQ section "AWQ 的数学原理": activation scaling per input
  *               channel x~_j = x_j * alpha_j with W~_{:,j} = W_{:,j} / alpha_j
  *               (the alpha search needs calibration data: not restated).
@@ -38,6 +41,9 @@
  *     is stored as one byte per group; the same clamp(min=1e-8) guards s;
  *   - per-channel quantization is one group spanning the whole row
  *     (group = K);
+ *   - W8A16: one fp16 scale per output row (per-channel), the same binary32
+ *     arithmetic and clamp(min=1e-8) as the INT4 quantizer; codes are stored
+ *     as q + 128 in one byte, row-major [N, K];
  *   - AWQ's scaled activation is rounded once to fp16: x~ = fp16_rne(x * alpha),
  *     the product of two fp16 values being exact in binary32;
  *   - the GEMM reference is the exact dequantized weight (nib-8)*scale16 in
@@ -295,6 +301,84 @@ int orc_dequantize_f16(const uint8_t *qweight, const uint16_t *scales, const uin
             float v = (float)(nib - z) * s;
             out[n * K + k] = orc_float_to_half(v);
         }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* W8A16: per-channel symmetric INT8 ([P4] §2 formula with b = 8, INT8 */
+/* section "per-channel, 对称").                                        */
+/* ------------------------------------------------------------------ */
+
+/* W: fp16 bits [N, K]; q8: [N, K] bytes holding q + 128; scales: fp16 bits [N]. */
+int orc_quantize_w8(const uint16_t *W, int64_t N, int64_t K, uint8_t *q8, uint16_t *scales)
+{
+    if (N < 0 || K <= 0)
+        return -1;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+    for (int64_t n = 0; n < N; ++n) {
+        float amax = 0.0f;
+        for (int64_t k = 0; k < K; ++k) {
+            float a = fabsf((float)orc_half_to_double(W[n * K + k]));
+            if (a > amax)
+                amax = a;
+        }
+        float s = amax / 127.0f;   /* 2^(b-1) - 1 = 127 */
+        if (s < 1e-8f)
+            s = 1e-8f;
+        for (int64_t k = 0; k < K; ++k) {
+            float r = nearbyintf((float)orc_half_to_double(W[n * K + k]) / s);
+            if (r < -128.0f)
+                r = -128.0f;
+            if (r > 127.0f)
+                r = 127.0f;
+            q8[n * K + k] = (uint8_t)((int)r + 128);
+        }
+        scales[n] = orc_float_to_half(s);
+    }
+    return 0;
+}
+
+/* Exact dequantized row: (code - 128) * scale16, binary64. */
+static void dequant_row_w8(const uint8_t *qrow, uint16_t scale, int64_t K, double *out)
+{
+    double s = orc_half_to_double(scale);
+    for (int64_t k = 0; k < K; ++k)
+        out[k] = (double)((int)qrow[k] - 128) * s;
+}
+
+int orc_dequantize_w8(const uint8_t *q8, const uint16_t *scales, int64_t N, int64_t K,
+                      double *out)
+{
+    for (int64_t n = 0; n < N; ++n)
+        dequant_row_w8(q8 + n * K, scales[n], K, out + n * K);
+    return 0;
+}
+
+/* Rows `rows` of y = x * Wd^T for W8A16 weights; y is [M, nrows] binary64. */
+int orc_gemm_rows_w8(const uint16_t *x, int64_t M, int64_t K, const uint8_t *q8,
+                     const uint16_t *scales, int64_t N, const int64_t *rows, int64_t nrows,
+                     double *y)
+{
+    if (M < 0 || N < 0 || K <= 0 || K > 32768)
+        return -1;
+    for (int64_t r = 0; r < nrows; ++r)
+        if (rows[r] < 0 || rows[r] >= N)
+            return -1;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int64_t r = 0; r < nrows; ++r) {
+        double wd[32768];
+        dequant_row_w8(q8 + rows[r] * K, scales[rows[r]], K, wd);
+        for (int64_t m = 0; m < M; ++m) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += orc_half_to_double(x[m * K + k]) * wd[k];
+            y[m * nrows + r] = acc;
+        }
+    }
     return 0;
 }
 

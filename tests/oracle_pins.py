@@ -450,6 +450,63 @@ def pin_awq_scale_per_input_channel(o) -> None:
                                rtol=1e-12, atol=1e-12)
 
 
+# --------------------------------------------------------------------------
+# W8A16 per-channel INT8 (tutorial §2 formula with b = 8, INT8 section)
+# --------------------------------------------------------------------------
+
+def pin_w8_amax_and_scale(o) -> None:
+    """Every row's largest |w| maps to +-127 (code 128 +- 127), the scale is
+    numpy's fp16(max(fp32(amax) / 127, 1e-8)); an all-zero row stays zero."""
+    rng = np.random.default_rng(41)
+    w16 = _random_weights(rng, 24, 640)
+    w16[5] = 0
+    q8, s = o.quantize_w8(w16)
+    q = q8.astype(np.int64) - 128
+    w = w16.view(np.float16).astype(np.float64)
+    idx = np.abs(w).argmax(axis=1)
+    live = np.abs(w).max(axis=1) > 0
+    assert (q[live, idx[live]] == 127 * np.sign(w[live, idx[live]])).all()
+    assert (q[5] == 0).all()
+    a = np.abs(w16.view(np.float16).astype(np.float32)).max(axis=1)
+    ref = np.maximum(a / np.float32(127.0), np.float32(1e-8)).astype(np.float16).view(np.uint16)
+    assert np.array_equal(s, ref)
+
+
+def pin_w8_nearest_level(o) -> None:
+    """q is the integer nearest to fp32(w) / s32 (ties to even), checked by
+    rounding numpy's float32 quotient with numpy's round-half-even."""
+    rng = np.random.default_rng(42)
+    w16 = _random_weights(rng, 6, 256)
+    w16[0, :4] = _f16_bits([0.5, -1.5, 2.5, 127.0 * 2.0 ** -8])  # ties when s = 2^-8
+    w16[0, 4] = _f16_bits([127.0 * 2.0 ** -8])[0]
+    w16[0, 5:] = 0
+    q8, _ = o.quantize_w8(w16)
+    w32 = w16.view(np.float16).astype(np.float32)
+    s32 = np.maximum(np.abs(w32).max(axis=1) / np.float32(127.0), np.float32(1e-8))
+    ref = np.clip(np.rint(w32 / s32[:, None]), -128, 127).astype(np.int64)
+    assert np.array_equal(q8.astype(np.int64) - 128, ref)
+
+
+def pin_w8_round_trip_and_gemm(o) -> None:
+    """Round trip within half a step of the binary32 scale; against the stored
+    fp16 scale (|s16 - s32| <= 2^-11 s32) and |q| <= 128 that is
+    s16 (1 + 2^-10) (1/2 + 2^-21 + 128 * 2^-11).  y equals numpy's float64
+    matmul of the dequantised rows (decoded by numpy) on tiny shapes."""
+    rng = np.random.default_rng(43)
+    w16 = _random_weights(rng, 16, 512)
+    q8, s = o.quantize_w8(w16)
+    s64 = s.view(np.float16).astype(np.float64)
+    wd = (q8.astype(np.float64) - 128) * s64[:, None]
+    np.testing.assert_array_equal(o.dequantize_w8(q8, s), wd)
+    err = np.abs(w16.view(np.float16).astype(np.float64) - wd)
+    assert (err <= s64[:, None] * (1 + 2.0 ** -10) * (0.5 + 2.0 ** -21 + 2.0 ** -4)).all()
+    assert 0.2 < (err / s64[:, None]).mean() < 0.3
+    x16 = rng.standard_normal((3, 512)).astype(np.float16).view(np.uint16)
+    y = o.gemm_rows_w8(x16, q8, s)
+    np.testing.assert_allclose(y, x16.view(np.float16).astype(np.float64) @ wd.T, rtol=1e-12,
+                               atol=1e-12)
+
+
 ALL_PINS = (
     pin_half_to_double_exhaustive,
     pin_float_to_half_numpy,
@@ -474,4 +531,7 @@ ALL_PINS = (
     pin_group_sizes_symmetric,
     pin_awq_scale_numpy,
     pin_awq_scale_per_input_channel,
+    pin_w8_amax_and_scale,
+    pin_w8_nearest_level,
+    pin_w8_round_trip_and_gemm,
 )

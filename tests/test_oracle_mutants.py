@@ -45,6 +45,10 @@ MUTANTS = {
     "asym_stored_plus_8": ("(uint8_t)(((q[i + 1] & 0x0f) << 4) | (q[i] & 0x0f));",
                            "(uint8_t)((((q[i + 1] + 8) & 0x0f) << 4) | ((q[i] + 8) & 0x0f));"),
     "zeros_ignored": ("int z = zrow ? zrow[k / group] : 8;", "int z = 8;"),
+    "w8_divide_by_128": ("float s = amax / 127.0f;   /* 2^(b-1) - 1 = 127 */",
+                         "float s = amax / 128.0f;"),
+    "w8_offset_127": ("out[k] = (double)((int)qrow[k] - 128) * s;",
+                      "out[k] = (double)((int)qrow[k] - 127) * s;"),
     "awq_alpha_by_row": ("(float)orc_half_to_double(alpha[k]);", "(float)orc_half_to_double(alpha[m]);"),
     "awq_truncating": ("out[m * K + k] = orc_float_to_half(p);",
                        "out[m * K + k] = orc_float_to_half(p * (1.0f - 1.0f / 4096.0f));"),
