@@ -271,6 +271,31 @@ def formats_m1():
         res["five_shapes"] = {"us": round(tot_t, 2), "gbs": round(tot_b / tot_t / 1e3, 1)}
         out[name] = res
         torch.cuda.empty_cache()
+    # W8A16 (per-channel INT8): codes [N, K] bytes + fp16 scale per row
+    res = {}
+    for i, lin in enumerate(workloads.LLAMA3_8B):
+        sw, sx = synthetic.seeds("llama3_8b_decode", i)
+        W = synthetic.master_weight(lin.N, lin.K, sw, device="cuda")
+        q, s = w4.quantize_w8(W)
+        del W
+        x = synthetic.activations(1, lin.K, sx, device="cuda")
+        y = torch.empty((1, lin.N), dtype=torch.float16, device="cuda")
+        copies = max(2, -(-4 * l2_bytes() // q.numel()))
+        qs = [q] + [q.clone() for _ in range(copies - 1)]
+
+        def body():
+            for qq in qs:
+                w4.gemm_w8(x, qq, s, out=y)
+        g = capture(body, stream)
+        t = time_graph(g, stream, 10, 3) / copies
+        b = lin.N * lin.K + 2 * lin.N + 2 * lin.K + 2 * lin.N
+        res[lin.name] = {"us": round(t * 1e6, 3), "gbs": round(b / t / 1e9, 1)}
+        del qs, g, q, s
+    tot_t = sum(v["us"] for v in res.values())
+    tot_b = sum(l.N * l.K + 4 * l.N + 2 * l.K for l in workloads.LLAMA3_8B)
+    res["five_shapes"] = {"us": round(tot_t, 2), "gbs": round(tot_b / tot_t / 1e3, 1)}
+    out["w8a16_per_channel"] = res
+    torch.cuda.empty_cache()
     return out
 
 

@@ -216,6 +216,40 @@ int w4a16_gemm_ex(const void *x_f16, const void *alpha_f16, const void *repacked
                   const void *scales_f16, const void *zeros_u8, void *y_f16, int64_t M,
                   int64_t N, int64_t K, int32_t group, void *stream);
 
+/*
+ * w4a16_quantize_w8 -- W8A16 weights: per-channel symmetric INT8.
+ *
+ * Source: tutorial "量化的数学基石" §2 formula with b = 8 and its INT8
+ * section ("per-channel, 对称").  Per row n, in IEEE binary32 on the exactly
+ * upcast inputs:
+ *     s32 = max(max_k |W[n, k]| / 127, 1e-8)          (correctly rounded /)
+ *     q   = clamp(round_half_even(W[n, k] / s32), -128, 127)
+ *     codes[n, k] = q + 128;  scales_f16[n] = fp16_round_nearest_even(s32)
+ *
+ *   W_f16      [N, K] fp16.  N >= 1; K >= 128, K % 128 == 0.
+ *   codes_u8   [N, K] bytes, written (row-major; no repack step).
+ *   scales_f16 [N] fp16, written.
+ * Bit-identical to the library's CPU reference definition.
+ * Errors: NULL -> W4A16_ERR_NULL; bad N, K -> W4A16_ERR_SHAPE; misaligned
+ *         pointer -> W4A16_ERR_ALIGN.
+ */
+int w4a16_quantize_w8(const void *W_f16, int64_t N, int64_t K, void *codes_u8, void *scales_f16,
+                      void *stream);
+
+/*
+ * w4a16_gemm_w8 -- W8A16 decode GEMV:
+ *   y[m, n] = scale[n] * sum_k x[m, k] * (codes[n, k] - 128),
+ * exact q * x products accumulated in FP32, the per-row scale applied once,
+ * y rounded once to fp16.  M = 1..16; x[M, K] is held in shared memory whole
+ * beside the ring (as w4a16_gemm_ex: about 2 * M * K <= 200 KB), a shape
+ * that does not fit -> W4A16_ERR_SHAPE.  Graph-capturable, programmatic
+ * dependent launch; codes and scales are constants of the call as in
+ * w4a16_gemm.
+ * Errors: as w4a16_gemm.
+ */
+int w4a16_gemm_w8(const void *x_f16, const void *codes_u8, const void *scales_f16, void *y_f16,
+                  int64_t M, int64_t N, int64_t K, void *stream);
+
 /* Paths reported by w4a16_gemm_plan. */
 enum { W4A16_PATH_GEMV = 1, W4A16_PATH_TENSOR_CORE = 2 };
 

@@ -106,6 +106,13 @@ def test_gemm_ex_argument_errors(lib):
     assert g(FAKE, MISALIGNED, FAKE, FAKE, None, FAKE, 1, 8, 128, 32, None) == 3
 
 
+def test_w8_argument_errors(lib):
+    assert lib.w4a16_quantize_w8(None, 8, 128, FAKE, FAKE, None) == 1
+    assert lib.w4a16_quantize_w8(FAKE, 8, 200, FAKE, FAKE, None) == 2
+    assert lib.w4a16_gemm_w8(FAKE, FAKE, FAKE, FAKE, 17, 8, 128, None) == 2   # M <= 16
+    assert lib.w4a16_gemm_w8(FAKE, MISALIGNED, FAKE, FAKE, 1, 8, 128, None) == 3
+
+
 def test_device_status_rejects_null(lib):
     assert lib.w4a16_device_status(None) == 1
 

@@ -1,0 +1,59 @@
+"""W8A16 (per-channel symmetric INT8 weights, fp16 activations) vs the CPU
+oracle: codes and scales bit-exact; the GEMV within the GEMV bar (products
+q * x are exact, only FP32 sums and the final fp16 rounding of y round)."""
+from __future__ import annotations
+
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import assert_close, bits16, from_bits16, u8
+from parity_data import acts, quantized, sample_rows
+import w4a16_weight_only_gemm_gb300 as w4
+from w4a16_weight_only_gemm_gb300 import synthetic, workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@functools.lru_cache(maxsize=16)
+def quantized_w8(N: int, K: int, seed: int):
+    w16 = quantized(N, K, seed)[0]
+    return w16, *oracle.quantize_w8(w16)
+
+
+@pytest.mark.parametrize("N,K", [(1, 128), (130, 384), (1000, 2048), (4096, 14336)])
+def test_quantizer_bit_exact(w4lib, N, K):
+    w16, q_ref, s_ref = quantized_w8(N, K, 500 + N)
+    w16 = w16.copy()
+    w16[0] = 0  # an all-zero row
+    q_ref, s_ref = oracle.quantize_w8(w16)
+    q, s = w4.quantize_w8(from_bits16(w16))
+    torch.cuda.synchronize()
+    assert np.array_equal(q.cpu().numpy(), q_ref)
+    assert np.array_equal(bits16(s), s_ref)
+
+
+@pytest.mark.parametrize("N,K", [(1000, 2048), (4136, 1152), (300, 4096), (37, 128)])
+@pytest.mark.parametrize("M", [1, 5, 16])
+def test_gemv_every_row(w4lib, M, N, K):
+    _, q, s = quantized_w8(N, K, 510 + K)
+    x16 = acts(M, K, 511 + M)
+    y = w4.gemm_w8(from_bits16(x16), u8(q), from_bits16(s))
+    torch.cuda.synchronize()
+    assert_close(y.float().cpu().numpy(), oracle.gemm_rows_w8(x16, q, s), f"w8 M={M} N={N} K={K}")
+    assert w4.device_status() == 0
+
+
+@pytest.mark.parametrize("idx", range(len(workloads.LLAMA3_8B)))
+def test_llama3_8b_shapes_m1(w4lib, idx):
+    lin = workloads.LLAMA3_8B[idx]
+    sw, sx = synthetic.seeds("llama3_8b_decode", idx)
+    _, q, s = quantized_w8(lin.N, lin.K, sw)
+    x16 = acts(1, lin.K, sx)
+    y = w4.gemm_w8(from_bits16(x16), u8(q), from_bits16(s))
+    torch.cuda.synchronize()
+    rows = sample_rows(lin.N, 256, sw)
+    assert_close(y[:, rows].float().cpu().numpy(), oracle.gemm_rows_w8(x16, q, s, rows), lin.name)

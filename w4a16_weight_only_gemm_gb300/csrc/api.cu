@@ -207,6 +207,30 @@ int w4a16_gemm_ex(const void* x_f16, const void* alpha_f16, const void* repacked
                                      (int)M, N, K, group, static_cast<cudaStream_t>(stream), ctx));
 }
 
+int w4a16_quantize_w8(const void* W_f16, int64_t N, int64_t K, void* codes_u8, void* scales_f16,
+                      void* stream) {
+    if (!W_f16 || !codes_u8 || !scales_f16) return W4A16_ERR_NULL;
+    if (!good_nk(N, K)) return W4A16_ERR_SHAPE;
+    if (!aligned16(W_f16) || !aligned16(codes_u8) || !aligned16(scales_f16)) return W4A16_ERR_ALIGN;
+    DeviceCtx ctx;
+    if (int rc = device_ctx(&ctx)) return rc;
+    return from_cuda(launch_quantize_w8(W_f16, N, K, codes_u8, scales_f16,
+                                        static_cast<cudaStream_t>(stream), ctx));
+}
+
+int w4a16_gemm_w8(const void* x_f16, const void* codes_u8, const void* scales_f16, void* y_f16,
+                  int64_t M, int64_t N, int64_t K, void* stream) {
+    if (!x_f16 || !codes_u8 || !scales_f16 || !y_f16) return W4A16_ERR_NULL;
+    if (M < 1 || M > 16 || !good_nk(N, K) || N > (int64_t)1 << 28 || K > (int64_t)1 << 15)
+        return W4A16_ERR_SHAPE;
+    if (!aligned16(x_f16) || !aligned16(codes_u8) || !aligned16(scales_f16) || !aligned16(y_f16))
+        return W4A16_ERR_ALIGN;
+    DeviceCtx ctx;
+    if (int rc = device_ctx(&ctx)) return rc;
+    return from_cuda(launch_gemv_w8(x_f16, codes_u8, scales_f16, y_f16, (int)M, N, K,
+                                    static_cast<cudaStream_t>(stream), ctx));
+}
+
 int w4a16_gemm_plan(int64_t M, int64_t N, int64_t K, int* path, int* splits, int* ctas,
                     int* blocks_per_cta, int* rows_per_cta) {
     if (!path || !splits || !ctas || !blocks_per_cta || !rows_per_cta) return W4A16_ERR_NULL;

@@ -31,6 +31,11 @@ cudaError_t launch_quantize(const void* W, int64_t N, int64_t K, void* qweight, 
 cudaError_t launch_quantize_fmt(const void* W, int64_t N, int64_t K, int group, bool asym,
                                 void* qweight, void* scales, void* zeros, cudaStream_t stream,
                                 const DeviceCtx& ctx);
+// W8A16: per-channel symmetric INT8 codes (q + 128, [N, K] bytes) and the GEMV.
+cudaError_t launch_quantize_w8(const void* W, int64_t N, int64_t K, void* q8, void* scales,
+                               cudaStream_t stream, const DeviceCtx& ctx);
+cudaError_t launch_gemv_w8(const void* x, const void* q8, const void* scales, void* y, int M,
+                           int64_t N, int64_t K, cudaStream_t stream, const DeviceCtx& ctx);
 cudaError_t launch_repack(const void* qweight, int64_t N, int64_t K, void* repacked,
                           cudaStream_t stream, const DeviceCtx& ctx);
 cudaError_t launch_unrepack(const void* repacked, int64_t N, int64_t K, void* qweight,

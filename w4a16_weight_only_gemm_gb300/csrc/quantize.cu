@@ -227,6 +227,55 @@ __global__ void __launch_bounds__(kFmtThreads)
     __threadfence();
 }
 
+// ---------------------------------------------------------------------------
+// W8A16: per-channel symmetric INT8 (tutorial §2 formula with b = 8):
+// s = max(max_k |w| / 127, 1e-8), q = clamp(round(w / s), -128, 127), code =
+// q + 128, one warp per row, the row read twice (absmax, then codes), every
+// step the binary32 operation of the formula (correctly rounded divides).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kFmtThreads)
+    quantize_w8_kernel(const uint4* __restrict__ W, int64_t N, int K,
+                       uint2* __restrict__ q8, __half* __restrict__ scales) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (kFmtThreads / 32);
+    const int pieces = K / 8;  // 16-byte pieces per row
+    for (int64_t n = (int64_t)blockIdx.x * (kFmtThreads / 32) + threadIdx.x / 32; n < N;
+         n += warps) {
+        const uint4* row = W + n * pieces;
+        float amax = 0.0f;
+        for (int p = lane; p < pieces; p += 32) {
+            const uint4 raw = __ldg(row + p);
+            const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = __half22float2(h2[i]);
+                amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        float s = __fdiv_rn(amax, 127.0f);
+        if (s < 1e-8f) s = 1e-8f;
+        for (int p = lane; p < pieces; p += 32) {
+            const uint4 raw = __ldg(row + p);
+            const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+            uint32_t b[2] = {0, 0};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = __half22float2(h2[i]);
+                const float qa = fminf(fmaxf(rintf(__fdiv_rn(f.x, s)), -128.0f), 127.0f);
+                const float qb = fminf(fmaxf(rintf(__fdiv_rn(f.y, s)), -128.0f), 127.0f);
+                const uint32_t pair = (uint32_t)((int)qa + 128) | ((uint32_t)((int)qb + 128) << 8);
+                b[i / 2] |= pair << (16 * (i & 1));
+            }
+            q8[n * pieces + p] = make_uint2(b[0], b[1]);
+        }
+        if (lane == 0) scales[n] = __float2half_rn(s);
+    }
+    __threadfence();
+}
+
 }  // namespace
 
 cudaError_t launch_quantize(const void* W, int64_t N, int64_t K, void* qweight, void* scales,
@@ -258,6 +307,18 @@ cudaError_t launch_quantize(const void* W, int64_t N, int64_t K, void* qweight, 
 }  // namespace w4a16
 
 namespace w4a16 {
+
+cudaError_t launch_quantize_w8(const void* W, int64_t N, int64_t K, void* q8, void* scales,
+                               cudaStream_t stream, const DeviceCtx& ctx) {
+    int64_t blocks = (N + kFmtThreads / 32 - 1) / (kFmtThreads / 32);
+    const int64_t cap = (int64_t)ctx.num_sms * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    quantize_w8_kernel<<<(unsigned)blocks, kFmtThreads, 0, stream>>>(
+        static_cast<const uint4*>(W), N, (int)K, static_cast<uint2*>(q8),
+        static_cast<__half*>(scales));
+    return cudaGetLastError();
+}
 
 cudaError_t launch_quantize_fmt(const void* W, int64_t N, int64_t K, int group, bool asym,
                                 void* qweight, void* scales, void* zeros, cudaStream_t stream,

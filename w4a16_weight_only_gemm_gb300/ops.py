@@ -174,6 +174,36 @@ def gemm_ex(x: torch.Tensor, repacked: torch.Tensor, scales: torch.Tensor,
     return out
 
 
+def quantize_w8(W: torch.Tensor, stream=None):
+    """W8A16: W fp16 [N, K] -> (codes uint8 [N, K] holding q + 128, scales fp16 [N])."""
+    _need(W, torch.float16, "W")
+    N, K = W.shape
+    codes = torch.empty((N, K), dtype=torch.uint8, device=W.device)
+    s = torch.empty((N,), dtype=torch.float16, device=W.device)
+    _native.check(_native.lib().w4a16_quantize_w8(W.data_ptr(), N, K, codes.data_ptr(),
+                                                  s.data_ptr(), _stream_ptr(stream)),
+                  "w4a16_quantize_w8")
+    return codes, s
+
+
+def gemm_w8(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor,
+            out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """W8A16 GEMV: y[M, N] = x[M, K] @ ((codes - 128) * scales[:, None])^T, M <= 16."""
+    _need(x, torch.float16, "x")
+    _need(codes, torch.uint8, "codes")
+    _need(scales, torch.float16, "scales")
+    N, K = codes.shape
+    if x.dim() != 2 or x.shape[1] != K or scales.shape != (N,):
+        raise ValueError(f"x must be [M, {K}] and scales [{N}]")
+    M = x.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    _native.check(_native.lib().w4a16_gemm_w8(x.data_ptr(), codes.data_ptr(), scales.data_ptr(),
+                                              out.data_ptr(), M, N, K, _stream_ptr(stream)),
+                  "w4a16_gemm_w8")
+    return out
+
+
 def gemm_plan(M: int, N: int, K: int) -> dict:
     """The launch gemm() makes for (M, N, K) on the current device:
     {"path": "gemv" | "tensor_core", "splits", "ctas", "blocks_per_cta", "rows_per_cta"}."""
