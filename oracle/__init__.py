@@ -90,6 +90,10 @@ def _bind(lib):
     lib.orc_gemm_rows.argtypes = [p, i64, i64, p, p, p, i64, i64, p, i64, p]
     lib.orc_gemm_rows.restype = ctypes.c_int
     lib.orc_scale_activations.argtypes = [p, i64, i64, p, p]
+    lib.orc_pack_q4_0.argtypes = [p, p, i64, i64, p]
+    lib.orc_pack_q4_0.restype = ctypes.c_int
+    lib.orc_dequantize_q4_0.argtypes = [p, i64, i64, p]
+    lib.orc_dequantize_q4_0.restype = ctypes.c_int
     lib.orc_quantize_w8.argtypes = [p, i64, i64, p, p]
     lib.orc_quantize_w8.restype = ctypes.c_int
     lib.orc_dequantize_w8.argtypes = [p, p, i64, i64, p]
@@ -243,6 +247,41 @@ class Oracle:
         return out
 
     # ------------------------------------------------------------------
+    # GGUF Q4_0 blocks (tutorial GGUF section).  Pinned: a hand-derived
+    # block fixture; decode of packed blocks equals the group-32 dequantizer.
+    # ------------------------------------------------------------------
+    def quantize_q4_0(self, W16: np.ndarray) -> np.ndarray:
+        """Q4_0 blocks uint8 [N, K/32 * 18] (group-32 symmetric codes)."""
+        q, s = self.quantize(W16, 32)
+        return self.pack_q4_0(q, s)
+
+    def pack_q4_0(self, qweight: np.ndarray, scales: np.ndarray) -> np.ndarray:
+        qweight = _c(qweight, np.uint8)
+        scales = _c(scales, np.uint16)
+        N, K = qweight.shape[0], 2 * qweight.shape[1]
+        out = np.empty((N, K // 32 * 18), dtype=np.uint8)
+        if self._lib.orc_pack_q4_0(_ptr(qweight), _ptr(scales), N, K, _ptr(out)) != 0:
+            raise ValueError("oracle pack_q4_0 rejected shape")
+        return out
+
+    def dequantize_q4_0(self, blocks: np.ndarray, K: int) -> np.ndarray:
+        blocks = _c(blocks, np.uint8)
+        N = blocks.shape[0]
+        out = np.empty((N, K), dtype=np.float64)
+        if self._lib.orc_dequantize_q4_0(_ptr(blocks), N, K, _ptr(out)) != 0:
+            raise ValueError("oracle dequantize_q4_0 rejected shape")
+        return out
+
+    def gemm_q4_0(self, x16: np.ndarray, blocks: np.ndarray, rows=None) -> np.ndarray:
+        """Columns ``rows`` (default all) of y = x Wd^T with Wd decoded from Q4_0 blocks."""
+        x16 = _c(x16, np.uint16)
+        K = x16.shape[1]
+        blocks = _c(blocks, np.uint8)
+        sel = blocks if rows is None else blocks[np.asarray(rows)]
+        wd = self.dequantize_q4_0(sel, K)
+        return x16.view(np.float16).astype(np.float64) @ wd.T
+
+    # ------------------------------------------------------------------
     # W8A16 per-channel INT8 (tutorial §2 formula with b = 8, INT8 section).
     # Pinned: +-amax -> +-127, scale through numpy, nearest-level brute
     # force, round-trip bound, numpy GEMM.
@@ -364,6 +403,22 @@ def quantize(W16, group: int = GROUP):
 
 def quantize_asym(W16, group: int = GROUP):
     return default().quantize_asym(W16, group)
+
+
+def quantize_q4_0(W16):
+    return default().quantize_q4_0(W16)
+
+
+def pack_q4_0(qweight, scales):
+    return default().pack_q4_0(qweight, scales)
+
+
+def dequantize_q4_0(blocks, K):
+    return default().dequantize_q4_0(blocks, K)
+
+
+def gemm_q4_0(x16, blocks, rows=None):
+    return default().gemm_q4_0(x16, blocks, rows)
 
 
 def quantize_w8(W16):

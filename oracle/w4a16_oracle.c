@@ -22,6 +22,9 @@
  *          "INT8 对称量化的精度实测": per-channel symmetric INT8 weights
  *               (the §2 formula with b = 8: s = max|x| / 127,
  *               x_q = clamp(round(x/s), -128, 127)), fp16 activations;
+ *          GGUF section: the Q4_0 block, 32 weights in 18 bytes -- d (fp16)
+ *               then 16 bytes, byte i holding element 2i in its low nibble
+ *               and 2i+1 in its high nibble, decoded as (nibble - 8) * d;
  *          AWQ section "AWQ 的数学原理": activation scaling per input
  *               channel x~_j = x_j * alpha_j with W~_{:,j} = W_{:,j} / alpha_j
  *               (the alpha search needs calibration data: not restated).
@@ -44,6 +47,9 @@
  *   - W8A16: one fp16 scale per output row (per-channel), the same binary32
  *     arithmetic and clamp(min=1e-8) as the INT4 quantizer; codes are stored
  *     as q + 128 in one byte, row-major [N, K];
+ *   - Q4_0 codes are the §2/§3 symmetric quantizer with groups of 32 (the
+ *     pages give the block's decoder, not a separate quantizer), laid out
+ *     block after block along each row, rows one after another;
  *   - AWQ's scaled activation is rounded once to fp16: x~ = fp16_rne(x * alpha),
  *     the product of two fp16 values being exact in binary32;
  *   - the GEMM reference is the exact dequantized weight (nib-8)*scale16 in
@@ -379,6 +385,45 @@ int orc_gemm_rows_w8(const uint16_t *x, int64_t M, int64_t K, const uint8_t *q8,
             y[m * nrows + r] = acc;
         }
     }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* GGUF Q4_0 blocks ([P4] GGUF section).                                */
+/* ------------------------------------------------------------------ */
+
+/* (qweight [N, K/2] canonical bytes, scales [N, K/32]) -> blocks [N * K/32][18]. */
+int orc_pack_q4_0(const uint8_t *qweight, const uint16_t *scales, int64_t N, int64_t K,
+                  uint8_t *blocks)
+{
+    if (N < 0 || K <= 0 || K % 32 != 0)
+        return -1;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t b = 0; b < K / 32; ++b) {
+            uint8_t *blk = blocks + (n * (K / 32) + b) * 18;
+            uint16_t d = scales[n * (K / 32) + b];
+            blk[0] = (uint8_t)(d & 0xff);        /* little-endian fp16 */
+            blk[1] = (uint8_t)(d >> 8);
+            for (int i = 0; i < 16; ++i)         /* byte i: elements 2i (low), 2i+1 (high) */
+                blk[2 + i] = qweight[n * (K / 2) + b * 16 + i];
+        }
+    return 0;
+}
+
+/* Exact decode of Q4_0 blocks: out[n, k] = (nibble - 8) * d in binary64. */
+int orc_dequantize_q4_0(const uint8_t *blocks, int64_t N, int64_t K, double *out)
+{
+    if (N < 0 || K <= 0 || K % 32 != 0)
+        return -1;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t b = 0; b < K / 32; ++b) {
+            const uint8_t *blk = blocks + (n * (K / 32) + b) * 18;
+            double d = orc_half_to_double((uint16_t)(blk[0] | (blk[1] << 8)));
+            for (int i = 0; i < 16; ++i) {
+                out[n * K + b * 32 + 2 * i] = (double)((blk[2 + i] & 0x0f) - 8) * d;
+                out[n * K + b * 32 + 2 * i + 1] = (double)(((blk[2 + i] >> 4) & 0x0f) - 8) * d;
+            }
+        }
     return 0;
 }
 

@@ -507,6 +507,37 @@ def pin_w8_round_trip_and_gemm(o) -> None:
                                atol=1e-12)
 
 
+# --------------------------------------------------------------------------
+# GGUF Q4_0 blocks (tutorial GGUF section)
+# --------------------------------------------------------------------------
+
+def pin_q4_0_block_fixture(o) -> None:
+    """A hand-derived 18-byte block decodes to the fixture's values."""
+    rows = {r[0]: r[1:] for r in _read_fixture("q4_0_block.txt")}
+    blk = np.array([[int(b, 16) for b in rows["block"]]], dtype=np.uint8)
+    expect = [float(v) for v in rows["values"]] + [float(rows["values_rest"][0])] * int(
+        rows["values_rest"][1])
+    assert o.dequantize_q4_0(blk, 32).tolist() == [expect]
+    # and packing the same codes and scale gives the same block
+    q = blk[:, 2:]
+    s = np.array([[int(blk[0, 0]) | (int(blk[0, 1]) << 8)]], dtype=np.uint16)
+    assert np.array_equal(o.pack_q4_0(q, s), blk)
+
+
+def pin_q4_0_matches_group32(o) -> None:
+    """Blocks of group-32 symmetric codes decode to exactly the group-32
+    dequantized weights, 18 bytes per 32 weights; the GEMM follows."""
+    rng = np.random.default_rng(51)
+    w16 = _random_weights(rng, 7, 512)
+    q, s = o.quantize(w16, 32)
+    blocks = o.quantize_q4_0(w16)
+    assert blocks.shape == (7, 512 // 32 * 18)
+    np.testing.assert_array_equal(o.dequantize_q4_0(blocks, 512), o.dequantize(q, s, 32))
+    x16 = rng.standard_normal((2, 512)).astype(np.float16).view(np.uint16)
+    np.testing.assert_allclose(o.gemm_q4_0(x16, blocks), o.gemm(x16, q, s, 32), rtol=1e-12,
+                               atol=1e-12)
+
+
 ALL_PINS = (
     pin_half_to_double_exhaustive,
     pin_float_to_half_numpy,
@@ -532,6 +563,8 @@ ALL_PINS = (
     pin_awq_scale_numpy,
     pin_awq_scale_per_input_channel,
     pin_w8_amax_and_scale,
+    pin_q4_0_block_fixture,
+    pin_q4_0_matches_group32,
     pin_w8_nearest_level,
     pin_w8_round_trip_and_gemm,
 )

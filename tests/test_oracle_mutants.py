@@ -45,6 +45,10 @@ MUTANTS = {
     "asym_stored_plus_8": ("(uint8_t)(((q[i + 1] & 0x0f) << 4) | (q[i] & 0x0f));",
                            "(uint8_t)((((q[i + 1] + 8) & 0x0f) << 4) | ((q[i] + 8) & 0x0f));"),
     "zeros_ignored": ("int z = zrow ? zrow[k / group] : 8;", "int z = 8;"),
+    "q4_0_nibbles_swapped": ("out[n * K + b * 32 + 2 * i] = (double)((blk[2 + i] & 0x0f) - 8) * d;",
+                             "out[n * K + b * 32 + 2 * i] = (double)(((blk[2 + i] >> 4) & 0x0f) - 8) * d;"),
+    "q4_0_scale_big_endian": ("blk[0] = (uint8_t)(d & 0xff);        /* little-endian fp16 */",
+                              "blk[0] = (uint8_t)(d >> 8);"),
     "w8_divide_by_128": ("float s = amax / 127.0f;   /* 2^(b-1) - 1 = 127 */",
                          "float s = amax / 128.0f;"),
     "w8_offset_127": ("out[k] = (double)((int)qrow[k] - 128) * s;",
