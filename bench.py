@@ -296,6 +296,31 @@ def formats_m1():
     res["five_shapes"] = {"us": round(tot_t, 2), "gbs": round(tot_b / tot_t / 1e3, 1)}
     out["w8a16_per_channel"] = res
     torch.cuda.empty_cache()
+    # GGUF Q4_0 blocks: 18 bytes per 32 weights (scales inline)
+    res = {}
+    for i, lin in enumerate(workloads.LLAMA3_8B):
+        sw, sx = synthetic.seeds("llama3_8b_decode", i)
+        W = synthetic.master_weight(lin.N, lin.K, sw, device="cuda")
+        blk = w4.quantize_q4_0(W)
+        del W
+        x = synthetic.activations(1, lin.K, sx, device="cuda")
+        y = torch.empty((1, lin.N), dtype=torch.float16, device="cuda")
+        copies = max(2, -(-4 * l2_bytes() // blk.numel()))
+        bs = [blk] + [blk.clone() for _ in range(copies - 1)]
+
+        def body():
+            for bb in bs:
+                w4.gemm_q4_0(x, bb, out=y)
+        g = capture(body, stream)
+        t = time_graph(g, stream, 10, 3) / copies
+        b = lin.N * lin.K // 32 * 18 + 2 * lin.K + 2 * lin.N
+        res[lin.name] = {"us": round(t * 1e6, 3), "gbs": round(b / t / 1e9, 1)}
+        del bs, g, blk
+    tot_t = sum(v["us"] for v in res.values())
+    tot_b = sum(l.N * l.K // 32 * 18 + 2 * l.K + 2 * l.N for l in workloads.LLAMA3_8B)
+    res["five_shapes"] = {"us": round(tot_t, 2), "gbs": round(tot_b / tot_t / 1e3, 1)}
+    out["q4_0_blocks"] = res
+    torch.cuda.empty_cache()
     return out
 
 

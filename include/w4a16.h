@@ -217,6 +217,36 @@ int w4a16_gemm_ex(const void *x_f16, const void *alpha_f16, const void *repacked
                   int64_t N, int64_t K, int32_t group, void *stream);
 
 /*
+ * w4a16_quantize_q4_0 -- weights in GGUF Q4_0 blocks.
+ *
+ * Source: tutorial GGUF section (a Q4_0 block: 32 weights in 18 bytes, d as
+ * little-endian fp16, then 16 bytes whose byte i holds element 2i in its low
+ * nibble and 2i + 1 in its high nibble, decoded as (nibble - 8) * d); the
+ * codes are the §2 / §3 symmetric quantizer with groups of 32 (the pages
+ * give the block's decoder, not a separate quantizer), i.e. exactly
+ * w4a16_quantize_ex(group 32, symmetric) laid out block after block.
+ *
+ *   W_f16      [N, K] fp16.  N >= 1; K >= 256, K % 256 == 0 (rows of whole
+ *              16-byte lines for the GEMV's copies).
+ *   blocks_u8  [N, K/32 * 18] bytes, written; block b of row n at byte
+ *              (n * K/32 + b) * 18.
+ * Bit-identical to the library's CPU reference definition.
+ * Errors: NULL -> W4A16_ERR_NULL; bad N, K -> W4A16_ERR_SHAPE; misaligned
+ *         pointer -> W4A16_ERR_ALIGN.
+ */
+int w4a16_quantize_q4_0(const void *W_f16, int64_t N, int64_t K, void *blocks_u8, void *stream);
+
+/*
+ * w4a16_gemm_q4_0 -- decode GEMV on Q4_0 blocks:
+ *   y[m, n] = sum_b d[n, b] * sum_{i<32} x[m, 32 b + i] * (nib[n, 32 b + i] - 8),
+ * exact q * x products, one FP32 rescale per block, y rounded once to fp16.
+ * M = 1..16; K % 256 == 0; x[M, K] held in shared memory whole (as
+ * w4a16_gemm_w8).  Errors: as w4a16_gemm_w8.
+ */
+int w4a16_gemm_q4_0(const void *x_f16, const void *blocks_u8, void *y_f16, int64_t M, int64_t N,
+                    int64_t K, void *stream);
+
+/*
  * w4a16_quantize_w8 -- W8A16 weights: per-channel symmetric INT8.
  *
  * Source: tutorial "量化的数学基石" §2 formula with b = 8 and its INT8

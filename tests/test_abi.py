@@ -106,6 +106,13 @@ def test_gemm_ex_argument_errors(lib):
     assert g(FAKE, MISALIGNED, FAKE, FAKE, None, FAKE, 1, 8, 128, 32, None) == 3
 
 
+def test_q4_0_argument_errors(lib):
+    assert lib.w4a16_quantize_q4_0(None, 8, 256, FAKE, None) == 1
+    assert lib.w4a16_quantize_q4_0(FAKE, 8, 384, FAKE, None) == 2   # K % 256
+    assert lib.w4a16_gemm_q4_0(FAKE, FAKE, FAKE, 17, 8, 256, None) == 2
+    assert lib.w4a16_gemm_q4_0(FAKE, MISALIGNED, FAKE, 1, 8, 256, None) == 3
+
+
 def test_w8_argument_errors(lib):
     assert lib.w4a16_quantize_w8(None, 8, 128, FAKE, FAKE, None) == 1
     assert lib.w4a16_quantize_w8(FAKE, 8, 200, FAKE, FAKE, None) == 2

@@ -1,0 +1,58 @@
+"""GGUF Q4_0 blocks (32 weights in 18 bytes, inline fp16 scale) vs the CPU
+oracle: blocks bit-exact; the GEMV within the GEMV bar (q * x products exact,
+one FP32 rescale per block, FP32 sums, y rounded once)."""
+from __future__ import annotations
+
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import assert_close, from_bits16, u8
+from parity_data import acts, quantized, sample_rows
+import w4a16_weight_only_gemm_gb300 as w4
+from w4a16_weight_only_gemm_gb300 import synthetic, workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@functools.lru_cache(maxsize=16)
+def blocks_of(N: int, K: int, seed: int):
+    w16 = quantized(N, K, seed)[0]
+    return w16, oracle.quantize_q4_0(w16)
+
+
+@pytest.mark.parametrize("N,K", [(1, 256), (130, 512), (1000, 2048), (4096, 14336)])
+def test_quantizer_bit_exact(w4lib, N, K):
+    w16, ref = blocks_of(N, K, 600 + N)
+    w16 = w16.copy()
+    w16[0, :64] = 0  # two all-zero blocks
+    ref = oracle.quantize_q4_0(w16)
+    got = w4.quantize_q4_0(from_bits16(w16))
+    torch.cuda.synchronize()
+    assert np.array_equal(got.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("N,K", [(1000, 2048), (4136, 1280), (300, 4096), (37, 256)])
+@pytest.mark.parametrize("M", [1, 5, 16])
+def test_gemv_every_row(w4lib, M, N, K):
+    _, blocks = blocks_of(N, K, 610 + K)
+    x16 = acts(M, K, 611 + M)
+    y = w4.gemm_q4_0(from_bits16(x16), u8(blocks))
+    torch.cuda.synchronize()
+    assert_close(y.float().cpu().numpy(), oracle.gemm_q4_0(x16, blocks), f"q4_0 M={M} N={N} K={K}")
+    assert w4.device_status() == 0
+
+
+@pytest.mark.parametrize("idx", range(len(workloads.LLAMA3_8B)))
+def test_llama3_8b_shapes_m1(w4lib, idx):
+    lin = workloads.LLAMA3_8B[idx]
+    sw, sx = synthetic.seeds("llama3_8b_decode", idx)
+    _, blocks = blocks_of(lin.N, lin.K, sw)
+    x16 = acts(1, lin.K, sx)
+    y = w4.gemm_q4_0(from_bits16(x16), u8(blocks))
+    torch.cuda.synchronize()
+    rows = sample_rows(lin.N, 256, sw)
+    assert_close(y[:, rows].float().cpu().numpy(), oracle.gemm_q4_0(x16, blocks, rows), lin.name)

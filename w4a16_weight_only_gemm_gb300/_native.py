@@ -32,6 +32,8 @@ SIGNATURES = {
     "w4a16_repack": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),
     "w4a16_unrepack": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),
     "w4a16_gemm": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "w4a16_quantize_q4_0": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),
+    "w4a16_gemm_q4_0": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _I64, _P]),
     "w4a16_quantize_w8": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P]),
     "w4a16_gemm_w8": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "w4a16_gemm_ex": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _P]),

@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(HERE, "libw4a16.so")
 STAMP = os.path.join(BUILD_DIR, "libw4a16.stamp")
 
 SOURCES = ("api.cu", "quantize.cu", "repack.cu", "gemv.cu", "gemv_fmt.cu", "gemv_w8.cu",
-           "gemm_tc.cu")
+           "gemv_q40.cu", "gemm_tc.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-Xcompiler", "-Wall", "--expt-relaxed-constexpr", "-I", INCLUDE]

@@ -207,6 +207,29 @@ int w4a16_gemm_ex(const void* x_f16, const void* alpha_f16, const void* repacked
                                      (int)M, N, K, group, static_cast<cudaStream_t>(stream), ctx));
 }
 
+int w4a16_quantize_q4_0(const void* W_f16, int64_t N, int64_t K, void* blocks_u8, void* stream) {
+    if (!W_f16 || !blocks_u8) return W4A16_ERR_NULL;
+    if (!good_nk(N, K) || K % 256 != 0) return W4A16_ERR_SHAPE;
+    if (!aligned16(W_f16) || !aligned16(blocks_u8)) return W4A16_ERR_ALIGN;
+    DeviceCtx ctx;
+    if (int rc = device_ctx(&ctx)) return rc;
+    return from_cuda(
+        launch_quantize_q4_0(W_f16, N, K, blocks_u8, static_cast<cudaStream_t>(stream), ctx));
+}
+
+int w4a16_gemm_q4_0(const void* x_f16, const void* blocks_u8, void* y_f16, int64_t M, int64_t N,
+                    int64_t K, void* stream) {
+    if (!x_f16 || !blocks_u8 || !y_f16) return W4A16_ERR_NULL;
+    if (M < 1 || M > 16 || !good_nk(N, K) || K % 256 != 0 || N > (int64_t)1 << 28 ||
+        K > (int64_t)1 << 15)
+        return W4A16_ERR_SHAPE;
+    if (!aligned16(x_f16) || !aligned16(blocks_u8) || !aligned16(y_f16)) return W4A16_ERR_ALIGN;
+    DeviceCtx ctx;
+    if (int rc = device_ctx(&ctx)) return rc;
+    return from_cuda(launch_gemv_q4_0(x_f16, blocks_u8, y_f16, (int)M, N, K,
+                                      static_cast<cudaStream_t>(stream), ctx));
+}
+
 int w4a16_quantize_w8(const void* W_f16, int64_t N, int64_t K, void* codes_u8, void* scales_f16,
                       void* stream) {
     if (!W_f16 || !codes_u8 || !scales_f16) return W4A16_ERR_NULL;

@@ -31,6 +31,11 @@ cudaError_t launch_quantize(const void* W, int64_t N, int64_t K, void* qweight, 
 cudaError_t launch_quantize_fmt(const void* W, int64_t N, int64_t K, int group, bool asym,
                                 void* qweight, void* scales, void* zeros, cudaStream_t stream,
                                 const DeviceCtx& ctx);
+// GGUF Q4_0 blocks (group-32 symmetric codes, 18 bytes per 32 weights) and the GEMV.
+cudaError_t launch_quantize_q4_0(const void* W, int64_t N, int64_t K, void* blocks,
+                                 cudaStream_t stream, const DeviceCtx& ctx);
+cudaError_t launch_gemv_q4_0(const void* x, const void* blocks, void* y, int M, int64_t N,
+                             int64_t K, cudaStream_t stream, const DeviceCtx& ctx);
 // W8A16: per-channel symmetric INT8 codes (q + 128, [N, K] bytes) and the GEMV.
 cudaError_t launch_quantize_w8(const void* W, int64_t N, int64_t K, void* q8, void* scales,
                                cudaStream_t stream, const DeviceCtx& ctx);

@@ -158,7 +158,11 @@ __global__ void __launch_bounds__(kQuantThreads)
 // ---------------------------------------------------------------------------
 constexpr int kFmtThreads = 256;
 
-template <bool ASYM>
+// Q40: the GGUF Q4_0 block layout (tutorial GGUF section) instead of
+// separate codes and scales -- group 32, symmetric; group g's block is the 18
+// bytes at g * 18: the fp16 scale, then the 16 code bytes (lane tl's 4 bytes
+// at offset 2 + 4 tl, stored as two 16-bit halves: blocks are 2-byte aligned).
+template <bool ASYM, bool Q40>
 __global__ void __launch_bounds__(kFmtThreads)
     quantize_fmt_kernel(const uint4* __restrict__ W, int64_t groups_total, int group, int L,
                         uint32_t* __restrict__ qweight, __half* __restrict__ scales,
@@ -216,10 +220,21 @@ __global__ void __launch_bounds__(kFmtThreads)
                 const uint32_t nb = (uint32_t)(int)(ASYM ? qb : qb + 8.0f);
                 word |= (na | (nb << 4)) << (8 * i);
             }
-            qweight[grp * (group / 8) + p * L + tl] = word;
+            if (Q40) {
+                uint16_t* b = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(qweight) +
+                                                          grp * 18 + 2 + 4 * tl);
+                b[0] = (uint16_t)(word & 0xffffu);
+                b[1] = (uint16_t)(word >> 16);
+            } else {
+                qweight[grp * (group / 8) + p * L + tl] = word;
+            }
         }
         if (live && tl == 0) {
-            scales[grp] = __float2half_rn(s);
+            if (Q40)
+                *reinterpret_cast<__half*>(reinterpret_cast<uint8_t*>(qweight) + grp * 18) =
+                    __float2half_rn(s);
+            else
+                scales[grp] = __float2half_rn(s);
             if (ASYM) zeros[grp] = (uint8_t)(int)z;
         }
     }
@@ -308,6 +323,21 @@ cudaError_t launch_quantize(const void* W, int64_t N, int64_t K, void* qweight, 
 
 namespace w4a16 {
 
+cudaError_t launch_quantize_q4_0(const void* W, int64_t N, int64_t K, void* blocks_out,
+                                 cudaStream_t stream, const DeviceCtx& ctx) {
+    const int L = 4;  // group 32: 8 weights per lane
+    const int64_t groups = N * (K / 32);
+    const int64_t per_block = kFmtThreads / L;
+    int64_t blocks = (groups + per_block - 1) / per_block;
+    const int64_t cap = (int64_t)ctx.num_sms * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    quantize_fmt_kernel<false, true><<<(unsigned)blocks, kFmtThreads, 0, stream>>>(
+        static_cast<const uint4*>(W), groups, 32, L, static_cast<uint32_t*>(blocks_out), nullptr,
+        nullptr);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_quantize_w8(const void* W, int64_t N, int64_t K, void* q8, void* scales,
                                cudaStream_t stream, const DeviceCtx& ctx) {
     int64_t blocks = (N + kFmtThreads / 32 - 1) / (kFmtThreads / 32);
@@ -334,11 +364,11 @@ cudaError_t launch_quantize_fmt(const void* W, int64_t N, int64_t K, int group, 
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     if (asym)
-        quantize_fmt_kernel<true><<<(unsigned)blocks, kFmtThreads, 0, stream>>>(
+        quantize_fmt_kernel<true, false><<<(unsigned)blocks, kFmtThreads, 0, stream>>>(
             static_cast<const uint4*>(W), groups, group, L, static_cast<uint32_t*>(qweight),
             static_cast<__half*>(scales), static_cast<uint8_t*>(zeros));
     else
-        quantize_fmt_kernel<false><<<(unsigned)blocks, kFmtThreads, 0, stream>>>(
+        quantize_fmt_kernel<false, false><<<(unsigned)blocks, kFmtThreads, 0, stream>>>(
             static_cast<const uint4*>(W), groups, group, L, static_cast<uint32_t*>(qweight),
             static_cast<__half*>(scales), nullptr);
     return cudaGetLastError();

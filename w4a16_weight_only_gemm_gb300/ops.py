@@ -174,6 +174,33 @@ def gemm_ex(x: torch.Tensor, repacked: torch.Tensor, scales: torch.Tensor,
     return out
 
 
+def quantize_q4_0(W: torch.Tensor, stream=None) -> torch.Tensor:
+    """W fp16 [N, K] -> GGUF Q4_0 blocks uint8 [N, K/32 * 18] (K % 256 == 0)."""
+    _need(W, torch.float16, "W")
+    N, K = W.shape
+    blocks = torch.empty((N, K // 32 * 18), dtype=torch.uint8, device=W.device)
+    _native.check(_native.lib().w4a16_quantize_q4_0(W.data_ptr(), N, K, blocks.data_ptr(),
+                                                    _stream_ptr(stream)), "w4a16_quantize_q4_0")
+    return blocks
+
+
+def gemm_q4_0(x: torch.Tensor, blocks: torch.Tensor, out: torch.Tensor | None = None,
+              stream=None) -> torch.Tensor:
+    """y[M, N] = x[M, K] @ decode(blocks)^T for GGUF Q4_0 blocks [N, K/32 * 18], M <= 16."""
+    _need(x, torch.float16, "x")
+    _need(blocks, torch.uint8, "blocks")
+    N = blocks.shape[0]
+    K = x.shape[-1]
+    if x.dim() != 2 or blocks.shape[1] != K // 32 * 18:
+        raise ValueError(f"x must be [M, K] and blocks [N, K/32*18]")
+    M = x.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    _native.check(_native.lib().w4a16_gemm_q4_0(x.data_ptr(), blocks.data_ptr(), out.data_ptr(),
+                                                M, N, K, _stream_ptr(stream)), "w4a16_gemm_q4_0")
+    return out
+
+
 def quantize_w8(W: torch.Tensor, stream=None):
     """W8A16: W fp16 [N, K] -> (codes uint8 [N, K] holding q + 128, scales fp16 [N])."""
     _need(W, torch.float16, "W")
