@@ -55,7 +55,8 @@ def parse_args():
                    help="headline step only (no per-shape, stack, sweep, quantizer sections)")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="budget of the CPU oracle baseline sample")
-    p.add_argument("--section", choices=("prefill", "quantizer", "stack", "per_shape", "formats"),
+    p.add_argument("--section", choices=("prefill", "quantizer", "stack", "per_shape", "formats",
+                                         "formats_prefill"),
                    default=None,
                    help="run one section alone and print its JSON (profiling aid; not the "
                         "benchmark line)")
@@ -451,6 +452,7 @@ def extras(layers):
     out["quantizer"] = quantizer_throughput()
     out["prefill_m512"] = prefill()
     out["formats_m1"] = formats_m1()
+    out["formats_prefill_m512"] = formats_prefill()
     return out
 
 
@@ -476,6 +478,42 @@ def prefill():
                          "cublas_fp16_us": round(tc * 1e6, 2),
                          "cublas_fp16_tflops": round(flops / tc / 1e12, 1)}
         del layer, wd, g, gc
+    return out
+
+
+def formats_prefill():
+    """M = 512 prompt pass on the two prefill shapes for format variants of
+    w4a16_gemm_ex (tcgen05 path with the variants' dequantisers): group-32
+    asymmetric, per-channel symmetric, and group-128 symmetric codes with an
+    AWQ activation scale."""
+    import w4a16_weight_only_gemm_gb300 as w4
+    out = {}
+    peaks = load_peaks()
+    M = workloads.PREFILL_M
+    stream = torch.cuda.Stream()
+    for name, group, asym, awq in (("g32_asym", 32, True, False),
+                                   ("per_channel_sym", w4.PER_CHANNEL, False, False),
+                                   ("g128_sym_awq", 128, False, True)):
+        res = {}
+        for i, lin in enumerate(workloads.PREFILL):
+            sw, sx = synthetic.seeds("prefill", i)
+            W = synthetic.master_weight(lin.N, lin.K, sw, device="cuda")
+            q, sc, z = w4.quantize_ex(W, group, asymmetric=asym)
+            r = w4.repack(q)
+            del W, q
+            x = synthetic.activations(M, lin.K, sx, device="cuda")
+            alpha = (torch.rand(lin.K, device="cuda") * 1.5 + 0.5).half() if awq else None
+            y = torch.empty((M, lin.N), dtype=torch.float16, device="cuda")
+            g = capture(lambda: w4.gemm_ex(x, r, sc, z, group, out=y, alpha=alpha), stream)
+            t = time_graph(g, stream, 20, 3)
+            tf = 2.0 * M * lin.N * lin.K / t / 1e12
+            plan = w4.gemm_ex_plan(M, lin.N, lin.K, group, asym, awq)
+            res[lin.name] = {"us": round(t * 1e6, 2), "tflops": round(tf, 1),
+                             "frac_of_measured_bf16_peak": round(tf / peaks.get("bf16_tflops", 1900.0), 3),
+                             "cluster": plan["splits"], "ctas": plan["ctas"]}
+            del g, r, sc, z, x, y
+        out[name] = res
+        torch.cuda.empty_cache()
     return out
 
 
@@ -645,7 +683,7 @@ def main():
         from w4a16_weight_only_gemm_gb300 import build
         build.build()
         run = {"prefill": prefill, "quantizer": quantizer_throughput, "stack": stack_8b,
-               "formats": formats_m1,
+               "formats": formats_m1, "formats_prefill": formats_prefill,
                "per_shape": lambda: {lin.name: per_shape_us(lin, "llama3_8b_decode", i)
                                      for i, lin in enumerate(workloads.LLAMA3_8B)}}
         print(json.dumps({"section": args.section, "result": run[args.section]()}), flush=True)

@@ -201,16 +201,20 @@ int w4a16_gemm(const void *x_f16, const void *repacked, const void *scales_f16, 
  *              not depend on the format).
  *   scales_f16 [N, K/g] fp16; zeros_u8 [N, K/g] bytes or NULL.
  *   group      32, 64, 128 or W4A16_GROUP_PER_CHANNEL (g = K).
- *   M          1..16 (decode GEMV).  The activations x[M, K] are held in
- *              shared memory whole beside the weight ring: about
- *              2 * M * K <= 200 KB (M = 1: any K up to 32768; M = 16: K up to
- *              6144); a shape that does not fit -> W4A16_ERR_SHAPE.
+ *   M          1 .. 2^22.  M <= 16 runs the variant decode GEMV while
+ *              x[M, K] fits in its shared memory beside the weight ring
+ *              (about 2 * M * K <= 200 KB: M = 1 any K up to 32768, M = 16
+ *              K up to 6144); larger M, or a shape that does not fit, runs
+ *              the tcgen05 tensor-core GEMM of w4a16_gemm with the variant's
+ *              dequantisers.  There alpha multiplies the fp16 dequantised
+ *              weight instead of x: y[m, n] = sum_k x[m, k] *
+ *              fp16(fp16((nib - z) * scale) * alpha[k]), the same product
+ *              with its rounding on the weight operand.
  * Group 128 with symmetric codes and no alpha runs w4a16_gemm's kernels
  * (exact q * x products, one FP32 rescale per group).  The other calls dequantise
  * (nib - z) * scale once to fp16 per weight (the tutorial's own fp16
  * dequantised weight) and accumulate in FP32; the accuracy bar is the same.
- * Errors: as w4a16_gemm; a group other than the above, or M > 16 for a
- * format other than group 128 symmetric or with alpha -> W4A16_ERR_SHAPE.
+ * Errors: as w4a16_gemm; a group other than the above -> W4A16_ERR_SHAPE.
  */
 int w4a16_gemm_ex(const void *x_f16, const void *alpha_f16, const void *repacked,
                   const void *scales_f16, const void *zeros_u8, void *y_f16, int64_t M,
@@ -306,6 +310,27 @@ enum { W4A16_PATH_GEMV = 1, W4A16_PATH_TENSOR_CORE = 2 };
  */
 int w4a16_gemm_plan(int64_t M, int64_t N, int64_t K, int *path, int *splits, int *ctas,
                     int *blocks_per_cta, int *rows_per_cta);
+
+/*
+ * w4a16_gemm_ex_plan -- the launch w4a16_gemm_ex makes for (M, N, K) with
+ * the given group (32, 64, 128 or W4A16_GROUP_PER_CHANNEL), zero points
+ * (nonzero: asymmetric codes) and AWQ scale (nonzero: alpha given), without
+ * launching anything.
+ *
+ *   *path         W4A16_PATH_GEMV (M <= 16 with x[M, K] fitting in the
+ *                 variant GEMV's shared memory) or W4A16_PATH_TENSOR_CORE.
+ *   *splits       as w4a16_gemm_plan (1 for the variant GEMV).
+ *   *ctas         CTAs launched.
+ *   *rows_per_cta weight rows per CTA: 16, 32 or 64 for the variant GEMV,
+ *                 128 for the tensor-core GEMM.
+ * Group 128 with symmetric codes and no alpha reports w4a16_gemm_plan's
+ * launch (the call runs w4a16_gemm).
+ * Errors: NULL output -> W4A16_ERR_NULL; bad M, N, K or group ->
+ *         W4A16_ERR_SHAPE; no supported device -> W4A16_ERR_DEVICE /
+ *         W4A16_ERR_CUDA.
+ */
+int w4a16_gemm_ex_plan(int64_t M, int64_t N, int64_t K, int32_t group, int32_t zero_points,
+                       int32_t alpha, int *path, int *splits, int *ctas, int *rows_per_cta);
 
 /*
  * w4a16_device_status -- synchronises the current device, returns in

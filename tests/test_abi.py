@@ -100,10 +100,21 @@ def test_gemm_ex_argument_errors(lib):
     g = lib.w4a16_gemm_ex
     assert g(FAKE, None, FAKE, None, None, FAKE, 1, 8, 128, 32, None) == 1
     assert g(FAKE, None, FAKE, FAKE, None, FAKE, 1, 8, 128, 16, None) == 2     # group 16
-    assert g(FAKE, None, FAKE, FAKE, FAKE, FAKE, 17, 8, 128, 32, None) == 2    # variants: M <= 16
-    assert g(FAKE, FAKE, FAKE, FAKE, None, FAKE, 17, 8, 128, 128, None) == 2   # alpha: M <= 16
+    assert g(FAKE, None, FAKE, FAKE, FAKE, FAKE, 0, 8, 128, 32, None) == 2     # M >= 1
+    assert g(FAKE, FAKE, FAKE, FAKE, None, FAKE, (1 << 22) + 1, 8, 128, 128, None) == 2
+    assert g(FAKE, None, FAKE, FAKE, None, FAKE, 1, 8, 192, 128, None) == 2    # K % 128
     assert g(FAKE, None, FAKE, FAKE, MISALIGNED, FAKE, 1, 8, 128, 32, None) == 3
     assert g(FAKE, MISALIGNED, FAKE, FAKE, None, FAKE, 1, 8, 128, 32, None) == 3
+
+
+def test_gemm_ex_plan_argument_errors(lib):
+    p = lib.w4a16_gemm_ex_plan
+    out = [ctypes.c_int(0) for _ in range(4)]
+    refs = [ctypes.byref(o) for o in out]
+    assert p(17, 8, 128, 32, 1, 0, None, *refs[1:]) == 1
+    assert p(0, 8, 128, 32, 1, 0, *refs) == 2
+    assert p(17, 8, 128, 48, 0, 0, *refs) == 2                                 # group 48
+    assert p(17, 8, 130, 32, 0, 1, *refs) == 2
 
 
 def test_q4_0_argument_errors(lib):

@@ -77,12 +77,70 @@ def test_group128_symmetric_is_the_default_gemm(w4lib):
     assert torch.equal(w4.gemm_ex(x, r, st, None, 128), w4.gemm(x, r, st))
 
 
-def test_shape_that_does_not_fit_is_rejected(w4lib):
-    q, s, z = quantized_fmt(256, 14336, 312, 32, True)
-    x = from_bits16(acts(16, 14336, 313))
-    with pytest.raises(w4.ops._native.W4A16Error, match="SHAPE"):
-        w4.gemm_ex(x, w4.repack(u8(q)), from_bits16(s), u8(z), 32)
+def test_shape_beyond_the_gemv_runs_on_tensor_cores(w4lib):
+    """M = 16 with K = 14336: x[16, K] does not fit beside the GEMV's ring, so
+    the call takes the tensor-core GEMM; every output compared."""
+    N, K, M = 256, 14336, 16
+    assert w4.gemm_ex_plan(M, N, K, 32, True)["path"] == "tensor_core"
+    q, s, z = quantized_fmt(N, K, 312, 32, True)
+    x16 = acts(M, K, 313)
+    assert_close(run_fmt(x16, q, s, z, 32), oracle.gemm(x16, q, s, 32, zeros=z), "M=16 K=14336")
     assert w4.device_status() == 0
+
+
+# --------------------------------------------------------------------------
+# Prefill (M > 16): the tcgen05 GEMM with the variants' dequantisers
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("group,asym", FORMATS)
+@pytest.mark.parametrize("M,N,K", [(20, 1000, 1152), (200, 4136, 384), (300, 2000, 2048)])
+def test_formats_prefill_every_output(w4lib, M, N, K, group, asym):
+    assert w4.gemm_ex_plan(M, N, K, group, asym)["path"] == "tensor_core"
+    q, s, z = quantized_fmt(N, K, 500 + M, group, asym)
+    x16 = acts(M, K, 501 + M)
+    assert_close(run_fmt(x16, q, s, z, group), oracle.gemm(x16, q, s, group, zeros=z),
+                 f"prefill M={M} N={N} K={K} g={group} asym={asym}")
+    assert w4.device_status() == 0
+
+
+@pytest.mark.parametrize("group,asym", [(32, True), (w4.PER_CHANNEL, False), (64, False)])
+def test_formats_prefill_launch_shapes(w4lib, group, asym):
+    """One CTA per 128 x 128 tile, CTA pairs (2-CTA MMAs, an odd last block),
+    and pairs splitting K through the cluster, with ragged M: every output
+    compared, and two calls of a split launch give the same bits."""
+    seen = set()
+    for M, N, K in [(20, 1000, 1152), (200, 19300, 256), (300, 19000, 384), (300, 8000, 1920),
+                    (300, 4000, 16384), (300, 1000, 18944)]:
+        plan = w4.gemm_ex_plan(M, N, K, group, asym)
+        assert plan["path"] == "tensor_core", plan
+        seen.add(plan["splits"])
+        q, s, z = quantized_fmt(N, K, 600, group, asym)
+        x16 = acts(M, K, 601)
+        r = w4.repack(u8(q))
+        st, zt = from_bits16(s), (u8(z) if z is not None else None)
+        x = from_bits16(x16)
+        y1 = w4.gemm_ex(x, r, st, zt, group)
+        y2 = w4.gemm_ex(x, r, st, zt, group)
+        torch.cuda.synchronize()
+        assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+        assert_close(y1.float().cpu().numpy().astype(np.float64),
+                     oracle.gemm(x16, q, s, group, zeros=z), f"M={M} N={N} K={K} {plan}")
+        del r, st, zt, x, y1, y2
+    assert {1, 2} <= seen and seen & {4, 6, 8}, seen
+    assert w4.device_status() == 0
+
+
+@pytest.mark.parametrize("idx", range(len(workloads.PREFILL)))
+def test_formats_prefill_full_size(w4lib, idx):
+    """M = 512 prompt pass on the prefill shapes with group-32 asymmetric
+    codes; oracle on sampled rows."""
+    lin = workloads.PREFILL[idx]
+    sw, sx = synthetic.seeds("prefill", idx)
+    q, s, z = quantized_fmt(lin.N, lin.K, sw, 32, True)
+    x16 = acts(workloads.PREFILL_M, lin.K, sx)
+    y = run_fmt(x16, q, s, z, 32)
+    rows = sample_rows(lin.N, 96, sw)
+    assert_close(y[:, rows], oracle.gemm_rows(x16, q, s, rows, 32, zeros=z), lin.name)
 
 
 # --------------------------------------------------------------------------
@@ -104,8 +162,10 @@ def _awq_case(N, K, seed, group, asym):
 
 
 @pytest.mark.parametrize("group,asym", [(128, False), (128, True), (32, True), (w4.PER_CHANNEL, False)])
-@pytest.mark.parametrize("M", [1, 7, 16])
+@pytest.mark.parametrize("M", [1, 7, 16, 40, 200, 300])
 def test_awq_activation_scale(w4lib, M, group, asym):
+    """Decode (M <= 16) and prefill: one CTA per tile (40), CTA pairs (200),
+    pairs with two x tiles splitting K (300)."""
     N, K = 1000, 2048
     alpha16, q, s, z = _awq_case(N, K, 400, group, asym)
     x16 = acts(M, K, 401 + M)

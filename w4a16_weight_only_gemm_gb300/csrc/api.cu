@@ -200,11 +200,15 @@ int w4a16_gemm_ex(const void* x_f16, const void* alpha_f16, const void* repacked
         return W4A16_ERR_ALIGN;
     if (group == W4A16_GROUP && !zeros_u8 && !alpha_f16)
         return w4a16_gemm(x_f16, repacked, scales_f16, y_f16, M, N, K, stream);
-    if (M > 16) return W4A16_ERR_SHAPE;
     DeviceCtx ctx;
     if (int rc = device_ctx(&ctx)) return rc;
-    return from_cuda(launch_gemv_fmt(x_f16, alpha_f16, repacked, scales_f16, zeros_u8, y_f16,
-                                     (int)M, N, K, group, static_cast<cudaStream_t>(stream), ctx));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // Decode GEMV while x fits in its shared memory, else the tensor cores.
+    if (M <= 16 && gemv_fmt_fits((int)M, N, K, group, zeros_u8 != nullptr, ctx))
+        return from_cuda(launch_gemv_fmt(x_f16, alpha_f16, repacked, scales_f16, zeros_u8, y_f16,
+                                         (int)M, N, K, group, s, ctx));
+    return from_cuda(launch_gemm_tc_fmt(x_f16, alpha_f16, repacked, scales_f16, zeros_u8, y_f16, M,
+                                        N, K, group, s, ctx));
 }
 
 int w4a16_quantize_q4_0(const void* W_f16, int64_t N, int64_t K, void* blocks_u8, void* stream) {
@@ -274,6 +278,33 @@ int w4a16_gemm_plan(int64_t M, int64_t N, int64_t K, int* path, int* splits, int
             gemv_plan_info((int)M, N, K, ctx, splits, ctas, blocks_per_cta, rows_per_cta)))
         return rc;
     *path = W4A16_PATH_GEMV;
+    return W4A16_OK;
+}
+
+int w4a16_gemm_ex_plan(int64_t M, int64_t N, int64_t K, int32_t group, int32_t zero_points,
+                       int32_t alpha, int* path, int* splits, int* ctas, int* rows_per_cta) {
+    if (!path || !splits || !ctas || !rows_per_cta) return W4A16_ERR_NULL;
+    if (M < 1 || M > (int64_t)1 << 22 || !good_nk(N, K) || N > (int64_t)1 << 28 ||
+        K > (int64_t)1 << 15)
+        return W4A16_ERR_SHAPE;
+    if (group == W4A16_GROUP_PER_CHANNEL) group = (int32_t)K;
+    if (!(group == 32 || group == 64 || group == 128 || group == K)) return W4A16_ERR_SHAPE;
+    if (group == W4A16_GROUP && !zero_points && !alpha) {
+        int blocks_per_cta = 0;
+        return w4a16_gemm_plan(M, N, K, path, splits, ctas, &blocks_per_cta, rows_per_cta);
+    }
+    DeviceCtx ctx;
+    if (int rc = device_ctx(&ctx)) return rc;
+    if (M <= 16 && gemv_fmt_fits((int)M, N, K, group, zero_points != 0, ctx)) {
+        *path = W4A16_PATH_GEMV;
+        *splits = 1;
+        return from_cuda(
+            gemv_fmt_plan_info((int)M, N, K, group, zero_points != 0, ctx, ctas, rows_per_cta));
+    }
+    *path = W4A16_PATH_TENSOR_CORE;
+    gemm_tc_plan_info(M, N, K, ctx, splits, ctas, true);
+    if (*splits == 0) return W4A16_ERR_CUDA;
+    *rows_per_cta = 128;
     return W4A16_OK;
 }
 

@@ -87,6 +87,14 @@ struct TcArgs {
     // rounded down to 8 (a split's own groups only); else the whole
     // [128][G] slab by bulk copy (slab_ld = G).
     int slab_ld, slab_tma;
+    // Format variants (FMT kernels; G = 0, no slab): the scale of weight row
+    // n for k is scales[n * gcount + (k >> gshift)] (gshift 5, 6, 7 for
+    // groups of 32, 64, 128; 31 per channel), its zero point
+    // zeros[n * gcount + (k >> gshift)] (NULL: symmetric, z = 8), and an
+    // optional AWQ activation scale alpha[k] (NULL: none).
+    const uint8_t* zeros;
+    const __half* alpha;
+    int gshift, gcount;
 };
 
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -99,6 +107,65 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, __half2 s) {
     __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&a), s);
     return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// The format coefficients one dequantising thread needs for one k-block:
+// the scales and zero points of its rows r0 / r0 + 8 for its 16 k (one group
+// at every group size) and alpha at those 16 k.
+struct FmtCoef {
+    __half s0, s1;
+    int z0, z1;
+    uint4 al0, al1;
+};
+
+__device__ __forceinline__ FmtCoef fmt_coef(const TcArgs& a, int kblock, int n0, int tq) {
+    FmtCoef c;
+    c.s0 = c.s1 = __ushort_as_half(0);
+    c.z0 = c.z1 = 8;
+    c.al0 = c.al1 = make_uint4(0u, 0u, 0u, 0u);
+    const int kk = kblock * kBK;
+    const int gi = (kk + 16 * tq) >> a.gshift;
+    const int n1 = n0 + 8;
+    if (n0 < a.N) {
+        c.s0 = __ldg(a.scales + (size_t)n0 * a.gcount + gi);
+        if (a.zeros) c.z0 = __ldg(a.zeros + (size_t)n0 * a.gcount + gi);
+    }
+    if (n1 < a.N) {
+        c.s1 = __ldg(a.scales + (size_t)n1 * a.gcount + gi);
+        if (a.zeros) c.z1 = __ldg(a.zeros + (size_t)n1 * a.gcount + gi);
+    }
+    if (a.alpha) {
+        const uint4* p = reinterpret_cast<const uint4*>(a.alpha + kk + 16 * tq);
+        c.al0 = __ldg(p);
+        c.al1 = __ldg(p + 1);
+    }
+    return c;
+}
+
+// (nib - z) for the 8 nibbles of a kernel-layout word, exactly: the low
+// nibbles (rows r0, zero point z0) OR-ed into the mantissa of 1024.0 minus
+// (1024 + z0); the high nibbles (rows r1, z1) give 1024 + 16 nib, times 1/16
+// minus (64 + z1).  r[0] / r[2]: rows r0, r[1] / r[3]: rows r1, as dequant8
+// (which is this with z = 8).
+__device__ __forceinline__ void dequant8_z(uint32_t w, __half2 lo_off, __half2 hi_off,
+                                           uint32_t (&r)[4]) {
+    constexpr uint32_t kMagic = 0x64006400u;  // (1024.0, 1024.0)
+    constexpr uint32_t kLut = (0xF0 & 0xCC) | 0xAA;  // (a & b) | c
+    const uint32_t lo0 = lop3<kLut>(w, 0x000F000Fu, kMagic);
+    const uint32_t hi0 = lop3<kLut>(w, 0x00F000F0u, kMagic);
+    const uint32_t w8 = w >> 8;
+    const uint32_t lo1 = lop3<kLut>(w8, 0x000F000Fu, kMagic);
+    const uint32_t hi1 = lop3<kLut>(w8, 0x00F000F0u, kMagic);
+    const __half2 kSixteenth = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));
+    __half2 v;
+    v = __hsub2(*reinterpret_cast<const __half2*>(&lo0), lo_off);
+    r[0] = *reinterpret_cast<uint32_t*>(&v);
+    v = __hfma2(*reinterpret_cast<const __half2*>(&hi0), kSixteenth, hi_off);
+    r[1] = *reinterpret_cast<uint32_t*>(&v);
+    v = __hsub2(*reinterpret_cast<const __half2*>(&lo1), lo_off);
+    r[2] = *reinterpret_cast<uint32_t*>(&v);
+    v = __hfma2(*reinterpret_cast<const __half2*>(&hi1), kSixteenth, hi_off);
+    r[3] = *reinterpret_cast<uint32_t*>(&v);
 }
 
 // Rounds 32 FP32 accumulators to fp16 and stores them at y[m, n .. n + 31]
@@ -139,7 +206,16 @@ __device__ __forceinline__ uint32_t swz128(int r, int c) {
 // (MMA t in columns 256 t ..).  Each SM reads (16 XT + 16) KB of operands per
 // 64-wide k-block for 2 XT times the FLOPs of the single-CTA tile, and every
 // stage hand-off covers XT times more MMA work.
-template <bool PAIR, int XT>
+// FMT = true: the format variants.  The dequantisers read each k-block's
+// group scales and zero points from global memory (one k-block of their set
+// ahead) and form fp16((nib - z) * s) from the exact difference nib - z.
+// With an AWQ scale they multiply it into the weight tile as well,
+// fp16(fp16((nib - z) * s) * alpha[k]): the product x * alpha * Wd with its
+// rounding on the weight operand.  Scaling this CTA's x tiles in shared memory
+// instead (the decode kernel's placement) re-scaled every x tile once per
+// weight-block column and added half again to the shared-memory traffic of a
+// k-block: 30 % slower at M = 512.
+template <bool PAIR, int XT, bool FMT = false>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap smap,
                    const __grid_constant__ TcArgs a) {
@@ -337,7 +413,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // stage ts = i % NS and its pass parity, advanced by two k-blocks a step
         int ts = set % NS;
         uint32_t tph = (uint32_t)((set / NS) & 1);
+        // FMT: coefficients of this set's k-blocks, loaded one k-block of the
+        // set ahead (the dequantisers are rarely kept waiting on a stage, so a
+        // load issued just before the wait would stall them)
+        [[maybe_unused]] FmtCoef cf;
+        if constexpr (FMT) {
+            if (set < nkb) cf = fmt_coef(a, kb0 + set, rb * kTileW + r0, tq);
+        }
         for (int i = set; ok && i < nkb; i += 2) {
+            [[maybe_unused]] FmtCoef nx;
+            if constexpr (FMT) {
+                if (i + 2 < nkb) nx = fmt_coef(a, kb0 + i + 2, rb * kTileW + r0, tq);
+            }
             // The stage's copies were issued after its previous MMAs finished,
             // so their arrival also means the dequantised slot is free.
             if (!mbar_wait(base + kBarLoadFull + 8 * ts, tph, a.timeout_ns, a.status)) {
@@ -345,22 +432,48 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 break;
             }
             if (wvalid) {
-                const int grp = (kb0 + i) >> 1;  // two 64-wide k-blocks per scale group
                 const uint32_t wst = base + kOffW + ts * kWStageBytes;
                 const uint32_t ast = base + kOffA + ts * kAStageBytes;
                 const uint4 pk = lds128(wst + (dw * 32 + lane) * 16);
-                const __half2 s0 = __half2half2(slab[r0 * a.slab_ld + grp - slab_g0]);
-                const __half2 s1 = __half2half2(slab[r1 * a.slab_ld + grp - slab_g0]);
+                __half2 s0, s1;
+                [[maybe_unused]] __half2 lo_off, hi_off;  // 1024 + z0, -(64 + z1): exact
+                if constexpr (FMT) {
+                    s0 = __half2half2(cf.s0);
+                    s1 = __half2half2(cf.s1);
+                    lo_off = __half2half2(__int2half_rn(1024 + cf.z0));
+                    hi_off = __half2half2(__int2half_rn(-64 - cf.z1));
+                } else {
+                    const int grp = (kb0 + i) >> 1;  // two 64-wide k-blocks per scale group
+                    s0 = __half2half2(slab[r0 * a.slab_ld + grp - slab_g0]);
+                    s1 = __half2half2(slab[r1 * a.slab_ld + grp - slab_g0]);
+                }
                 const uint32_t wrd[4] = {pk.x, pk.y, pk.z, pk.w};
                 uint32_t o0[8], o1[8];  // rows r0 / r1, k = 16 tq .. 16 tq + 15
 #pragma unroll
                 for (int ws = 0; ws < 4; ++ws) {
                     uint32_t af[4];
-                    dequant8(wrd[ws], af);
+                    if constexpr (FMT)
+                        dequant8_z(wrd[ws], lo_off, hi_off, af);
+                    else
+                        dequant8(wrd[ws], af);
                     o0[2 * ws] = hmul2_u32(af[0], s0);
                     o0[2 * ws + 1] = hmul2_u32(af[2], s0);
                     o1[2 * ws] = hmul2_u32(af[1], s1);
                     o1[2 * ws + 1] = hmul2_u32(af[3], s1);
+                }
+                if constexpr (FMT) {
+                    if (a.alpha) {
+                        // AWQ: o[j] holds k = 16 tq + 2 j, + 1 of rows r0 / r1;
+                        // fp16(Wd * alpha), alpha on the weight operand
+                        const uint32_t alw[8] = {cf.al0.x, cf.al0.y, cf.al0.z, cf.al0.w,
+                                                 cf.al1.x, cf.al1.y, cf.al1.z, cf.al1.w};
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const __half2 aj = *reinterpret_cast<const __half2*>(&alw[j]);
+                            o0[j] = hmul2_u32(o0[j], aj);
+                            o1[j] = hmul2_u32(o1[j], aj);
+                        }
+                    }
                 }
                 sts128(ast + swz128(r0, 2 * tq), o0[0], o0[1], o0[2], o0[3]);
                 sts128(ast + swz128(r0, 2 * tq + 1), o0[4], o0[5], o0[6], o0[7]);
@@ -379,6 +492,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             } else {
                 mbar_arrive(base + kBarAFull + 8 * ts);
             }
+            if constexpr (FMT) cf = nx;
             ts += 2;
             if (ts >= NS) {
                 ts -= NS;
@@ -570,13 +684,14 @@ int tc_stages(const TcPlan& p, int ld, const DeviceCtx& ctx) {
 //    co-resident.
 // Cost = waves x k-blocks per CTA x the measured time of one k-block of the
 // tile on a busy GPU (about 0.36, 0.63 and 0.84 us at M = 512), plus about a
-// microsecond per 64-column round of a split reduction.
-TcPlan tc_plan(int64_t M, int64_t N, int64_t K, const DeviceCtx& ctx) {
+// microsecond per 64-column round of a split reduction.  fmt: the format
+// variants' kernels, which hold no scale slab.
+TcPlan tc_plan(int64_t M, int64_t N, int64_t K, const DeviceCtx& ctx, bool fmt = false) {
     constexpr double kSingleKb = 0.36, kPairKb = 0.63, kPair2Kb = 0.84, kRound = 1.0;
     const int NB = (int)((N + kTileW - 1) / kTileW);
     const long long pairs = (NB + 1) / 2;
     const long long nkb = K / kBK;
-    const int G = (int)(K / kGroup);
+    const int G = fmt ? 0 : (int)(K / kGroup);
     auto waves = [&](long long ctas) { return (double)((ctas + ctx.num_sms - 1) / ctx.num_sms); };
 
     TcPlan best;  // single-CTA tiles
@@ -615,14 +730,15 @@ TcPlan tc_plan(int64_t M, int64_t N, int64_t K, const DeviceCtx& ctx) {
             if (ctas > ctx.num_sms || nkb < 8 * S) continue;
             // a split holds only its own groups' scales, leaving room for a
             // deeper ring (3 stages run a k-block about 25 % slower than 4)
-            const int ld = split_slab_ld(nkb, S, G);
+            const int ld = fmt ? 0 : split_slab_ld(nkb, S, G);
             const int nst = tc_stages(p, ld ? ld : G, ctx);
             const uint32_t smem = tc_smem(nst, 2, ld ? ld : G);
             const uint32_t ring = (uint32_t)nst * (kAStageBytes + 2 * kXStageBytes + kWStageBytes);
             // the S receive slots of the reduction live in the ring
             if ((uint32_t)S * kRedSlotFloats * 4 > ring) continue;
-            const long long fit =
-                (long long)max_active_clusters((const void*)gemm_tc_kernel<true, 2>, S, smem);
+            const void* fn = fmt ? (const void*)gemm_tc_kernel<true, 2, true>
+                                 : (const void*)gemm_tc_kernel<true, 2>;
+            const long long fit = (long long)max_active_clusters(fn, S, smem);
             if (fit * 2 * S < ctas) continue;  // not one co-resident wave
             t = (double)((nkb + S - 1) / S) * kPair2Kb * (nst >= 4 ? 1.0 : 1.25) +
                 kRound * ((4 * kTileW / S + 63) / 64 + 1);
@@ -644,7 +760,9 @@ cudaError_t ensure_tc_attrs(const DeviceCtx& ctx) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && attr_done[dev]) return cudaSuccess;
-    for (auto fn : {gemm_tc_kernel<false, 1>, gemm_tc_kernel<true, 1>, gemm_tc_kernel<true, 2>}) {
+    for (auto fn : {gemm_tc_kernel<false, 1>, gemm_tc_kernel<true, 1>, gemm_tc_kernel<true, 2>,
+                    gemm_tc_kernel<false, 1, true>, gemm_tc_kernel<true, 1, true>,
+                    gemm_tc_kernel<true, 2, true>}) {
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              ctx.max_smem_optin);
         if (e != cudaSuccess) return e;
@@ -656,24 +774,28 @@ cudaError_t ensure_tc_attrs(const DeviceCtx& ctx) {
 }  // namespace
 
 void gemm_tc_plan_info(int64_t M, int64_t N, int64_t K, const DeviceCtx& ctx, int* cluster,
-                       int* ctas) {
+                       int* ctas, bool fmt) {
     if (ensure_tc_attrs(ctx) != cudaSuccess) {
         *cluster = 0;
         *ctas = 0;
         return;
     }
-    const TcPlan p = tc_plan(M, N, K, ctx);
+    const TcPlan p = tc_plan(M, N, K, ctx, fmt);
     *cluster = p.cluster;
     *ctas = (int)p.ctas;
 }
 
-cudaError_t launch_gemm_tc(const void* x, const void* repacked, const void* scales, void* y,
-                           int64_t M, int64_t N, int64_t K, cudaStream_t stream,
-                           const DeviceCtx& ctx) {
-    const int G = (int)(K / kGroup);
+namespace {
+
+// Encodes the maps, sizes the ring and launches the plan's kernel; `a`
+// carries the operands (and the format fields when FMT).
+template <bool FMT>
+cudaError_t launch_tc(TcArgs a, const void* x, int64_t M, int64_t N, int64_t K, cudaStream_t stream,
+                      const DeviceCtx& ctx) {
+    const int G = FMT ? 0 : (int)(K / kGroup);
     cudaError_t e = ensure_tc_attrs(ctx);
     if (e != cudaSuccess) return e;
-    const TcPlan plan = tc_plan(M, N, K, ctx);
+    const TcPlan plan = tc_plan(M, N, K, ctx, FMT);
     const int ld = plan.slab_ld ? plan.slab_ld : G;
     const int nst = tc_stages(plan, ld, ctx);
     const uint32_t smem = tc_smem(nst, plan.xt, ld);
@@ -694,29 +816,25 @@ cudaError_t launch_gemm_tc(const void* x, const void* repacked, const void* scal
         const cuuint64_t sdims[2] = {(cuuint64_t)G, (cuuint64_t)N};
         const cuuint64_t sstrides[1] = {(cuuint64_t)G * 2};
         const cuuint32_t sbox[2] = {(cuuint32_t)plan.slab_ld, (cuuint32_t)kTileW};
-        if (encode(&smap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(scales), sdims,
+        if (encode(&smap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(a.scales), sdims,
                    sstrides, sbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
 
-    TcArgs args{};
-    args.wq = static_cast<const uint8_t*>(repacked);
-    args.scales = static_cast<const __half*>(scales);
-    args.y = static_cast<__half*>(y);
-    args.status = ctx.status;
-    args.timeout_ns = ctx.timeout_ns;
-    args.M = (int)M;
-    args.N = (int)N;
-    args.K = (int)K;
-    args.G = G;
-    args.nst = nst;
-    args.off_x = kOffA + (uint32_t)nst * kAStageBytes;
-    args.off_w = args.off_x + (uint32_t)nst * plan.xt * kXStageBytes;
-    args.off_slab = args.off_w + (uint32_t)nst * kWStageBytes;
-    args.splits = plan.splits;
-    args.slab_ld = ld;
-    args.slab_tma = plan.slab_ld ? 1 : 0;
+    a.status = ctx.status;
+    a.timeout_ns = ctx.timeout_ns;
+    a.M = (int)M;
+    a.N = (int)N;
+    a.K = (int)K;
+    a.G = G;
+    a.nst = nst;
+    a.off_x = kOffA + (uint32_t)nst * kAStageBytes;
+    a.off_w = a.off_x + (uint32_t)nst * plan.xt * kXStageBytes;
+    a.off_slab = a.off_w + (uint32_t)nst * kWStageBytes;
+    a.splits = plan.splits;
+    a.slab_ld = ld;
+    a.slab_tma = plan.slab_ld ? 1 : 0;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(plan.gx, plan.gy, (unsigned)plan.splits);
@@ -732,9 +850,36 @@ cudaError_t launch_gemm_tc(const void* x, const void* repacked, const void* scal
     attrs[1].val.clusterDim.z = (unsigned)plan.splits;
     cfg.attrs = attrs;
     cfg.numAttrs = plan.cluster > 1 ? 2 : 1;
-    if (plan.cluster == 1) return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<false, 1>, map, smap, args);
-    if (plan.xt == 1) return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true, 1>, map, smap, args);
-    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true, 2>, map, smap, args);
+    if (plan.cluster == 1) return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<false, 1, FMT>, map, smap, a);
+    if (plan.xt == 1) return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true, 1, FMT>, map, smap, a);
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true, 2, FMT>, map, smap, a);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(const void* x, const void* repacked, const void* scales, void* y,
+                           int64_t M, int64_t N, int64_t K, cudaStream_t stream,
+                           const DeviceCtx& ctx) {
+    TcArgs a{};
+    a.wq = static_cast<const uint8_t*>(repacked);
+    a.scales = static_cast<const __half*>(scales);
+    a.y = static_cast<__half*>(y);
+    return launch_tc<false>(a, x, M, N, K, stream, ctx);
+}
+
+cudaError_t launch_gemm_tc_fmt(const void* x, const void* alpha, const void* repacked,
+                               const void* scales, const void* zeros, void* y, int64_t M, int64_t N,
+                               int64_t K, int group, cudaStream_t stream, const DeviceCtx& ctx) {
+    if (!(group == 32 || group == 64 || group == 128 || group == K)) return cudaErrorInvalidValue;
+    TcArgs a{};
+    a.wq = static_cast<const uint8_t*>(repacked);
+    a.scales = static_cast<const __half*>(scales);
+    a.y = static_cast<__half*>(y);
+    a.zeros = static_cast<const uint8_t*>(zeros);
+    a.alpha = static_cast<const __half*>(alpha);
+    a.gshift = group == K ? 31 : (group == 32 ? 5 : group == 64 ? 6 : 7);
+    a.gcount = (int)(K / group);
+    return launch_tc<true>(a, x, M, N, K, stream, ctx);
 }
 
 }  // namespace w4a16

@@ -505,4 +505,25 @@ cudaError_t launch_gemv_fmt(const void* x, const void* alpha, const void* repack
     return launch_fmt_mt<2>(a, stream, ctx);
 }
 
+cudaError_t gemv_fmt_plan_info(int M, int64_t N, int64_t K, int group, bool zp, const DeviceCtx& ctx,
+                               int* ctas, int* rows_per_cta) {
+    cudaError_t e = M <= 8 ? ensure_fmt_attr<1>() : ensure_fmt_attr<2>();
+    if (e != cudaSuccess) return e;
+    const int Gs = (int)(K / group);
+    const FmtPlan p = M <= 8 ? plan_fmt<1>(M, (int)N, (int)K, Gs, zp, ctx)
+                             : plan_fmt<2>(M, (int)N, (int)K, Gs, zp, ctx);
+    if (p.T == 0) return cudaErrorInvalidValue;
+    *rows_per_cta = 16 * p.T;
+    *ctas = (int)((N + 16 * p.T - 1) / (16 * p.T));
+    return cudaSuccess;
+}
+
+bool gemv_fmt_fits(int M, int64_t N, int64_t K, int group, bool zp, const DeviceCtx& ctx) {
+    FmtPlan p;
+    const int Gs = (int)(K / group);
+    if ((N + 63) / 64 > 65535) return false;
+    return M <= 8 ? fmt_layout<1>(p, M, (int)K, Gs, zp, 1, 3, ctx)
+                  : fmt_layout<2>(p, M, (int)K, Gs, zp, 1, 3, ctx);
+}
+
 }  // namespace w4a16

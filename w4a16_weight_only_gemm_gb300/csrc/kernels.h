@@ -54,6 +54,18 @@ cudaError_t gemv_weight_map(const void* repacked, int64_t N, int64_t K, int T, C
 cudaError_t launch_gemv_fmt(const void* x, const void* alpha, const void* repacked,
                             const void* scales, const void* zeros, void* y, int M, int64_t N,
                             int64_t K, int group, cudaStream_t stream, const DeviceCtx& ctx);
+// Whether the decode GEMV of the format variants has a shared-memory layout
+// for (M, K): x[M, K] and the smallest unit's scales beside a 3-stage ring.
+bool gemv_fmt_fits(int M, int64_t N, int64_t K, int group, bool zp, const DeviceCtx& ctx);
+// The launch the variant GEMV would make: CTAs and weight rows per CTA.
+cudaError_t gemv_fmt_plan_info(int M, int64_t N, int64_t K, int group, bool zp, const DeviceCtx& ctx,
+                               int* ctas, int* rows_per_cta);
+// Tensor-core GEMM of the format variants (any M; same arguments as
+// launch_gemv_fmt): fp16((nib - z) * s) weight tiles, times alpha[k] in the
+// tile when an AWQ scale is given.
+cudaError_t launch_gemm_tc_fmt(const void* x, const void* alpha, const void* repacked,
+                               const void* scales, const void* zeros, void* y, int64_t M, int64_t N,
+                               int64_t K, int group, cudaStream_t stream, const DeviceCtx& ctx);
 cudaError_t launch_gemv(const void* x, const void* repacked, const void* scales, void* y, int M,
                         int64_t N, int64_t K, cudaStream_t stream, const DeviceCtx& ctx);
 // The launch the decode GEMV would make: K split (cluster size), CTAs, the
@@ -63,8 +75,9 @@ cudaError_t gemv_plan_info(int M, int64_t N, int64_t K, const DeviceCtx& ctx, in
 // The launch the tensor-core GEMM would make: cluster size (1: one CTA per
 // 128 x 128 tile; 2: CTA pairs with 2-CTA MMAs; 4, 6 or 8: CTA pairs
 // splitting K two, three or four ways, reduced over the cluster) and CTAs.
+// fmt: the format variants' kernels (no scale slab).
 void gemm_tc_plan_info(int64_t M, int64_t N, int64_t K, const DeviceCtx& ctx, int* cluster,
-                       int* ctas);
+                       int* ctas, bool fmt = false);
 cudaError_t launch_gemm_tc(const void* x, const void* repacked, const void* scales, void* y,
                            int64_t M, int64_t N, int64_t K, cudaStream_t stream,
                            const DeviceCtx& ctx);

@@ -243,6 +243,21 @@ def gemm_plan(M: int, N: int, K: int) -> dict:
             "blocks_per_cta": out[3].value, "rows_per_cta": out[4].value}
 
 
+def gemm_ex_plan(M: int, N: int, K: int, group: int, asymmetric: bool = False,
+                 alpha: bool = False) -> dict:
+    """The launch gemm_ex() makes for (M, N, K) with this group, zero points
+    (asymmetric) and AWQ scale (alpha): {"path": "gemv" | "tensor_core",
+    "splits", "ctas", "rows_per_cta"}."""
+    out = [ctypes.c_int(0) for _ in range(4)]
+    _native.check(_native.lib().w4a16_gemm_ex_plan(int(M), int(N), int(K), int(group),
+                                                   int(bool(asymmetric)), int(bool(alpha)),
+                                                   *[ctypes.byref(o) for o in out]),
+                  "w4a16_gemm_ex_plan")
+    path = {1: "gemv", 2: "tensor_core"}[out[0].value]
+    return {"path": path, "splits": out[1].value, "ctas": out[2].value,
+            "rows_per_cta": out[3].value}
+
+
 def device_status() -> int:
     """Synchronise and return (and clear) the kernels' recorded status code."""
     st = ctypes.c_int(0)
