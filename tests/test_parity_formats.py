@@ -130,6 +130,20 @@ def test_formats_prefill_launch_shapes(w4lib, group, asym):
     assert w4.device_status() == 0
 
 
+@pytest.mark.parametrize("M,N,K,group,asym", [
+    (17, 1, 128, 32, True),                    # one weight row, one k-block pair
+    (129, 130, 32768, w4.PER_CHANNEL, True),   # the largest K, per-channel zero points
+    (130, 257, 32768, 32, False),              # the largest K at group 32 (1024 groups a row)
+    (1500, 384, 256, 64, True),                # many x tiles, few k-blocks
+])
+def test_formats_prefill_edges(w4lib, M, N, K, group, asym):
+    q, s, z = quantized_fmt(N, K, 700 + N, group, asym)
+    x16 = acts(M, K, 701)
+    assert_close(run_fmt(x16, q, s, z, group), oracle.gemm(x16, q, s, group, zeros=z),
+                 f"edge M={M} N={N} K={K} g={group} asym={asym}")
+    assert w4.device_status() == 0
+
+
 @pytest.mark.parametrize("idx", range(len(workloads.PREFILL)))
 def test_formats_prefill_full_size(w4lib, idx):
     """M = 512 prompt pass on the prefill shapes with group-32 asymmetric
