@@ -46,6 +46,18 @@ def test_gemv_every_row(w4lib, M, N, K):
     assert w4.device_status() == 0
 
 
+def test_out_is_checked(w4lib):
+    """A caller's y of the wrong shape or dtype is refused before any launch."""
+    _, blocks = blocks_of(64, 256, 530)
+    x = from_bits16(acts(2, 256, 531))
+    for bad in (torch.empty((2, 65), dtype=torch.float16, device="cuda"),
+                torch.empty((2, 64), dtype=torch.float32, device="cuda"),
+                torch.empty((64, 2), dtype=torch.float16, device="cuda").t()):
+        with pytest.raises(ValueError):
+            w4.gemm_q4_0(x, u8(blocks), out=bad)
+    assert w4.device_status() == 0
+
+
 @pytest.mark.parametrize("idx", range(len(workloads.LLAMA3_8B)))
 def test_llama3_8b_shapes_m1(w4lib, idx):
     lin = workloads.LLAMA3_8B[idx]

@@ -16,9 +16,18 @@ from . import _native
 GROUP = 128
 
 
-def _stream_ptr(stream) -> int:
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return int(s.cuda_stream)
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream_ptr(stream, device: torch.device | None = None) -> int:
+    """The cudaStream_t of `stream`, else of the current stream of `device`
+    (the raw-handle query costs a fraction of building a Stream object: a
+    decode call is a few microseconds of host time)."""
+    if stream is not None:
+        return int(stream.cuda_stream)
+    if _raw_stream is not None and device is not None and device.index is not None:
+        return int(_raw_stream(device.index))
+    return int(torch.cuda.current_stream().cuda_stream)
 
 
 def _need(t: torch.Tensor, dtype, name: str) -> None:
@@ -95,6 +104,17 @@ def unrepack(repacked: torch.Tensor, N: int, K: int, stream=None) -> torch.Tenso
     return q
 
 
+def _out_tensor(out: torch.Tensor | None, M: int, N: int, device) -> torch.Tensor:
+    """`out` checked to be a contiguous fp16 CUDA [M, N] tensor (the kernels
+    write exactly M x N halves there), or a new one."""
+    if out is None:
+        return torch.empty((M, N), dtype=torch.float16, device=device)
+    _need(out, torch.float16, "out")
+    if tuple(out.shape) != (M, N):
+        raise ValueError(f"out must be [{M}, {N}], got {tuple(out.shape)}")
+    return out
+
+
 def _check_weights(repacked: torch.Tensor, scales: torch.Tensor) -> tuple[int, int]:
     _need(repacked, torch.uint8, "repacked")
     _need(scales, torch.float16, "scales")
@@ -119,7 +139,7 @@ def _gemm(x: torch.Tensor, repacked: torch.Tensor, scales: torch.Tensor, N: int,
         if tuple(out.shape) != (M, N):
             raise ValueError("out has the wrong shape")
     rc = _native.lib().w4a16_gemm(x.data_ptr(), repacked.data_ptr(), scales.data_ptr(),
-                                  out.data_ptr(), M, N, K, _stream_ptr(stream))
+                                  out.data_ptr(), M, N, K, _stream_ptr(stream, x.device))
     if rc:
         _native.check(rc, "w4a16_gemm")
     return out
@@ -169,7 +189,7 @@ def gemm_ex(x: torch.Tensor, repacked: torch.Tensor, scales: torch.Tensor,
     rc = _native.lib().w4a16_gemm_ex(x.data_ptr(), alpha.data_ptr() if alpha is not None else None,
                                      repacked.data_ptr(), scales.data_ptr(),
                                      zeros.data_ptr() if zeros is not None else None,
-                                     out.data_ptr(), M, N, K, group, _stream_ptr(stream))
+                                     out.data_ptr(), M, N, K, group, _stream_ptr(stream, x.device))
     _native.check(rc, "w4a16_gemm_ex")
     return out
 
@@ -194,10 +214,9 @@ def gemm_q4_0(x: torch.Tensor, blocks: torch.Tensor, out: torch.Tensor | None = 
     if x.dim() != 2 or blocks.shape[1] != K // 32 * 18:
         raise ValueError(f"x must be [M, K] and blocks [N, K/32*18]")
     M = x.shape[0]
-    if out is None:
-        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    out = _out_tensor(out, M, N, x.device)
     _native.check(_native.lib().w4a16_gemm_q4_0(x.data_ptr(), blocks.data_ptr(), out.data_ptr(),
-                                                M, N, K, _stream_ptr(stream)), "w4a16_gemm_q4_0")
+                                                M, N, K, _stream_ptr(stream, x.device)), "w4a16_gemm_q4_0")
     return out
 
 
@@ -223,10 +242,9 @@ def gemm_w8(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor,
     if x.dim() != 2 or x.shape[1] != K or scales.shape != (N,):
         raise ValueError(f"x must be [M, {K}] and scales [{N}]")
     M = x.shape[0]
-    if out is None:
-        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    out = _out_tensor(out, M, N, x.device)
     _native.check(_native.lib().w4a16_gemm_w8(x.data_ptr(), codes.data_ptr(), scales.data_ptr(),
-                                              out.data_ptr(), M, N, K, _stream_ptr(stream)),
+                                              out.data_ptr(), M, N, K, _stream_ptr(stream, x.device)),
                   "w4a16_gemm_w8")
     return out
 
