@@ -12,9 +12,9 @@
 // half-warp, and each lane writes its 4 packed bytes (the group's 64 bytes
 // are one coalesced segment).  Each half-warp issues the loads of four
 // groups before quantizing them, and the grid is one resident wave.  256 B
-// are read and 66 B written per group; the per-element work is four
-// floating-point instructions (fma-rounding, its residual, the tie test),
-// which keeps the issue rate near the HBM rate.
+// are read and 66 B written per group; the per-element work (fma-rounding,
+// its residual, the tie test) runs on pairs through the packed binary32
+// instructions, about two instructions per element.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -80,18 +80,29 @@ __device__ __forceinline__ void quantize_group(const uint4 raw, uint32_t& packed
         w[2 * i] = f.x;
         w[2 * i + 1] = f.y;
     }
-    // e = kTieSq - d^2 with d = w y - q is negative exactly when |d| >
-    // sqrt(kTieSq) ~ 1/2 - 1e-5 (the fma rounds once, so its sign is exact):
-    // OR-ing the sign bits flags a near tie without min/max instructions.
+    // Pairs of elements go through the packed binary32 instructions, each
+    // component rounded exactly as the scalar form: t = RN(w y + kRound),
+    // d = RN(q - w y) with q = t - kRound, and e = RN(d^2 - kTieSq), which is
+    // negative exactly when |d| < sqrt(kTieSq) ~ 1/2 - 1e-5 (the fma rounds
+    // once, so its sign is exact).  AND-ing the sign bits leaves bit 31 clear
+    // when some element is a near tie (e = +0 counts as one: the exact
+    // fallback below is always correct).
     constexpr float kTieSq = 0.25f - 1.0e-5f;
-    uint32_t tie_bits = 0;
+    const float2 y2 = make_float2(y, y), ny2 = make_float2(-y, -y);
+    const float2 kr2 = make_float2(kRound, kRound), nkr2 = make_float2(-kRound, -kRound);
+    const float2 ntie2 = make_float2(-kTieSq, -kTieSq);
+    uint32_t clear_bits = 0xffffffffu;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        t[i] = __fmaf_rn(w[i], y, kRound);
-        const float d = __fmaf_rn(w[i], y, -__fsub_rn(t[i], kRound));  // w y - q
-        tie_bits |= __float_as_uint(__fmaf_rn(-d, d, kTieSq));
+    for (int i = 0; i < 4; ++i) {
+        const float2 wv = make_float2(w[2 * i], w[2 * i + 1]);
+        const float2 tv = __ffma2_rn(wv, y2, kr2);
+        const float2 d = __ffma2_rn(wv, ny2, __fadd2_rn(tv, nkr2));  // q - w y
+        const float2 e = __ffma2_rn(d, d, ntie2);
+        clear_bits &= __float_as_uint(e.x) & __float_as_uint(e.y);
+        t[2 * i] = tv.x;
+        t[2 * i + 1] = tv.y;
     }
-    if (__any_sync(0xffffffffu, (tie_bits >> 31) != 0)) {
+    if (__any_sync(0xffffffffu, (clear_bits >> 31) == 0)) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) t[i] = __fadd_rn(__fdiv_rn(w[i], s), kRound);
     }
