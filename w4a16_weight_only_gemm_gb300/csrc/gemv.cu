@@ -130,18 +130,27 @@ __device__ __forceinline__ void mma_group(uint32_t w_addr, uint32_t cs, uint32_t
                 mma_16816(g[c % NCH][MT - 1], af, b1[2 * s], b1[2 * s + 1], g[c % NCH][MT - 1]);
         }
     }
+    // The rescale runs on (column 2t, 2t + 1) pairs through the packed binary32
+    // instructions; each component rounds as the scalar fma.
+    const float2 s00 = make_float2(s0, s0), s11 = make_float2(s1, s1);
+    const float c1 = -72.0f * s1;
+    const float2 c11 = make_float2(c1, c1);
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
-        float v[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) v[e] = NCH == 2 ? g[0][mt][e] + g[NCH - 1][mt][e] : g[0][mt][e];
+        float2 v01 = make_float2(g[0][mt][0], g[0][mt][1]);
+        float2 v23 = make_float2(g[0][mt][2], g[0][mt][3]);
+        if (NCH == 2) {
+            v01 = __fadd2_rn(v01, make_float2(g[NCH - 1][mt][0], g[NCH - 1][mt][1]));
+            v23 = __fadd2_rn(v23, make_float2(g[NCH - 1][mt][2], g[NCH - 1][mt][3]));
+        }
         // rows r1 carry 72 * sum_k x[m, k] over the group (dequant8_bias72)
         const float2 sx = lds64f(sx_addr + mt * 32);
-        const float c1 = -72.0f * s1;
-        acc[mt][0] = fmaf(s0, v[0], acc[mt][0]);
-        acc[mt][1] = fmaf(s0, v[1], acc[mt][1]);
-        acc[mt][2] = fmaf(c1, sx.x, fmaf(s1, v[2], acc[mt][2]));
-        acc[mt][3] = fmaf(c1, sx.y, fmaf(s1, v[3], acc[mt][3]));
+        const float2 a01 = __ffma2_rn(s00, v01, make_float2(acc[mt][0], acc[mt][1]));
+        const float2 a23 = __ffma2_rn(c11, sx, __ffma2_rn(s11, v23, make_float2(acc[mt][2], acc[mt][3])));
+        acc[mt][0] = a01.x;
+        acc[mt][1] = a01.y;
+        acc[mt][2] = a23.x;
+        acc[mt][3] = a23.y;
     }
 }
 
