@@ -428,17 +428,20 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const GemvArg
                 const int e = task >> 3, gl = e / a.M, m = e - gl * a.M;
                 float sum = 0.0f;
                 if (ok && task < total) {
+                    // 16 values as 8 pairs, summed by a tree of packed
+                    // binary32 adds (depth 4), then the pair's two halves
                     const uint32_t src = sbase + a.off_x + m * a.xs_stride + gl * 256 + (task & 7) * 32;
                     const uint4 p[2] = {lds128(src), lds128(src + 16)};
+                    const uint32_t wv[8] = {p[0].x, p[0].y, p[0].z, p[0].w, p[1].x, p[1].y, p[1].z, p[1].w};
+                    float2 f[8];
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint32_t wv[4] = {p[h].x, p[h].y, p[h].z, p[h].w};
+                    for (int i = 0; i < 8; ++i)
+                        f[i] = __half22float2(*reinterpret_cast<const __half2*>(&wv[i]));
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[i]));
-                            sum += f.x + f.y;
-                        }
-                    }
+                    for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+                        for (int i = 0; i < w; ++i) f[i] = __fadd2_rn(f[i], f[i + w]);
+                    sum = f[0].x + f[0].y;
                 }
                 sum += __shfl_xor_sync(0xffffffffu, sum, 4);
                 sum += __shfl_xor_sync(0xffffffffu, sum, 2);
