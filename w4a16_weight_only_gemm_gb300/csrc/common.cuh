@@ -289,25 +289,21 @@ __device__ __forceinline__ void dequant8(uint32_t w, uint32_t (&r)[4]) {
     r[3] = *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Variant for the GEMV: the low nibbles (positions 0..3, the fragment rows
-// r0) are exact q as in dequant8; the high nibbles (positions 4..7 of each
-// half, rows r1) are OR-ed into the mantissa of 64.0 (0x5400), giving
-// 64 + n = 72 + q with no further instruction.  The MMA of r1 rows then
-// carries 72 * sum(x) extra, which the caller removes once per group.
-__device__ __forceinline__ void dequant8_bias72(uint32_t w, uint32_t (&r)[4]) {
-    constexpr uint32_t kMagic1024 = 0x64006400u;  // (1024.0, 1024.0)
-    constexpr uint32_t kMagic64 = 0x54005400u;    // (64.0, 64.0)
+// Variant for the GEMV: all 8 nibbles OR-ed into the mantissa of 64.0
+// (0x5400, where the fp16 ulp is 1/16) with no further instruction.  The low
+// nibbles (positions 0..3 of each half, the fragment rows r0) read
+// 64 + n/16, the high nibbles (positions 4..7, rows r1) 64 + n, exactly
+// (n = q + 8).  An MMA over them carries 64 * sum(x) on both rows and the
+// 1/16 factor on rows r0; the caller removes both once per group:
+//   sum x q = 16 G0 - 1032 sum(x)   (rows r0),   G1 - 72 sum(x)   (rows r1).
+__device__ __forceinline__ void dequant8_bias64(uint32_t w, uint32_t (&r)[4]) {
+    constexpr uint32_t kMagic64 = 0x54005400u;       // (64.0, 64.0)
     constexpr uint32_t kLut = (0xF0 & 0xCC) | 0xAA;  // (a & b) | c
-    const uint32_t lo0 = lop3<kLut>(w, 0x000F000Fu, kMagic1024);
     const uint32_t w8 = w >> 8;
-    const uint32_t lo1 = lop3<kLut>(w8, 0x000F000Fu, kMagic1024);
+    r[0] = lop3<kLut>(w, 0x000F000Fu, kMagic64);
     r[1] = lop3<kLut>(w, 0x00F000F0u, kMagic64);
+    r[2] = lop3<kLut>(w8, 0x000F000Fu, kMagic64);
     r[3] = lop3<kLut>(w8, 0x00F000F0u, kMagic64);
-    const __half2 k1032 = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
-    __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&lo0), k1032);
-    r[0] = *reinterpret_cast<uint32_t*>(&v);
-    v = __hsub2(*reinterpret_cast<const __half2*>(&lo1), k1032);
-    r[2] = *reinterpret_cast<uint32_t*>(&v);
 }
 
 __device__ __forceinline__ float2 lds64f(uint32_t addr) {

@@ -16,13 +16,14 @@
 //    one tensor-map box.  The fp16 scale slab of the CTA's rows (contiguous
 //    in the canonical layout) arrives the same way into one of two buffers,
 //    and the x slice of the CTA's K range once per thread block.
-//  * Consumers: per 64-wide chunk a lane reads 16 bytes of its tile, expands
-//    each 32-bit word into an mma.m16n8k16 A fragment with lop3 + one f16x2
-//    op per nibble pair (exact q), and multiplies it with x fragments read
-//    from shared memory.  M <= 8 uses one n8 MMA per 16 k, M <= 16 two.
-//    Every 128-wide group accumulates in a fresh FP32 fragment that is scaled
-//    once by its fp16 scale and added to the FP32 running sum: q * x products
-//    are exact and only FP32 sums round.
+//  * Consumers: per 64-wide chunk a lane reads 16 bytes of its tile, turns
+//    each 32-bit word into an mma.m16n8k16 A fragment with one lop3 per
+//    nibble pair (the nibbles OR-ed into the mantissa of 64.0: exact values
+//    64 + n/16 and 64 + n), and multiplies it with x fragments read from
+//    shared memory.  M <= 8 uses one n8 MMA per 16 k, M <= 16 two.  Every
+//    128-wide group accumulates in a fresh FP32 fragment; the group rescale
+//    removes the 64 and 1/16 with the group's x sums and applies the fp16
+//    scale: the products are exact and only FP32 sums round.
 //  * Work split, chosen per shape by a launch-time model: sub-block units
 //    (the warps of a tile add their partial sums in shared memory, in a
 //    fixed order); or whole blocks with the K range split over the S CTAs of
@@ -124,17 +125,19 @@ __device__ __forceinline__ void mma_group(uint32_t w_addr, uint32_t cs, uint32_t
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
             uint32_t af[4];
-            dequant8_bias72(wrd[s], af);
+            dequant8_bias64(wrd[s], af);
             mma_16816(g[c % NCH][0], af, b0[2 * s], b0[2 * s + 1], g[c % NCH][0]);
             if (MT == 2)
                 mma_16816(g[c % NCH][MT - 1], af, b1[2 * s], b1[2 * s + 1], g[c % NCH][MT - 1]);
         }
     }
     // The rescale runs on (column 2t, 2t + 1) pairs through the packed binary32
-    // instructions; each component rounds as the scalar fma.
-    const float2 s00 = make_float2(s0, s0), s11 = make_float2(s1, s1);
-    const float c1 = -72.0f * s1;
-    const float2 c11 = make_float2(c1, c1);
+    // instructions; each component rounds as the scalar fma.  Rows r0 fed
+    // 64 + n/16 and rows r1 fed 64 + n (dequant8_bias64) give
+    // s0 (16 G0 - 1032 Sx) and s1 (G1 - 72 Sx) over the group's x sums Sx.
+    const float2 s00 = make_float2(16.0f * s0, 16.0f * s0), s11 = make_float2(s1, s1);
+    const float c0 = -1032.0f * s0, c1 = -72.0f * s1;
+    const float2 c00 = make_float2(c0, c0), c11 = make_float2(c1, c1);
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
         float2 v01 = make_float2(g[0][mt][0], g[0][mt][1]);
@@ -143,9 +146,8 @@ __device__ __forceinline__ void mma_group(uint32_t w_addr, uint32_t cs, uint32_t
             v01 = __fadd2_rn(v01, make_float2(g[NCH - 1][mt][0], g[NCH - 1][mt][1]));
             v23 = __fadd2_rn(v23, make_float2(g[NCH - 1][mt][2], g[NCH - 1][mt][3]));
         }
-        // rows r1 carry 72 * sum_k x[m, k] over the group (dequant8_bias72)
         const float2 sx = lds64f(sx_addr + mt * 32);
-        const float2 a01 = __ffma2_rn(s00, v01, make_float2(acc[mt][0], acc[mt][1]));
+        const float2 a01 = __ffma2_rn(s00, v01, __ffma2_rn(c00, sx, make_float2(acc[mt][0], acc[mt][1])));
         const float2 a23 = __ffma2_rn(c11, sx, __ffma2_rn(s11, v23, make_float2(acc[mt][2], acc[mt][3])));
         acc[mt][0] = a01.x;
         acc[mt][1] = a01.y;
@@ -418,7 +420,7 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const GemvArg
 
         bool ok = mbar_wait(sbase + kBarX, 0, a.timeout_ns, a.status);
         // Activation sums per group and row, Sx[gl][m] in FP32, for the bias
-        // correction of dequant8_bias72: 8 threads per (group, row), 16
+        // correction of dequant8_bias64: 8 threads per (group, row), 16
         // values each, combined with xor-shuffles in a fixed order.
         {
             float* sxw = reinterpret_cast<float*>(smem + a.off_sx);
