@@ -592,14 +592,22 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const GemvArg
             }
             asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
             if (ks == 0 && ok) {
-                for (int w2 = 1; w2 < W; ++w2) {
+                // every partial's load issued before the first add; the adds
+                // keep warp order
 #pragma unroll
-                    for (int mt = 0; mt < MT; ++mt) {
-                        const float4 v = red[((warp + w2) * MT + mt) * 32 + lane];
-                        part[mt][0] += v.x;
-                        part[mt][1] += v.y;
-                        part[mt][2] += v.z;
-                        part[mt][3] += v.w;
+                for (int mt = 0; mt < MT; ++mt) {
+                    float4 v[kConsumerWarps - 1];
+#pragma unroll
+                    for (int w2 = 1; w2 < kConsumerWarps; ++w2)
+                        if (w2 < W) v[w2 - 1] = red[((warp + w2) * MT + mt) * 32 + lane];
+#pragma unroll
+                    for (int w2 = 1; w2 < kConsumerWarps; ++w2) {
+                        if (w2 < W) {
+                            part[mt][0] += v[w2 - 1].x;
+                            part[mt][1] += v[w2 - 1].y;
+                            part[mt][2] += v[w2 - 1].z;
+                            part[mt][3] += v[w2 - 1].w;
+                        }
                     }
                 }
                 const int rbase = block_of(0) * kBlockRows + t0 * 16;
