@@ -134,10 +134,10 @@ __device__ __forceinline__ void mma_group(uint32_t w_addr, uint32_t cs, uint32_t
     // The rescale runs on (column 2t, 2t + 1) pairs through the packed binary32
     // instructions; each component rounds as the scalar fma.  Rows r0 fed
     // 64 + n/16 and rows r1 fed 64 + n (dequant8_bias64) give
-    // s0 (16 G0 - 1032 Sx) and s1 (G1 - 72 Sx) over the group's x sums Sx.
+    // 16 s0 (G0 - 64.5 Sx) and s1 (G1 - 72 Sx) over the group's x sums Sx:
+    // the bias is removed before the scale is applied.
     const float2 s00 = make_float2(16.0f * s0, 16.0f * s0), s11 = make_float2(s1, s1);
-    const float c0 = -1032.0f * s0, c1 = -72.0f * s1;
-    const float2 c00 = make_float2(c0, c0), c11 = make_float2(c1, c1);
+    const float2 b0 = make_float2(-64.5f, -64.5f), b1 = make_float2(-72.0f, -72.0f);
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
         float2 v01 = make_float2(g[0][mt][0], g[0][mt][1]);
@@ -147,8 +147,8 @@ __device__ __forceinline__ void mma_group(uint32_t w_addr, uint32_t cs, uint32_t
             v23 = __fadd2_rn(v23, make_float2(g[NCH - 1][mt][2], g[NCH - 1][mt][3]));
         }
         const float2 sx = lds64f(sx_addr + mt * 32);
-        const float2 a01 = __ffma2_rn(s00, v01, __ffma2_rn(c00, sx, make_float2(acc[mt][0], acc[mt][1])));
-        const float2 a23 = __ffma2_rn(c11, sx, __ffma2_rn(s11, v23, make_float2(acc[mt][2], acc[mt][3])));
+        const float2 a01 = __ffma2_rn(s00, __ffma2_rn(b0, sx, v01), make_float2(acc[mt][0], acc[mt][1]));
+        const float2 a23 = __ffma2_rn(s11, __ffma2_rn(b1, sx, v23), make_float2(acc[mt][2], acc[mt][3]));
         acc[mt][0] = a01.x;
         acc[mt][1] = a01.y;
         acc[mt][2] = a23.x;
