@@ -1,7 +1,7 @@
 """CPU oracle for the W4A16 group-wise path -- TEST INFRASTRUCTURE ONLY.
 
 This package is a plain, slow, obviously correct restatement of what the path
-computes, used to judge the CUDA library.  Only ``tests/``, the smoke check
+computes, used to check the CUDA library.  Only ``tests/``, the smoke check
 in ``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` may import
 it.  The product library never imports, links or calls it, and it imports
 nothing from the product package.
