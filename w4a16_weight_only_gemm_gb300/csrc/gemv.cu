@@ -102,9 +102,21 @@ __device__ __forceinline__ void mma_group(uint32_t w_addr, uint32_t cs, uint32_t
     // group halve the dependent-latency path of a lane (M <= 16 has two
     // chains already, one per n8 tile, and no registers to spare).
     constexpr int NCH = MT == 1 ? 2 : 1;
+    // Chain 0 starts from the group's bias, -64.5 Sx (rows r0) and -72 Sx
+    // (rows r1), so the MMAs themselves remove it; further chains from zero.
     float g[NCH][MT][4];
 #pragma unroll
-    for (int c = 0; c < NCH; ++c)
+    for (int mt = 0; mt < MT; ++mt) {
+        const float2 sx = lds64f(sx_addr + mt * 32);
+        const float2 c0 = __fmul2_rn(make_float2(-64.5f, -64.5f), sx);
+        const float2 c1 = __fmul2_rn(make_float2(-72.0f, -72.0f), sx);
+        g[0][mt][0] = c0.x;
+        g[0][mt][1] = c0.y;
+        g[0][mt][2] = c1.x;
+        g[0][mt][3] = c1.y;
+    }
+#pragma unroll
+    for (int c = 1; c < NCH; ++c)
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -133,11 +145,10 @@ __device__ __forceinline__ void mma_group(uint32_t w_addr, uint32_t cs, uint32_t
     }
     // The rescale runs on (column 2t, 2t + 1) pairs through the packed binary32
     // instructions; each component rounds as the scalar fma.  Rows r0 fed
-    // 64 + n/16 and rows r1 fed 64 + n (dequant8_bias64) give
-    // 16 s0 (G0 - 64.5 Sx) and s1 (G1 - 72 Sx) over the group's x sums Sx:
-    // the bias is removed before the scale is applied.
+    // 64 + n/16 and rows r1 fed 64 + n (dequant8_bias64), their chains
+    // started from the bias, give 16 s0 (G0 - 64.5 Sx) and s1 (G1 - 72 Sx)
+    // over the group's x sums Sx.
     const float2 s00 = make_float2(16.0f * s0, 16.0f * s0), s11 = make_float2(s1, s1);
-    const float2 b0 = make_float2(-64.5f, -64.5f), b1 = make_float2(-72.0f, -72.0f);
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
         float2 v01 = make_float2(g[0][mt][0], g[0][mt][1]);
@@ -146,9 +157,8 @@ __device__ __forceinline__ void mma_group(uint32_t w_addr, uint32_t cs, uint32_t
             v01 = __fadd2_rn(v01, make_float2(g[NCH - 1][mt][0], g[NCH - 1][mt][1]));
             v23 = __fadd2_rn(v23, make_float2(g[NCH - 1][mt][2], g[NCH - 1][mt][3]));
         }
-        const float2 sx = lds64f(sx_addr + mt * 32);
-        const float2 a01 = __ffma2_rn(s00, __ffma2_rn(b0, sx, v01), make_float2(acc[mt][0], acc[mt][1]));
-        const float2 a23 = __ffma2_rn(s11, __ffma2_rn(b1, sx, v23), make_float2(acc[mt][2], acc[mt][3]));
+        const float2 a01 = __ffma2_rn(s00, v01, make_float2(acc[mt][0], acc[mt][1]));
+        const float2 a23 = __ffma2_rn(s11, v23, make_float2(acc[mt][2], acc[mt][3]));
         acc[mt][0] = a01.x;
         acc[mt][1] = a01.y;
         acc[mt][2] = a23.x;
