@@ -231,8 +231,10 @@ class Oracle:
                        group: int = GROUP, zeros: np.ndarray | None = None) -> np.ndarray:
         """The tutorial's own fp16 dequantized weight fp16(float(q) * float(s)).
 
-        Returns uint16 fp16 bits [N, K].  Pinned: equals the single fp16
-        rounding (numpy) of the exact dequantized value."""
+        Returns uint16 fp16 bits [N, K].  Pinned by the hand-derived fixture
+        ``tests/golden/dequant_f16.txt`` (ties, subnormals, overflow, zero
+        points) and by numpy's single float16 rounding of the exact binary64
+        dequantized value on random codes."""
         qweight = _c(qweight, np.uint8)
         scales = _c(scales, np.uint16)
         zeros = None if zeros is None else _c(zeros, np.uint8)

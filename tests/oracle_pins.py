@@ -507,6 +507,44 @@ def pin_w8_round_trip_and_gemm(o) -> None:
                                atol=1e-12)
 
 
+def pin_dequant_f16_fixture(o) -> None:
+    """The tutorial's fp16 dequantized weight matches hand-derived bits:
+    exact products, ties to even (up and down), subnormal results, overflow
+    to infinity, and the asymmetric zero point subtracted from the nibble."""
+    for row in _read_fixture("dequant_f16.txt"):
+        nib, z, sbits, ebits = int(row[1]), row[2], int(row[3], 16), int(row[4], 16)
+        q = np.full((1, 64), nib | (nib << 4), dtype=np.uint8)  # K = 128, one group
+        s = np.array([[sbits]], dtype=np.uint16)
+        zeros = None if z == "-" else np.array([[int(z)]], dtype=np.uint8)
+        out = o.dequantize_f16(q, s, GROUP, zeros)
+        assert out.shape == (1, 128)
+        assert (out == ebits).all(), f"nib {nib} z {z} s {sbits:#06x}: {out[0, 0]:#06x} != {ebits:#06x}"
+    # two groups with different scales: each element takes its own group's scale
+    q = np.full((1, 128), 0xFF, dtype=np.uint8)  # nibble 15 (q = 7), K = 256
+    s = _f16_bits([[0.5, 0.25]])
+    out = o.dequantize_f16(q, s, GROUP)
+    assert (out[0, :128] == 0x4300).all() and (out[0, 128:] == 0x3F00).all()  # 3.5, 1.75
+
+
+def pin_dequant_f16_single_rounding(o) -> None:
+    """On random codes and scales the fp16 dequantized weight is numpy's IEEE
+    float16 rounding of the exact binary64 dequantized value (the binary32
+    product of an fp16 scale and |q| <= 15 is exact, so one rounding is all
+    there is), symmetric and asymmetric, for groups of 32 and 128."""
+    rng = np.random.default_rng(61)
+    for group, asym in ((128, False), (32, True)):
+        N, K = 5, 256
+        q = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+        s = _f16_bits(rng.uniform(-3.0, 3.0, size=(N, K // group)) * 10.0 ** rng.integers(
+            -4, 3, size=(N, K // group)))
+        zeros = rng.integers(0, 16, size=(N, K // group), dtype=np.uint8) if asym else None
+        nib = _nibbles(q).astype(np.float64)
+        zz = 8.0 if zeros is None else np.repeat(zeros.astype(np.float64), group, axis=1)
+        exact = (nib - zz) * np.repeat(s.view(np.float16).astype(np.float64), group, axis=1)
+        want = exact.astype(np.float16).view(np.uint16)
+        np.testing.assert_array_equal(o.dequantize_f16(q, s, group, zeros), want)
+
+
 # --------------------------------------------------------------------------
 # GGUF Q4_0 blocks (tutorial GGUF section)
 # --------------------------------------------------------------------------
@@ -567,4 +605,6 @@ ALL_PINS = (
     pin_q4_0_matches_group32,
     pin_w8_nearest_level,
     pin_w8_round_trip_and_gemm,
+    pin_dequant_f16_fixture,
+    pin_dequant_f16_single_rounding,
 )

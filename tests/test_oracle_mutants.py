@@ -4,7 +4,9 @@ wrong divisor, an off-by-one offset, a reversed operand, a truncating
 conversion, a wrong exponent bias, a wrong group stride, a transposed scale
 store, a scale taken from the wrong group; for the asymmetric quantizer a
 range that leaves out 0, a wrong divisor, a wrong-signed or truncated zero
-point, the symmetric +8 offset, zero points ignored by the dequantizer).  The pin suite must reject every
+point, the symmetric +8 offset, zero points ignored by the dequantizer; for the
+fp16 dequantized weight a swapped zero point, a truncating rounding, a scale
+of the wrong group, a wrong offset).  The pin suite must reject every
 one of them; a mutant that passes all pins means the pins are too weak."""
 from __future__ import annotations
 
@@ -54,6 +56,13 @@ MUTANTS = {
     "w8_offset_127": ("out[k] = (double)((int)qrow[k] - 128) * s;",
                       "out[k] = (double)((int)qrow[k] - 127) * s;"),
     "awq_alpha_by_row": ("(float)orc_half_to_double(alpha[k]);", "(float)orc_half_to_double(alpha[m]);"),
+    "f16_dequant_zero_swapped": ("float v = (float)(nib - z) * s;", "float v = (float)(z - nib) * s;"),
+    "f16_dequant_truncating": ("out[n * K + k] = orc_float_to_half(v);",
+                               "out[n * K + k] = orc_float_to_half(v * (1.0f - 1.0f / 4096.0f));"),
+    "f16_dequant_scale_group_zero": ("float s = (float)orc_half_to_double(scales[n * (K / group) + k / group]);",
+                                     "float s = (float)orc_half_to_double(scales[n * (K / group)]);"),
+    "f16_dequant_offset_7": ("int z = zeros ? zeros[n * (K / group) + k / group] : 8;",
+                             "int z = zeros ? zeros[n * (K / group) + k / group] : 7;"),
     "awq_truncating": ("out[m * K + k] = orc_float_to_half(p);",
                        "out[m * K + k] = orc_float_to_half(p * (1.0f - 1.0f / 4096.0f));"),
 }
