@@ -312,6 +312,22 @@ int w4a16_gemm_plan(int64_t M, int64_t N, int64_t K, int *path, int *splits, int
                     int *blocks_per_cta, int *rows_per_cta);
 
 /*
+ * w4a16_gemm_plan_tail -- the last round of a persistent GEMV launch (more
+ * 128-row blocks than CTAs, each CTA walking blocks y, y + ctas, ...).  When
+ * the blocks do not divide evenly, the R blocks of the partial last round run
+ * as R * 128 / tail_rows units of tail_rows weight rows (16, 32 or 64) over
+ * the whole K range, one per CTA, so that round costs tail_rows / 128 of a
+ * block instead of a whole one on a few CTAs.
+ *
+ *   *tail_rows   rows of each tail unit, 0 when the launch has no such round
+ *                (not persistent, blocks divide evenly, or more than half a
+ *                round left over) or M > 16.
+ *   *tail_units  number of tail units (0 with tail_rows = 0).
+ * Errors: as w4a16_gemm_plan.
+ */
+int w4a16_gemm_plan_tail(int64_t M, int64_t N, int64_t K, int *tail_rows, int *tail_units);
+
+/*
  * w4a16_gemm_ex_plan -- the launch w4a16_gemm_ex makes for (M, N, K) with
  * the given group (32, 64, 128 or W4A16_GROUP_PER_CHANNEL), zero points
  * (nonzero: asymmetric codes) and AWQ scale (nonzero: alpha given), without

@@ -93,6 +93,30 @@ def test_persistent_path_all_rows(w4lib, M, N, K):
     assert_close(run_gemm(x16, q, s), oracle.gemm(x16, q, s), f"M={M} N={N} K={K} {plan}")
 
 
+@pytest.mark.parametrize("M", [1, 9])
+@pytest.mark.parametrize("K", [256, 1152])
+@pytest.mark.parametrize("tail_rows", [16, 32, 64])
+def test_persistent_tail_units_all_rows(w4lib, M, K, tail_rows):
+    """A persistent launch whose last round is partial runs those blocks as
+    units of 16, 32 or 64 rows, one per CTA after its whole blocks.  The
+    shape puts R left-over blocks on G CTAs (R * 128 / tail_rows <= G) and
+    ends in a ragged block (91 rows), so some tail units are partly or
+    wholly beyond N; K = 1152 ends the units' streams in a partial stage.
+    Every row is checked, and a repeat call is bit-identical."""
+    G = w4.gemm_plan(M, 200_000, K)["ctas"]
+    rem = {16: G // 8, 32: G // 4, 64: G // 2}[tail_rows]
+    N = 128 * (G + rem) - 37
+    plan = w4.gemm_plan(M, N, K)
+    tail = w4.gemm_plan_tail(M, N, K)
+    assert plan["blocks_per_cta"] > 1 and plan["ctas"] == G, plan
+    assert tail == {"tail_rows": tail_rows, "tail_units": rem * 128 // tail_rows}, (tail, plan)
+    w16, q, s = quantized(N, K, 71)
+    x16 = acts(M, K, 72 + M)
+    y = run_gemm(x16, q, s)
+    assert_close(y, oracle.gemm(x16, q, s), f"M={M} N={N} K={K} {plan} {tail}")
+    assert np.array_equal(run_gemm(x16, q, s), y)
+
+
 # Launches made of sub-block units (16, 32 or 64 weight rows per CTA over the
 # whole K range): ragged row tails inside a tile, and K ranges that end in a
 # partial ring stage (K = 11008: 172 chunks; K = 1920: 30).

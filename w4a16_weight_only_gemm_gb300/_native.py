@@ -38,6 +38,7 @@ SIGNATURES = {
     "w4a16_gemm_w8": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "w4a16_gemm_ex": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _P]),
     "w4a16_gemm_plan": (ctypes.c_int, [_I64, _I64, _I64] + [ctypes.POINTER(ctypes.c_int)] * 5),
+    "w4a16_gemm_plan_tail": (ctypes.c_int, [_I64, _I64, _I64] + [ctypes.POINTER(ctypes.c_int)] * 2),
     "w4a16_gemm_ex_plan": (ctypes.c_int, [_I64, _I64, _I64, ctypes.c_int32, ctypes.c_int32,
                                           ctypes.c_int32] + [ctypes.POINTER(ctypes.c_int)] * 4),
     "w4a16_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int)]),

@@ -274,11 +274,27 @@ int w4a16_gemm_plan(int64_t M, int64_t N, int64_t K, int* path, int* splits, int
         *rows_per_cta = 128;
         return W4A16_OK;
     }
-    if (int rc = from_cuda(
-            gemv_plan_info((int)M, N, K, ctx, splits, ctas, blocks_per_cta, rows_per_cta)))
+    int tail_rows = 0, tail_units = 0;
+    if (int rc = from_cuda(gemv_plan_info((int)M, N, K, ctx, splits, ctas, blocks_per_cta,
+                                          rows_per_cta, &tail_rows, &tail_units)))
         return rc;
     *path = W4A16_PATH_GEMV;
     return W4A16_OK;
+}
+
+int w4a16_gemm_plan_tail(int64_t M, int64_t N, int64_t K, int* tail_rows, int* tail_units) {
+    if (!tail_rows || !tail_units) return W4A16_ERR_NULL;
+    if (M < 1 || M > (int64_t)1 << 22 || !good_nk(N, K) || N > (int64_t)1 << 28 ||
+        K > (int64_t)1 << 15)
+        return W4A16_ERR_SHAPE;
+    *tail_rows = 0;
+    *tail_units = 0;
+    if (M > 16) return W4A16_OK;
+    DeviceCtx ctx;
+    if (int rc = device_ctx(&ctx)) return rc;
+    int splits = 0, ctas = 0, blocks = 0, rows = 0;
+    return from_cuda(gemv_plan_info((int)M, N, K, ctx, &splits, &ctas, &blocks, &rows, tail_rows,
+                                    tail_units));
 }
 
 int w4a16_gemm_ex_plan(int64_t M, int64_t N, int64_t K, int32_t group, int32_t zero_points,

@@ -85,6 +85,10 @@ struct GemvArgs {
     int n_sbuf;              // scale buffers: 2 when a CTA walks several blocks
     int nstages;             // ring stages (<= kMaxStages)
     int rpo;                 // rows owned per CTA in the split reduction
+    // Persistent whole-block launches whose last round is partial: the
+    // blocks from tail_base on run as tail_units sub-block units of tail_T
+    // tiles (tail_T = 0: no tail), unit u on CTA u after its whole blocks.
+    int tail_T, tail_base, tail_units;
     uint32_t off_ring, off_x, off_s, off_red, off_sx;
 };
 
@@ -185,6 +189,126 @@ __device__ __forceinline__ void store_y(const GemvArgs& a, int R0, int R1, int t
     }
 }
 
+// The consumer side of a sub-block unit of T tiles over the K range of the
+// CTA: a stage holds GPS = 8 / T groups of the unit's T tiles (chunk c of
+// tile i at c * cs + i * 512 bytes); the W = 8 / T warps of a tile take
+// groups 2 ks, 2 ks + 1 of every stage.  Returns false on a time-out.
+template <int MT>
+__device__ __forceinline__ bool unit_stages(const GemvArgs& a, uint32_t sbase, int nstg, int ng,
+                                            int GPS, int ks, uint32_t wl, uint32_t cs, uint32_t x0,
+                                            uint32_t x1, uint32_t sxl, const __half* sc0,
+                                            const __half* sc1, int lane, int& slot, uint32_t& phase,
+                                            float (&acc)[MT][4]) {
+    const int NS = a.nstages;
+    for (int st = 0; st < nstg; ++st) {
+        if (!mbar_wait(sbase + kBarFull + 8 * slot, phase, a.timeout_ns, a.status)) return false;
+        const int gs = min(GPS, ng - st * GPS);     // groups in this stage
+        const int gsl0 = ks * kGroupsPerWarpStage;  // this warp's first group in it
+        const int gl0 = st * GPS + gsl0;
+        const uint32_t wa = wl + slot * kStageBytes + gsl0 * 2 * cs;
+        if (gs == GPS) {
+#pragma unroll
+            for (int gi = 0; gi < kGroupsPerWarpStage; ++gi)
+                mma_group<MT>(wa + gi * 2 * cs, cs, x0 + (gl0 + gi) * 256, x1 + (gl0 + gi) * 256,
+                              sxl + (gl0 + gi) * 64, __half2float(sc0[gl0 + gi]),
+                              __half2float(sc1[gl0 + gi]), acc);
+        } else {
+            for (int gi = 0; gi < kGroupsPerWarpStage && gsl0 + gi < gs; ++gi)
+                mma_group<MT>(wa + gi * 2 * cs, cs, x0 + (gl0 + gi) * 256, x1 + (gl0 + gi) * 256,
+                              sxl + (gl0 + gi) * 64, __half2float(sc0[gl0 + gi]),
+                              __half2float(sc1[gl0 + gi]), acc);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sbase + kBarEmpty + 8 * slot);
+        if (++slot == NS) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+    return true;
+}
+
+// The W warps of a unit's tile hold sums over disjoint groups of its rows:
+// the first adds the others' in warp order (fixed, so repeated calls agree
+// bit for bit) and writes rows rbase + R0 and rbase + R1.  All consumer
+// warps of the CTA take part (named barrier 1).
+template <int MT>
+__device__ __forceinline__ void unit_reduce_store(const GemvArgs& a, uint8_t* smem, int warp, int lane,
+                                                  int ks, int W, bool ok, float (&part)[MT][4],
+                                                  int rbase, int R0, int R1, int t) {
+    float4* red = reinterpret_cast<float4*>(smem + a.off_red);  // [warp][MT][lane]
+    if (ks > 0) {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+            red[(warp * MT + mt) * 32 + lane] =
+                make_float4(part[mt][0], part[mt][1], part[mt][2], part[mt][3]);
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+    if (ks == 0 && ok) {
+        // every partial's load issued before the first add; the adds keep
+        // warp order
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            float4 v[kConsumerWarps - 1];
+#pragma unroll
+            for (int w2 = 1; w2 < kConsumerWarps; ++w2)
+                if (w2 < W) v[w2 - 1] = red[((warp + w2) * MT + mt) * 32 + lane];
+#pragma unroll
+            for (int w2 = 1; w2 < kConsumerWarps; ++w2) {
+                if (w2 < W) {
+                    part[mt][0] += v[w2 - 1].x;
+                    part[mt][1] += v[w2 - 1].y;
+                    part[mt][2] += v[w2 - 1].z;
+                    part[mt][3] += v[w2 - 1].w;
+                }
+            }
+        }
+        store_y<MT>(a, rbase + R0, rbase + R1, t, part);
+    }
+}
+
+// The consumer side of a CTA's tail unit after its whole blocks (persistent
+// launches with a partial last round): tT tiles of block t_rb from tile t_t0,
+// W2 = 8 / tT warps per tile over the K range.  Every consumer warp reaches
+// the reduction's barrier, whatever `ok` says.  Kept out of line so that the
+// whole-block loop keeps its registers.
+template <int MT>
+__device__ __noinline__ bool tail_unit_consume(const GemvArgs& a, uint8_t* smem, uint32_t sbase,
+                                               uint32_t ring, int nblk, int nck, int ng, int g0,
+                                               uint32_t x0, uint32_t x1, uint32_t sxl, int slot,
+                                               uint32_t phase, bool ok) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int tT = a.tail_T;
+    const int t_rb = a.tail_base + (int)blockIdx.y / (kConsumerWarps / tT);
+    const int t_t0 = ((int)blockIdx.y % (kConsumerWarps / tT)) * tT;
+    const int sbuf = nblk % a.n_sbuf;
+    const int W2 = kConsumerWarps / tT;
+    const int ti2 = warp / W2, ks2 = warp - ti2 * W2;
+    const int tr0 = ti2 * 16 + g, tr1 = tr0 + 8;
+    const uint32_t tcs = (uint32_t)(tT * kTileBytes);
+    const uint32_t twl = ring + ti2 * kTileBytes + lane * 16;
+    const int tCPS = kStageBytes / (tT * kTileBytes);
+    const int tnstg = (nck + tCPS - 1) / tCPS;
+    float tacc[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) tacc[mt][e] = 0.0f;
+    if (ok && !mbar_wait(sbase + kBarSFull + 8 * sbuf, (nblk / a.n_sbuf) & 1, a.timeout_ns, a.status))
+        ok = false;
+    if (ok) {
+        const __half* tsc0 =
+            reinterpret_cast<const __half*>(smem + a.off_s + sbuf * a.slab_bytes) + tr0 * a.G + g0;
+        if (!unit_stages<MT>(a, sbase, tnstg, ng, tCPS / 2, ks2, twl, tcs, x0, x1, sxl, tsc0,
+                             tsc0 + 8 * a.G, lane, slot, phase, tacc))
+            ok = false;
+    }
+    unit_reduce_store<MT>(a, smem, warp, lane, ks2, W2, ok, tacc, t_rb * kBlockRows + t_t0 * 16, tr0,
+                          tr1, t);
+    return ok;
+}
+
 // WHOLE: the CTA computes whole 128-row blocks (T = 8, stage geometry fixed
 // at compile time); otherwise sub-block units of a.T tiles.  The weight map
 // (`wmap`) views the kernel layout as rows of 4 KB chunks (512 eight-byte
@@ -210,7 +334,16 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const GemvArg
     // Whole blocks: the CTA walks blocks y, y + gridDim.y, ...  Sub-block
     // units: CTA y owns rows [16 T y, 16 T (y + 1)), tiles t0 .. t0 + T - 1
     // of block 16 T y / 128.
-    const int nblk = whole ? (a.NB - (int)blockIdx.y + (int)gridDim.y - 1) / (int)gridDim.y : 1;
+    const int nblk = !whole ? 1
+                     : a.tail_T ? a.tail_base / (int)gridDim.y
+                                : (a.NB - (int)blockIdx.y + (int)gridDim.y - 1) / (int)gridDim.y;
+    // The tail unit of this CTA (persistent launches with a partial last
+    // round): tT tiles from tile t_t0 of block t_rb.  Evaluated where used.
+    auto has_tail = [&]() { return whole && a.tail_T > 0 && (int)blockIdx.y < a.tail_units; };
+#define W4A16_TAIL_GEOMETRY                                                         \
+    const int tT = a.tail_T;                                                        \
+    const int t_rb = a.tail_base + (int)blockIdx.y / (kConsumerWarps / tT);         \
+    const int t_t0 = ((int)blockIdx.y % (kConsumerWarps / tT)) * tT;
     const int t0 = whole ? 0 : ((int)blockIdx.y * T) & (kConsumerWarps - 1);
     auto block_of = [&](int j) {
         return whole ? (int)blockIdx.y + j * (int)gridDim.y : ((int)blockIdx.y * T) / kConsumerWarps;
@@ -314,6 +447,67 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const GemvArg
                         mbar_arrive_expect_tx(sbase + kBarFull + 8 * slot, nc * kChunkBytes);
                         bulk_g2s_hint(ring + slot * kStageBytes, w + (size_t)st * kStageBytes,
                                       nc * kChunkBytes, sbase + kBarFull + 8 * slot, pol);
+                        ++it;
+                        if (++slot == NS) {
+                            slot = 0;
+                            ++round;
+                        }
+                    }
+                }
+                if (ok && has_tail()) {
+                    // The tail unit: scale slab of its 16 tT rows, then boxes of
+                    // tT tiles x 32 / tT chunks through the tensor map.
+                    W4A16_TAIL_GEOMETRY
+                    const int sbuf = nblk % a.n_sbuf;
+                    if (nblk >= a.n_sbuf &&
+                        !mbar_wait(sbase + kBarSEmpty + 8 * sbuf, ((nblk / a.n_sbuf) - 1) & 1,
+                                   a.timeout_ns, a.status))
+                        ok = false;
+                    const int r0 = t_rb * kBlockRows + t_t0 * 16;
+                    if (ok) {
+                        const int rows = max(0, min(16 * tT, a.N - r0));
+                        const uint32_t bytes = (uint32_t)(rows * a.G * 2);
+                        const uint32_t bulk = bytes & ~15u;
+                        const __half* src = a.scales + (size_t)r0 * a.G;
+                        __half* dst = reinterpret_cast<__half*>(smem + a.off_s + sbuf * a.slab_bytes);
+                        for (uint32_t e = bulk / 2; e < bytes / 2; ++e) dst[e] = src[e];  // ragged tail
+                        mbar_arrive_expect_tx(sbase + kBarSFull + 8 * sbuf, bulk);
+                        if (bulk)
+                            bulk_g2s(sbase + a.off_s + sbuf * a.slab_bytes, src, bulk,
+                                     sbase + kBarSFull + 8 * sbuf);
+                        sb_issued = nblk + 1;
+                    }
+                    const int tCPS = kStageBytes / (tT * kTileBytes);
+                    const int tnstg = (C + tCPS - 1) / tCPS;
+                    const int box_x = t_t0 * (kTileBytes / 8);
+                    const int cy0 = t_rb * C;
+                    for (int st = 0; ok && st < tnstg; ++st) {
+                        if (it >= NS && !x_issued) issue_x();
+                        if (it >= NS &&
+                            !mbar_wait(sbase + kBarEmpty + 8 * slot, (round - 1) & 1, a.timeout_ns,
+                                       a.status)) {
+                            ok = false;
+                            break;
+                        }
+                        if (*abort_flag) {
+                            ok = false;
+                            break;
+                        }
+                        const int nc = min(tCPS, C - st * tCPS);
+                        const uint32_t dst = ring + slot * kStageBytes;
+                        const uint32_t bar = sbase + kBarFull + 8 * slot;
+                        if (nc == tCPS) {
+                            mbar_arrive_expect_tx(bar, kStageBytes);
+                            tma_load_2d_hint(dst, wmap, box_x, cy0 + st * tCPS, bar, pol);
+                        } else {
+                            const uint32_t rowb = (uint32_t)(tT * kTileBytes);
+                            const uint8_t* src = a.wq + (size_t)(cy0 + st * tCPS) * kChunkBytes +
+                                                 (size_t)t_t0 * kTileBytes;
+                            mbar_arrive_expect_tx(bar, nc * rowb);
+                            for (int c = 0; c < nc; ++c)
+                                bulk_g2s_hint(dst + c * rowb, src + (size_t)c * kChunkBytes, rowb, bar,
+                                              pol);
+                        }
                         ++it;
                         if (++slot == NS) {
                             slot = 0;
@@ -529,36 +723,9 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const GemvArg
             } else {
                 // Sub-block units: a stage holds GPS groups of T tiles; the W
                 // warps of a tile take two groups each.
-                for (int st = 0; st < nstg; ++st) {
-                    if (!mbar_wait(sbase + kBarFull + 8 * slot, phase, a.timeout_ns, a.status)) {
-                        ok = false;
-                        break;
-                    }
-                    const int gs = min(GPS, ng - st * GPS);     // groups in this stage
-                    const int gsl0 = ks * kGroupsPerWarpStage;  // this warp's first group in it
-                    const int gl0 = st * GPS + gsl0;
-                    const uint32_t wa = wl + slot * kStageBytes + gsl0 * 2 * cs;
-                    if (gs == GPS) {
-#pragma unroll
-                        for (int gi = 0; gi < kGroupsPerWarpStage; ++gi)
-                            mma_group<MT>(wa + gi * 2 * cs, cs, x0 + (gl0 + gi) * 256,
-                                          x1 + (gl0 + gi) * 256, sxl + (gl0 + gi) * 64,
-                                          __half2float(sc0[gl0 + gi]), __half2float(sc1[gl0 + gi]),
-                                          acc);
-                    } else {
-                        for (int gi = 0; gi < kGroupsPerWarpStage && gsl0 + gi < gs; ++gi)
-                            mma_group<MT>(wa + gi * 2 * cs, cs, x0 + (gl0 + gi) * 256,
-                                          x1 + (gl0 + gi) * 256, sxl + (gl0 + gi) * 64,
-                                          __half2float(sc0[gl0 + gi]), __half2float(sc1[gl0 + gi]),
-                                          acc);
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(sbase + kBarEmpty + 8 * slot);
-                    if (++slot == NS) {
-                        slot = 0;
-                        phase ^= 1u;
-                    }
-                }
+                if (!unit_stages<MT>(a, sbase, nstg, ng, GPS, ks, wl, cs, x0, x1, sxl, sc0, sc1, lane,
+                                     slot, phase, acc))
+                    ok = false;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(sbase + kBarSEmpty + 8 * sbuf);
@@ -590,39 +757,12 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const GemvArg
             }
         }
         if constexpr (!WHOLE) {
-            // The W warps of a tile hold sums over disjoint groups of its
-            // rows: the first adds the others' in warp order (fixed, so
-            // repeated calls agree bit for bit) and writes the rows.
-            float4* red = reinterpret_cast<float4*>(smem + a.off_red);  // [warp][MT][lane]
-            if (ks > 0) {
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt)
-                    red[(warp * MT + mt) * 32 + lane] =
-                        make_float4(part[mt][0], part[mt][1], part[mt][2], part[mt][3]);
-            }
-            asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-            if (ks == 0 && ok) {
-                // every partial's load issued before the first add; the adds
-                // keep warp order
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    float4 v[kConsumerWarps - 1];
-#pragma unroll
-                    for (int w2 = 1; w2 < kConsumerWarps; ++w2)
-                        if (w2 < W) v[w2 - 1] = red[((warp + w2) * MT + mt) * 32 + lane];
-#pragma unroll
-                    for (int w2 = 1; w2 < kConsumerWarps; ++w2) {
-                        if (w2 < W) {
-                            part[mt][0] += v[w2 - 1].x;
-                            part[mt][1] += v[w2 - 1].y;
-                            part[mt][2] += v[w2 - 1].z;
-                            part[mt][3] += v[w2 - 1].w;
-                        }
-                    }
-                }
-                const int rbase = block_of(0) * kBlockRows + t0 * 16;
-                store_y<MT>(a, rbase + row0, rbase + row1, t, part);
-            }
+            unit_reduce_store<MT>(a, smem, warp, lane, ks, W, ok, part,
+                                  block_of(0) * kBlockRows + t0 * 16, row0, row1, t);
+        } else {
+            if (has_tail())
+                ok = tail_unit_consume<MT>(a, smem, sbase, ring, nblk, nck, ng, g0, x0, x1, sxl, slot,
+                                           phase, ok);
         }
         if (!ok) *abort_flag = 1;
     }
@@ -648,11 +788,14 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const GemvArg
     }
 }
 
+#undef W4A16_TAIL_GEOMETRY
+
 // Whole 128-row blocks per CTA (split or persistent launches).
+// (The tensor map is used only by the tail units of a persistent launch.)
 template <int MT>
 __global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2)
-    gemv_kernel(const __grid_constant__ GemvArgs a) {
-    gemv_body<MT, true>(nullptr, a);
+    gemv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ GemvArgs a) {
+    gemv_body<MT, true>(&wmap, a);
 }
 
 // Sub-block units of a.T tiles, weights copied through the tensor map.
@@ -671,6 +814,7 @@ struct GemvPlan {
     int xs_stride = 0;
     int slab_bytes = 0;
     int rpo = 0;
+    int tail_T = 0, tail_base = 0, tail_units = 0;  // persistent launches: last-round units
     uint32_t off_ring = 0, off_x = 0, off_s = 0, off_red = 0, off_sx = 0, smem = 0;
     double cost = 0.0;
 };
@@ -720,7 +864,8 @@ cudaError_t ensure_smem_attr() {
 }
 
 // Shared-memory layout of a launch with K split S, T tiles per CTA and
-// `nsb` scale buffers.
+// `nsb` scale buffers (a persistent launch always reserves the in-CTA
+// reduction buffer of its tail units).
 template <int MT>
 bool layout(GemvPlan& p, int M, int G, int S, int T, int nsb, const DeviceCtx& ctx,
             int nst = kStages) {
@@ -739,8 +884,8 @@ bool layout(GemvPlan& p, int M, int G, int S, int T, int nsb, const DeviceCtx& c
     p.off_red = p.off_s + nsb * p.slab_bytes;
     p.rpo = (kBlockRows + S - 1) / S;
     const int red_bytes = S > 1 ? S * p.rpo * 16 * 4
-                          : T < kConsumerWarps ? kConsumerWarps * MT * 32 * 16
-                                               : 0;
+                          : T < kConsumerWarps || nsb == 2 ? kConsumerWarps * MT * 32 * 16
+                                                           : 0;
     p.off_sx = p.off_red + red_bytes;
     p.smem = p.off_sx + ng_max * 16 * 4;
     return (int)p.smem <= ctx.max_smem_optin;
@@ -801,6 +946,18 @@ GemvPlan plan_gemv(int M, int N, int K, const DeviceCtx& ctx) {
                     }
                 }
                 p.grid_y = ctx.num_sms * occ;
+                // A partial last round of R blocks runs as units of T tiles,
+                // the smallest T that gives each of the first CTAs at most one
+                // (T / 8 of a block-time instead of a whole one).
+                const int rem = NB % p.grid_y;
+                for (int tt = 1; rem > 0 && tt < kConsumerWarps; tt *= 2) {
+                    if (rem * (kConsumerWarps / tt) <= p.grid_y) {
+                        p.tail_T = tt;
+                        p.tail_base = NB - rem;
+                        p.tail_units = rem * (kConsumerWarps / tt);
+                        break;
+                    }
+                }
                 p.cost = 0.0;
                 return p;
             }
@@ -929,9 +1086,13 @@ cudaError_t launch_gemv_mt(GemvArgs args, int M, cudaStream_t stream, const Devi
     args.off_sx = p.off_sx;
     args.rpo = p.rpo;
     args.T = p.T;
-    CUtensorMap wmap;
-    if (p.T < kConsumerWarps) {
-        const cudaError_t me = weight_map(args.wq, args.NB, args.K, p.T, &wmap);
+    args.tail_T = p.tail_T;
+    args.tail_base = p.tail_base;
+    args.tail_units = p.tail_units;
+    CUtensorMap wmap = {};
+    if (p.T < kConsumerWarps || p.tail_T > 0) {
+        const cudaError_t me =
+            weight_map(args.wq, args.NB, args.K, p.T < kConsumerWarps ? p.T : p.tail_T, &wmap);
         if (me != cudaSuccess) return me;
     }
     cudaLaunchConfig_t cfg = {};
@@ -954,7 +1115,7 @@ cudaError_t launch_gemv_mt(GemvArgs args, int M, cudaStream_t stream, const Devi
     cfg.attrs = attrs;
     cfg.numAttrs = na;
     if (p.T < kConsumerWarps) return cudaLaunchKernelEx(&cfg, gemv_unit_kernel<MT>, wmap, args);
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<MT>, args);
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<MT>, wmap, args);
 }
 
 }  // namespace
@@ -965,7 +1126,8 @@ cudaError_t gemv_weight_map(const void* repacked, int64_t N, int64_t K, int T, C
 }
 
 cudaError_t gemv_plan_info(int M, int64_t N, int64_t K, const DeviceCtx& ctx, int* splits,
-                           int* ctas, int* blocks_per_cta, int* rows_per_cta) {
+                           int* ctas, int* blocks_per_cta, int* rows_per_cta, int* tail_rows,
+                           int* tail_units) {
     cudaError_t e = M <= 8 ? ensure_smem_attr<1>() : ensure_smem_attr<2>();
     if (e != cudaSuccess) return e;
     const GemvPlan p = M <= 8 ? cached_plan<1>(M, (int)N, (int)K, ctx)
@@ -976,6 +1138,8 @@ cudaError_t gemv_plan_info(int M, int64_t N, int64_t K, const DeviceCtx& ctx, in
     *ctas = p.S * p.grid_y;
     *blocks_per_cta = p.T == kConsumerWarps ? (NB + p.grid_y - 1) / p.grid_y : 1;
     *rows_per_cta = 16 * p.T;
+    *tail_rows = 16 * p.tail_T;
+    *tail_units = p.tail_units;
     return cudaSuccess;
 }
 

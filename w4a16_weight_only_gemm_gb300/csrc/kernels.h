@@ -69,9 +69,12 @@ cudaError_t launch_gemm_tc_fmt(const void* x, const void* alpha, const void* rep
 cudaError_t launch_gemv(const void* x, const void* repacked, const void* scales, void* y, int M,
                         int64_t N, int64_t K, cudaStream_t stream, const DeviceCtx& ctx);
 // The launch the decode GEMV would make: K split (cluster size), CTAs, the
-// most 128-row blocks one CTA walks and the weight rows of one CTA's unit.
+// most 128-row blocks one CTA walks, the weight rows of one CTA's unit, and
+// for a persistent launch with a partial last round the rows of each tail
+// unit and their number (0, 0 without one).
 cudaError_t gemv_plan_info(int M, int64_t N, int64_t K, const DeviceCtx& ctx, int* splits,
-                           int* ctas, int* blocks_per_cta, int* rows_per_cta);
+                           int* ctas, int* blocks_per_cta, int* rows_per_cta, int* tail_rows,
+                           int* tail_units);
 // The launch the tensor-core GEMM would make: cluster size (1: one CTA per
 // 128 x 128 tile; 2: CTA pairs with 2-CTA MMAs; 4, 6 or 8: CTA pairs
 // splitting K two, three or four ways, reduced over the cluster) and CTAs.

@@ -261,6 +261,16 @@ def gemm_plan(M: int, N: int, K: int) -> dict:
             "blocks_per_cta": out[3].value, "rows_per_cta": out[4].value}
 
 
+def gemm_plan_tail(M: int, N: int, K: int) -> dict:
+    """The partial last round of a persistent decode launch for (M, N, K):
+    {"tail_rows": rows per tail unit (0: no such round), "tail_units": count}."""
+    out = [ctypes.c_int(0) for _ in range(2)]
+    _native.check(_native.lib().w4a16_gemm_plan_tail(int(M), int(N), int(K),
+                                                     *[ctypes.byref(o) for o in out]),
+                  "w4a16_gemm_plan_tail")
+    return {"tail_rows": out[0].value, "tail_units": out[1].value}
+
+
 def gemm_ex_plan(M: int, N: int, K: int, group: int, asymmetric: bool = False,
                  alpha: bool = False) -> dict:
     """The launch gemm_ex() makes for (M, N, K) with this group, zero points
