@@ -359,7 +359,12 @@ int w4a16_device_status(int *status);
 
 /*
  * Upper bound, in nanoseconds, of every wait inside the library's kernels
- * (default 2e9, i.e. two seconds).  Applies to launches made after the call.
+ * (default 2e9, i.e. two seconds; 0 is taken as 1).  Applies to launches made
+ * after the call.  A wait that gives up records W4A16_ERR_TIMEOUT (see
+ * w4a16_device_status); the kernel then issues no more copies and waits for
+ * those in flight before it exits.  That last wait is bounded by the larger
+ * of this value and 100 ms, so a short limit cannot let a block exit while a
+ * copy still writes into its shared memory.  Safe to call from any thread.
  */
 void w4a16_set_wait_timeout_ns(uint64_t timeout_ns);
 

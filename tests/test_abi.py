@@ -140,3 +140,22 @@ def test_python_layer_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_native, "library_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="no fallback"):
         _native.lib()
+
+
+def test_operands_on_one_device():
+    """The wrappers launch on the operands' device: operands on different
+    devices (or an explicit stream on another device) are refused before any
+    call into the library."""
+    from types import SimpleNamespace
+
+    import torch
+
+    from w4a16_weight_only_gemm_gb300 import ops
+
+    d0, d1 = torch.device("cuda:0"), torch.device("cuda:1")
+    a, b = SimpleNamespace(device=d0), SimpleNamespace(device=d1)
+    assert ops._device_of(None, ("x", a), ("scales", a), ("out", None)) == d0
+    with pytest.raises(ValueError, match="scales"):
+        ops._device_of(None, ("x", a), ("scales", b))
+    with pytest.raises(ValueError, match="stream"):
+        ops._device_of(SimpleNamespace(device=d1), ("x", a))

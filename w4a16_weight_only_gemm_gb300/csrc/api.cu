@@ -1,5 +1,6 @@
 // api.cu -- the C ABI (include/w4a16.h): argument checks, per-device set-up,
 // dispatch to the kernels, the device status word and its self-test.
+#include <atomic>
 #include <mutex>
 
 #include "../../include/w4a16.h"
@@ -13,7 +14,7 @@ namespace {
 __device__ unsigned g_device_status;
 
 constexpr int kMaxDevices = 64;
-uint64_t g_timeout_ns = 2000000000ull;
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};  // read at every launch, set from any thread
 
 struct DeviceSlot {
     std::once_flag once;
@@ -46,7 +47,7 @@ int device_ctx(DeviceCtx* out) {
     if (slot.init_error != cudaSuccess) return W4A16_ERR_CUDA;
     if (!slot.supported) return W4A16_ERR_DEVICE;
     *out = slot.ctx;
-    out->timeout_ns = g_timeout_ns;
+    out->timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
     return W4A16_OK;
 }
 
@@ -342,7 +343,7 @@ int w4a16_device_status(int* status) {
 }
 
 void w4a16_set_wait_timeout_ns(uint64_t timeout_ns) {
-    g_timeout_ns = timeout_ns == 0 ? 1 : timeout_ns;
+    g_timeout_ns.store(timeout_ns == 0 ? 1 : timeout_ns, std::memory_order_relaxed);
 }
 
 int w4a16_selftest_wait_timeout(uint64_t timeout_ns, void* stream) {

@@ -96,6 +96,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     }
 }
 
+// Bound of a drain wait: before a CTA exits, every copy it issued must have
+// landed in its shared memory, so the wait for those copies never gives up
+// sooner than this, however short the caller's wait limit (still bounded).
+constexpr uint64_t kDrainFloorNs = 100000000ull;  // 100 ms
+
+__device__ __forceinline__ uint64_t drain_bound(uint64_t timeout_ns) {
+    return timeout_ns > kDrainFloorNs ? timeout_ns : kDrainFloorNs;
+}
+
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
                                                   uint64_t timeout_ns, unsigned* status) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
@@ -228,6 +237,13 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_
 // Split cluster barrier: every thread of every CTA arrives, later waits.
 __device__ __forceinline__ void cluster_arrive() {
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+// Arrival with no memory ordering: used once at the start, so that a later
+// cluster_wait() guarantees every CTA of the cluster is running (its shared
+// memory may then be written remotely).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void cluster_wait() {

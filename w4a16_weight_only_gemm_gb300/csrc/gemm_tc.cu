@@ -340,10 +340,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             if (!ok) *abort_flag = 1;
             // Drain the copies in flight before the block may exit.
-            mbar_wait(base + kBarSlab, 0, a.timeout_ns, a.status);
+            const uint64_t dt = drain_bound(a.timeout_ns);
+            mbar_wait(base + kBarSlab, 0, dt, a.status);
             for (int i = (issued > NS ? issued - NS : 0); i < issued; ++i)
-                mbar_wait(base + kBarLoadFull + 8 * (i % NS), (i / NS) & 1, a.timeout_ns,
-                          a.status);
+                mbar_wait(base + kBarLoadFull + 8 * (i % NS), (i / NS) & 1, dt, a.status);
         }
         __syncwarp();
     } else if (warp == 1) {

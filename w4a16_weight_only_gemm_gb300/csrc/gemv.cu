@@ -40,6 +40,7 @@
 //    grid-dependency wait.
 // Every wait is bounded (common.cuh); on a time-out the CTA records it in the
 // status word, stops issuing copies, drains those in flight and exits.
+#include <atomic>
 #include <mutex>
 #include <utility>
 #include <vector>
@@ -367,6 +368,10 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const GemvArg
         fence_barrier_init();
     }
     __syncthreads();
+    // K split over a cluster: the partial sums go into peer CTAs' shared
+    // memory, which must not be written before those CTAs run.  Every thread
+    // arrives here and waits (cluster_wait) once before the exchange.
+    if (S > 1) cluster_arrive_relaxed();
     // Dependents may start their own prologue (and L2 prefetch) right away;
     // their griddepcontrol.wait still waits for this grid to complete.
     grid_launch_dependents();
@@ -518,12 +523,12 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const GemvArg
                 if (!x_issued) issue_x();
                 if (!ok) *abort_flag = 1;
                 // Drain: every issued copy must land before the CTA may exit.
-                mbar_wait(sbase + kBarX, 0, a.timeout_ns, a.status);
+                const uint64_t dt = drain_bound(a.timeout_ns);
+                mbar_wait(sbase + kBarX, 0, dt, a.status);
                 for (int i = (it > NS ? it - NS : 0); i < it; ++i)
-                    mbar_wait(sbase + kBarFull + 8 * (i % NS), (i / NS) & 1, a.timeout_ns, a.status);
+                    mbar_wait(sbase + kBarFull + 8 * (i % NS), (i / NS) & 1, dt, a.status);
                 for (int j = (sb_issued > a.n_sbuf ? sb_issued - a.n_sbuf : 0); j < sb_issued; ++j)
-                    mbar_wait(sbase + kBarSFull + 8 * (j % a.n_sbuf), (j / a.n_sbuf) & 1, a.timeout_ns,
-                              a.status);
+                    mbar_wait(sbase + kBarSFull + 8 * (j % a.n_sbuf), (j / a.n_sbuf) & 1, dt, a.status);
             }
         } else {
             // Sub-block units (one block, one scale buffer): a tensor-map box of
@@ -599,16 +604,19 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const GemvArg
                 if (!x_issued) issue_x();
                 if (!ok) *abort_flag = 1;
                 // Drain: every issued copy must land before the CTA may exit.
-                mbar_wait(sbase + kBarX, 0, a.timeout_ns, a.status);
+                const uint64_t dt = drain_bound(a.timeout_ns);
+                mbar_wait(sbase + kBarX, 0, dt, a.status);
                 for (int i = (it > NS ? it - NS : 0); i < it; ++i)
-                    mbar_wait(sbase + kBarFull + 8 * (i % NS), (i / NS) & 1, a.timeout_ns, a.status);
-                mbar_wait(sbase + kBarSFull, 0, a.timeout_ns, a.status);
+                    mbar_wait(sbase + kBarFull + 8 * (i % NS), (i / NS) & 1, dt, a.status);
+                mbar_wait(sbase + kBarSFull, 0, dt, a.status);
             }
         }
         __syncwarp();
+        if (S > 1) cluster_wait();
     } else {
         // =============================== consumers ==============================
         grid_dependency_wait();
+        if (S > 1) cluster_wait();  // every peer runs: their reduction slots exist
         const int g = lane >> 2, t = lane & 3;
         const int ti = warp / W;         // tile of this warp within the CTA's rows
         const int ks = warp - ti * W;    // its share of every stage's groups
@@ -850,16 +858,16 @@ int max_active_clusters(int S, uint32_t smem) {
 
 template <int MT>
 cudaError_t ensure_smem_attr() {
-    static bool done[64] = {};
+    static std::atomic<bool> done[64];  // per device; racing callers only repeat the set-up
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+    if (dev >= 0 && dev < 64 && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(gemv_kernel<MT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(gemv_unit_kernel<MT>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+    if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev].store(true, std::memory_order_release);
     return e;
 }
 

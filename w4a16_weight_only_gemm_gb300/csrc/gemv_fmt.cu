@@ -25,6 +25,7 @@
 // symmetric) keeps the exact-product kernels of gemv.cu.
 // Every wait is bounded; on a time-out the CTA records it in the status
 // word, stops issuing copies, drains those in flight and exits.
+#include <atomic>
 #include <mutex>
 #include <utility>
 #include <vector>
@@ -237,10 +238,11 @@ __global__ void __launch_bounds__(kFThreads, MT == 1 ? 3 : 2)
             }
             if (!x_issued) issue_x();
             if (!ok) *abort_flag = 1;
-            mbar_wait(sbase + kFBarX, 0, a.timeout_ns, a.status);
+            const uint64_t dt = drain_bound(a.timeout_ns);
+            mbar_wait(sbase + kFBarX, 0, dt, a.status);
             for (int i = (it > NS ? it - NS : 0); i < it; ++i)
-                mbar_wait(sbase + kFBarFull + 8 * (i % NS), (i / NS) & 1, a.timeout_ns, a.status);
-            mbar_wait(sbase + kFBarS, 0, a.timeout_ns, a.status);
+                mbar_wait(sbase + kFBarFull + 8 * (i % NS), (i / NS) & 1, dt, a.status);
+            mbar_wait(sbase + kFBarS, 0, dt, a.status);
         }
         __syncwarp();
         return;
@@ -373,13 +375,13 @@ int fmt_occupancy(uint32_t smem) {
 
 template <int MT>
 cudaError_t ensure_fmt_attr() {
-    static bool done[64] = {};
+    static std::atomic<bool> done[64];  // per device; racing callers only repeat the set-up
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+    if (dev >= 0 && dev < 64 && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
     const cudaError_t e = cudaFuncSetAttribute(
         gemv_fmt_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+    if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev].store(true, std::memory_order_release);
     return e;
 }
 

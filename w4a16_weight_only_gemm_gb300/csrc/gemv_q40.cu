@@ -19,6 +19,7 @@
 // mma.m16n8k16 (the activations' k order permuted the same way) fill a fresh
 // FP32 fragment, scaled once by each row's block scale into the sum.  Every
 // wait is bounded.
+#include <atomic>
 #include <mutex>
 #include <utility>
 #include <vector>
@@ -149,9 +150,10 @@ __global__ void __launch_bounds__(kQThreads, MT == 1 ? 3 : 2)
             }
             if (!x_issued) issue_x();
             if (!ok) *abort_flag = 1;
-            mbar_wait(sbase + kQBarX, 0, a.timeout_ns, a.status);
+            const uint64_t dt = drain_bound(a.timeout_ns);
+            mbar_wait(sbase + kQBarX, 0, dt, a.status);
             for (int i = (it > NS ? it - NS : 0); i < it; ++i)
-                mbar_wait(sbase + kQBarFull + 8 * (i % NS), (i / NS) & 1, a.timeout_ns, a.status);
+                mbar_wait(sbase + kQBarFull + 8 * (i % NS), (i / NS) & 1, dt, a.status);
         }
         __syncwarp();
         return;
@@ -280,13 +282,13 @@ int q40_occupancy(uint32_t smem) {
 
 template <int MT>
 cudaError_t ensure_q40_attr() {
-    static bool done[64] = {};
+    static std::atomic<bool> done[64];  // per device; racing callers only repeat the set-up
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+    if (dev >= 0 && dev < 64 && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
     const cudaError_t e = cudaFuncSetAttribute(
         gemv_q40_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+    if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev].store(true, std::memory_order_release);
     return e;
 }
 

@@ -18,6 +18,7 @@
 // the chunk permuted identically for the activations) accumulate the exact
 // products in FP32, and the per-row scale multiplies the sum once at the end.
 // Programmatic dependent launch as in gemv.cu.  Every wait is bounded.
+#include <atomic>
 #include <mutex>
 #include <utility>
 #include <vector>
@@ -140,9 +141,10 @@ __global__ void __launch_bounds__(kWThreads, MT == 1 ? 3 : 2)
             }
             if (!x_issued) issue_x();
             if (!ok) *abort_flag = 1;
-            mbar_wait(sbase + kWBarX, 0, a.timeout_ns, a.status);
+            const uint64_t dt = drain_bound(a.timeout_ns);
+            mbar_wait(sbase + kWBarX, 0, dt, a.status);
             for (int i = (it > NS ? it - NS : 0); i < it; ++i)
-                mbar_wait(sbase + kWBarFull + 8 * (i % NS), (i / NS) & 1, a.timeout_ns, a.status);
+                mbar_wait(sbase + kWBarFull + 8 * (i % NS), (i / NS) & 1, dt, a.status);
         }
         __syncwarp();
         return;
@@ -267,13 +269,13 @@ int w8_occupancy(uint32_t smem) {
 
 template <int MT>
 cudaError_t ensure_w8_attr() {
-    static bool done[64] = {};
+    static std::atomic<bool> done[64];  // per device; racing callers only repeat the set-up
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+    if (dev >= 0 && dev < 64 && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
     const cudaError_t e = cudaFuncSetAttribute(
         gemv_w8_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+    if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev].store(true, std::memory_order_release);
     return e;
 }
 

@@ -30,6 +30,33 @@ def _stream_ptr(stream, device: torch.device | None = None) -> int:
     return int(torch.cuda.current_stream().cuda_stream)
 
 
+def _device_of(stream, *named) -> torch.device:
+    """The one device of the named tensors (None entries skipped), checked to
+    be shared by all of them and by an explicit `stream`; the library launches
+    on the current device, so a mix would hand it foreign pointers."""
+    dev = None
+    for name, t in named:
+        if t is None:
+            continue
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, the other operands on {dev}")
+    if stream is not None and dev is not None and getattr(stream, "device", dev) != dev:
+        raise ValueError(f"stream is on {stream.device}, the operands on {dev}")
+    return dev
+
+
+def _call(dev: torch.device, fn, *args) -> int:
+    """fn(*args) with `dev` the current CUDA device (switched only when it is
+    not already current: the common case costs one device query)."""
+    idx = dev.index
+    if idx is None or idx == torch.cuda.current_device():
+        return fn(*args)
+    with torch.cuda.device(idx):
+        return fn(*args)
+
+
 def _need(t: torch.Tensor, dtype, name: str) -> None:
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
@@ -43,10 +70,11 @@ def quantize(W: torch.Tensor, group: int = GROUP, stream=None):
     """W fp16 [N, K] -> (qweight uint8 [N, K/2], scales fp16 [N, K/128])."""
     _need(W, torch.float16, "W")
     N, K = W.shape
-    q = torch.empty((N, K // 2), dtype=torch.uint8, device=W.device)
-    s = torch.empty((N, K // GROUP), dtype=torch.float16, device=W.device)
-    rc = _native.lib().w4a16_quantize(W.data_ptr(), N, K, group, q.data_ptr(), s.data_ptr(),
-                                      _stream_ptr(stream))
+    dev = _device_of(stream, ("W", W))
+    q = torch.empty((N, K // 2), dtype=torch.uint8, device=dev)
+    s = torch.empty((N, K // GROUP), dtype=torch.float16, device=dev)
+    rc = _call(dev, _native.lib().w4a16_quantize, W.data_ptr(), N, K, group, q.data_ptr(),
+               s.data_ptr(), _stream_ptr(stream, dev))
     _native.check(rc, "w4a16_quantize")
     return q, s
 
@@ -63,12 +91,13 @@ def quantize_ex(W: torch.Tensor, group: int = GROUP, asymmetric: bool = False, s
     g = K if group == PER_CHANNEL else group
     if g <= 0 or K % g:
         raise ValueError(f"K={K} is not a multiple of group={group}")
-    q = torch.empty((N, K // 2), dtype=torch.uint8, device=W.device)
-    s = torch.empty((N, K // g), dtype=torch.float16, device=W.device)
-    z = torch.empty((N, K // g), dtype=torch.uint8, device=W.device) if asymmetric else None
-    rc = _native.lib().w4a16_quantize_ex(W.data_ptr(), N, K, group, int(asymmetric), q.data_ptr(),
-                                         s.data_ptr(), z.data_ptr() if asymmetric else None,
-                                         _stream_ptr(stream))
+    dev = _device_of(stream, ("W", W))
+    q = torch.empty((N, K // 2), dtype=torch.uint8, device=dev)
+    s = torch.empty((N, K // g), dtype=torch.float16, device=dev)
+    z = torch.empty((N, K // g), dtype=torch.uint8, device=dev) if asymmetric else None
+    rc = _call(dev, _native.lib().w4a16_quantize_ex, W.data_ptr(), N, K, group, int(asymmetric),
+               q.data_ptr(), s.data_ptr(), z.data_ptr() if asymmetric else None,
+               _stream_ptr(stream, dev))
     _native.check(rc, "w4a16_quantize_ex")
     return q, s, z
 
@@ -85,9 +114,10 @@ def repack(qweight: torch.Tensor, stream=None) -> torch.Tensor:
     """Canonical [N, K/2] packed bytes -> kernel-layout bytes (1-D uint8)."""
     _need(qweight, torch.uint8, "qweight")
     N, K2 = qweight.shape
-    out = torch.empty(repacked_bytes(N, 2 * K2), dtype=torch.uint8, device=qweight.device)
-    rc = _native.lib().w4a16_repack(qweight.data_ptr(), N, 2 * K2, out.data_ptr(),
-                                    _stream_ptr(stream))
+    dev = _device_of(stream, ("qweight", qweight))
+    out = torch.empty(repacked_bytes(N, 2 * K2), dtype=torch.uint8, device=dev)
+    rc = _call(dev, _native.lib().w4a16_repack, qweight.data_ptr(), N, 2 * K2, out.data_ptr(),
+               _stream_ptr(stream, dev))
     _native.check(rc, "w4a16_repack")
     return out
 
@@ -97,9 +127,10 @@ def unrepack(repacked: torch.Tensor, N: int, K: int, stream=None) -> torch.Tenso
     _need(repacked, torch.uint8, "repacked")
     if repacked.numel() != repacked_bytes(N, K):
         raise ValueError("repacked buffer size does not match N, K")
-    q = torch.empty((N, K // 2), dtype=torch.uint8, device=repacked.device)
-    rc = _native.lib().w4a16_unrepack(repacked.data_ptr(), N, K, q.data_ptr(),
-                                      _stream_ptr(stream))
+    dev = _device_of(stream, ("repacked", repacked))
+    q = torch.empty((N, K // 2), dtype=torch.uint8, device=dev)
+    rc = _call(dev, _native.lib().w4a16_unrepack, repacked.data_ptr(), N, K, q.data_ptr(),
+               _stream_ptr(stream, dev))
     _native.check(rc, "w4a16_unrepack")
     return q
 
@@ -129,17 +160,16 @@ def _gemm(x: torch.Tensor, repacked: torch.Tensor, scales: torch.Tensor, N: int,
     _need(x, torch.float16, "x")
     if x.dim() != 2 or x.shape[1] != K:
         raise ValueError(f"x must be [M, {K}]")
-    if x.device != scales.device:
-        raise ValueError("x and the weights are on different devices")
+    dev = _device_of(stream, ("x", x), ("repacked", repacked), ("scales", scales), ("out", out))
     M = x.shape[0]
     if out is None:
-        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+        out = torch.empty((M, N), dtype=torch.float16, device=dev)
     else:
         _need(out, torch.float16, "out")
         if tuple(out.shape) != (M, N):
             raise ValueError("out has the wrong shape")
-    rc = _native.lib().w4a16_gemm(x.data_ptr(), repacked.data_ptr(), scales.data_ptr(),
-                                  out.data_ptr(), M, N, K, _stream_ptr(stream, x.device))
+    rc = _call(dev, _native.lib().w4a16_gemm, x.data_ptr(), repacked.data_ptr(), scales.data_ptr(),
+               out.data_ptr(), M, N, K, _stream_ptr(stream, dev))
     if rc:
         _native.check(rc, "w4a16_gemm")
     return out
@@ -180,16 +210,18 @@ def gemm_ex(x: torch.Tensor, repacked: torch.Tensor, scales: torch.Tensor,
         raise ValueError(f"scales must be [N, {K}/{g}]")
     if repacked.numel() != repacked_bytes(N, K):
         raise ValueError("repacked buffer size does not match N, K")
+    dev = _device_of(stream, ("x", x), ("alpha", alpha), ("repacked", repacked),
+                     ("scales", scales), ("zeros", zeros), ("out", out))
     if out is None:
-        out = torch.empty((M, N), dtype=torch.float16, device=x.device)
+        out = torch.empty((M, N), dtype=torch.float16, device=dev)
     else:
         _need(out, torch.float16, "out")
         if tuple(out.shape) != (M, N):
             raise ValueError("out has the wrong shape")
-    rc = _native.lib().w4a16_gemm_ex(x.data_ptr(), alpha.data_ptr() if alpha is not None else None,
-                                     repacked.data_ptr(), scales.data_ptr(),
-                                     zeros.data_ptr() if zeros is not None else None,
-                                     out.data_ptr(), M, N, K, group, _stream_ptr(stream, x.device))
+    rc = _call(dev, _native.lib().w4a16_gemm_ex, x.data_ptr(),
+               alpha.data_ptr() if alpha is not None else None, repacked.data_ptr(),
+               scales.data_ptr(), zeros.data_ptr() if zeros is not None else None,
+               out.data_ptr(), M, N, K, group, _stream_ptr(stream, dev))
     _native.check(rc, "w4a16_gemm_ex")
     return out
 
@@ -198,9 +230,10 @@ def quantize_q4_0(W: torch.Tensor, stream=None) -> torch.Tensor:
     """W fp16 [N, K] -> GGUF Q4_0 blocks uint8 [N, K/32 * 18] (K % 256 == 0)."""
     _need(W, torch.float16, "W")
     N, K = W.shape
-    blocks = torch.empty((N, K // 32 * 18), dtype=torch.uint8, device=W.device)
-    _native.check(_native.lib().w4a16_quantize_q4_0(W.data_ptr(), N, K, blocks.data_ptr(),
-                                                    _stream_ptr(stream)), "w4a16_quantize_q4_0")
+    dev = _device_of(stream, ("W", W))
+    blocks = torch.empty((N, K // 32 * 18), dtype=torch.uint8, device=dev)
+    _native.check(_call(dev, _native.lib().w4a16_quantize_q4_0, W.data_ptr(), N, K,
+                        blocks.data_ptr(), _stream_ptr(stream, dev)), "w4a16_quantize_q4_0")
     return blocks
 
 
@@ -214,9 +247,10 @@ def gemm_q4_0(x: torch.Tensor, blocks: torch.Tensor, out: torch.Tensor | None = 
     if x.dim() != 2 or blocks.shape[1] != K // 32 * 18:
         raise ValueError(f"x must be [M, K] and blocks [N, K/32*18]")
     M = x.shape[0]
-    out = _out_tensor(out, M, N, x.device)
-    _native.check(_native.lib().w4a16_gemm_q4_0(x.data_ptr(), blocks.data_ptr(), out.data_ptr(),
-                                                M, N, K, _stream_ptr(stream, x.device)), "w4a16_gemm_q4_0")
+    dev = _device_of(stream, ("x", x), ("blocks", blocks), ("out", out))
+    out = _out_tensor(out, M, N, dev)
+    _native.check(_call(dev, _native.lib().w4a16_gemm_q4_0, x.data_ptr(), blocks.data_ptr(),
+                        out.data_ptr(), M, N, K, _stream_ptr(stream, dev)), "w4a16_gemm_q4_0")
     return out
 
 
@@ -224,11 +258,11 @@ def quantize_w8(W: torch.Tensor, stream=None):
     """W8A16: W fp16 [N, K] -> (codes uint8 [N, K] holding q + 128, scales fp16 [N])."""
     _need(W, torch.float16, "W")
     N, K = W.shape
-    codes = torch.empty((N, K), dtype=torch.uint8, device=W.device)
-    s = torch.empty((N,), dtype=torch.float16, device=W.device)
-    _native.check(_native.lib().w4a16_quantize_w8(W.data_ptr(), N, K, codes.data_ptr(),
-                                                  s.data_ptr(), _stream_ptr(stream)),
-                  "w4a16_quantize_w8")
+    dev = _device_of(stream, ("W", W))
+    codes = torch.empty((N, K), dtype=torch.uint8, device=dev)
+    s = torch.empty((N,), dtype=torch.float16, device=dev)
+    _native.check(_call(dev, _native.lib().w4a16_quantize_w8, W.data_ptr(), N, K, codes.data_ptr(),
+                        s.data_ptr(), _stream_ptr(stream, dev)), "w4a16_quantize_w8")
     return codes, s
 
 
@@ -242,9 +276,10 @@ def gemm_w8(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor,
     if x.dim() != 2 or x.shape[1] != K or scales.shape != (N,):
         raise ValueError(f"x must be [M, {K}] and scales [{N}]")
     M = x.shape[0]
-    out = _out_tensor(out, M, N, x.device)
-    _native.check(_native.lib().w4a16_gemm_w8(x.data_ptr(), codes.data_ptr(), scales.data_ptr(),
-                                              out.data_ptr(), M, N, K, _stream_ptr(stream, x.device)),
+    dev = _device_of(stream, ("x", x), ("codes", codes), ("scales", scales), ("out", out))
+    out = _out_tensor(out, M, N, dev)
+    _native.check(_call(dev, _native.lib().w4a16_gemm_w8, x.data_ptr(), codes.data_ptr(),
+                        scales.data_ptr(), out.data_ptr(), M, N, K, _stream_ptr(stream, dev)),
                   "w4a16_gemm_w8")
     return out
 
