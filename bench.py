@@ -154,16 +154,28 @@ class ClockSampler:
 # ----------------------------------------------------------------------------
 # GPU side
 # ----------------------------------------------------------------------------
-def make_layer(lin, workload: str, idx: int, M: int = 1):
+PARITY_ROWS = 64  # sampled rows of every timed layer checked against the oracle
+
+
+def make_layer(lin, workload: str, idx: int, M: int = 1, keep_rows: int = 0):
+    """A quantized layer on the GPU; with keep_rows, the master weight's rows
+    at `keep_rows` sampled indices are kept on the host (the oracle quantizes
+    them itself for the parity check of the CPU-baseline leg)."""
     import w4a16_weight_only_gemm_gb300 as w4
     sw, sx = synthetic.seeds(workload, idx)
     W = synthetic.master_weight(lin.N, lin.K, sw, device="cuda")
     q, s = w4.quantize(W)
     r = w4.repack(q)
+    layer = {"lin": lin, "r": r, "s": s, "M": M}
+    if keep_rows:
+        rows = np.sort(np.random.default_rng(sw).choice(lin.N, size=min(keep_rows, lin.N),
+                                                        replace=False))
+        layer["rows"] = rows
+        layer["W_rows"] = W[torch.from_numpy(rows).cuda()].cpu()
     del W, q
-    x = synthetic.activations(M, lin.K, sx, device="cuda")
-    y = torch.empty((M, lin.N), dtype=torch.float16, device="cuda")
-    return {"lin": lin, "r": r, "s": s, "x": x, "y": y, "M": M}
+    layer["x"] = synthetic.activations(M, lin.K, sx, device="cuda")
+    layer["y"] = torch.empty((M, lin.N), dtype=torch.float16, device="cuda")
+    return layer
 
 
 def gemm_call(layer, r=None, s=None):
@@ -330,7 +342,8 @@ def run_ours(args, rank, world):
     from w4a16_weight_only_gemm_gb300 import build
     build.build()
     dev = torch.cuda.current_device()
-    layers = [make_layer(lin, "llama3_8b_decode", i) for i, lin in enumerate(workloads.LLAMA3_8B)]
+    layers = [make_layer(lin, "llama3_8b_decode", i, keep_rows=PARITY_ROWS if rank == 0 else 0)
+              for i, lin in enumerate(workloads.LLAMA3_8B)]
     step_bytes = sum(workloads.algorithmic_bytes(1, lin.N, lin.K) for lin in workloads.LLAMA3_8B)
     stream = torch.cuda.Stream()
 
@@ -390,7 +403,7 @@ def run_ours(args, rank, world):
     if rank == 0 and not args.skip_extras:
         result["sections"] = extras(layers)
     if rank == 0:
-        result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        result["cpu_baseline"], result["parity"] = cpu_baseline(args.cpu_seconds, layers)
     return result
 
 
@@ -617,35 +630,61 @@ def oracle_inputs(rows_per_shape: int = 64):
     return prepared
 
 
-def oracle_pass(prepared) -> int:
+def oracle_pass(prepared, keep: bool = False):
     """One pass of the oracle over the sampled rows; returns algorithmic bytes
-    of the work done (packed rows + their scales + x + the outputs)."""
+    of the work done (packed rows + their scales + x + the outputs), or with
+    keep=True the outputs themselves."""
     import oracle
-    done = 0
+    done, ys = 0, []
     for lin, q, s, x in prepared:
         rows = np.arange(q.shape[0])
-        oracle.gemm_rows(x, q, s, rows)
+        y = oracle.gemm_rows(x, q, s, rows)
+        if keep:
+            ys.append(y)
         done += q.shape[0] * (lin.K // 2 + 2 * (lin.K // 128) + 2) + 2 * lin.K
-    return done
+    return ys if keep else done
 
 
 ORACLE_SAMPLE = ("{rows} sampled rows of each of the 5 decode shapes (M=1) per pass; "
                  "binary64 oracle, OpenMP over rows")
 
 
-def cpu_baseline(seconds: float, rows_per_shape: int = 64):
+def cpu_baseline(seconds: float, layers):
+    """The oracle timed on the host cores over the timed layers' sampled rows
+    (their master-weight rows quantized by the oracle itself, the layers' own
+    activations), and -- as a by-product, outside any timed region -- the
+    parity of the GPU outputs of the last timed step at those rows."""
     import oracle
-    prepared = oracle_inputs(rows_per_shape)
-    oracle_pass(prepared)
+    prepared = []
+    for l in layers:
+        w16 = l["W_rows"].contiguous().view(torch.int16).numpy().view(np.uint16)
+        q, s = oracle.quantize(w16)
+        x = l["x"].cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+        prepared.append((l["lin"], q, s, x))
+    ys = oracle_pass(prepared, keep=True)
+    worst_max, worst_l2 = 0.0, 0.0
+    for l, y_ref in zip(layers, ys):
+        y = l["y"][:, torch.from_numpy(l["rows"]).cuda()].float().cpu().numpy().astype(np.float64)
+        err = np.abs(y - y_ref)
+        worst_max = max(worst_max, float(err.max() / np.abs(y_ref).max()))
+        worst_l2 = max(worst_l2, float(np.linalg.norm(err) / np.linalg.norm(y_ref)))
+    parity = {"rows_per_layer": len(layers[0]["rows"]), "layers": len(layers),
+              "max_rel": round(worst_max, 6), "l2": round(worst_l2, 6),
+              "bar": {"max_rel": 2e-3, "l2": 1e-3},
+              "pass": bool(worst_max <= 2e-3 and worst_l2 <= 1e-3),
+              "how": "GPU y of the last timed step at sampled rows vs the binary64 oracle on the "
+                     "oracle's own quantization of the same master-weight rows (worst layer)"}
     done, passes = 0, 0
     t0 = time.perf_counter()
     while time.perf_counter() - t0 < seconds:
         done += oracle_pass(prepared)
         passes += 1
     secs = time.perf_counter() - t0
-    return {"value": round(done / secs / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
-            "kind": "oracle", "sample": f"{passes} passes: " + ORACLE_SAMPLE.format(rows=rows_per_shape),
+    rows = len(layers[0]["rows"])
+    base = {"value": round(done / secs / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "sample": f"{passes} passes: " + ORACLE_SAMPLE.format(rows=rows),
             "seconds": round(secs, 2)}
+    return base, parity
 
 
 def run_reference(args, rank, world):

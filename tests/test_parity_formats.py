@@ -55,6 +55,20 @@ def test_formats_every_row(w4lib, M, N, K, group, asym):
     assert w4.device_status() == 0
 
 
+@pytest.mark.parametrize("kind", synthetic.OFFSET_KINDS)
+@pytest.mark.parametrize("group,asym", [(32, False), (128, True), (w4.PER_CHANNEL, True)])
+@pytest.mark.parametrize("M", [1, 9, 16])
+def test_formats_offset_activations(w4lib, M, group, asym, kind):
+    """Activations with a large common offset (4 + N(0,1), |N(0,3)|, one group
+    of 468.75) on the variant decode GEMV, every row."""
+    N, K = 1000, 2048
+    q, s, z = quantized_fmt(N, K, 310, group, asym)
+    from gpu_util import bits16
+    x16 = bits16(synthetic.activations_offset(M, K, 311 + M, kind))
+    y = run_fmt(x16, q, s, z, group)
+    assert_close(y, oracle.gemm(x16, q, s, group, zeros=z), f"{kind} g={group} asym={asym} M={M}")
+
+
 @pytest.mark.parametrize("group,asym", FORMATS)
 @pytest.mark.parametrize("idx", range(len(workloads.LLAMA3_8B)))
 def test_formats_llama3_8b_m1(w4lib, idx, group, asym):

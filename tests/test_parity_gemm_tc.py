@@ -45,6 +45,15 @@ def test_shapes_and_tails(w4lib, M, N, K):
     assert_close(run_gemm(x16, q, s), oracle.gemm(x16, q, s), f"M={M} N={N} K={K}")
 
 
+@pytest.mark.parametrize("kind", synthetic.OFFSET_KINDS)
+@pytest.mark.parametrize("M,N,K", [(40, 1000, 1152), (300, 512, 4096)])
+def test_offset_activations(w4lib, kind, M, N, K):
+    """Activations with a large common offset, every output."""
+    w16, q, s = quantized(N, K, 75)
+    x16 = bits16(synthetic.activations_offset(M, K, 76, kind))
+    assert_close(run_gemm(x16, q, s), oracle.gemm(x16, q, s), f"{kind} M={M} N={N} K={K}")
+
+
 def test_every_nibble_value(w4lib):
     rng = np.random.default_rng(81)
     N, K, M = 384, 1024, 96

@@ -117,6 +117,41 @@ def test_persistent_tail_units_all_rows(w4lib, M, K, tail_rows):
     assert np.array_equal(run_gemm(x16, q, s), y)
 
 
+# The bias-64 decode feeds 64 + n / 16 and 64 + n to the MMAs and removes
+# 64.5 * sum(x) and 72 * sum(x) per group in FP32: its rounding grows with
+# |sum(x)| over a group.  Activations with a large common offset (real decode
+# activations are not zero-mean) on each kind of launch.
+OFFSET_CANDIDATES = {
+    "unit": [(4096, 4096), (6144, 4096), (1000, 2048), (16384, 2048), (8000, 1920), (16384, 1024),
+             (4096, 512)],
+    "split": [(264, 18944), (136, 18944), (1000, 1152), (4096, 4096), (4096, 14336)],
+    "persistent": [(50000, 1152), (70001, 1152)],
+}
+
+
+def _launch_of(plan) -> str:
+    if plan["blocks_per_cta"] > 1:
+        return "persistent"
+    if plan["splits"] > 1:
+        return "split"
+    return "unit" if plan["rows_per_cta"] < 128 else "whole"
+
+
+@pytest.mark.parametrize("kind", synthetic.OFFSET_KINDS)
+@pytest.mark.parametrize("M", [1, 9, 16])
+@pytest.mark.parametrize("launch", ["unit", "split", "persistent"])
+def test_offset_activations_all_rows(w4lib, kind, M, launch):
+    """The first candidate shape the planner launches this way, every row."""
+    shapes = [(N, K) for N, K in OFFSET_CANDIDATES[launch]
+              if _launch_of(w4.gemm_plan(M, N, K)) == launch]
+    assert shapes, (launch, M, [w4.gemm_plan(M, N, K) for N, K in OFFSET_CANDIDATES[launch]])
+    N, K = shapes[0]
+    w16, q, s = quantized(N, K, 81)
+    x16 = bits16(synthetic.activations_offset(M, K, 82 + M, kind))
+    assert_close(run_gemm(x16, q, s), oracle.gemm(x16, q, s),
+                 f"{kind} M={M} {launch} N={N} K={K} {w4.gemm_plan(M, N, K)}")
+
+
 # Launches made of sub-block units (16, 32 or 64 weight rows per CTA over the
 # whole K range): ragged row tails inside a tile, and K ranges that end in a
 # partial ring stage (K = 11008: 172 chunks; K = 1920: 30).

@@ -305,23 +305,6 @@ __device__ __forceinline__ void dequant8(uint32_t w, uint32_t (&r)[4]) {
     r[3] = *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Variant for the GEMV: all 8 nibbles OR-ed into the mantissa of 64.0
-// (0x5400, where the fp16 ulp is 1/16) with no further instruction.  The low
-// nibbles (positions 0..3 of each half, the fragment rows r0) read
-// 64 + n/16, the high nibbles (positions 4..7, rows r1) 64 + n, exactly
-// (n = q + 8).  An MMA over them carries 64 * sum(x) on both rows and the
-// 1/16 factor on rows r0; the caller removes both once per group:
-//   sum x q = 16 G0 - 1032 sum(x)   (rows r0),   G1 - 72 sum(x)   (rows r1).
-__device__ __forceinline__ void dequant8_bias64(uint32_t w, uint32_t (&r)[4]) {
-    constexpr uint32_t kMagic64 = 0x54005400u;       // (64.0, 64.0)
-    constexpr uint32_t kLut = (0xF0 & 0xCC) | 0xAA;  // (a & b) | c
-    const uint32_t w8 = w >> 8;
-    r[0] = lop3<kLut>(w, 0x000F000Fu, kMagic64);
-    r[1] = lop3<kLut>(w, 0x00F000F0u, kMagic64);
-    r[2] = lop3<kLut>(w8, 0x000F000Fu, kMagic64);
-    r[3] = lop3<kLut>(w8, 0x00F000F0u, kMagic64);
-}
-
 __device__ __forceinline__ float2 lds64f(uint32_t addr) {
     float2 v;
     asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));

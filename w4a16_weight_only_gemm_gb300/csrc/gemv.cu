@@ -17,13 +17,13 @@
 //    in the canonical layout) arrives the same way into one of two buffers,
 //    and the x slice of the CTA's K range once per thread block.
 //  * Consumers: per 64-wide chunk a lane reads 16 bytes of its tile, turns
-//    each 32-bit word into an mma.m16n8k16 A fragment with one lop3 per
-//    nibble pair (the nibbles OR-ed into the mantissa of 64.0: exact values
-//    64 + n/16 and 64 + n), and multiplies it with x fragments read from
-//    shared memory.  M <= 8 uses one n8 MMA per 16 k, M <= 16 two.  Every
-//    128-wide group accumulates in a fresh FP32 fragment; the group rescale
-//    removes the 64 and 1/16 with the group's x sums and applies the fp16
-//    scale: the products are exact and only FP32 sums round.
+//    each 32-bit word into an mma.m16n8k16 A fragment of exact codes
+//    q = n - 8 in fp16 (one lop3 per nibble pair OR-ing it into the mantissa
+//    of 1024.0, then one subtraction or fma per register), and multiplies it
+//    with x fragments read from shared memory.  M <= 8 uses one n8 MMA per
+//    16 k, M <= 16 two.  Every 128-wide group accumulates in fresh FP32
+//    fragments and is scaled once by its fp16 scale: the products are exact
+//    and only FP32 sums round.
 //  * Work split, chosen per shape by a launch-time model: sub-block units
 //    (the warps of a tile add their partial sums in shared memory, in a
 //    fixed order); or whole blocks with the K range split over the S CTAs of
@@ -90,38 +90,32 @@ struct GemvArgs {
     // blocks from tail_base on run as tail_units sub-block units of tail_T
     // tiles (tail_T = 0: no tail), unit u on CTA u after its whole blocks.
     int tail_T, tail_base, tail_units;
-    uint32_t off_ring, off_x, off_s, off_red, off_sx;
+    uint32_t off_ring, off_x, off_s, off_red;
 };
 
 __device__ __forceinline__ int split_group_begin(int split, int S, int G) {
     return (int)(((long long)split * G) / S);
 }
 
-// One 128-wide group (two chunks) of one consumer lane: 8 MMAs into a fresh
-// FP32 fragment, then scaled into acc.
+// One 128-wide group (two chunks) of one consumer lane: 8 MMAs into fresh
+// FP32 fragments, then scaled into acc.  The A fragments hold the exact codes
+// q = n - 8 in fp16 (dequant8), so every product q * x is exact and the FP32
+// sums carry only the group's own dot product.  (Feeding 64 + n and removing
+// 64 * sum(x) afterwards is cheaper by 4 instructions per 8 weights, but the
+// MMA adds its products at the precision of the running sum: activations with
+// a large common offset make that sum ~64 sum(x) and lose the dot product's
+// low bits, beyond the accuracy bar for x = 4 + N(0, 1).)
 template <int MT>
 __device__ __forceinline__ void mma_group(uint32_t w_addr, uint32_t cs, uint32_t x0_addr,
-                                          uint32_t x1_addr, uint32_t sx_addr, float s0, float s1,
+                                          uint32_t x1_addr, float s0, float s1,
                                           float (&acc)[MT][4]) {
     // M <= 8: one FP32 fragment per chunk -- two independent MMA chains per
     // group halve the dependent-latency path of a lane (M <= 16 has two
     // chains already, one per n8 tile, and no registers to spare).
     constexpr int NCH = MT == 1 ? 2 : 1;
-    // Chain 0 starts from the group's bias, -64.5 Sx (rows r0) and -72 Sx
-    // (rows r1), so the MMAs themselves remove it; further chains from zero.
     float g[NCH][MT][4];
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-        const float2 sx = lds64f(sx_addr + mt * 32);
-        const float2 c0 = __fmul2_rn(make_float2(-64.5f, -64.5f), sx);
-        const float2 c1 = __fmul2_rn(make_float2(-72.0f, -72.0f), sx);
-        g[0][mt][0] = c0.x;
-        g[0][mt][1] = c0.y;
-        g[0][mt][2] = c1.x;
-        g[0][mt][3] = c1.y;
-    }
-#pragma unroll
-    for (int c = 1; c < NCH; ++c)
+    for (int c = 0; c < NCH; ++c)
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -142,18 +136,15 @@ __device__ __forceinline__ void mma_group(uint32_t w_addr, uint32_t cs, uint32_t
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
             uint32_t af[4];
-            dequant8_bias64(wrd[s], af);
+            dequant8(wrd[s], af);
             mma_16816(g[c % NCH][0], af, b0[2 * s], b0[2 * s + 1], g[c % NCH][0]);
             if (MT == 2)
                 mma_16816(g[c % NCH][MT - 1], af, b1[2 * s], b1[2 * s + 1], g[c % NCH][MT - 1]);
         }
     }
     // The rescale runs on (column 2t, 2t + 1) pairs through the packed binary32
-    // instructions; each component rounds as the scalar fma.  Rows r0 fed
-    // 64 + n/16 and rows r1 fed 64 + n (dequant8_bias64), their chains
-    // started from the bias, give 16 s0 (G0 - 64.5 Sx) and s1 (G1 - 72 Sx)
-    // over the group's x sums Sx.
-    const float2 s00 = make_float2(16.0f * s0, 16.0f * s0), s11 = make_float2(s1, s1);
+    // instructions; each component rounds as the scalar fma.
+    const float2 s00 = make_float2(s0, s0), s11 = make_float2(s1, s1);
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
         float2 v01 = make_float2(g[0][mt][0], g[0][mt][1]);
@@ -197,7 +188,7 @@ __device__ __forceinline__ void store_y(const GemvArgs& a, int R0, int R1, int t
 template <int MT>
 __device__ __forceinline__ bool unit_stages(const GemvArgs& a, uint32_t sbase, int nstg, int ng,
                                             int GPS, int ks, uint32_t wl, uint32_t cs, uint32_t x0,
-                                            uint32_t x1, uint32_t sxl, const __half* sc0,
+                                            uint32_t x1, const __half* sc0,
                                             const __half* sc1, int lane, int& slot, uint32_t& phase,
                                             float (&acc)[MT][4]) {
     const int NS = a.nstages;
@@ -211,13 +202,11 @@ __device__ __forceinline__ bool unit_stages(const GemvArgs& a, uint32_t sbase, i
 #pragma unroll
             for (int gi = 0; gi < kGroupsPerWarpStage; ++gi)
                 mma_group<MT>(wa + gi * 2 * cs, cs, x0 + (gl0 + gi) * 256, x1 + (gl0 + gi) * 256,
-                              sxl + (gl0 + gi) * 64, __half2float(sc0[gl0 + gi]),
-                              __half2float(sc1[gl0 + gi]), acc);
+                              __half2float(sc0[gl0 + gi]), __half2float(sc1[gl0 + gi]), acc);
         } else {
             for (int gi = 0; gi < kGroupsPerWarpStage && gsl0 + gi < gs; ++gi)
                 mma_group<MT>(wa + gi * 2 * cs, cs, x0 + (gl0 + gi) * 256, x1 + (gl0 + gi) * 256,
-                              sxl + (gl0 + gi) * 64, __half2float(sc0[gl0 + gi]),
-                              __half2float(sc1[gl0 + gi]), acc);
+                              __half2float(sc0[gl0 + gi]), __half2float(sc1[gl0 + gi]), acc);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(sbase + kBarEmpty + 8 * slot);
@@ -276,7 +265,7 @@ __device__ __forceinline__ void unit_reduce_store(const GemvArgs& a, uint8_t* sm
 template <int MT>
 __device__ __noinline__ bool tail_unit_consume(const GemvArgs& a, uint8_t* smem, uint32_t sbase,
                                                uint32_t ring, int nblk, int nck, int ng, int g0,
-                                               uint32_t x0, uint32_t x1, uint32_t sxl, int slot,
+                                               uint32_t x0, uint32_t x1, int slot,
                                                uint32_t phase, bool ok) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
@@ -301,7 +290,7 @@ __device__ __noinline__ bool tail_unit_consume(const GemvArgs& a, uint8_t* smem,
     if (ok) {
         const __half* tsc0 =
             reinterpret_cast<const __half*>(smem + a.off_s + sbuf * a.slab_bytes) + tr0 * a.G + g0;
-        if (!unit_stages<MT>(a, sbase, tnstg, ng, tCPS / 2, ks2, twl, tcs, x0, x1, sxl, tsc0,
+        if (!unit_stages<MT>(a, sbase, tnstg, ng, tCPS / 2, ks2, twl, tcs, x0, x1, tsc0,
                              tsc0 + 8 * a.G, lane, slot, phase, tacc))
             ok = false;
     }
@@ -631,40 +620,6 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const GemvArg
         const uint32_t wl = ring + ti * kTileBytes + lane * 16;
 
         bool ok = mbar_wait(sbase + kBarX, 0, a.timeout_ns, a.status);
-        // Activation sums per group and row, Sx[gl][m] in FP32, for the bias
-        // correction of dequant8_bias64: 8 threads per (group, row), 16
-        // values each, combined with xor-shuffles in a fixed order.
-        {
-            float* sxw = reinterpret_cast<float*>(smem + a.off_sx);
-            const int total = ng * a.M * 8;
-            for (int base = 0; base < total; base += kConsumers) {
-                const int task = base + (int)threadIdx.x;
-                const int e = task >> 3, gl = e / a.M, m = e - gl * a.M;
-                float sum = 0.0f;
-                if (ok && task < total) {
-                    // 16 values as 8 pairs, summed by a tree of packed
-                    // binary32 adds (depth 4), then the pair's two halves
-                    const uint32_t src = sbase + a.off_x + m * a.xs_stride + gl * 256 + (task & 7) * 32;
-                    const uint4 p[2] = {lds128(src), lds128(src + 16)};
-                    const uint32_t wv[8] = {p[0].x, p[0].y, p[0].z, p[0].w, p[1].x, p[1].y, p[1].z, p[1].w};
-                    float2 f[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        f[i] = __half22float2(*reinterpret_cast<const __half2*>(&wv[i]));
-#pragma unroll
-                    for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-                        for (int i = 0; i < w; ++i) f[i] = __fadd2_rn(f[i], f[i + w]);
-                    sum = f[0].x + f[0].y;
-                }
-                sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-                sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-                sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-                if (task < total && (task & 7) == 0) sxw[gl * 16 + m] = sum;
-            }
-            asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-        }
-        const uint32_t sxl = sbase + a.off_sx + t * 8;  // this lane's columns 2t, 2t + 1
         const int NS = a.nstages;
         int slot = 0;
         uint32_t phase = 0;  // parity of the ring's current pass
@@ -702,7 +657,7 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const GemvArg
                     for (int gi = 0; gi < 2; ++gi) {
                         const int gl = st * 2 + gi;
                         mma_group<MT>(wa + gi * 2 * kChunkBytes, kChunkBytes, x0 + xs_off + gi * 256,
-                                      x1 + xs_off + gi * 256, sxl + gl * 64, __half2float(sc0[gl]),
+                                      x1 + xs_off + gi * 256, __half2float(sc0[gl]),
                                       __half2float(sc1[gl]), acc);
                     }
                     __syncwarp();
@@ -718,7 +673,7 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const GemvArg
                     } else {
                         const int gl = nfull * 2;
                         mma_group<MT>(wl + slot * kStageBytes, kChunkBytes, x0 + xs_off, x1 + xs_off,
-                                      sxl + gl * 64, __half2float(sc0[gl]), __half2float(sc1[gl]),
+                                      __half2float(sc0[gl]), __half2float(sc1[gl]),
                                       acc);
                         __syncwarp();
                         if (lane == 0) mbar_arrive(sbase + kBarEmpty + 8 * slot);
@@ -731,7 +686,7 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const GemvArg
             } else {
                 // Sub-block units: a stage holds GPS groups of T tiles; the W
                 // warps of a tile take two groups each.
-                if (!unit_stages<MT>(a, sbase, nstg, ng, GPS, ks, wl, cs, x0, x1, sxl, sc0, sc1, lane,
+                if (!unit_stages<MT>(a, sbase, nstg, ng, GPS, ks, wl, cs, x0, x1, sc0, sc1, lane,
                                      slot, phase, acc))
                     ok = false;
             }
@@ -769,7 +724,7 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const GemvArg
                                   block_of(0) * kBlockRows + t0 * 16, row0, row1, t);
         } else {
             if (has_tail())
-                ok = tail_unit_consume<MT>(a, smem, sbase, ring, nblk, nck, ng, g0, x0, x1, sxl, slot,
+                ok = tail_unit_consume<MT>(a, smem, sbase, ring, nblk, nck, ng, g0, x0, x1, slot,
                                            phase, ok);
         }
         if (!ok) *abort_flag = 1;
@@ -823,7 +778,7 @@ struct GemvPlan {
     int slab_bytes = 0;
     int rpo = 0;
     int tail_T = 0, tail_base = 0, tail_units = 0;  // persistent launches: last-round units
-    uint32_t off_ring = 0, off_x = 0, off_s = 0, off_red = 0, off_sx = 0, smem = 0;
+    uint32_t off_ring = 0, off_x = 0, off_s = 0, off_red = 0, smem = 0;
     double cost = 0.0;
 };
 
@@ -894,8 +849,7 @@ bool layout(GemvPlan& p, int M, int G, int S, int T, int nsb, const DeviceCtx& c
     const int red_bytes = S > 1 ? S * p.rpo * 16 * 4
                           : T < kConsumerWarps || nsb == 2 ? kConsumerWarps * MT * 32 * 16
                                                            : 0;
-    p.off_sx = p.off_red + red_bytes;
-    p.smem = p.off_sx + ng_max * 16 * 4;
+    p.smem = p.off_red + red_bytes;
     return (int)p.smem <= ctx.max_smem_optin;
 }
 
@@ -1091,7 +1045,6 @@ cudaError_t launch_gemv_mt(GemvArgs args, int M, cudaStream_t stream, const Devi
     args.off_x = p.off_x;
     args.off_s = p.off_s;
     args.off_red = p.off_red;
-    args.off_sx = p.off_sx;
     args.rpo = p.rpo;
     args.T = p.T;
     args.tail_T = p.tail_T;

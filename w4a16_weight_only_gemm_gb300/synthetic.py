@@ -43,6 +43,33 @@ def activations(M: int, K: int, seed: int, device: str = "cpu") -> torch.Tensor:
     return torch.randn(M, K, generator=g, dtype=torch.float32, device=device).half()
 
 
+# Activation laws with a large common offset, as real decode activations have
+# (they are not zero-mean): the group sums of x are then far from 0.
+OFFSET_KINDS = ("shift4", "abs3", "big_group")
+
+
+def activations_offset(M: int, K: int, seed: int, kind: str, device: str = "cpu") -> torch.Tensor:
+    """fp16 [M, K] activations with a common offset:
+
+    * ``shift4``: 4 + N(0, 1);
+    * ``abs3``: |N(0, 3)| (all positive, like the output of a SiLU gate);
+    * ``big_group``: N(0, 1) with the first 128 values of every row set to
+      60000 / 128 = 468.75 (one group summing to 60000, still finite in fp16).
+    """
+    g = torch.Generator(device=device).manual_seed(seed)
+    z = torch.randn(M, K, generator=g, dtype=torch.float32, device=device)
+    if kind == "shift4":
+        x = z + 4.0
+    elif kind == "abs3":
+        x = (z * 3.0).abs()
+    elif kind == "big_group":
+        x = z.clone()
+        x[:, :128] = 60000.0 / 128.0
+    else:
+        raise ValueError(f"unknown activation kind {kind!r}")
+    return x.half()
+
+
 # Base seed of each workload; tensor i of a workload uses seed_W = base + 10*i
 # and seed_x = seed_W + 2.  The single 4096x4096 GEMV uses (0, 2).
 WORKLOAD_SEED_BASE = {
