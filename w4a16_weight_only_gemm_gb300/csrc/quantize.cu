@@ -7,14 +7,19 @@
 //   q   = clamp(round_half_even(fl(w / s32)), -8, 7)  (fl: IEEE division),
 //   scale = fp16(s32) rounded to nearest even, byte = (q_odd+8)<<4 | (q_even+8).
 //
-// One half-warp per group: each of the 16 lanes loads 8 fp16 values with a
-// single 16-byte load, the absmax is reduced with xor-shuffles inside the
-// half-warp, and each lane writes its 4 packed bytes (the group's 64 bytes
-// are one coalesced segment).  Each half-warp issues the loads of four
-// groups before quantizing them, and the grid is one resident wave.  256 B
-// are read and 66 B written per group; the per-element work (fma-rounding,
-// its residual, the tie test) runs on pairs through the packed binary32
-// instructions, about two instructions per element.
+// One team of 8 lanes per group: each lane loads 16 fp16 values with two
+// 16-byte loads, the absmax is reduced with three xor-shuffles inside the
+// team, and each lane writes its 8 packed bytes (the group's 64 bytes are one
+// coalesced segment).  The per-group scalar work (reduction, scale, its
+// reciprocal) is shared by 16 elements a lane.  A team issues the loads of
+// its next group before quantizing the current one (software pipelining in
+// registers: 30.5 -> 28.7 us on [14336, 4096]; more groups per iteration raise
+// register pressure and were slower), and the grid is one resident wave.
+// 256 B are read and 66 B written per group; the per-element work
+// (fma-rounding, its residual, the tie test) runs on pairs through the packed
+// binary32 instructions, about two instructions per element.
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -22,7 +27,8 @@ namespace w4a16 {
 namespace {
 
 constexpr int kQuantThreads = 256;
-constexpr int kQuantUnroll = 4;  // groups per half-warp per iteration, loads issued together
+constexpr int kQuantTeam = 8;    // lanes per group, 16 weights each
+constexpr int kQuantUnroll = 1;  // groups per team per iteration (the next ones' loads are in flight)
 
 // s32 = RN(a / 7) for an fp16 absmax a, by Markstein's theorem on FMA
 // division (P. Markstein, IBM J. Res. Dev. 34(1), 1990): with y = RN(1/7)
@@ -49,7 +55,7 @@ __device__ __forceinline__ float rcp_nr(float s) {
 // leaves q + 8 in the low 4 bits of the sum.
 constexpr float kRound = 12582920.0f;
 
-// Quantizes one group held as 8 fp16 values per lane of a half-warp.
+// Quantizes one group held as 16 fp16 values per lane of an 8-lane team.
 //
 // q = round_half_even(fl(w / s)) is formed from the exact product w * y of
 // the refined reciprocal, rounded by the fma with kRound: |w y - w / s| <=
@@ -59,23 +65,26 @@ constexpr float kRound = 12582920.0f;
 // sees that (exact ties included) the warp takes the correctly rounded
 // divide for all its elements.  No clamp is needed: s >= (max|w| / 7)(1 -
 // 2^-24) bounds |w / s| below 7.5, so q already lies in [-7, 7].
-__device__ __forceinline__ void quantize_group(const uint4 raw, uint32_t& packed, float& scale) {
-    const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+// packed[0] holds the lane's elements 0..7 (element 2j in the low nibble of
+// byte j), packed[1] elements 8..15.
+__device__ __forceinline__ void quantize_group(const uint4 (&raw)[2], uint32_t (&packed)[2],
+                                               float& scale) {
+    const __half2* h2 = reinterpret_cast<const __half2*>(&raw[0]);  // 8 pairs (raw is contiguous)
     __half2 m2 = __habs2(h2[0]);
 #pragma unroll
-    for (int i = 1; i < 4; ++i) m2 = __hmax2(m2, __habs2(h2[i]));
+    for (int i = 1; i < 8; ++i) m2 = __hmax2(m2, __habs2(h2[i]));
     float amax = fmaxf(__low2float(m2), __high2float(m2));
 #pragma unroll
-    for (int off = 8; off > 0; off >>= 1)
+    for (int off = kQuantTeam / 2; off > 0; off >>= 1)
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
 
     float s = div7_rn(amax);
     if (s < 1e-8f) s = 1e-8f;
     const float y = rcp_nr(s);
 
-    float w[8], t[8];
+    float w[16], t[16];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 8; ++i) {
         const float2 f = __half22float2(h2[i]);
         w[2 * i] = f.x;
         w[2 * i + 1] = f.y;
@@ -93,7 +102,7 @@ __device__ __forceinline__ void quantize_group(const uint4 raw, uint32_t& packed
     const float2 ntie2 = make_float2(-kTieSq, -kTieSq);
     uint32_t clear_bits = 0xffffffffu;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 8; ++i) {
         const float2 wv = make_float2(w[2 * i], w[2 * i + 1]);
         const float2 tv = __ffma2_rn(wv, y2, kr2);
         const float2 d = __ffma2_rn(wv, ny2, __fadd2_rn(tv, nkr2));  // q - w y
@@ -104,47 +113,66 @@ __device__ __forceinline__ void quantize_group(const uint4 raw, uint32_t& packed
     }
     if (__any_sync(0xffffffffu, (clear_bits >> 31) == 0)) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) t[i] = __fadd_rn(__fdiv_rn(w[i], s), kRound);
+        for (int i = 0; i < 16; ++i) t[i] = __fadd_rn(__fdiv_rn(w[i], s), kRound);
     }
     // Each t holds 0x4B400000 + (q + 8): sum t_i 16^i (Horner, integer
     // multiply-adds) and remove the constant part once; the nibbles q + 8
     // occupy disjoint bits, so no carries cross between them.
-    uint32_t acc = __float_as_uint(t[7]);
 #pragma unroll
-    for (int i = 6; i >= 0; --i) acc = acc * 16u + __float_as_uint(t[i]);
-    packed = acc - 0x4B400000u * 0x11111111u;
+    for (int h = 0; h < 2; ++h) {
+        uint32_t acc = __float_as_uint(t[8 * h + 7]);
+#pragma unroll
+        for (int i = 6; i >= 0; --i) acc = acc * 16u + __float_as_uint(t[8 * h + i]);
+        packed[h] = acc - 0x4B400000u * 0x11111111u;
+    }
     scale = s;
 }
 
 __global__ void __launch_bounds__(kQuantThreads)
     quantize_kernel(const uint4* __restrict__ W, int64_t groups_total,
-                    uint32_t* __restrict__ qweight, __half* __restrict__ scales) {
-    const int lane16 = threadIdx.x & 15;
-    const int64_t stride = (int64_t)gridDim.x * (kQuantThreads / 16);
+                    uint2* __restrict__ qweight, __half* __restrict__ scales) {
+    constexpr int kTeams = kQuantThreads / kQuantTeam;
+    const int tl = threadIdx.x & (kQuantTeam - 1);
+    const int64_t stride = (int64_t)gridDim.x * kTeams;
     // group `grp` = row grp / G, group grp % G; its 128 halves are contiguous
-    // at element offset grp * 128 of the row-major matrix.  The two
-    // half-warps of a warp differ only in bit 0 of g0 (stride is a multiple
-    // of 16), so the loop test on g0 with that bit cleared is warp-uniform
-    // and the full-warp shuffles always see every lane; groups past the end
-    // load nothing and store nothing.
-    for (int64_t g0 = (int64_t)blockIdx.x * (kQuantThreads / 16) + (threadIdx.x >> 4);
-         (g0 & ~(int64_t)1) < groups_total; g0 += kQuantUnroll * stride) {
-        uint4 raw[kQuantUnroll];
+    // at element offset grp * 128 of the row-major matrix (16 uint4; lane tl
+    // takes 2 tl and 2 tl + 1).  The four teams of a warp differ only in the
+    // low two bits of g0 (stride is a multiple of 4), so the loop test on g0
+    // with those bits cleared is warp-uniform and the full-warp shuffles always
+    // see every lane; groups past the end load nothing and store nothing.
+    int64_t g0 = (int64_t)blockIdx.x * kTeams + (threadIdx.x / kQuantTeam);
+    uint4 raw[kQuantUnroll][2];
+#pragma unroll
+    for (int u = 0; u < kQuantUnroll; ++u) {
+        const int64_t grp = g0 + u * stride;
+        const bool live = grp < groups_total;
+        raw[u][0] = live ? __ldcs(W + grp * 16 + 2 * tl) : make_uint4(0, 0, 0, 0);
+        raw[u][1] = live ? __ldcs(W + grp * 16 + 2 * tl + 1) : make_uint4(0, 0, 0, 0);
+    }
+    for (; (g0 & ~(int64_t)3) < groups_total; g0 += kQuantUnroll * stride) {
+        uint4 nxt[kQuantUnroll][2];  // the next iteration's groups, loading meanwhile
 #pragma unroll
         for (int u = 0; u < kQuantUnroll; ++u) {
-            const int64_t grp = g0 + u * stride;
-            raw[u] = grp < groups_total ? __ldcs(W + grp * 16 + lane16) : make_uint4(0, 0, 0, 0);
+            const int64_t grp = g0 + (kQuantUnroll + u) * stride;
+            const bool live = grp < groups_total;
+            nxt[u][0] = live ? __ldcs(W + grp * 16 + 2 * tl) : make_uint4(0, 0, 0, 0);
+            nxt[u][1] = live ? __ldcs(W + grp * 16 + 2 * tl + 1) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int u = 0; u < kQuantUnroll; ++u) {
             const int64_t grp = g0 + u * stride;
-            uint32_t packed;
+            uint32_t packed[2];
             float sc;
             quantize_group(raw[u], packed, sc);
             if (grp < groups_total) {
-                qweight[grp * 16 + lane16] = packed;
-                if (lane16 == 0) scales[grp] = __float2half_rn(sc);
+                qweight[grp * kQuantTeam + tl] = make_uint2(packed[0], packed[1]);
+                if (tl == 0) scales[grp] = __float2half_rn(sc);
             }
+        }
+#pragma unroll
+        for (int u = 0; u < kQuantUnroll; ++u) {
+            raw[u][0] = nxt[u][0];
+            raw[u][1] = nxt[u][1];
         }
     }
     // Publish the packed weights and scales device-wide before this block
@@ -308,24 +336,24 @@ cudaError_t launch_quantize(const void* W, int64_t N, int64_t K, void* qweight, 
                             cudaStream_t stream, const DeviceCtx& ctx) {
     const int G = (int)(K / kGroup);
     const int64_t groups = N * G;
-    const int64_t per_block = kQuantThreads / 16;
+    const int64_t per_block = kQuantThreads / kQuantTeam;
     int64_t blocks = (groups + per_block - 1) / per_block;
-    static int occ[64] = {};  // resident blocks per SM, per device (one resident wave)
+    static std::atomic<int> occ[64];  // resident blocks per SM, per device (one resident wave)
     int dev = 0;
     cudaGetDevice(&dev);
-    int per_sm = (dev >= 0 && dev < 64) ? occ[dev] : 0;
+    int per_sm = (dev >= 0 && dev < 64) ? occ[dev].load(std::memory_order_relaxed) : 0;
     if (per_sm == 0) {
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quantize_kernel, kQuantThreads,
                                                           0) != cudaSuccess ||
             per_sm < 1)
             per_sm = 1;
-        if (dev >= 0 && dev < 64) occ[dev] = per_sm;
+        if (dev >= 0 && dev < 64) occ[dev].store(per_sm, std::memory_order_relaxed);
     }
     const int64_t cap = (int64_t)ctx.num_sms * per_sm;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     quantize_kernel<<<(unsigned)blocks, kQuantThreads, 0, stream>>>(
-        static_cast<const uint4*>(W), groups, static_cast<uint32_t*>(qweight),
+        static_cast<const uint4*>(W), groups, static_cast<uint2*>(qweight),
         static_cast<__half*>(scales));
     return cudaGetLastError();
 }
