@@ -168,16 +168,48 @@ def pin_amax_maps_to_seven(o) -> None:
     assert np.abs(qv).max() == 7
 
 
+def _round_exact(x, frac_bits: int, min_exp: int):
+    """Round a non-negative Fraction to the nearest binary floating-point value
+    with `frac_bits` fraction bits and minimum normal exponent `min_exp`
+    (ties to even), in exact rational arithmetic; returns a Fraction."""
+    from fractions import Fraction
+    if x == 0:
+        return Fraction(0)
+    e = x.numerator.bit_length() - x.denominator.bit_length()
+    while Fraction(2) ** e > x:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= x:
+        e += 1
+    quantum = Fraction(2) ** (max(e, min_exp) - frac_bits)
+    m = x / quantum
+    lo = m.numerator // m.denominator
+    rem = m - lo
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and lo % 2 == 1):
+        lo += 1
+    return lo * quantum
+
+
 def pin_scale_is_fp16_of_amax_over_7(o) -> None:
-    """Stored scale == numpy fp16(max(fp32(amax) / fp32(7), fp32(1e-8)))."""
-    rng = np.random.default_rng(8)
-    w16 = _random_weights(rng, 32, 2048)
-    w16[3, :GROUP] = 0
-    w16[5, GROUP:2 * GROUP] = 0x0001
+    """For every finite non-negative fp16 absmax a (31,744 groups, one each),
+    the stored scale is binary16-RNE of max(binary32-RNE(a / 7), binary32-RNE
+    (1e-8)) -- the tutorial §3 reading (fp32 arithmetic, fp16 scale at the
+    end) -- evaluated here in exact rational arithmetic, not with hardware
+    division."""
+    from fractions import Fraction
+    amax_bits = np.arange(0, 0x7C00, dtype=np.uint16)
+    n = amax_bits.size
+    w16 = np.zeros((n, GROUP), dtype=np.uint16)
+    w16[:, 5] = amax_bits
+    w16[:, 77] = amax_bits ^ 0x8000  # the same magnitude negative
     _, s = o.quantize(w16, GROUP)
-    a = np.abs(w16.view(np.float16).astype(np.float32)).reshape(32, -1, GROUP).max(-1)
-    ref = np.maximum(a / np.float32(7.0), np.float32(1e-8)).astype(np.float16).view(np.uint16)
-    assert np.array_equal(s, ref)
+    floor32 = _round_exact(Fraction(1, 10 ** 8), 23, -126)
+    want = np.empty(n, dtype=np.uint16)
+    for i, b in enumerate(amax_bits.tolist()):
+        a = Fraction(np.uint16(b).view(np.float16).item())
+        s32 = max(_round_exact(a / 7, 23, -126), floor32)
+        s16 = _round_exact(s32, 10, -14)
+        want[i] = np.float16(float(s16)).view(np.uint16)  # exact: s16 is an fp16 value
+    np.testing.assert_array_equal(s[:, 0], want)
 
 
 def pin_nearest_level_brute_force(o) -> None:
