@@ -301,10 +301,12 @@ enum { W4A16_PATH_GEMV = 1, W4A16_PATH_TENSOR_CORE = 2 };
  *   *ctas            CTAs launched.
  *   *blocks_per_cta  most 128-row blocks one CTA walks (> 1: persistent).
  *   *rows_per_cta    weight rows one CTA computes of each block it handles:
- *                    128 (a whole block; the tensor-core GEMM always), or for
- *                    the GEMV 16, 32 or 64 (1, 2 or 4 of a block's 16-row
- *                    tiles over the whole K range, the CTA's warps splitting
- *                    K and reducing in its own shared memory).
+ *                    128 (a whole block), or for the GEMV 16, 32 or 64 (1, 2
+ *                    or 4 of a block's 16-row tiles over the whole K range,
+ *                    the CTA's warps splitting K and reducing in its own
+ *                    shared memory), or for the tensor-core GEMM's CTA pairs
+ *                    with two x tiles 96 (six 16-row tiles; a pair covers 192
+ *                    weight rows).
  * Errors: NULL output -> W4A16_ERR_NULL; bad M, N, K -> W4A16_ERR_SHAPE;
  *         no supported device -> W4A16_ERR_DEVICE / W4A16_ERR_CUDA.
  */

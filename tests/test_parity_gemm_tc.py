@@ -45,6 +45,33 @@ def test_shapes_and_tails(w4lib, M, N, K):
     assert_close(run_gemm(x16, q, s), oracle.gemm(x16, q, s), f"M={M} N={N} K={K}")
 
 
+@pytest.mark.parametrize("M,N,K", [(300, 14336, 1152), (512, 14336, 512), (300, 2000, 18944),
+                                   (512, 4096, 14336), (290, 977, 4096)])
+def test_pairs_of_96_row_ctas(w4lib, M, N, K):
+    """CTA pairs with two x tiles and 96 weight rows per CTA (N = 192 MMAs;
+    a CTA's six tiles straddle kernel-layout blocks in two of every four
+    CTAs), with and without a K split over the cluster; ragged N leaves the
+    last CTAs partly or wholly past N.  Every output, and a repeat call is
+    bit-identical."""
+    plan = w4.gemm_plan(M, N, K)
+    if plan["rows_per_cta"] != 96:
+        pytest.skip(f"planner chose {plan} for this shape on this device")
+    w16, q, s = quantized(N, K, 73)
+    x16 = acts(M, K, 74)
+    y = run_gemm(x16, q, s)
+    assert_close(y, oracle.gemm(x16, q, s), f"M={M} N={N} K={K} {plan}")
+    assert np.array_equal(run_gemm(x16, q, s), y)
+
+
+def test_pairs_of_96_row_ctas_covered(w4lib):
+    """The cases above reach the 96-row CTAs both unsplit and split."""
+    plans = [w4.gemm_plan(M, N, K) for M, N, K in
+             [(300, 14336, 1152), (512, 14336, 512), (300, 2000, 18944), (512, 4096, 14336),
+              (290, 977, 4096)]]
+    picked = [p for p in plans if p["rows_per_cta"] == 96]
+    assert any(p["splits"] == 2 for p in picked) and any(p["splits"] > 2 for p in picked), plans
+
+
 @pytest.mark.parametrize("kind", synthetic.OFFSET_KINDS)
 @pytest.mark.parametrize("M,N,K", [(40, 1000, 1152), (300, 512, 4096)])
 def test_offset_activations(w4lib, kind, M, N, K):

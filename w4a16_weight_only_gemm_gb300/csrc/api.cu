@@ -269,10 +269,9 @@ int w4a16_gemm_plan(int64_t M, int64_t N, int64_t K, int* path, int* splits, int
     if (int rc = device_ctx(&ctx)) return rc;
     if (M > 16) {
         *path = W4A16_PATH_TENSOR_CORE;
-        gemm_tc_plan_info(M, N, K, ctx, splits, ctas);
+        gemm_tc_plan_info(M, N, K, ctx, splits, ctas, false, rows_per_cta);
         if (*splits == 0) return W4A16_ERR_CUDA;
         *blocks_per_cta = 1;
-        *rows_per_cta = 128;
         return W4A16_OK;
     }
     int tail_rows = 0, tail_units = 0;

@@ -50,9 +50,7 @@ constexpr int kTileX = 128;                     // activation rows per tile (MMA
 constexpr int kBK = kChunkK;                    // 64: one kernel-layout chunk
 constexpr int kMaxStages = 6;                   // ring: x tile, packed and dequantised weights
 constexpr int kSingleStages = 4;                // ring of the single-CTA tile
-constexpr int kAStageBytes = kTileW * kBK * 2;  // 16 KB fp16, 128B-swizzled
 constexpr int kXStageBytes = kTileX * kBK * 2;  // 16 KB
-constexpr int kWStageBytes = kTileW * kBK / 2;  // 4 KB packed
 
 constexpr int kBarLoadFull = 0;                      // [stages] x + packed weights landed
 constexpr int kBarAFull = kBarLoadFull + 8 * kMaxStages;  // [stages] dequantised tile written
@@ -215,7 +213,12 @@ __device__ __forceinline__ uint32_t swz128(int r, int c) {
 // instead (the decode kernel's placement) re-scaled every x tile once per
 // weight-block column and added half again to the shared-memory traffic of a
 // k-block: 30 % slower at M = 512.
-template <bool PAIR, int XT, bool FMT = false>
+// TW: weight rows per CTA, 128 (a kernel-layout block) or, for CTA pairs with
+// two x tiles, 96 (six 16-row tiles: a pair covers 192 weight rows with
+// N = 192 MMAs, so N = 14336 fills 150 CTAs instead of 112).  A CTA's tiles
+// are tiles TW x / 16 .. + TW / 16 - 1 of the layout, at most two contiguous
+// runs of each 64-wide chunk (one per 128-row block they touch).
+template <bool PAIR, int XT, bool FMT = false, int TW = kTileW>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap smap,
                    const __grid_constant__ TcArgs a) {
@@ -227,7 +230,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortFlag);
 
     static_assert(XT == 1 || (PAIR && XT == 2), "two x tiles per stage need CTA pairs");
-    constexpr uint32_t kCols = PAIR ? 2 * kTileW * XT : kTileW;  // accumulator columns
+    static_assert(TW == kTileW || (PAIR && XT == 2 && TW == 96), "96-row CTAs: pairs, two x tiles");
+    constexpr int kAStg = TW * kBK * 2;   // dequantised weight tile of a stage
+    constexpr int kWStg = TW * kBK / 2;   // packed weights of a stage
+    constexpr int kTilesW = TW / 16;      // 16-row tiles of this CTA
+    constexpr uint32_t kCols = PAIR ? 2 * TW * XT : TW;  // accumulator columns
+    // tensor memory is allocated in powers of two
+    constexpr uint32_t kAlloc = kCols <= 128 ? 128 : kCols <= 256 ? 256 : 512;
     constexpr int kXBytes = XT * kXStageBytes;                     // x bytes per stage
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -239,11 +248,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const bool leader = rank == 0;
     const uint16_t pair_mask = (uint16_t)(3u << lead);
     // This CTA's 128-row weight block and first x row; y columns start at n_out.
-    const int rb = PAIR ? (int)blockIdx.x : (int)blockIdx.x;
-    const int n_out = PAIR ? ((int)blockIdx.x >> 1) * 2 * kTileW : (int)blockIdx.x * kTileW;
+    const int r_start = (int)blockIdx.x * TW;  // first weight row of this CTA
+    const int n_out = PAIR ? ((int)blockIdx.x >> 1) * 2 * TW : (int)blockIdx.x * TW;
     const int m0 = PAIR ? (int)blockIdx.y * 2 * kTileX * XT + rank * kTileX : (int)blockIdx.y * kTileX;
     const int NB = (a.N + kTileW - 1) / kTileW;
-    const bool wvalid = rb < NB;  // the odd CTA of the last pair may hold no weights
+    const bool wvalid = r_start < a.N;  // the odd CTA of the last pair may hold no weights
+    // its tiles in the layout (padded to NB blocks): run 1 = tiles wt0 .. wt0 + wn1 - 1
+    // of block wb, run 2 = tiles 0 .. wn2 - 1 of block wb + 1
+    const int wtile = r_start / 16;
+    const int wvalid_tiles = wvalid ? min(kTilesW, NB * 8 - wtile) : 0;
+    const int wb = wtile >> 3, wt0 = wtile & 7;
+    const int wn1 = min(wvalid_tiles, 8 - wt0), wn2 = wvalid_tiles - wn1;
     // this CTA's k-blocks: kb0 .. kb0 + nkb - 1 (all of K unless split)
     const int kb0 = (int)(((long long)blockIdx.z * (a.K / kBK)) / a.splits);
     const int nkb = (int)((((long long)blockIdx.z + 1) * (a.K / kBK)) / a.splits) - kb0;
@@ -251,9 +266,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // The single-CTA tile always runs kSingleStages stages at fixed offsets
     // (compile-time constants there); pairs size their ring per launch.
     const int NS = PAIR ? a.nst : kSingleStages;
-    const uint32_t kOffX = PAIR ? a.off_x : kOffA + kSingleStages * kAStageBytes;
+    const uint32_t kOffX = PAIR ? a.off_x : kOffA + kSingleStages * kAStg;
     const uint32_t kOffW = PAIR ? a.off_w : kOffX + kSingleStages * kXStageBytes;
-    const uint32_t kOffSlab = PAIR ? a.off_slab : kOffW + kSingleStages * kWStageBytes;
+    const uint32_t kOffSlab = PAIR ? a.off_slab : kOffW + kSingleStages * kWStg;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -270,10 +285,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     if (warp == 1) {
         if (PAIR) {
-            tmem_alloc_pair(base + kTmemSlot, kCols);
+            tmem_alloc_pair(base + kTmemSlot, kAlloc);
             tmem_relinquish_pair();
         } else {
-            tmem_alloc(base + kTmemSlot, kCols);
+            tmem_alloc(base + kTmemSlot, kAlloc);
             tmem_relinquish();
         }
     }
@@ -292,19 +307,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ============================ TMA producer ============================
         if (lane == 0) {
             tma_prefetch_map(&xmap);
-            const uint8_t* w = a.wq + ((size_t)rb * (a.K / kBK) + kb0) * kWStageBytes;
-            if (wvalid)
-                for (int i = 0; i < NS && i < nkb; ++i)
-                    bulk_prefetch_l2(w + (size_t)i * kWStageBytes, kWStageBytes);
+            // chunk kb of block b starts at (b C + kb) 4 KB; tile t at + 512 t
+            const size_t C = (size_t)(a.K / kBK);
+            const uint8_t* w1 = a.wq + ((size_t)wb * C + kb0) * 4096 + (size_t)wt0 * 512;
+            const uint8_t* w2 = a.wq + ((size_t)(wb + 1) * C + kb0) * 4096;
+            for (int i = 0; i < NS && i < nkb; ++i) {
+                if (wn1) bulk_prefetch_l2(w1 + (size_t)i * 4096, (uint32_t)wn1 * 512);
+                if (wn2) bulk_prefetch_l2(w2 + (size_t)i * 4096, (uint32_t)wn2 * 512);
+            }
             grid_dependency_wait();
-            if (a.slab_tma) {  // this split's groups of the block's 128 rows
-                mbar_arrive_expect_tx(base + kBarSlab, (uint32_t)(kTileW * a.slab_ld * 2));
-                tma_load_2d(base + kOffSlab, &smap, slab_g0, rb * kTileW, base + kBarSlab);
-            } else {  // the block's scale slab (rows x G fp16, contiguous)
-                const int rows = max(0, min(kTileW, a.N - rb * kTileW));
+            if (a.slab_tma) {  // this split's groups of the CTA's TW rows
+                mbar_arrive_expect_tx(base + kBarSlab, (uint32_t)(TW * a.slab_ld * 2));
+                tma_load_2d(base + kOffSlab, &smap, slab_g0, r_start, base + kBarSlab);
+            } else {  // the CTA's scale slab (rows x G fp16, contiguous)
+                const int rows = max(0, min(TW, a.N - r_start));
                 const uint32_t bytes = (uint32_t)(rows * a.G * 2);
                 const uint32_t bulk = bytes & ~15u;
-                const __half* src = a.scales + (size_t)rb * kTileW * a.G;
+                const __half* src = a.scales + (size_t)r_start * a.G;
                 __half* dst = reinterpret_cast<__half*>(smem + kOffSlab);
                 for (uint32_t e = bulk / 2; e < bytes / 2; ++e) dst[e] = src[e];
                 mbar_arrive_expect_tx(base + kBarSlab, bulk);
@@ -324,14 +343,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     break;
                 }
                 mbar_arrive_expect_tx(base + kBarLoadFull + 8 * ts,
-                                      kXBytes + (wvalid ? kWStageBytes : 0));
+                                      kXBytes + (uint32_t)wvalid_tiles * 512);
 #pragma unroll
                 for (int xt = 0; xt < XT; ++xt)
                     tma_load_2d(base + kOffX + ts * kXBytes + xt * kXStageBytes, &xmap, (kb0 + i) * kBK,
                                 m0 + xt * 2 * kTileX, base + kBarLoadFull + 8 * ts);
-                if (wvalid)
-                    bulk_g2s(base + kOffW + ts * kWStageBytes, w + (size_t)i * kWStageBytes,
-                             kWStageBytes, base + kBarLoadFull + 8 * ts);
+                if (wn1)
+                    bulk_g2s(base + kOffW + ts * kWStg, w1 + (size_t)i * 4096, (uint32_t)wn1 * 512,
+                             base + kBarLoadFull + 8 * ts);
+                if (wn2)
+                    bulk_g2s(base + kOffW + ts * kWStg + (uint32_t)wn1 * 512, w2 + (size_t)i * 4096,
+                             (uint32_t)wn2 * 512, base + kBarLoadFull + 8 * ts);
                 issued = i + 1;
                 if (++ts == NS) {
                     ts = 0;
@@ -350,7 +372,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ============================= MMA issuer =============================
         if (lane == 0 && leader) {
             // A = x rows (M), B = weight rows (N), both K-major.
-            const uint32_t idesc = umma_idesc_f16_f32(PAIR ? 2 * kTileX : kTileX, PAIR ? 2 * kTileW : kTileW);
+            const uint32_t idesc = umma_idesc_f16_f32(PAIR ? 2 * kTileX : kTileX, PAIR ? 2 * TW : TW);
             bool ok = true;
             for (int i = 0, ts = 0, tr = 0; i < nkb; ++i) {
                 // the dequantisers waited for the stage's copies: A full implies x landed
@@ -364,13 +386,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t xa = base + kOffX + ts * kXBytes;
-                const uint32_t wa = base + kOffA + ts * kAStageBytes;
+                const uint32_t wa = base + kOffA + ts * kAStg;
 #pragma unroll
                 for (int j = 0; j < kBK / 16; ++j) {
                     if (PAIR) {
 #pragma unroll
                         for (int xt = 0; xt < XT; ++xt)
-                            tc_mma_f16_pair(tmem + (uint32_t)(xt * 2 * kTileW),
+                            tc_mma_f16_pair(tmem + (uint32_t)(xt * 2 * TW),
                                             umma_desc_sw128(xa + xt * kXStageBytes + 32 * j),
                                             umma_desc_sw128(wa + 32 * j), idesc, (i | j) != 0);
                     } else
@@ -418,12 +440,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // load issued just before the wait would stall them)
         [[maybe_unused]] FmtCoef cf;
         if constexpr (FMT) {
-            if (set < nkb) cf = fmt_coef(a, kb0 + set, rb * kTileW + r0, tq);
+            if (set < nkb) cf = fmt_coef(a, kb0 + set, r_start + r0, tq);
         }
         for (int i = set; ok && i < nkb; i += 2) {
             [[maybe_unused]] FmtCoef nx;
             if constexpr (FMT) {
-                if (i + 2 < nkb) nx = fmt_coef(a, kb0 + i + 2, rb * kTileW + r0, tq);
+                if (i + 2 < nkb) nx = fmt_coef(a, kb0 + i + 2, r_start + r0, tq);
             }
             // The stage's copies were issued after its previous MMAs finished,
             // so their arrival also means the dequantised slot is free.
@@ -431,9 +453,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 ok = false;
                 break;
             }
-            if (wvalid) {
-                const uint32_t wst = base + kOffW + ts * kWStageBytes;
-                const uint32_t ast = base + kOffA + ts * kAStageBytes;
+            if (wvalid && dw < kTilesW) {
+                const uint32_t wst = base + kOffW + ts * kWStg;
+                const uint32_t ast = base + kOffA + ts * kAStg;
                 const uint4 pk = lds128(wst + (dw * 32 + lane) * 16);
                 __half2 s0, s1;
                 [[maybe_unused]] __half2 lo_off, hi_off;  // 1024 + z0, -(64 + z1): exact
@@ -506,7 +528,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (acc_ok) tc_fence_after_sync();
         const int q = warp & 3;           // TMEM lane quarter = rows of y
         const int cc = (warp - 4) >> 2;   // column chunk = weight rows
-        constexpr int kChunkCols = (int)kCols / 4;  // 32 (single), 64 or 128 (pair)
+        constexpr int kChunkCols = (int)kCols / 4;  // 32 (single), 64, 128 or 96 (pair)
         const int row = q * 32 + lane;    // accumulator row (TMEM lane)
         if (a.splits == 1) {  // split K: reduced over the cluster below
             if (acc_ok) {
@@ -514,11 +536,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int half = 0; half < kChunkCols / 32; ++half) {
                     const int col = cc * kChunkCols + half * 32;
                     // pair: columns 256 t .. belong to MMA t, i.e. x rows m0 + 256 t
-                    const int xt = PAIR ? col / (2 * kTileW) : 0;
+                    const int xt = PAIR ? col / (2 * TW) : 0;
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)col, v);
                     tmem_ld_wait();
-                    store_y32(a, m0 + xt * 2 * kTileX + row, n_out + (PAIR ? col % (2 * kTileW) : col),
+                    store_y32(a, m0 + xt * 2 * kTileX + row, n_out + (PAIR ? col % (2 * TW) : col),
                               v);
                 }
             }
@@ -589,8 +611,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     uint32_t v[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(sum[e]);
-                    const int xt = col / (2 * kTileW);
-                    store_y32(a, m0 + xt * 2 * kTileX + row, n_out + col % (2 * kTileW), v);
+                    const int xt = col / (2 * TW);
+                    store_y32(a, m0 + xt * 2 * kTileX + row, n_out + col % (2 * TW), v);
                 }
             }
             tc_fence_before_sync();
@@ -602,9 +624,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 1) {
         tc_fence_after_sync();
         if (PAIR)
-            tmem_dealloc_pair(tmem, kCols);
+            tmem_dealloc_pair(tmem, kAlloc);
         else
-            tmem_dealloc(tmem, kCols);
+            tmem_dealloc(tmem, kAlloc);
     }
 }
 
@@ -617,6 +639,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 //  * otherwise one CTA per 128 x 128 tile (cluster 1).
 struct TcPlan {
     int cluster = 1, xt = 1, splits = 1;
+    int tw = kTileW;  // weight rows per CTA: 128, or 96 for pairs with two x tiles
     int slab_ld = 0;  // > 0: split slab of this many groups per row (tensor-map copy)
     unsigned gx = 0, gy = 0;
     long long ctas = 0;
@@ -642,9 +665,9 @@ int max_active_clusters(const void* fn, int cluster_z, uint32_t smem) {
 // Shared memory of a launch: `nst` ring stages with xt x tiles each, next to
 // a scale slab of `ld` groups per row, +1 KB slack for aligning the window to
 // 1024 bytes.
-uint32_t tc_smem(int nst, int xt, int ld) {
-    const uint32_t slab = ((kTileW * ld * 2 + 127) / 128) * 128;
-    const uint32_t stage = (uint32_t)(kAStageBytes + xt * kXStageBytes + kWStageBytes);
+uint32_t tc_smem(int nst, int xt, int ld, int tw = kTileW) {
+    const uint32_t slab = ((tw * ld * 2 + 127) / 128) * 128;
+    const uint32_t stage = (uint32_t)(tw * kBK * 2 + xt * kXStageBytes + tw * kBK / 2);
     return kOffA + (uint32_t)nst * stage + slab + 1024;
 }
 
@@ -669,7 +692,7 @@ int split_slab_ld(long long nkb, int S, int G) {
 int tc_stages(const TcPlan& p, int ld, const DeviceCtx& ctx) {
     if (p.cluster == 1) return kSingleStages;
     int nst = kMaxStages;
-    while (nst > 2 && tc_smem(nst, p.xt, ld) > (uint32_t)ctx.max_smem_optin) --nst;
+    while (nst > 2 && tc_smem(nst, p.xt, ld, p.tw) > (uint32_t)ctx.max_smem_optin) --nst;
     return nst;
 }
 
@@ -687,7 +710,8 @@ int tc_stages(const TcPlan& p, int ld, const DeviceCtx& ctx) {
 // microsecond per 64-column round of a split reduction.  fmt: the format
 // variants' kernels, which hold no scale slab.
 TcPlan tc_plan(int64_t M, int64_t N, int64_t K, const DeviceCtx& ctx, bool fmt = false) {
-    constexpr double kSingleKb = 0.36, kPairKb = 0.63, kPair2Kb = 0.84, kRound = 1.0;
+    constexpr double kSingleKb = 0.36, kPairKb = 0.63, kPair2Kb = 0.84, kPair2Kb96 = 0.66,
+                     kRound = 1.0;
     const int NB = (int)((N + kTileW - 1) / kTileW);
     const long long pairs = (NB + 1) / 2;
     const long long nkb = K / kBK;
@@ -713,14 +737,23 @@ TcPlan tc_plan(int64_t M, int64_t N, int64_t K, const DeviceCtx& ctx, bool fmt =
             best = p;
         }
     }
-    if (M > 2 * kTileX) {
+    // CTA pairs with two x tiles, 128 or 96 weight rows per CTA (one kernel-
+    // layout block, or six of its 16-row tiles: 192 rows per pair, which
+    // spreads N = 14336 over 150 CTAs instead of 112), each optionally
+    // splitting K.
+    for (int tw : {kTileW, 96}) {
+        if (M <= 2 * kTileX) break;
+        const double per_kb = tw == kTileW ? kPair2Kb : kPair2Kb96;
         TcPlan p;
         p.cluster = 2;
         p.xt = 2;
-        p.gx = (unsigned)(2 * pairs);
+        p.tw = tw;
+        const long long tiles = (N + tw - 1) / tw;
+        const long long tw_pairs = (tiles + 1) / 2;
+        p.gx = (unsigned)(2 * tw_pairs);
         p.gy = (unsigned)((M + 4 * kTileX - 1) / (4 * kTileX));
         p.ctas = (long long)p.gx * p.gy;
-        double t = waves(p.ctas) * nkb * kPair2Kb * (tc_stages(p, G, ctx) >= 4 ? 1.0 : 1.25);
+        double t = waves(p.ctas) * nkb * per_kb * (tc_stages(p, G, ctx) >= 4 ? 1.0 : 1.25);
         if (t < t_best) {
             t_best = t;
             best = p;
@@ -732,16 +765,18 @@ TcPlan tc_plan(int64_t M, int64_t N, int64_t K, const DeviceCtx& ctx, bool fmt =
             // deeper ring (3 stages run a k-block about 25 % slower than 4)
             const int ld = fmt ? 0 : split_slab_ld(nkb, S, G);
             const int nst = tc_stages(p, ld ? ld : G, ctx);
-            const uint32_t smem = tc_smem(nst, 2, ld ? ld : G);
-            const uint32_t ring = (uint32_t)nst * (kAStageBytes + 2 * kXStageBytes + kWStageBytes);
+            const uint32_t smem = tc_smem(nst, 2, ld ? ld : G, tw);
+            const uint32_t ring = (uint32_t)nst * (tw * kBK * 2 + 2 * kXStageBytes + tw * kBK / 2);
             // the S receive slots of the reduction live in the ring
             if ((uint32_t)S * kRedSlotFloats * 4 > ring) continue;
-            const void* fn = fmt ? (const void*)gemm_tc_kernel<true, 2, true>
-                                 : (const void*)gemm_tc_kernel<true, 2>;
+            const void* fn = tw == kTileW ? (fmt ? (const void*)gemm_tc_kernel<true, 2, true>
+                                                 : (const void*)gemm_tc_kernel<true, 2>)
+                                          : (fmt ? (const void*)gemm_tc_kernel<true, 2, true, 96>
+                                                 : (const void*)gemm_tc_kernel<true, 2, false, 96>);
             const long long fit = (long long)max_active_clusters(fn, S, smem);
             if (fit * 2 * S < ctas) continue;  // not one co-resident wave
-            t = (double)((nkb + S - 1) / S) * kPair2Kb * (nst >= 4 ? 1.0 : 1.25) +
-                kRound * ((4 * kTileW / S + 63) / 64 + 1);
+            t = (double)((nkb + S - 1) / S) * per_kb * (nst >= 4 ? 1.0 : 1.25) +
+                kRound * ((4 * tw / S + 63) / 64 + 1);
             if (t < t_best) {
                 t_best = t;
                 best = p;
@@ -762,7 +797,8 @@ cudaError_t ensure_tc_attrs(const DeviceCtx& ctx) {
     if (dev >= 0 && dev < 64 && attr_done[dev]) return cudaSuccess;
     for (auto fn : {gemm_tc_kernel<false, 1>, gemm_tc_kernel<true, 1>, gemm_tc_kernel<true, 2>,
                     gemm_tc_kernel<false, 1, true>, gemm_tc_kernel<true, 1, true>,
-                    gemm_tc_kernel<true, 2, true>}) {
+                    gemm_tc_kernel<true, 2, true>, gemm_tc_kernel<true, 2, false, 96>,
+                    gemm_tc_kernel<true, 2, true, 96>}) {
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              ctx.max_smem_optin);
         if (e != cudaSuccess) return e;
@@ -774,7 +810,7 @@ cudaError_t ensure_tc_attrs(const DeviceCtx& ctx) {
 }  // namespace
 
 void gemm_tc_plan_info(int64_t M, int64_t N, int64_t K, const DeviceCtx& ctx, int* cluster,
-                       int* ctas, bool fmt) {
+                       int* ctas, bool fmt, int* rows_per_cta) {
     if (ensure_tc_attrs(ctx) != cudaSuccess) {
         *cluster = 0;
         *ctas = 0;
@@ -783,6 +819,7 @@ void gemm_tc_plan_info(int64_t M, int64_t N, int64_t K, const DeviceCtx& ctx, in
     const TcPlan p = tc_plan(M, N, K, ctx, fmt);
     *cluster = p.cluster;
     *ctas = (int)p.ctas;
+    if (rows_per_cta) *rows_per_cta = p.tw;
 }
 
 namespace {
@@ -798,7 +835,7 @@ cudaError_t launch_tc(TcArgs a, const void* x, int64_t M, int64_t N, int64_t K, 
     const TcPlan plan = tc_plan(M, N, K, ctx, FMT);
     const int ld = plan.slab_ld ? plan.slab_ld : G;
     const int nst = tc_stages(plan, ld, ctx);
-    const uint32_t smem = tc_smem(nst, plan.xt, ld);
+    const uint32_t smem = tc_smem(nst, plan.xt, ld, plan.tw);
     if ((int)smem > ctx.max_smem_optin) return cudaErrorInvalidValue;
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
@@ -815,7 +852,7 @@ cudaError_t launch_tc(TcArgs a, const void* x, int64_t M, int64_t N, int64_t K, 
     if (plan.slab_ld) {
         const cuuint64_t sdims[2] = {(cuuint64_t)G, (cuuint64_t)N};
         const cuuint64_t sstrides[1] = {(cuuint64_t)G * 2};
-        const cuuint32_t sbox[2] = {(cuuint32_t)plan.slab_ld, (cuuint32_t)kTileW};
+        const cuuint32_t sbox[2] = {(cuuint32_t)plan.slab_ld, (cuuint32_t)plan.tw};
         if (encode(&smap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(a.scales), sdims,
                    sstrides, sbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -829,9 +866,9 @@ cudaError_t launch_tc(TcArgs a, const void* x, int64_t M, int64_t N, int64_t K, 
     a.K = (int)K;
     a.G = G;
     a.nst = nst;
-    a.off_x = kOffA + (uint32_t)nst * kAStageBytes;
+    a.off_x = kOffA + (uint32_t)nst * (uint32_t)(plan.tw * kBK * 2);
     a.off_w = a.off_x + (uint32_t)nst * plan.xt * kXStageBytes;
-    a.off_slab = a.off_w + (uint32_t)nst * kWStageBytes;
+    a.off_slab = a.off_w + (uint32_t)nst * (uint32_t)(plan.tw * kBK / 2);
     a.splits = plan.splits;
     a.slab_ld = ld;
     a.slab_tma = plan.slab_ld ? 1 : 0;
@@ -852,6 +889,7 @@ cudaError_t launch_tc(TcArgs a, const void* x, int64_t M, int64_t N, int64_t K, 
     cfg.numAttrs = plan.cluster > 1 ? 2 : 1;
     if (plan.cluster == 1) return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<false, 1, FMT>, map, smap, a);
     if (plan.xt == 1) return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true, 1, FMT>, map, smap, a);
+    if (plan.tw == 96) return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true, 2, FMT, 96>, map, smap, a);
     return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<true, 2, FMT>, map, smap, a);
 }
 

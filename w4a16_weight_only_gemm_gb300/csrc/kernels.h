@@ -77,10 +77,11 @@ cudaError_t gemv_plan_info(int M, int64_t N, int64_t K, const DeviceCtx& ctx, in
                            int* tail_units);
 // The launch the tensor-core GEMM would make: cluster size (1: one CTA per
 // 128 x 128 tile; 2: CTA pairs with 2-CTA MMAs; 4, 6 or 8: CTA pairs
-// splitting K two, three or four ways, reduced over the cluster) and CTAs.
-// fmt: the format variants' kernels (no scale slab).
+// splitting K two, three or four ways, reduced over the cluster), CTAs and
+// (if rows_per_cta) the weight rows of one CTA (128, or 96 for pairs with two
+// x tiles).  fmt: the format variants' kernels (no scale slab).
 void gemm_tc_plan_info(int64_t M, int64_t N, int64_t K, const DeviceCtx& ctx, int* cluster,
-                       int* ctas, bool fmt = false);
+                       int* ctas, bool fmt = false, int* rows_per_cta = nullptr);
 cudaError_t launch_gemm_tc(const void* x, const void* repacked, const void* scales, void* y,
                            int64_t M, int64_t N, int64_t K, cudaStream_t stream,
                            const DeviceCtx& ctx);
