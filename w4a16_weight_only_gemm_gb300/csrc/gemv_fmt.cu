@@ -15,14 +15,16 @@
 // a ring of 16 KB stages filled with one tensor-map box each (T tiles x
 // 32 / T chunks), the tile's warps splitting every stage's groups and adding
 // their sums in shared memory in warp order, programmatic dependent launch.
-// What differs is the dequantisation.  A lane's 16 k of a 64-wide chunk,
-// k = 64 c + 16 t .. + 15, lie inside one group even for groups of 32, so
-// each lane decodes (nib - z) exactly in fp16 (magic 1024, then subtract the
-// row's 1024 + z) and multiplies it by the row's fp16 scale before the MMA:
+// What differs is the dequantisation.  Each lane decodes (nib - z) exactly in
+// fp16 (magic 1024, then subtract the row's 1024 + z).  With groups of 64,
+// 128 or per channel a whole 64-wide chunk lies in one group, so the chunk's
+// four MMAs take the exact codes into a fresh FP32 fragment that the rows'
+// scales multiply once (CHUNK_SCALE: exact products, FP32 sums).  With groups
+// of 32 the two halves of a chunk differ in group, and one MMA spans both, so
+// each lane multiplies its (nib - z) by the row's fp16 scale before the MMA:
 // one fp16 rounding of (q - z) * s per weight -- the tutorial's own fp16
-// dequantised weight -- and FP32 accumulation.  No per-group FP32 rescale
-// and no activation sums are needed.  The default format (groups of 128,
-// symmetric) keeps the exact-product kernels of gemv.cu.
+// dequantised weight.  No activation sums are needed.  The default format
+// (groups of 128, symmetric) keeps the kernels of gemv.cu.
 // Every wait is bounded; on a time-out the CTA records it in the status
 // word, stops issuing copies, drains those in flight and exits.
 #include <atomic>
@@ -95,10 +97,33 @@ __device__ __forceinline__ void dequant8_fmt(uint32_t w, __half2 zc0, __half2 zc
     r[3] = *reinterpret_cast<uint32_t*>(&v);
 }
 
+// (nib - z) for one lane's 32-bit word, exactly, in the same register order.
+__device__ __forceinline__ void dequant8_zq(uint32_t w, __half2 zc0, __half2 nzc1,
+                                            uint32_t (&r)[4]) {
+    constexpr uint32_t kMagic = 0x64006400u;  // (1024.0, 1024.0)
+    constexpr uint32_t kLut = (0xF0 & 0xCC) | 0xAA;  // (a & b) | c
+    const uint32_t lo0 = lop3<kLut>(w, 0x000F000Fu, kMagic);
+    const uint32_t hi0 = lop3<kLut>(w, 0x00F000F0u, kMagic);
+    const uint32_t w8 = w >> 8;
+    const uint32_t lo1 = lop3<kLut>(w8, 0x000F000Fu, kMagic);
+    const uint32_t hi1 = lop3<kLut>(w8, 0x00F000F0u, kMagic);
+    const __half2 kSixteenth = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));
+    __half2 v;
+    v = __hsub2(*reinterpret_cast<const __half2*>(&lo0), zc0);
+    r[0] = *reinterpret_cast<uint32_t*>(&v);
+    v = __hsub2(*reinterpret_cast<const __half2*>(&lo1), zc0);
+    r[2] = *reinterpret_cast<uint32_t*>(&v);
+    v = __hfma2(*reinterpret_cast<const __half2*>(&hi0), kSixteenth, nzc1);
+    r[1] = *reinterpret_cast<uint32_t*>(&v);
+    v = __hfma2(*reinterpret_cast<const __half2*>(&hi1), kSixteenth, nzc1);
+    r[3] = *reinterpret_cast<uint32_t*>(&v);
+}
+
 // One 128-wide group (two chunks) of one consumer lane, dequantised with
 // the scale and zero point of the lane's group in each chunk, accumulated
-// into acc (two MMA chains for M <= 8).
-template <int MT>
+// into acc (two MMA chains for M <= 8).  CHUNK_SCALE: the chunk's exact
+// products summed in a fresh FP32 fragment, scaled once per row.
+template <int MT, bool CHUNK_SCALE>
 __device__ __forceinline__ void mma_group_fmt(uint32_t w_addr, uint32_t cs, uint32_t x0_addr,
                                               uint32_t x1_addr, const __half* sc0,
                                               const __half* sc1, const uint8_t* zr0,
@@ -124,17 +149,46 @@ __device__ __forceinline__ void mma_group_fmt(uint32_t w_addr, uint32_t cs, uint
         const uint32_t wrd[4] = {wv.x, wv.y, wv.z, wv.w};
         const uint32_t b0[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
         const uint32_t b1[8] = {xa1.x, xa1.y, xa1.z, xa1.w, xb1.x, xb1.y, xb1.z, xb1.w};
+        if constexpr (CHUNK_SCALE) {
+            float ch[MT][4];
 #pragma unroll
-        for (int s = 0; s < 4; ++s) {
-            uint32_t af[4];
-            dequant8_fmt(wrd[s], zc0, zc1, s0, s1, af);
-            mma_16816(acc[c][0], af, b0[2 * s], b0[2 * s + 1], acc[c][0]);
-            if (MT == 2) mma_16816(acc[c][MT - 1], af, b1[2 * s], b1[2 * s + 1], acc[c][MT - 1]);
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) ch[mt][e] = 0.0f;
+            const __half2 nzc1 = __hneg2(zc1);
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                uint32_t af[4];
+                dequant8_zq(wrd[s], zc0, nzc1, af);
+                mma_16816(ch[0], af, b0[2 * s], b0[2 * s + 1], ch[0]);
+                if (MT == 2) mma_16816(ch[MT - 1], af, b1[2 * s], b1[2 * s + 1], ch[MT - 1]);
+            }
+            const float2 f0 = __half22float2(s0), f1 = __half22float2(s1);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                const float2 a01 = __ffma2_rn(f0, make_float2(ch[mt][0], ch[mt][1]),
+                                              make_float2(acc[c][mt][0], acc[c][mt][1]));
+                const float2 a23 = __ffma2_rn(f1, make_float2(ch[mt][2], ch[mt][3]),
+                                              make_float2(acc[c][mt][2], acc[c][mt][3]));
+                acc[c][mt][0] = a01.x;
+                acc[c][mt][1] = a01.y;
+                acc[c][mt][2] = a23.x;
+                acc[c][mt][3] = a23.y;
+            }
+        } else {
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                uint32_t af[4];
+                dequant8_fmt(wrd[s], zc0, zc1, s0, s1, af);
+                mma_16816(acc[c][0], af, b0[2 * s], b0[2 * s + 1], acc[c][0]);
+                if (MT == 2)
+                    mma_16816(acc[c][MT - 1], af, b1[2 * s], b1[2 * s + 1], acc[c][MT - 1]);
+            }
         }
     }
 }
 
-template <int MT>
+template <int MT, bool CHUNK_SCALE>
 __global__ void __launch_bounds__(kFThreads, MT == 1 ? 3 : 2)
     gemv_fmt_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ FmtArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -305,7 +359,7 @@ __global__ void __launch_bounds__(kFThreads, MT == 1 ? 3 : 2)
                     const int gl = st * GPS + gsl;  // 128-group index along the row
                     // the scale group of this lane's k in chunks 2 gl and 2 gl + 1
                     const int k0 = gl * 128 + 16 * t;
-                    mma_group_fmt<MT>(wl + slot * kFStageBytes + gsl * 2 * cs, cs, x0 + gl * 256,
+                    mma_group_fmt<MT, CHUNK_SCALE>(wl + slot * kFStageBytes + gsl * 2 * cs, cs, x0 + gl * 256,
                                       x1 + gl * 256, sc0, sc1, zr0, zr1, k0 >> a.gshift,
                                       (k0 + 64) >> a.gshift, acc);
                 }
@@ -366,11 +420,14 @@ struct FmtPlan {
 
 template <int MT>
 int fmt_occupancy(uint32_t smem) {
-    int blocks = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, gemv_fmt_kernel<MT>, kFThreads,
+    // both scale modes have the same launch bounds; the larger register count decides
+    int b0 = 0, b1 = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b0, gemv_fmt_kernel<MT, false>, kFThreads,
+                                                      smem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, gemv_fmt_kernel<MT, true>, kFThreads,
                                                       smem) != cudaSuccess)
         return 0;
-    return blocks;
+    return b0 < b1 ? b0 : b1;
 }
 
 template <int MT>
@@ -379,8 +436,11 @@ cudaError_t ensure_fmt_attr() {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
-    const cudaError_t e = cudaFuncSetAttribute(
-        gemv_fmt_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    cudaError_t e = cudaFuncSetAttribute(
+        gemv_fmt_kernel<MT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemv_fmt_kernel<MT, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev].store(true, std::memory_order_release);
     return e;
 }
@@ -481,7 +541,9 @@ cudaError_t launch_fmt_mt(FmtArgs a, cudaStream_t stream, const DeviceCtx& ctx) 
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_fmt_kernel<MT>, wmap, a);
+    // groups of 64 and more: a whole chunk in one group, scaled in FP32
+    if (a.gshift >= 6) return cudaLaunchKernelEx(&cfg, gemv_fmt_kernel<MT, true>, wmap, a);
+    return cudaLaunchKernelEx(&cfg, gemv_fmt_kernel<MT, false>, wmap, a);
 }
 
 }  // namespace
