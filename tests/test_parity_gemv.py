@@ -93,7 +93,7 @@ def test_persistent_path_all_rows(w4lib, M, N, K):
     assert_close(run_gemm(x16, q, s), oracle.gemm(x16, q, s), f"M={M} N={N} K={K} {plan}")
 
 
-@pytest.mark.parametrize("M", [1, 9])
+@pytest.mark.parametrize("M", [1, 4])
 @pytest.mark.parametrize("K", [256, 1152])
 @pytest.mark.parametrize("tail_rows", [16, 32, 64])
 def test_persistent_tail_units_all_rows(w4lib, M, K, tail_rows):
@@ -117,10 +117,32 @@ def test_persistent_tail_units_all_rows(w4lib, M, K, tail_rows):
     assert np.array_equal(run_gemm(x16, q, s), y)
 
 
-# The bias-64 decode feeds 64 + n / 16 and 64 + n to the MMAs and removes
-# 64.5 * sum(x) and 72 * sum(x) per group in FP32: its rounding grows with
-# |sum(x)| over a group.  Activations with a large common offset (real decode
-# activations are not zero-mean) on each kind of launch.
+@pytest.mark.parametrize("M", [5, 9, 16])
+@pytest.mark.parametrize("K", [256, 1152])
+def test_persistent_x_in_ring_all_rows(w4lib, M, K):
+    """With M > 4 a whole-block launch streams x with every ring stage (a
+    swizzled box of 4 chunks x M rows) instead of one CTA-wide slice, and a
+    partial last round runs as whole blocks.  K = 1152 ends each block in a
+    half stage whose box reaches past K (filled with zeros); N ends in a
+    ragged block.  Every row is checked, and a repeat call is bit-identical."""
+    G = w4.gemm_plan(M, 200_000, K)["ctas"]
+    N = 128 * (G + G // 3) - 37
+    plan = w4.gemm_plan(M, N, K)
+    assert plan["blocks_per_cta"] == 2 and plan["ctas"] == G, plan
+    assert w4.gemm_plan_tail(M, N, K) == {"tail_rows": 0, "tail_units": 0}
+    w16, q, s = quantized(N, K, 73)
+    x16 = acts(M, K, 74 + M)
+    y = run_gemm(x16, q, s)
+    assert_close(y, oracle.gemm(x16, q, s), f"M={M} N={N} K={K} {plan}")
+    assert np.array_equal(run_gemm(x16, q, s), y)
+
+
+# Activations with a large common offset (real decode activations are not
+# zero-mean) make the group sums of x large; a decode that fed biased codes to
+# the MMAs and removed bias * sum(x) afterwards would lose the dot product's
+# low bits there.  Each kind of launch on such activations.
+# (Persistent launches take, at M <= 4, the decode of unbiased codes whose x
+# sums are removed after the MMAs.)
 OFFSET_CANDIDATES = {
     "unit": [(4096, 4096), (6144, 4096), (1000, 2048), (16384, 2048), (8000, 1920), (16384, 1024),
              (4096, 512)],
@@ -138,7 +160,7 @@ def _launch_of(plan) -> str:
 
 
 @pytest.mark.parametrize("kind", synthetic.OFFSET_KINDS)
-@pytest.mark.parametrize("M", [1, 9, 16])
+@pytest.mark.parametrize("M", [1, 3, 9, 16])
 @pytest.mark.parametrize("launch", ["unit", "split", "persistent"])
 def test_offset_activations_all_rows(w4lib, kind, M, launch):
     """The first candidate shape the planner launches this way, every row."""
@@ -150,6 +172,31 @@ def test_offset_activations_all_rows(w4lib, kind, M, launch):
     x16 = bits16(synthetic.activations_offset(M, K, 82 + M, kind))
     assert_close(run_gemm(x16, q, s), oracle.gemm(x16, q, s),
                  f"{kind} M={M} {launch} N={N} K={K} {w4.gemm_plan(M, N, K)}")
+
+
+# Unit launches at M <= 4 whose warps each see 16 or more groups per round
+# of the x-sum pass (ceil(8 G M / 256) rounds, G = K / 128) take the decode of
+# unbiased codes.
+LONG_UNIT_CANDIDATES = [(28672, 4096), (14336, 4096), (4096, 14336), (8192, 14336)]
+
+
+@pytest.mark.parametrize("kind", ("normal",) + synthetic.OFFSET_KINDS)
+@pytest.mark.parametrize("M", [1])
+def test_long_units_all_rows(w4lib, kind, M):
+    """The first candidate the planner runs as such units, every row."""
+    def long_unit(N, K):
+        p = w4.gemm_plan(M, N, K)
+        G, T = K // 128, p["rows_per_cta"] // 16
+        return _launch_of(p) == "unit" and G * T // 8 >= 16 * -(-G * M * 8 // 256)
+    shapes = [(N, K) for N, K in LONG_UNIT_CANDIDATES if long_unit(N, K)]
+    assert shapes, (M, [w4.gemm_plan(M, N, K) for N, K in LONG_UNIT_CANDIDATES])
+    N, K = shapes[0]
+    w16, q, s = quantized(N, K, 83)
+    x = (synthetic.activations(M, K, 84 + M) if kind == "normal"
+         else synthetic.activations_offset(M, K, 84 + M, kind))
+    x16 = bits16(x)
+    assert_close(run_gemm(x16, q, s), oracle.gemm(x16, q, s),
+                 f"{kind} M={M} N={N} K={K} {w4.gemm_plan(M, N, K)}")
 
 
 # Launches made of sub-block units (16, 32 or 64 weight rows per CTA over the

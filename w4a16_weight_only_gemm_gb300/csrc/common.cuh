@@ -178,6 +178,16 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// 3-D tiled load; c0 is the innermost coordinate (elements).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
 // L2 prefetch of one 2-D box.
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int c0, int c1) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
@@ -303,6 +313,20 @@ __device__ __forceinline__ void dequant8(uint32_t w, uint32_t (&r)[4]) {
     r[2] = *reinterpret_cast<uint32_t*>(&v);
     v = __hfma2(*reinterpret_cast<const __half2*>(&hi1), kSixteenth, kMinus72);
     r[3] = *reinterpret_cast<uint32_t*>(&v);
+}
+
+// The same word as unbiased codes n in fp16 subnormals, with no arithmetic:
+// a nibble masked into bits 0..3 of a half is n * 2^-24 exactly, into bits
+// 4..7 it is n * 2^-20.  r[0] / r[2] (positions 0, 4 and 2, 6) carry 2^-24,
+// r[1] / r[3] (positions 1, 5 and 3, 7) carry 2^-20; in the layout's
+// fragment order that is one factor per weight row (rows r0: 2^-24, rows
+// r1: 2^-20), removed with the zero point 8 in the FP32 group rescale.
+__device__ __forceinline__ void dequant8_subnormal(uint32_t w, uint32_t (&r)[4]) {
+    r[0] = w & 0x000F000Fu;
+    r[1] = w & 0x00F000F0u;
+    const uint32_t w8 = w >> 8;
+    r[2] = w8 & 0x000F000Fu;
+    r[3] = w8 & 0x00F000F0u;
 }
 
 __device__ __forceinline__ float2 lds64f(uint32_t addr) {

@@ -15,7 +15,10 @@
 //    bulk copy per stage); a unit's T tiles of 32 / T consecutive chunks are
 //    one tensor-map box.  The fp16 scale slab of the CTA's rows (contiguous
 //    in the canonical layout) arrives the same way into one of two buffers,
-//    and the x slice of the CTA's K range once per thread block.
+//    and the x slice of the CTA's K range once per thread block -- or, for
+//    whole blocks with M > 4, each stage's 4 chunks of x for all M rows in
+//    the stage itself (one swizzled tensor-map box), so that the CTA's
+//    shared memory no longer grows with M x K.
 //  * Consumers: per 64-wide chunk a lane reads 16 bytes of its tile, turns
 //    each 32-bit word into an mma.m16n8k16 A fragment of exact codes
 //    q = n - 8 in fp16 (one lop3 per nibble pair OR-ing it into the mantissa
@@ -23,7 +26,11 @@
 //    with x fragments read from shared memory.  M <= 8 uses one n8 MMA per
 //    16 k, M <= 16 two.  Every 128-wide group accumulates in fresh FP32
 //    fragments and is scaled once by its fp16 scale: the products are exact
-//    and only FP32 sums round.
+//    and only FP32 sums round.  Persistent launches and long units with
+//    M <= 4 feed the unbiased codes n instead, as fp16 subnormals that the
+//    masks alone produce (n 2^-24, n 2^-20), and take the zero point off in
+//    the FP32 rescale with per-group x sums computed once per CTA: 5 instead
+//    of 9 instructions per 8 weights, products still exact.
 //  * Work split, chosen per shape by a launch-time model: sub-block units
 //    (the warps of a tile add their partial sums in shared memory, in a
 //    fixed order); or whole blocks with the K range split over the S CTAs of
@@ -90,8 +97,22 @@ struct GemvArgs {
     // blocks from tail_base on run as tail_units sub-block units of tail_T
     // tiles (tail_T = 0: no tail), unit u on CTA u after its whole blocks.
     int tail_T, tail_base, tail_units;
-    uint32_t off_ring, off_x, off_s, off_red;
+    // Whole-block launches with M > 4 stream x through the ring: every stage
+    // holds, after its 16 KB of weights, the stage's 4 chunks of x for all M
+    // rows (one 3-D tensor-map box, 128-byte swizzled, 1024-aligned inside
+    // xs_stage bytes); xs_stage = 0: x is one CTA-wide slice instead.
+    int xs_stage;
+    int stage_stride;        // bytes between ring stages (16 KB + xs_stage)
+    // off_sx: the x sums of the subnormal-code decode, [group][16] floats
+    uint32_t off_ring, off_x, off_s, off_red, off_sx;
 };
+
+__device__ __forceinline__ uint32_t align1024(uint32_t a) { return (a + 1023u) & ~1023u; }
+
+// x addresses of a stage's chunk pair (cc0, cc0 + 1) when x rides in the
+// ring: the box lands as [chunk][row][128 bytes] with 16-byte units swizzled
+// by the 128-byte row's index within its 1024-byte atom.
+
 
 __device__ __forceinline__ int split_group_begin(int split, int S, int G) {
     return (int)(((long long)split * G) / S);
@@ -105,10 +126,52 @@ __device__ __forceinline__ int split_group_begin(int split, int S, int G) {
 // MMA adds its products at the precision of the running sum: activations with
 // a large common offset make that sum ~64 sum(x) and lose the dot product's
 // low bits, beyond the accuracy bar for x = 4 + N(0, 1).)
-template <int MT>
-__device__ __forceinline__ void mma_group(uint32_t w_addr, uint32_t cs, uint32_t x0_addr,
-                                          uint32_t x1_addr, float s0, float s1,
-                                          float (&acc)[MT][4]) {
+// x addresses: xa[c][h] the h-th 16 bytes of this lane's activations (row
+// min(g, M - 1)) in chunk c of the group, xb[c][h] the same for row
+// min(g + 8, M - 1) (read only when M > 8).
+struct XAddr {
+    uint32_t a[2][2], b[2][2];
+};
+
+// The x of a CTA-wide slice: rows xs_stride bytes apart, chunks 128 bytes.
+__device__ __forceinline__ XAddr x_slice(uint32_t x0_addr, uint32_t x1_addr) {
+    XAddr x;
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            x.a[c][h] = x0_addr + c * 128 + h * 16;
+            x.b[c][h] = x1_addr + c * 128 + h * 16;
+        }
+    return x;
+}
+
+// x in a ring stage (whole-block launches with M > 4): the stage's box is
+// [4 chunks][M rows][128 bytes], the 16-byte unit u of 128-byte row q stored
+// at unit u ^ (q & 7); rows r0 / r1 of chunks cc0, cc0 + 1.
+__device__ __forceinline__ XAddr x_stage(uint32_t xbase, int M, int cc0, int r0, int r1, int t) {
+    XAddr x;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        const int q0 = (cc0 + c) * M + r0, q1 = (cc0 + c) * M + r1;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            x.a[c][h] = xbase + (uint32_t)q0 * 128u + ((uint32_t)((2 * t + h) ^ (q0 & 7)) << 4);
+            x.b[c][h] = xbase + (uint32_t)q1 * 128u + ((uint32_t)((2 * t + h) ^ (q1 & 7)) << 4);
+        }
+    }
+    return x;
+}
+
+// SUB: the A fragments hold the unbiased codes n as fp16 subnormals
+// (dequant8_subnormal, no arithmetic): the MMAs give 2^-24 sum(n x) for rows
+// r0 and 2^-20 sum(n x) for rows r1, and the rescale takes off 8 sum(x) with
+// the group's x sums (sx_addr: this lane's columns 2t, 2t + 1, FP32).  The
+// MMA's running sums then reach ~sum(n x) rather than the result, within a
+// small factor of it for offset activations (the bias of 64 + n was not).
+template <int MT, bool SUB = false>
+__device__ __forceinline__ void mma_group(uint32_t w_addr, uint32_t cs, const XAddr& xad, float s0,
+                                          float s1, uint32_t sx_addr, float (&acc)[MT][4]) {
     // M <= 8: one FP32 fragment per chunk -- two independent MMA chains per
     // group halve the dependent-latency path of a lane (M <= 16 has two
     // chains already, one per n8 tile, and no registers to spare).
@@ -123,12 +186,12 @@ __device__ __forceinline__ void mma_group(uint32_t w_addr, uint32_t cs, uint32_t
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
         const uint4 wv = lds128(w_addr + c * cs);
-        const uint4 xa = lds128(x0_addr + c * 128);
-        const uint4 xb = lds128(x0_addr + c * 128 + 16);
+        const uint4 xa = lds128(xad.a[c][0]);
+        const uint4 xb = lds128(xad.a[c][1]);
         uint4 xa1 = xa, xb1 = xb;
         if (MT == 2) {
-            xa1 = lds128(x1_addr + c * 128);
-            xb1 = lds128(x1_addr + c * 128 + 16);
+            xa1 = lds128(xad.b[c][0]);
+            xb1 = lds128(xad.b[c][1]);
         }
         const uint32_t wrd[4] = {wv.x, wv.y, wv.z, wv.w};
         const uint32_t b0[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
@@ -136,7 +199,10 @@ __device__ __forceinline__ void mma_group(uint32_t w_addr, uint32_t cs, uint32_t
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
             uint32_t af[4];
-            dequant8(wrd[s], af);
+            if (SUB)
+                dequant8_subnormal(wrd[s], af);
+            else
+                dequant8(wrd[s], af);
             mma_16816(g[c % NCH][0], af, b0[2 * s], b0[2 * s + 1], g[c % NCH][0]);
             if (MT == 2)
                 mma_16816(g[c % NCH][MT - 1], af, b1[2 * s], b1[2 * s + 1], g[c % NCH][MT - 1]);
@@ -144,7 +210,9 @@ __device__ __forceinline__ void mma_group(uint32_t w_addr, uint32_t cs, uint32_t
     }
     // The rescale runs on (column 2t, 2t + 1) pairs through the packed binary32
     // instructions; each component rounds as the scalar fma.
-    const float2 s00 = make_float2(s0, s0), s11 = make_float2(s1, s1);
+    // SUB: s (2^24 or 2^20) G - 8 s Sx, in two fmas.
+    const float f0 = SUB ? 16777216.0f * s0 : s0, f1 = SUB ? 1048576.0f * s1 : s1;
+    const float2 s00 = make_float2(f0, f0), s11 = make_float2(f1, f1);
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
         float2 v01 = make_float2(g[0][mt][0], g[0][mt][1]);
@@ -153,8 +221,15 @@ __device__ __forceinline__ void mma_group(uint32_t w_addr, uint32_t cs, uint32_t
             v01 = __fadd2_rn(v01, make_float2(g[NCH - 1][mt][0], g[NCH - 1][mt][1]));
             v23 = __fadd2_rn(v23, make_float2(g[NCH - 1][mt][2], g[NCH - 1][mt][3]));
         }
-        const float2 a01 = __ffma2_rn(s00, v01, make_float2(acc[mt][0], acc[mt][1]));
-        const float2 a23 = __ffma2_rn(s11, v23, make_float2(acc[mt][2], acc[mt][3]));
+        float2 c01 = make_float2(acc[mt][0], acc[mt][1]);
+        float2 c23 = make_float2(acc[mt][2], acc[mt][3]);
+        if (SUB) {
+            const float2 sx = lds64f(sx_addr + mt * 32);
+            c01 = __ffma2_rn(make_float2(-8.0f * s0, -8.0f * s0), sx, c01);
+            c23 = __ffma2_rn(make_float2(-8.0f * s1, -8.0f * s1), sx, c23);
+        }
+        const float2 a01 = __ffma2_rn(s00, v01, c01);
+        const float2 a23 = __ffma2_rn(s11, v23, c23);
         acc[mt][0] = a01.x;
         acc[mt][1] = a01.y;
         acc[mt][2] = a23.x;
@@ -185,10 +260,10 @@ __device__ __forceinline__ void store_y(const GemvArgs& a, int R0, int R1, int t
 // CTA: a stage holds GPS = 8 / T groups of the unit's T tiles (chunk c of
 // tile i at c * cs + i * 512 bytes); the W = 8 / T warps of a tile take
 // groups 2 ks, 2 ks + 1 of every stage.  Returns false on a time-out.
-template <int MT>
+template <int MT, bool SUB = false>
 __device__ __forceinline__ bool unit_stages(const GemvArgs& a, uint32_t sbase, int nstg, int ng,
                                             int GPS, int ks, uint32_t wl, uint32_t cs, uint32_t x0,
-                                            uint32_t x1, const __half* sc0,
+                                            uint32_t x1, uint32_t sxl, const __half* sc0,
                                             const __half* sc1, int lane, int& slot, uint32_t& phase,
                                             float (&acc)[MT][4]) {
     const int NS = a.nstages;
@@ -197,16 +272,20 @@ __device__ __forceinline__ bool unit_stages(const GemvArgs& a, uint32_t sbase, i
         const int gs = min(GPS, ng - st * GPS);     // groups in this stage
         const int gsl0 = ks * kGroupsPerWarpStage;  // this warp's first group in it
         const int gl0 = st * GPS + gsl0;
-        const uint32_t wa = wl + slot * kStageBytes + gsl0 * 2 * cs;
+        const uint32_t wa = wl + slot * a.stage_stride + gsl0 * 2 * cs;
         if (gs == GPS) {
 #pragma unroll
             for (int gi = 0; gi < kGroupsPerWarpStage; ++gi)
-                mma_group<MT>(wa + gi * 2 * cs, cs, x0 + (gl0 + gi) * 256, x1 + (gl0 + gi) * 256,
-                              __half2float(sc0[gl0 + gi]), __half2float(sc1[gl0 + gi]), acc);
+                mma_group<MT, SUB>(wa + gi * 2 * cs, cs,
+                                   x_slice(x0 + (gl0 + gi) * 256, x1 + (gl0 + gi) * 256),
+                                   __half2float(sc0[gl0 + gi]), __half2float(sc1[gl0 + gi]),
+                                   sxl + (gl0 + gi) * 64, acc);
         } else {
             for (int gi = 0; gi < kGroupsPerWarpStage && gsl0 + gi < gs; ++gi)
-                mma_group<MT>(wa + gi * 2 * cs, cs, x0 + (gl0 + gi) * 256, x1 + (gl0 + gi) * 256,
-                              __half2float(sc0[gl0 + gi]), __half2float(sc1[gl0 + gi]), acc);
+                mma_group<MT, SUB>(wa + gi * 2 * cs, cs,
+                                   x_slice(x0 + (gl0 + gi) * 256, x1 + (gl0 + gi) * 256),
+                                   __half2float(sc0[gl0 + gi]), __half2float(sc1[gl0 + gi]),
+                                   sxl + (gl0 + gi) * 64, acc);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(sbase + kBarEmpty + 8 * slot);
@@ -262,10 +341,10 @@ __device__ __forceinline__ void unit_reduce_store(const GemvArgs& a, uint8_t* sm
 // W2 = 8 / tT warps per tile over the K range.  Every consumer warp reaches
 // the reduction's barrier, whatever `ok` says.  Kept out of line so that the
 // whole-block loop keeps its registers.
-template <int MT>
+template <int MT, bool SUB>
 __device__ __noinline__ bool tail_unit_consume(const GemvArgs& a, uint8_t* smem, uint32_t sbase,
                                                uint32_t ring, int nblk, int nck, int ng, int g0,
-                                               uint32_t x0, uint32_t x1, int slot,
+                                               uint32_t x0, uint32_t x1, uint32_t sxl, int slot,
                                                uint32_t phase, bool ok) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
@@ -290,7 +369,7 @@ __device__ __noinline__ bool tail_unit_consume(const GemvArgs& a, uint8_t* smem,
     if (ok) {
         const __half* tsc0 =
             reinterpret_cast<const __half*>(smem + a.off_s + sbuf * a.slab_bytes) + tr0 * a.G + g0;
-        if (!unit_stages<MT>(a, sbase, tnstg, ng, tCPS / 2, ks2, twl, tcs, x0, x1, tsc0,
+        if (!unit_stages<MT, SUB>(a, sbase, tnstg, ng, tCPS / 2, ks2, twl, tcs, x0, x1, sxl, tsc0,
                              tsc0 + 8 * a.G, lane, slot, phase, tacc))
             ok = false;
     }
@@ -304,8 +383,11 @@ __device__ __noinline__ bool tail_unit_consume(const GemvArgs& a, uint8_t* smem,
 // (`wmap`) views the kernel layout as rows of 4 KB chunks (512 eight-byte
 // elements, one row per block-chunk); sub-block launches copy a box of T
 // tiles x 32 / T chunks per ring stage through it.
-template <int MT, bool WHOLE>
-__device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const GemvArgs& a) {
+// XS: x streamed through the ring (whole blocks, M > 4; a.xs_stage > 0).
+// SUB: the subnormal-code decode (persistent whole-block launches, M <= 4).
+template <int MT, bool WHOLE, bool XS = false, bool SUB = false>
+__device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const CUtensorMap* xmap,
+                                          const GemvArgs& a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -329,7 +411,7 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const GemvArg
                                 : (a.NB - (int)blockIdx.y + (int)gridDim.y - 1) / (int)gridDim.y;
     // The tail unit of this CTA (persistent launches with a partial last
     // round): tT tiles from tile t_t0 of block t_rb.  Evaluated where used.
-    auto has_tail = [&]() { return whole && a.tail_T > 0 && (int)blockIdx.y < a.tail_units; };
+    auto has_tail = [&]() { return whole && !XS && a.tail_T > 0 && (int)blockIdx.y < a.tail_units; };
 #define W4A16_TAIL_GEOMETRY                                                         \
     const int tT = a.tail_T;                                                        \
     const int t_rb = a.tail_base + (int)blockIdx.y / (kConsumerWarps / tT);         \
@@ -387,17 +469,28 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const GemvArg
                 // stages and scale slab load while the previous kernel is still
                 // running.  x (its output, possibly) loads only after the wait.
                 bool x_issued = false;
+                const int NS = a.nstages;
+                const uint32_t stride = (uint32_t)a.stage_stride;
+                constexpr bool xs = XS;
+                const uint32_t xbox = 512u * (uint32_t)a.M;  // one stage's x: 4 chunks x M rows x 128 B
+                int it = 0, slot = 0, round = 0;  // slot = it % NS, round = it / NS
                 auto issue_x = [&]() {
                     grid_dependency_wait();
-                    const uint32_t xbytes = (uint32_t)nck * (kChunkK * 2);
-                    mbar_arrive_expect_tx(sbase + kBarX, xbytes * a.M);
-                    for (int m = 0; m < a.M; ++m)
-                        bulk_g2s(sbase + a.off_x + m * a.xs_stride,
-                                 a.x + (size_t)m * a.K + (size_t)g0 * kGroup, xbytes, sbase + kBarX);
+                    if (xs) {
+                        // the x of the stages issued so far (at most the first ring pass;
+                        // their barriers already expect these bytes)
+                        for (int i = 0; i < it; ++i)
+                            tma_load_3d(align1024(ring + (uint32_t)(i % NS) * stride + kStageBytes), xmap,
+                                        0, 0, 2 * g0 + 4 * (i % nstg), sbase + kBarFull + 8 * (i % NS));
+                    } else {
+                        const uint32_t xbytes = (uint32_t)nck * (kChunkK * 2);
+                        mbar_arrive_expect_tx(sbase + kBarX, xbytes * a.M);
+                        for (int m = 0; m < a.M; ++m)
+                            bulk_g2s(sbase + a.off_x + m * a.xs_stride,
+                                     a.x + (size_t)m * a.K + (size_t)g0 * kGroup, xbytes, sbase + kBarX);
+                    }
                     x_issued = true;
                 };
-                const int NS = a.nstages;
-                int it = 0, slot = 0, round = 0;  // slot = it % NS, round = it / NS
                 bool ok = true;
                 int sb_issued = 0;
                 for (int j = 0; ok && j < nblk; ++j) {
@@ -438,9 +531,13 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const GemvArg
                             break;
                         }
                         const int nc = min(CPS, nck - st * CPS);
-                        mbar_arrive_expect_tx(sbase + kBarFull + 8 * slot, nc * kChunkBytes);
-                        bulk_g2s_hint(ring + slot * kStageBytes, w + (size_t)st * kStageBytes,
+                        mbar_arrive_expect_tx(sbase + kBarFull + 8 * slot,
+                                              nc * kChunkBytes + (xs ? xbox : 0u));
+                        bulk_g2s_hint(ring + slot * stride, w + (size_t)st * kStageBytes,
                                       nc * kChunkBytes, sbase + kBarFull + 8 * slot, pol);
+                        if (xs && x_issued)
+                            tma_load_3d(align1024(ring + slot * stride + kStageBytes), xmap, 0, 0,
+                                        2 * g0 + 4 * st, sbase + kBarFull + 8 * slot);
                         ++it;
                         if (++slot == NS) {
                             slot = 0;
@@ -488,7 +585,7 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const GemvArg
                             break;
                         }
                         const int nc = min(tCPS, C - st * tCPS);
-                        const uint32_t dst = ring + slot * kStageBytes;
+                        const uint32_t dst = ring + slot * stride;
                         const uint32_t bar = sbase + kBarFull + 8 * slot;
                         if (nc == tCPS) {
                             mbar_arrive_expect_tx(bar, kStageBytes);
@@ -513,7 +610,7 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const GemvArg
                 if (!ok) *abort_flag = 1;
                 // Drain: every issued copy must land before the CTA may exit.
                 const uint64_t dt = drain_bound(a.timeout_ns);
-                mbar_wait(sbase + kBarX, 0, dt, a.status);
+                if (!xs) mbar_wait(sbase + kBarX, 0, dt, a.status);
                 for (int i = (it > NS ? it - NS : 0); i < it; ++i)
                     mbar_wait(sbase + kBarFull + 8 * (i % NS), (i / NS) & 1, dt, a.status);
                 for (int j = (sb_issued > a.n_sbuf ? sb_issued - a.n_sbuf : 0); j < sb_issued; ++j)
@@ -570,7 +667,7 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const GemvArg
                         break;
                     }
                     const int nc = min(CPS, nck - it * CPS);
-                    const uint32_t dst = ring + slot * kStageBytes;
+                    const uint32_t dst = ring + slot * (uint32_t)a.stage_stride;
                     const uint32_t bar = sbase + kBarFull + 8 * slot;
                     if (nc == CPS) {
                         mbar_arrive_expect_tx(bar, kStageBytes);
@@ -619,7 +716,43 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const GemvArg
         const uint32_t cs = (uint32_t)(T * kTileBytes);  // bytes between chunks in a stage
         const uint32_t wl = ring + ti * kTileBytes + lane * 16;
 
-        bool ok = mbar_wait(sbase + kBarX, 0, a.timeout_ns, a.status);
+        // x arrives once per CTA, or (whole blocks, M > 4) with every stage
+        bool ok = XS ? true : mbar_wait(sbase + kBarX, 0, a.timeout_ns, a.status);
+        if constexpr (SUB) {
+            // x sums per group and row, Sx[gl][m] in FP32 (rows m >= M zero):
+            // 8 threads per (group, row), 16 values each as 8 pairs summed by
+            // a tree of packed adds, then xor-shuffles in a fixed order.
+            float* sxw = reinterpret_cast<float*>(smem + a.off_sx);
+            const int total = ng * a.M * 8;
+            for (int base = 0; base < total; base += kConsumers) {
+                const int task = base + (int)threadIdx.x;
+                const int e = task >> 3, gl = e / a.M, m = e - gl * a.M;
+                float sum = 0.0f;
+                if (ok && task < total) {
+                    const uint32_t src = sbase + a.off_x + m * a.xs_stride + gl * 256 + (task & 7) * 32;
+                    const uint4 p[2] = {lds128(src), lds128(src + 16)};
+                    const uint32_t wv[8] = {p[0].x, p[0].y, p[0].z, p[0].w,
+                                            p[1].x, p[1].y, p[1].z, p[1].w};
+                    float2 f[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        f[i] = __half22float2(*reinterpret_cast<const __half2*>(&wv[i]));
+#pragma unroll
+                    for (int w2 = 4; w2 >= 1; w2 >>= 1)
+#pragma unroll
+                        for (int i = 0; i < w2; ++i) f[i] = __fadd2_rn(f[i], f[i + w2]);
+                    sum = f[0].x + f[0].y;
+                }
+                sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+                sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+                sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+                if (task < total && (task & 7) == 0) sxw[gl * 16 + m] = sum;
+            }
+            for (int i = (int)threadIdx.x; i < ng * 16; i += kConsumers)
+                if ((i & 15) >= a.M) sxw[i] = 0.0f;
+            asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+        }
+        const uint32_t sxl = sbase + a.off_sx + t * 8;  // Sx of this lane's columns 2t, 2t + 1
         const int NS = a.nstages;
         int slot = 0;
         uint32_t phase = 0;  // parity of the ring's current pass
@@ -652,13 +785,17 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const GemvArg
                         ok = false;
                         break;
                     }
-                    const uint32_t wa = wl + slot * kStageBytes;
+                    const uint32_t sa = ring + slot * (uint32_t)a.stage_stride;
+                    const uint32_t wa = wl + slot * (uint32_t)a.stage_stride;
 #pragma unroll
                     for (int gi = 0; gi < 2; ++gi) {
                         const int gl = st * 2 + gi;
-                        mma_group<MT>(wa + gi * 2 * kChunkBytes, kChunkBytes, x0 + xs_off + gi * 256,
-                                      x1 + xs_off + gi * 256, __half2float(sc0[gl]),
-                                      __half2float(sc1[gl]), acc);
+                        const XAddr xad =
+                            XS ? x_stage(align1024(sa + kStageBytes), a.M, 2 * gi, xr0, xr1, t)
+                               : x_slice(x0 + xs_off + gi * 256, x1 + xs_off + gi * 256);
+                        mma_group<MT, SUB>(wa + gi * 2 * kChunkBytes, kChunkBytes, xad,
+                                           __half2float(sc0[gl]), __half2float(sc1[gl]),
+                                           sxl + gl * 64, acc);
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(sbase + kBarEmpty + 8 * slot);
@@ -672,9 +809,12 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const GemvArg
                         ok = false;
                     } else {
                         const int gl = nfull * 2;
-                        mma_group<MT>(wl + slot * kStageBytes, kChunkBytes, x0 + xs_off, x1 + xs_off,
-                                      __half2float(sc0[gl]), __half2float(sc1[gl]),
-                                      acc);
+                        const uint32_t sa = ring + slot * (uint32_t)a.stage_stride;
+                        const XAddr xad = XS ? x_stage(align1024(sa + kStageBytes), a.M, 0, xr0, xr1, t)
+                                             : x_slice(x0 + xs_off, x1 + xs_off);
+                        mma_group<MT, SUB>(wl + slot * (uint32_t)a.stage_stride, kChunkBytes, xad,
+                                           __half2float(sc0[gl]), __half2float(sc1[gl]),
+                                           sxl + gl * 64, acc);
                         __syncwarp();
                         if (lane == 0) mbar_arrive(sbase + kBarEmpty + 8 * slot);
                     }
@@ -686,8 +826,8 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const GemvArg
             } else {
                 // Sub-block units: a stage holds GPS groups of T tiles; the W
                 // warps of a tile take two groups each.
-                if (!unit_stages<MT>(a, sbase, nstg, ng, GPS, ks, wl, cs, x0, x1, sc0, sc1, lane,
-                                     slot, phase, acc))
+                if (!unit_stages<MT, SUB>(a, sbase, nstg, ng, GPS, ks, wl, cs, x0, x1, sxl, sc0, sc1,
+                                          lane, slot, phase, acc))
                     ok = false;
             }
             __syncwarp();
@@ -724,8 +864,8 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const GemvArg
                                   block_of(0) * kBlockRows + t0 * 16, row0, row1, t);
         } else {
             if (has_tail())
-                ok = tail_unit_consume<MT>(a, smem, sbase, ring, nblk, nck, ng, g0, x0, x1, slot,
-                                           phase, ok);
+                ok = tail_unit_consume<MT, SUB>(a, smem, sbase, ring, nblk, nck, ng, g0, x0, x1, sxl,
+                                                slot, phase, ok);
         }
         if (!ok) *abort_flag = 1;
     }
@@ -755,17 +895,39 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const GemvArg
 
 // Whole 128-row blocks per CTA (split or persistent launches).
 // (The tensor map is used only by the tail units of a persistent launch.)
-template <int MT>
+// Variants of the whole-block kernel: x as a CTA-wide slice, x through the
+// ring (M > 4), or the subnormal-code decode (persistent launches, M <= 4).
+enum GemvVariant { kVarSlice = 0, kVarXRing = 1, kVarSubnormal = 2 };
+
+template <int MT, int VAR>
 __global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2)
-    gemv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ GemvArgs a) {
-    gemv_body<MT, true>(&wmap, a);
+    gemv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
+                const __grid_constant__ GemvArgs a) {
+    gemv_body<MT, true, VAR == kVarXRing, VAR == kVarSubnormal>(&wmap, &xmap, a);
+}
+
+// (The subnormal-code variant exists for M <= 8 only.)
+template <int MT>
+const void* gemv_kernel_ptr(int var) {
+    if constexpr (MT == 1)
+        if (var == kVarSubnormal) return reinterpret_cast<const void*>(gemv_kernel<1, kVarSubnormal>);
+    return var == kVarXRing ? reinterpret_cast<const void*>(gemv_kernel<MT, kVarXRing>)
+                            : reinterpret_cast<const void*>(gemv_kernel<MT, kVarSlice>);
 }
 
 // Sub-block units of a.T tiles, weights copied through the tensor map.
-template <int MT>
+template <int MT, int VAR>
 __global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2)
     gemv_unit_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ GemvArgs a) {
-    gemv_body<MT, false>(&wmap, a);
+    gemv_body<MT, false, false, VAR == kVarSubnormal>(&wmap, nullptr, a);
+}
+
+template <int MT>
+const void* gemv_unit_kernel_ptr(int var) {
+    if constexpr (MT == 1)
+        if (var == kVarSubnormal)
+            return reinterpret_cast<const void*>(gemv_unit_kernel<1, kVarSubnormal>);
+    return reinterpret_cast<const void*>(gemv_unit_kernel<MT, kVarSlice>);
 }
 
 struct GemvPlan {
@@ -778,23 +940,25 @@ struct GemvPlan {
     int slab_bytes = 0;
     int rpo = 0;
     int tail_T = 0, tail_base = 0, tail_units = 0;  // persistent launches: last-round units
-    uint32_t off_ring = 0, off_x = 0, off_s = 0, off_red = 0, smem = 0;
+    int xs_stage = 0, stage_stride = kStageBytes;    // x in the ring (whole blocks, M > 4)
+    int var = kVarSlice;                              // whole-block kernel variant
+    uint32_t off_ring = 0, off_x = 0, off_s = 0, off_red = 0, off_sx = 0, smem = 0;
     double cost = 0.0;
 };
 
 template <int MT, bool WHOLE = true>
-int occupancy(uint32_t smem) {
+int occupancy(uint32_t smem, int var = kVarSlice) {
     int blocks = 0;
     const cudaError_t e =
-        WHOLE ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, gemv_kernel<MT>, kGemvThreads,
-                                                              smem)
-              : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, gemv_unit_kernel<MT>,
+        WHOLE ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, gemv_kernel_ptr<MT>(var),
+                                                              kGemvThreads, smem)
+              : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, gemv_unit_kernel_ptr<MT>(var),
                                                               kGemvThreads, smem);
     return e == cudaSuccess ? blocks : 0;
 }
 
 template <int MT>
-int max_active_clusters(int S, uint32_t smem) {
+int max_active_clusters(int S, uint32_t smem, int var) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)S, 1, 1);
     cfg.blockDim = dim3(kGemvThreads, 1, 1);
@@ -807,7 +971,7 @@ int max_active_clusters(int S, uint32_t smem) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemv_kernel<MT>, &cfg) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemv_kernel_ptr<MT>(var), &cfg) != cudaSuccess) return 0;
     return n;
 }
 
@@ -817,11 +981,16 @@ cudaError_t ensure_smem_attr() {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(gemv_kernel<MT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    cudaError_t e = cudaSuccess;
+    for (int var : {kVarSlice, kVarXRing, kVarSubnormal})  // (M > 8: no subnormal variant)
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gemv_kernel_ptr<MT>(var),
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(gemv_unit_kernel<MT>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        for (int var : {kVarSlice, kVarSubnormal})
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(gemv_unit_kernel_ptr<MT>(var),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev].store(true, std::memory_order_release);
     return e;
 }
@@ -831,10 +1000,17 @@ cudaError_t ensure_smem_attr() {
 // reduction buffer of its tail units).
 template <int MT>
 bool layout(GemvPlan& p, int M, int G, int S, int T, int nsb, const DeviceCtx& ctx,
-            int nst = kStages) {
+            int nst = kStages, bool subnormal = false) {
     p.S = S;
     p.T = T;
     p.n_sbuf = nsb;
+    // whole blocks with M > 4: x rides in the ring (4 chunks x M rows per
+    // stage, 1024-aligned in a slot with 1 KB of slack) instead of a CTA-wide
+    // M x K slice, which at M = 16, K = 4096 alone takes 128 KB
+    const bool xs = T == kConsumerWarps && M > 4;
+    p.xs_stage = xs ? ((512 * M + 1023) / 1024) * 1024 + 1024 : 0;
+    p.stage_stride = kStageBytes + p.xs_stage;
+    p.var = xs ? kVarXRing : subnormal ? kVarSubnormal : kVarSlice;
     const int ng_max = (G + S - 1) / S;
     // a CTA that sees only one block needs no more stages than it fills
     const int fill = (2 * ng_max * T * kTileBytes + kStageBytes - 1) / kStageBytes;
@@ -842,14 +1018,15 @@ bool layout(GemvPlan& p, int M, int G, int S, int T, int nsb, const DeviceCtx& c
     p.xs_stride = ng_max * kGroup * 2 + 16;  // +16 B keeps x rows conflict-free
     p.slab_bytes = ((16 * T * G * 2 + 127) / 128) * 128;
     p.off_ring = kBarAreaBytes;
-    p.off_x = p.off_ring + p.nstages * kStageBytes;
-    p.off_s = p.off_x + ((M * p.xs_stride + 127) / 128) * 128;
+    p.off_x = p.off_ring + p.nstages * p.stage_stride;
+    p.off_s = p.off_x + (xs ? 0 : ((M * p.xs_stride + 127) / 128) * 128);
     p.off_red = p.off_s + nsb * p.slab_bytes;
     p.rpo = (kBlockRows + S - 1) / S;
     const int red_bytes = S > 1 ? S * p.rpo * 16 * 4
                           : T < kConsumerWarps || nsb == 2 ? kConsumerWarps * MT * 32 * 16
                                                            : 0;
-    p.smem = p.off_red + red_bytes;
+    p.off_sx = p.off_red + red_bytes;
+    p.smem = p.off_sx + (p.var == kVarSubnormal ? ng_max * 16 * 4 : 0);
     return (int)p.smem <= ctx.max_smem_optin;
 }
 
@@ -863,6 +1040,7 @@ bool layout(GemvPlan& p, int M, int G, int S, int T, int nsb, const DeviceCtx& c
 // range) adds to both.  A K split adds the cluster barrier and the exchange
 // of partial sums through distributed shared memory.
 constexpr double kWaveUs = 1.5;
+constexpr int kSubnormalMinGroups = 16;  // groups per warp and x-sum round
 constexpr double kSmBytesPerUs = 36.0e3;
 constexpr double kCtaBytesPerUs = 14.0e3;
 constexpr double kXBytesPerUs = 16.0e3;
@@ -894,15 +1072,18 @@ GemvPlan plan_gemv(int M, int N, int K, const DeviceCtx& ctx) {
     const int NB = (N + kBlockRows - 1) / kBlockRows;
     {
         GemvPlan p;
-        if (layout<MT>(p, M, G, 1, kConsumerWarps, 2, ctx)) {
-            const int occ = occupancy<MT>(p.smem);
+        // Persistent launches with M <= 4 take the subnormal-code decode: its
+        // x-sum pass costs ~0.3 us once per CTA, paid back over many blocks.
+        const bool sn = MT == 1 && M <= 4;
+        if (layout<MT>(p, M, G, 1, kConsumerWarps, 2, ctx, kStages, sn)) {
+            const int occ = occupancy<MT>(p.smem, p.var);
             if (occ > 0 && NB > ctx.num_sms * occ) {
                 // The deepest ring that keeps the same CTAs per SM: more bytes
                 // in flight per CTA, for the same number of streams.
                 for (int nst = kMaxStages; nst > kStages; --nst) {
                     GemvPlan q;
-                    if (layout<MT>(q, M, G, 1, kConsumerWarps, 2, ctx, nst) &&
-                        occupancy<MT>(q.smem) == occ) {
+                    if (layout<MT>(q, M, G, 1, kConsumerWarps, 2, ctx, nst, sn) &&
+                        occupancy<MT>(q.smem, q.var) == occ) {
                         p = q;
                         break;
                     }
@@ -912,7 +1093,7 @@ GemvPlan plan_gemv(int M, int N, int K, const DeviceCtx& ctx) {
                 // the smallest T that gives each of the first CTAs at most one
                 // (T / 8 of a block-time instead of a whole one).
                 const int rem = NB % p.grid_y;
-                for (int tt = 1; rem > 0 && tt < kConsumerWarps; tt *= 2) {
+                for (int tt = 1; rem > 0 && p.xs_stage == 0 && tt < kConsumerWarps; tt *= 2) {
                     if (rem * (kConsumerWarps / tt) <= p.grid_y) {
                         p.tail_T = tt;
                         p.tail_base = NB - rem;
@@ -928,14 +1109,33 @@ GemvPlan plan_gemv(int M, int N, int K, const DeviceCtx& ctx) {
     GemvPlan best;
     const int max_s = G < kMaxSplits ? G : kMaxSplits;
     for (int S = 1; S <= max_s; ++S) {
+        // Clusters live inside one GPC: count co-resident clusters, not SM slots.
+        auto slots_of = [&](const GemvPlan& q) -> long long {
+            const int occ = occupancy<MT>(q.smem, q.var);
+            if (occ == 0) return 0;
+            return S == 1 ? (long long)ctx.num_sms * occ
+                          : (long long)max_active_clusters<MT>(S, q.smem, q.var) * S;
+        };
         GemvPlan p;
         if (!layout<MT>(p, M, G, S, kConsumerWarps, 1, ctx)) continue;
-        const int occ = occupancy<MT>(p.smem);
-        if (occ == 0) continue;
-        // Clusters live inside one GPC: count co-resident clusters, not SM slots.
-        const long long slots =
-            S == 1 ? (long long)ctx.num_sms * occ : (long long)max_active_clusters<MT>(S, p.smem) * S;
+        long long slots = slots_of(p);
         if (slots == 0) continue;
+        // Unsplit: the deepest ring that needs no more waves -- more bytes in
+        // flight per CTA, and no SM given more CTAs than the grid needs (a grid
+        // of 2 per SM on 3 slots per SM leaves some SMs 3 CTAs and others 1).
+        // (Clusters of 5 to 8 with fewer CTAs per SM measured slower.)
+        const long long units = (long long)NB * S;
+        const long long waves = (units + slots - 1) / slots;
+        for (int nst = kMaxStages; S == 1 && nst > p.nstages; --nst) {
+            GemvPlan q;
+            if (!layout<MT>(q, M, G, S, kConsumerWarps, 1, ctx, nst) || q.nstages != nst) continue;
+            const long long qs = slots_of(q);
+            if (qs > 0 && (units + qs - 1) / qs <= waves) {
+                p = q;
+                slots = qs;
+                break;
+            }
+        }
         const int ng = (G + S - 1) / S;
         p.grid_y = NB;
         p.cost = launch_cost<MT>((long long)NB * S, slots, (double)ng * kBlockRows * kGroup / 2,
@@ -944,16 +1144,22 @@ GemvPlan plan_gemv(int M, int N, int K, const DeviceCtx& ctx) {
     }
     for (int T = 1; T < kConsumerWarps; T *= 2) {
         GemvPlan p;
-        if (!layout<MT>(p, M, G, 1, T, 1, ctx)) continue;
-        const int occ = occupancy<MT, false>(p.smem);
+        // The subnormal-code decode saves 4 instructions per 8 weights; its
+        // x-sum pass (ceil(8 G M / 256) rounds, on the path before the first
+        // MMA) pays off only with >= 16 groups per warp and round (units of
+        // 64 rows at K = 4096 and M = 1: yes; 16 rows at K = 14336: no).
+        const int sx_rounds = (G * M * 8 + kConsumers - 1) / kConsumers;
+        const bool sn = MT == 1 && M <= 4 && G * T / kConsumerWarps >= kSubnormalMinGroups * sx_rounds;
+        if (!layout<MT>(p, M, G, 1, T, 1, ctx, kStages, sn)) continue;
+        const int occ = occupancy<MT, false>(p.smem, p.var);
         if (occ == 0) continue;
         const long long units = ((long long)N + 16 * T - 1) / (16 * T);
         const long long fit = (units + ctx.num_sms - 1) / ctx.num_sms;
         const int need = fit < occ ? (int)fit : occ;
         for (int nst = kMaxStages; nst > p.nstages; --nst) {
             GemvPlan q;
-            if (layout<MT>(q, M, G, 1, T, 1, ctx, nst) && q.nstages == nst &&
-                occupancy<MT, false>(q.smem) >= need) {
+            if (layout<MT>(q, M, G, 1, T, 1, ctx, nst, sn) && q.nstages == nst &&
+                occupancy<MT, false>(q.smem, q.var) >= need) {
                 p = q;
                 break;
             }
@@ -1031,6 +1237,44 @@ cudaError_t weight_map(const uint8_t* wq, int NB, int K, int T, CUtensorMap* out
     return cudaSuccess;
 }
 
+// The tensor map of x for launches that stream it through the ring: x[M, K]
+// as [K / 64 chunks][M rows][64 halves], a box of 4 chunks x M rows (one
+// stage), 128-byte swizzled.  Cached per (x, M, K): a decode loop reuses its
+// activation buffers.
+cudaError_t x_map(const void* x, int M, int K, CUtensorMap* out) {
+    struct Entry {
+        const void* x;
+        int M, K;
+        CUtensorMap map;
+    };
+    static std::mutex mu;
+    static std::vector<Entry> cache;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (const Entry& e : cache)
+            if (e.x == x && e.M == M && e.K == K) {
+                *out = e.map;
+                return cudaSuccess;
+            }
+    }
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode) return cudaErrorNotSupported;
+    Entry e{x, M, K, {}};
+    const cuuint64_t dims[3] = {(cuuint64_t)kChunkK, (cuuint64_t)M, (cuuint64_t)(K / kChunkK)};
+    const cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)kChunkK * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)kChunkK, (cuuint32_t)M, 4};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (encode(&e.map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(x), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    *out = e.map;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache.size() >= 4096) cache.clear();
+    cache.push_back(e);
+    return cudaSuccess;
+}
+
 template <int MT>
 cudaError_t launch_gemv_mt(GemvArgs args, int M, cudaStream_t stream, const DeviceCtx& ctx) {
     cudaError_t e = ensure_smem_attr<MT>();
@@ -1050,6 +1294,14 @@ cudaError_t launch_gemv_mt(GemvArgs args, int M, cudaStream_t stream, const Devi
     args.tail_T = p.tail_T;
     args.tail_base = p.tail_base;
     args.tail_units = p.tail_units;
+    args.xs_stage = p.xs_stage;
+    args.stage_stride = p.stage_stride;
+    args.off_sx = p.off_sx;
+    CUtensorMap xmap = {};
+    if (p.xs_stage) {
+        const cudaError_t xe = x_map(args.x, M, args.K, &xmap);
+        if (xe != cudaSuccess) return xe;
+    }
     CUtensorMap wmap = {};
     if (p.T < kConsumerWarps || p.tail_T > 0) {
         const cudaError_t me =
@@ -1075,8 +1327,12 @@ cudaError_t launch_gemv_mt(GemvArgs args, int M, cudaStream_t stream, const Devi
     }
     cfg.attrs = attrs;
     cfg.numAttrs = na;
-    if (p.T < kConsumerWarps) return cudaLaunchKernelEx(&cfg, gemv_unit_kernel<MT>, wmap, args);
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<MT>, wmap, args);
+    if (p.T < kConsumerWarps) {
+        void* kargs[] = {&wmap, &args};
+        return cudaLaunchKernelExC(&cfg, gemv_unit_kernel_ptr<MT>(p.var), kargs);
+    }
+    void* kargs[] = {&wmap, &xmap, &args};
+    return cudaLaunchKernelExC(&cfg, gemv_kernel_ptr<MT>(p.var), kargs);
 }
 
 }  // namespace
