@@ -46,6 +46,21 @@ def test_gemv_every_row(w4lib, M, N, K):
     assert w4.device_status() == 0
 
 
+@pytest.mark.parametrize("M", [1, 9])
+def test_many_units_every_row(w4lib, M):
+    """More units than one wave of CTAs holds, the last one ragged
+    (N = 60001); a repeat call is bit-identical."""
+    N, K = 60001, 1024
+    _, blocks = blocks_of(N, K, 620)
+    x16 = acts(M, K, 621 + M)
+    y = w4.gemm_q4_0(from_bits16(x16), u8(blocks))
+    torch.cuda.synchronize()
+    assert_close(y.float().cpu().numpy(), oracle.gemm_q4_0(x16, blocks), f"q4_0 M={M}")
+    assert np.array_equal(w4.gemm_q4_0(from_bits16(x16), u8(blocks)).cpu().numpy(),
+                          y.cpu().numpy())
+    assert w4.device_status() == 0
+
+
 def test_out_is_checked(w4lib):
     """A caller's y of the wrong shape or dtype is refused before any launch."""
     _, blocks = blocks_of(64, 256, 530)
