@@ -729,8 +729,20 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const CUtenso
                 const int e = task >> 3, gl = e / a.M, m = e - gl * a.M;
                 float sum = 0.0f;
                 if (ok && task < total) {
-                    const uint32_t src = sbase + a.off_x + m * a.xs_stride + gl * 256 + (task & 7) * 32;
-                    const uint4 p[2] = {lds128(src), lds128(src + 16)};
+                    uint4 p[2];
+                    if (XS) {
+                        // x rides in the ring: read the CTA's K range from global memory
+                        // (after the grid-dependency wait, so the previous kernel's x is there)
+                        const uint4* src = reinterpret_cast<const uint4*>(
+                            a.x + (size_t)m * a.K + (size_t)(g0 + gl) * kGroup + (task & 7) * 16);
+                        p[0] = src[0];
+                        p[1] = src[1];
+                    } else {
+                        const uint32_t src =
+                            sbase + a.off_x + m * a.xs_stride + gl * 256 + (task & 7) * 32;
+                        p[0] = lds128(src);
+                        p[1] = lds128(src + 16);
+                    }
                     const uint32_t wv[8] = {p[0].x, p[0].y, p[0].z, p[0].w,
                                             p[1].x, p[1].y, p[1].z, p[1].w};
                     float2 f[8];
@@ -897,20 +909,24 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const CUtenso
 // (The tensor map is used only by the tail units of a persistent launch.)
 // Variants of the whole-block kernel: x as a CTA-wide slice, x through the
 // ring (M > 4), or the subnormal-code decode (persistent launches, M <= 4).
-enum GemvVariant { kVarSlice = 0, kVarXRing = 1, kVarSubnormal = 2 };
+enum GemvVariant { kVarSlice = 0, kVarXRing = 1, kVarSubnormal = 2, kVarXRingSubnormal = 3 };
 
 template <int MT, int VAR>
 __global__ void __launch_bounds__(kGemvThreads, MT == 1 ? 3 : 2)
     gemv_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
                 const __grid_constant__ GemvArgs a) {
-    gemv_body<MT, true, VAR == kVarXRing, VAR == kVarSubnormal>(&wmap, &xmap, a);
+    gemv_body<MT, true, VAR == kVarXRing || VAR == kVarXRingSubnormal,
+              VAR == kVarSubnormal || VAR == kVarXRingSubnormal>(&wmap, &xmap, a);
 }
 
-// (The subnormal-code variant exists for M <= 8 only.)
+// (The subnormal-code variant with x as a CTA-wide slice exists for M <= 8
+// only: above that x always rides in the ring.)
 template <int MT>
 const void* gemv_kernel_ptr(int var) {
     if constexpr (MT == 1)
         if (var == kVarSubnormal) return reinterpret_cast<const void*>(gemv_kernel<1, kVarSubnormal>);
+    if (var == kVarXRingSubnormal)
+        return reinterpret_cast<const void*>(gemv_kernel<MT, kVarXRingSubnormal>);
     return var == kVarXRing ? reinterpret_cast<const void*>(gemv_kernel<MT, kVarXRing>)
                             : reinterpret_cast<const void*>(gemv_kernel<MT, kVarSlice>);
 }
@@ -982,7 +998,7 @@ cudaError_t ensure_smem_attr() {
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
     cudaError_t e = cudaSuccess;
-    for (int var : {kVarSlice, kVarXRing, kVarSubnormal})  // (M > 8: no subnormal variant)
+    for (int var : {kVarSlice, kVarXRing, kVarSubnormal, kVarXRingSubnormal})
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(gemv_kernel_ptr<MT>(var),
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
@@ -1010,7 +1026,7 @@ bool layout(GemvPlan& p, int M, int G, int S, int T, int nsb, const DeviceCtx& c
     const bool xs = T == kConsumerWarps && M > 4;
     p.xs_stage = xs ? ((512 * M + 1023) / 1024) * 1024 + 1024 : 0;
     p.stage_stride = kStageBytes + p.xs_stage;
-    p.var = xs ? kVarXRing : subnormal ? kVarSubnormal : kVarSlice;
+    p.var = xs ? (subnormal ? kVarXRingSubnormal : kVarXRing) : subnormal ? kVarSubnormal : kVarSlice;
     const int ng_max = (G + S - 1) / S;
     // a CTA that sees only one block needs no more stages than it fills
     const int fill = (2 * ng_max * T * kTileBytes + kStageBytes - 1) / kStageBytes;
@@ -1026,7 +1042,7 @@ bool layout(GemvPlan& p, int M, int G, int S, int T, int nsb, const DeviceCtx& c
                           : T < kConsumerWarps || nsb == 2 ? kConsumerWarps * MT * 32 * 16
                                                            : 0;
     p.off_sx = p.off_red + red_bytes;
-    p.smem = p.off_sx + (p.var == kVarSubnormal ? ng_max * 16 * 4 : 0);
+    p.smem = p.off_sx + (subnormal ? ng_max * 16 * 4 : 0);
     return (int)p.smem <= ctx.max_smem_optin;
 }
 
@@ -1072,9 +1088,10 @@ GemvPlan plan_gemv(int M, int N, int K, const DeviceCtx& ctx) {
     const int NB = (N + kBlockRows - 1) / kBlockRows;
     {
         GemvPlan p;
-        // Persistent launches with M <= 4 take the subnormal-code decode: its
-        // x-sum pass costs ~0.3 us once per CTA, paid back over many blocks.
-        const bool sn = MT == 1 && M <= 4;
+        // Persistent launches take the subnormal-code decode: its x-sum pass
+        // (~0.3 us once per CTA; from global memory when x rides in the ring)
+        // is paid back over many blocks.
+        const bool sn = true;
         if (layout<MT>(p, M, G, 1, kConsumerWarps, 2, ctx, kStages, sn)) {
             const int occ = occupancy<MT>(p.smem, p.var);
             if (occ > 0 && NB > ctx.num_sms * occ) {
