@@ -454,7 +454,12 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const CUtenso
             if (lane == 0) {
                 const uint64_t pol = l2_policy_evict_first();
                 const size_t block_stride = (size_t)C * kChunkBytes;
-                {   // L2 prefetch of the first block (weights of this split, scale slab).
+                // L2 prefetch of the first block's second ring pass, issued
+                // once the first pass is (the first copies go out unhindered);
+                // M > 8 with the subnormal decode issues it up front, where
+                // the kernel keeps its registers.
+                constexpr bool kLatePrefetch = !(MT == 2 && SUB);
+                if constexpr (!kLatePrefetch) {
                     const int rb = (int)blockIdx.y;
                     const uint8_t* w = a.wq + (size_t)rb * block_stride + 2 * (size_t)g0 * kChunkBytes;
                     const int pre = nstg < 2 * a.nstages ? nstg : 2 * a.nstages;
@@ -519,6 +524,12 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const CUtenso
                     // --- weight stages of block rb ---
                     const uint8_t* w = a.wq + (size_t)rb * block_stride + 2 * (size_t)g0 * kChunkBytes;
                     for (int st = 0; st < nstg; ++st) {
+                        if constexpr (kLatePrefetch) {
+                            if (it == NS && j == 0)
+                                for (int i = NS; i < nstg && i < 2 * NS; ++i)
+                                    bulk_prefetch_l2(w + (size_t)i * kStageBytes,
+                                                     min(CPS, nck - i * CPS) * kChunkBytes);
+                        }
                         if (it >= NS && !x_issued) issue_x();
                         if (it >= NS &&
                             !mbar_wait(sbase + kBarEmpty + 8 * slot, (round - 1) & 1, a.timeout_ns,
