@@ -638,10 +638,6 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const CUtenso
                 const int box_x = t0 * (kTileBytes / 8);     // map x coordinate of its tiles
                 const int cy0 = rb * C + 2 * g0;             // map row of its first chunk
                 tma_prefetch_map(wmap);
-                // L2 prefetch of the stages beyond the first ring pass (those
-                // inside it load now)
-                for (int i = NS; i < nstg && i < 2 * NS; ++i)
-                    if ((i + 1) * CPS <= nck) tma_prefetch_2d(wmap, box_x, cy0 + i * CPS);
                 {   // scale slab of the unit's rows
                     const int rows = min(16 * T, a.N - r0);
                     const uint32_t bytes = (uint32_t)(rows * a.G * 2);
@@ -667,6 +663,10 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const CUtenso
                 int it = 0, slot = 0, round = 0;  // slot = it % NS, round = it / NS
                 bool ok = true;
                 for (; it < nstg; ++it) {
+                    // L2 prefetch of the second ring pass once the first is issued
+                    if (it == NS)
+                        for (int i = NS; i < nstg && i < 2 * NS; ++i)
+                            if ((i + 1) * CPS <= nck) tma_prefetch_2d(wmap, box_x, cy0 + i * CPS);
                     if (it >= NS && !x_issued) issue_x();
                     if (it >= NS && !mbar_wait(sbase + kBarEmpty + 8 * slot, (round - 1) & 1,
                                                a.timeout_ns, a.status)) {
