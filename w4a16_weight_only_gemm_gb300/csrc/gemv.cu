@@ -443,7 +443,7 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const CUtenso
     // memory, which must not be written before those CTAs run.  Every thread
     // arrives here and waits (cluster_wait) once before the exchange.
     if (S > 1) cluster_arrive_relaxed();
-    // Dependents may start their own prologue (and L2 prefetch) right away;
+    // Dependents may start their own prologue (and first copies) right away;
     // their griddepcontrol.wait still waits for this grid to complete.
     grid_launch_dependents();
 
@@ -454,12 +454,9 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const CUtenso
             if (lane == 0) {
                 const uint64_t pol = l2_policy_evict_first();
                 const size_t block_stride = (size_t)C * kChunkBytes;
-                // L2 prefetch of the first block's second ring pass, issued
-                // once the first pass is (the first copies go out unhindered);
-                // M > 8 with the subnormal decode issues it up front, where
-                // the kernel keeps its registers.
-                constexpr bool kLatePrefetch = !(MT == 2 && SUB);
-                if constexpr (!kLatePrefetch) {
+                if constexpr (MT == 2 && SUB) {
+                    // L2 prefetch of the first block (x in the ring, M > 8): kept
+                    // only here, where dropping it leaves the kernel spilling
                     const int rb = (int)blockIdx.y;
                     const uint8_t* w = a.wq + (size_t)rb * block_stride + 2 * (size_t)g0 * kChunkBytes;
                     const int pre = nstg < 2 * a.nstages ? nstg : 2 * a.nstages;
@@ -524,12 +521,6 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const CUtenso
                     // --- weight stages of block rb ---
                     const uint8_t* w = a.wq + (size_t)rb * block_stride + 2 * (size_t)g0 * kChunkBytes;
                     for (int st = 0; st < nstg; ++st) {
-                        if constexpr (kLatePrefetch) {
-                            if (it == NS && j == 0)
-                                for (int i = NS; i < nstg && i < 2 * NS; ++i)
-                                    bulk_prefetch_l2(w + (size_t)i * kStageBytes,
-                                                     min(CPS, nck - i * CPS) * kChunkBytes);
-                        }
                         if (it >= NS && !x_issued) issue_x();
                         if (it >= NS &&
                             !mbar_wait(sbase + kBarEmpty + 8 * slot, (round - 1) & 1, a.timeout_ns,
@@ -663,10 +654,6 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const CUtenso
                 int it = 0, slot = 0, round = 0;  // slot = it % NS, round = it / NS
                 bool ok = true;
                 for (; it < nstg; ++it) {
-                    // L2 prefetch of the second ring pass once the first is issued
-                    if (it == NS)
-                        for (int i = NS; i < nstg && i < 2 * NS; ++i)
-                            if ((i + 1) * CPS <= nck) tma_prefetch_2d(wmap, box_x, cy0 + i * CPS);
                     if (it >= NS && !x_issued) issue_x();
                     if (it >= NS && !mbar_wait(sbase + kBarEmpty + 8 * slot, (round - 1) & 1,
                                                a.timeout_ns, a.status)) {
