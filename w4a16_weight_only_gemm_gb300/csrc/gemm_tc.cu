@@ -311,11 +311,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const size_t C = (size_t)(a.K / kBK);
             const uint8_t* w1 = a.wq + ((size_t)wb * C + kb0) * 4096 + (size_t)wt0 * 512;
             const uint8_t* w2 = a.wq + ((size_t)(wb + 1) * C + kb0) * 4096;
-            for (int i = 0; i < NS && i < nkb; ++i) {
-                if (wn1) bulk_prefetch_l2(w1 + (size_t)i * 4096, (uint32_t)wn1 * 512);
-                if (wn2) bulk_prefetch_l2(w2 + (size_t)i * 4096, (uint32_t)wn2 * 512);
-            }
-            grid_dependency_wait();
+            // Weights and scales are constants of the call: the scale slab and
+            // the first ring pass's packed weights load while the previous
+            // kernel may still run; x (its output, possibly) after the wait.
             if (a.slab_tma) {  // this split's groups of the CTA's TW rows
                 mbar_arrive_expect_tx(base + kBarSlab, (uint32_t)(TW * a.slab_ld * 2));
                 tma_load_2d(base + kOffSlab, &smap, slab_g0, r_start, base + kBarSlab);
@@ -329,9 +327,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 mbar_arrive_expect_tx(base + kBarSlab, bulk);
                 if (bulk) bulk_g2s(base + kOffSlab, src, bulk, base + kBarSlab);
             }
-            int issued = 0;
+            const int first = NS < nkb ? NS : nkb;  // the first ring pass
+            for (int i = 0; i < first; ++i) {
+                mbar_arrive_expect_tx(base + kBarLoadFull + 8 * i,
+                                      kXBytes + (uint32_t)wvalid_tiles * 512);
+                if (wn1)
+                    bulk_g2s(base + kOffW + i * kWStg, w1 + (size_t)i * 4096, (uint32_t)wn1 * 512,
+                             base + kBarLoadFull + 8 * i);
+                if (wn2)
+                    bulk_g2s(base + kOffW + i * kWStg + (uint32_t)wn1 * 512, w2 + (size_t)i * 4096,
+                             (uint32_t)wn2 * 512, base + kBarLoadFull + 8 * i);
+            }
+            grid_dependency_wait();
+            for (int i = 0; i < first; ++i)
+#pragma unroll
+                for (int xt = 0; xt < XT; ++xt)
+                    tma_load_2d(base + kOffX + i * kXBytes + xt * kXStageBytes, &xmap, (kb0 + i) * kBK,
+                                m0 + xt * 2 * kTileX, base + kBarLoadFull + 8 * i);
+            int issued = first;
             bool ok = true;
-            for (int i = 0, ts = 0, round = 0; i < nkb; ++i) {
+            for (int i = first, ts = first % NS, round = first / NS; i < nkb; ++i) {
                 if (i >= NS &&
                     !mbar_wait(base + kBarFree + 8 * ts, (round - 1) & 1, a.timeout_ns,
                                a.status)) {
