@@ -159,9 +159,15 @@ def _launch_of(plan) -> str:
     return "unit" if plan["rows_per_cta"] < 128 else "whole"
 
 
+# (At M = 1 the planner no longer splits K for these shapes: one CTA's x
+# slice is small, and units skip the cluster reduction.  The split kernel at
+# M = 1 is the one at M = 3.)
+OFFSET_LAUNCHES = [(launch, M) for launch in ("unit", "split", "persistent")
+                   for M in (1, 3, 9, 16) if (launch, M) != ("split", 1)]
+
+
 @pytest.mark.parametrize("kind", synthetic.OFFSET_KINDS)
-@pytest.mark.parametrize("M", [1, 3, 9, 16])
-@pytest.mark.parametrize("launch", ["unit", "split", "persistent"])
+@pytest.mark.parametrize("launch,M", OFFSET_LAUNCHES)
 def test_offset_activations_all_rows(w4lib, kind, M, launch):
     """The first candidate shape the planner launches this way, every row."""
     shapes = [(N, K) for N, K in OFFSET_CANDIDATES[launch]

@@ -1057,7 +1057,7 @@ constexpr double kWaveUs = 1.5;
 constexpr int kSubnormalMinGroups = 16;  // groups per warp and x-sum round
 constexpr double kSmBytesPerUs = 36.0e3;
 constexpr double kCtaBytesPerUs = 14.0e3;
-constexpr double kXBytesPerUs = 16.0e3;
+constexpr double kXBytesPerUs = 32.0e3;
 constexpr double kSplitReduceUs = 1.6;
 
 template <int MT>
