@@ -34,6 +34,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -806,10 +807,10 @@ TcPlan tc_plan(int64_t M, int64_t N, int64_t K, const DeviceCtx& ctx, bool fmt =
 }
 
 cudaError_t ensure_tc_attrs(const DeviceCtx& ctx) {
-    static bool attr_done[64] = {};
+    static std::atomic<bool> attr_done[64];  // per device; racing callers only repeat the set-up
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && attr_done[dev]) return cudaSuccess;
+    if (dev >= 0 && dev < 64 && attr_done[dev].load(std::memory_order_acquire)) return cudaSuccess;
     for (auto fn : {gemm_tc_kernel<false, 1>, gemm_tc_kernel<true, 1>, gemm_tc_kernel<true, 2>,
                     gemm_tc_kernel<false, 1, true>, gemm_tc_kernel<true, 1, true>,
                     gemm_tc_kernel<true, 2, true>, gemm_tc_kernel<true, 2, false, 96>,
@@ -818,7 +819,7 @@ cudaError_t ensure_tc_attrs(const DeviceCtx& ctx) {
                                              ctx.max_smem_optin);
         if (e != cudaSuccess) return e;
     }
-    if (dev >= 0 && dev < 64) attr_done[dev] = true;
+    if (dev >= 0 && dev < 64) attr_done[dev].store(true, std::memory_order_release);
     return cudaSuccess;
 }
 
