@@ -90,9 +90,18 @@ struct GemvArgs {
     int T;                   // 16-row tiles per CTA: 8 = whole blocks; 1, 2, 4 = sub-block units
     int xs_stride;           // bytes between x rows in shared memory
     int slab_bytes;          // bytes of one scale buffer (16 T rows x G, rounded)
-    int n_sbuf;              // scale buffers: 2 when a CTA walks several blocks
+    int n_sbuf;              // scale buffers: 2 when a CTA walks several blocks, else 1
     int nstages;             // ring stages (<= kMaxStages)
     int rpo;                 // rows owned per CTA in the split reduction
+    // Launch constants computed on the host, so that a CTA's producer gets
+    // to its first copy with few instructions (it shares the SM's issue slots
+    // with the previous kernel's CTAs): for units, chunks and groups per
+    // stage, warps per tile and stages per unit; for persistent launches the
+    // blocks per CTA (nb_q, plus one on the first nb_r CTAs); for a K split
+    // the first group of every split (g0s[S] = G).
+    int cps, gps, wpt, nstg_u;
+    int nb_q, nb_r;
+    int g0s[kMaxSplits + 1];
     // Persistent whole-block launches whose last round is partial: the
     // blocks from tail_base on run as tail_units sub-block units of tail_T
     // tiles (tail_T = 0: no tail), unit u on CTA u after its whole blocks.
@@ -109,14 +118,8 @@ struct GemvArgs {
 
 __device__ __forceinline__ uint32_t align1024(uint32_t a) { return (a + 1023u) & ~1023u; }
 
-// x addresses of a stage's chunk pair (cc0, cc0 + 1) when x rides in the
-// ring: the box lands as [chunk][row][128 bytes] with 16-byte units swizzled
-// by the 128-byte row's index within its 1024-byte atom.
-
-
-__device__ __forceinline__ int split_group_begin(int split, int S, int G) {
-    return (int)(((long long)split * G) / S);
-}
+// The first group of split `split` of S over G groups (host side).
+inline int split_group_begin(int split, int S, int G) { return (split * G) / S; }
 
 // One 128-wide group (two chunks) of one consumer lane: 8 MMAs into fresh
 // FP32 fragments, then scaled into acc.  The A fragments hold the exact codes
@@ -351,7 +354,7 @@ __device__ __noinline__ bool tail_unit_consume(const GemvArgs& a, uint8_t* smem,
     const int tT = a.tail_T;
     const int t_rb = a.tail_base + (int)blockIdx.y / (kConsumerWarps / tT);
     const int t_t0 = ((int)blockIdx.y % (kConsumerWarps / tT)) * tT;
-    const int sbuf = nblk % a.n_sbuf;
+    const int sbuf = nblk & (a.n_sbuf - 1);
     const int W2 = kConsumerWarps / tT;
     const int ti2 = warp / W2, ks2 = warp - ti2 * W2;
     const int tr0 = ti2 * 16 + g, tr1 = tr0 + 8;
@@ -364,7 +367,8 @@ __device__ __noinline__ bool tail_unit_consume(const GemvArgs& a, uint8_t* smem,
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) tacc[mt][e] = 0.0f;
-    if (ok && !mbar_wait(sbase + kBarSFull + 8 * sbuf, (nblk / a.n_sbuf) & 1, a.timeout_ns, a.status))
+    if (ok && !mbar_wait(sbase + kBarSFull + 8 * sbuf, (nblk >> (a.n_sbuf - 1)) & 1, a.timeout_ns,
+                         a.status))
         ok = false;
     if (ok) {
         const __half* tsc0 =
@@ -396,19 +400,18 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const CUtenso
     const int C = a.K / kChunkK;
     const int T = WHOLE ? kConsumerWarps : a.T;
     constexpr bool whole = WHOLE;
-    const int W = kConsumerWarps / T;        // warps per tile, sharing out its groups
-    const int CPS = kStageBytes / (T * kTileBytes);  // chunks per stage
-    const int GPS = CPS / 2;                         // groups per stage
-    const int g0 = split_group_begin(split, S, a.G);
-    const int ng = split_group_begin(split + 1, S, a.G) - g0;
+    // warps per tile (sharing out its groups), chunks and groups per stage
+    const int W = WHOLE ? 1 : a.wpt;
+    const int CPS = WHOLE ? kStageBytes / (kConsumerWarps * kTileBytes) : a.cps;
+    const int GPS = WHOLE ? CPS / 2 : a.gps;
+    const int g0 = a.g0s[split];
+    const int ng = a.g0s[split + 1] - g0;
     const int nck = 2 * ng;
-    const int nstg = (nck + CPS - 1) / CPS;
+    const int nstg = WHOLE ? (nck + CPS - 1) / CPS : a.nstg_u;
     // Whole blocks: the CTA walks blocks y, y + gridDim.y, ...  Sub-block
     // units: CTA y owns rows [16 T y, 16 T (y + 1)), tiles t0 .. t0 + T - 1
     // of block 16 T y / 128.
-    const int nblk = !whole ? 1
-                     : a.tail_T ? a.tail_base / (int)gridDim.y
-                                : (a.NB - (int)blockIdx.y + (int)gridDim.y - 1) / (int)gridDim.y;
+    const int nblk = !whole ? 1 : a.nb_q + ((int)blockIdx.y < a.nb_r ? 1 : 0);
     // The tail unit of this CTA (persistent launches with a partial last
     // round): tT tiles from tile t_t0 of block t_rb.  Evaluated where used.
     auto has_tail = [&]() { return whole && !XS && a.tail_T > 0 && (int)blockIdx.y < a.tail_units; };
@@ -498,9 +501,9 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const CUtenso
                 for (int j = 0; ok && j < nblk; ++j) {
                     const int rb = (int)blockIdx.y + j * (int)gridDim.y;
                     // --- scale slab of block rb ---
-                    const int sbuf = j % a.n_sbuf;
+                    const int sbuf = j & (a.n_sbuf - 1);
                     if (j >= a.n_sbuf &&
-                        !mbar_wait(sbase + kBarSEmpty + 8 * sbuf, ((j / a.n_sbuf) - 1) & 1,
+                        !mbar_wait(sbase + kBarSEmpty + 8 * sbuf, ((j >> (a.n_sbuf - 1)) - 1) & 1,
                                    a.timeout_ns, a.status)) {
                         ok = false;
                         break;
@@ -551,9 +554,9 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const CUtenso
                     // The tail unit: scale slab of its 16 tT rows, then boxes of
                     // tT tiles x 32 / tT chunks through the tensor map.
                     W4A16_TAIL_GEOMETRY
-                    const int sbuf = nblk % a.n_sbuf;
+                    const int sbuf = nblk & (a.n_sbuf - 1);
                     if (nblk >= a.n_sbuf &&
-                        !mbar_wait(sbase + kBarSEmpty + 8 * sbuf, ((nblk / a.n_sbuf) - 1) & 1,
+                        !mbar_wait(sbase + kBarSEmpty + 8 * sbuf, ((nblk >> (a.n_sbuf - 1)) - 1) & 1,
                                    a.timeout_ns, a.status))
                         ok = false;
                     const int r0 = t_rb * kBlockRows + t_t0 * 16;
@@ -616,7 +619,8 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const CUtenso
                 for (int i = (it > NS ? it - NS : 0); i < it; ++i)
                     mbar_wait(sbase + kBarFull + 8 * (i % NS), (i / NS) & 1, dt, a.status);
                 for (int j = (sb_issued > a.n_sbuf ? sb_issued - a.n_sbuf : 0); j < sb_issued; ++j)
-                    mbar_wait(sbase + kBarSFull + 8 * (j % a.n_sbuf), (j / a.n_sbuf) & 1, dt, a.status);
+                    mbar_wait(sbase + kBarSFull + 8 * (j & (a.n_sbuf - 1)), (j >> (a.n_sbuf - 1)) & 1, dt,
+                              a.status);
             }
         } else {
             // Sub-block units (one block, one scale buffer): a tensor-map box of
@@ -769,8 +773,8 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const CUtenso
         float part[MT][4] = {};  // sub-block units: this warp's sums, for the in-CTA reduction
         for (int j = 0; ok && j < nblk; ++j) {
             const int rb = block_of(j);
-            const int sbuf = j % a.n_sbuf;
-            if (!mbar_wait(sbase + kBarSFull + 8 * sbuf, (j / a.n_sbuf) & 1, a.timeout_ns,
+            const int sbuf = j & (a.n_sbuf - 1);
+            if (!mbar_wait(sbase + kBarSFull + 8 * sbuf, (j >> (a.n_sbuf - 1)) & 1, a.timeout_ns,
                            a.status)) {
                 ok = false;
                 break;
@@ -1309,6 +1313,18 @@ cudaError_t launch_gemv_mt(GemvArgs args, int M, cudaStream_t stream, const Devi
     args.tail_T = p.tail_T;
     args.tail_base = p.tail_base;
     args.tail_units = p.tail_units;
+    args.cps = kStageBytes / (p.T * kTileBytes);
+    args.gps = args.cps / 2;
+    args.wpt = kConsumerWarps / p.T;
+    args.nstg_u = (2 * args.G + args.cps - 1) / args.cps;
+    if (p.tail_T > 0) {
+        args.nb_q = p.tail_base / p.grid_y;  // every CTA: its whole blocks, then its tail unit
+        args.nb_r = 0;
+    } else {
+        args.nb_q = args.NB / p.grid_y;
+        args.nb_r = args.NB % p.grid_y;
+    }
+    for (int i = 0; i <= p.S; ++i) args.g0s[i] = split_group_begin(i, p.S, args.G);
     args.xs_stage = p.xs_stage;
     args.stage_stride = p.stage_stride;
     args.off_sx = p.off_sx;
