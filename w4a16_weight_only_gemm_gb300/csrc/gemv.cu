@@ -428,20 +428,6 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const CUtenso
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortFlag);
     const uint32_t ring = sbase + a.off_ring;
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < a.nstages; ++s) {
-            mbar_init(sbase + kBarFull + 8 * s, 1);
-            mbar_init(sbase + kBarEmpty + 8 * s, kConsumerWarps);
-        }
-        mbar_init(sbase + kBarX, 1);
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(sbase + kBarSFull + 8 * b, 1);
-            mbar_init(sbase + kBarSEmpty + 8 * b, kConsumerWarps);
-        }
-        *abort_flag = 0;
-        fence_barrier_init();
-    }
-    __syncthreads();
     // K split over a cluster: the partial sums go into peer CTAs' shared
     // memory, which must not be written before those CTAs run.  Every thread
     // arrives here and waits (cluster_wait) once before the exchange.
@@ -452,6 +438,25 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const CUtenso
 
     if (warp == kConsumerWarps) {
         // =============================== producer ===============================
+        // The producer initialises the barriers and goes straight on to its
+        // first copies; the consumer warps wait for the initialisation on
+        // named barrier 2 (the producer warp arrives, the consumers sync), so
+        // the copies do not wait for the slowest consumer warp to start.
+        if (lane == 0) {
+            for (int s = 0; s < a.nstages; ++s) {
+                mbar_init(sbase + kBarFull + 8 * s, 1);
+                mbar_init(sbase + kBarEmpty + 8 * s, kConsumerWarps);
+            }
+            mbar_init(sbase + kBarX, 1);
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(sbase + kBarSFull + 8 * b, 1);
+                mbar_init(sbase + kBarSEmpty + 8 * b, kConsumerWarps);
+            }
+            *abort_flag = 0;
+            fence_barrier_init();
+        }
+        __syncwarp();
+        asm volatile("bar.arrive 2, %0;" ::"n"(kGemvThreads) : "memory");
         if constexpr (WHOLE) {
             // Whole blocks: one bulk copy of CPS contiguous 4 KB chunks per stage.
             if (lane == 0) {
@@ -703,6 +708,7 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const CUtenso
         if (S > 1) cluster_wait();
     } else {
         // =============================== consumers ==============================
+        asm volatile("bar.sync 2, %0;" ::"n"(kGemvThreads) : "memory");  // barriers initialised
         grid_dependency_wait();
         if (S > 1) cluster_wait();  // every peer runs: their reduction slots exist
         const int g = lane >> 2, t = lane & 3;
