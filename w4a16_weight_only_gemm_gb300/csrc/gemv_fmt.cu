@@ -208,21 +208,24 @@ __global__ void __launch_bounds__(kFThreads, MT == 1 ? 3 : 2)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kFAbort);
     const uint32_t ring = sbase + a.off_ring;
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(sbase + kFBarFull + 8 * s, 1);
-            mbar_init(sbase + kFBarEmpty + 8 * s, kFWarps);
-        }
-        mbar_init(sbase + kFBarX, 1);
-        mbar_init(sbase + kFBarS, 1);
-        *abort_flag = 0;
-        fence_barrier_init();
-    }
-    __syncthreads();
     grid_launch_dependents();
 
     if (warp == kFWarps) {
         // =============================== producer ===============================
+        // The producer initialises the barriers and goes straight on to its
+        // first copies; the consumers wait for that on named barrier 2.
+        if (lane == 0) {
+            for (int s = 0; s < NS; ++s) {
+                mbar_init(sbase + kFBarFull + 8 * s, 1);
+                mbar_init(sbase + kFBarEmpty + 8 * s, kFWarps);
+            }
+            mbar_init(sbase + kFBarX, 1);
+            mbar_init(sbase + kFBarS, 1);
+            *abort_flag = 0;
+            fence_barrier_init();
+        }
+        __syncwarp();
+        asm volatile("bar.arrive 2, %0;" ::"n"(kFThreads) : "memory");
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();
             const int box_x = t0 * (kFTileBytes / 8);
@@ -303,6 +306,7 @@ __global__ void __launch_bounds__(kFThreads, MT == 1 ? 3 : 2)
     }
 
     // ================================ consumers =================================
+    asm volatile("bar.sync 2, %0;" ::"n"(kFThreads) : "memory");  // barriers initialised
     grid_dependency_wait();
     const int g = lane >> 2, t = lane & 3;
     const int ti = warp / W, ks = warp - ti * W;

@@ -87,20 +87,23 @@ __global__ void __launch_bounds__(kWThreads, MT == 1 ? 3 : 2)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kWAbort);
     const uint32_t ring = sbase + a.off_ring;
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(sbase + kWBarFull + 8 * s, 1);
-            mbar_init(sbase + kWBarEmpty + 8 * s, kWWarps);
-        }
-        mbar_init(sbase + kWBarX, 1);
-        *abort_flag = 0;
-        fence_barrier_init();
-    }
-    __syncthreads();
     grid_launch_dependents();
 
     if (warp == kWWarps) {
         // =============================== producer ===============================
+        // The producer initialises the barriers and goes straight on to its
+        // first copies; the consumers wait for that on named barrier 2.
+        if (lane == 0) {
+            for (int s = 0; s < NS; ++s) {
+                mbar_init(sbase + kWBarFull + 8 * s, 1);
+                mbar_init(sbase + kWBarEmpty + 8 * s, kWWarps);
+            }
+            mbar_init(sbase + kWBarX, 1);
+            *abort_flag = 0;
+            fence_barrier_init();
+        }
+        __syncwarp();
+        asm volatile("bar.arrive 2, %0;" ::"n"(kWThreads) : "memory");
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();
             tma_prefetch_map(&qmap);
@@ -151,6 +154,7 @@ __global__ void __launch_bounds__(kWThreads, MT == 1 ? 3 : 2)
     }
 
     // ================================ consumers =================================
+    asm volatile("bar.sync 2, %0;" ::"n"(kWThreads) : "memory");  // barriers initialised
     grid_dependency_wait();
     const int g = lane >> 2, t = lane & 3;
     const int ti = warp / W, ks = warp - ti * W;
