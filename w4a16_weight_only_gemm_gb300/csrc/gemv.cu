@@ -462,19 +462,6 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const CUtenso
             if (lane == 0) {
                 const uint64_t pol = l2_policy_evict_first();
                 const size_t block_stride = (size_t)C * kChunkBytes;
-                if constexpr (MT == 2 && SUB) {
-                    // L2 prefetch of the first block (x in the ring, M > 8): kept
-                    // only here, where dropping it leaves the kernel spilling
-                    const int rb = (int)blockIdx.y;
-                    const uint8_t* w = a.wq + (size_t)rb * block_stride + 2 * (size_t)g0 * kChunkBytes;
-                    const int pre = nstg < 2 * a.nstages ? nstg : 2 * a.nstages;
-                    for (int i = 0; i < pre; ++i)
-                        bulk_prefetch_l2(w + (size_t)i * kStageBytes,
-                                         min(CPS, nck - i * CPS) * kChunkBytes);
-                    const int rows = min(kBlockRows, a.N - rb * kBlockRows);
-                    const uint32_t sb = ((uint32_t)(rows * a.G * 2)) & ~15u;
-                    if (sb) bulk_prefetch_l2(a.scales + (size_t)rb * kBlockRows * a.G, sb);
-                }
                 // Weights and scales are constants of the call: the first ring
                 // stages and scale slab load while the previous kernel is still
                 // running.  x (its output, possibly) loads only after the wait.
