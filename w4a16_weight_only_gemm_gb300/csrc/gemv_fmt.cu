@@ -23,8 +23,14 @@
 // of 32 the two halves of a chunk differ in group, and one MMA spans both, so
 // each lane multiplies its (nib - z) by the row's fp16 scale before the MMA:
 // one fp16 rounding of (q - z) * s per weight -- the tutorial's own fp16
-// dequantised weight.  No activation sums are needed.  The default format
-// (groups of 128, symmetric) keeps the kernels of gemv.cu.
+// dequantised weight.  No activation sums are needed.  The group size is a
+// template parameter, so a lane's scale and zero-point offsets are a few
+// shifts of its group index.  The unit's scale and zero-point slabs are
+// copied group-blocked where the row length allows ([Gs / 8][16 T][8 scales],
+// [Gs / 16][16 T][16 zero points], one 3-D tensor-map box each): with the
+// row-major slab the 8 rows a warp reads at one group sit Gs * 2 bytes apart,
+// in one bank when that is a multiple of 128.  The default format (groups of
+// 128, symmetric) keeps the kernels of gemv.cu.
 // Every wait is bounded; on a time-out the CTA records it in the status
 // word, stops issuing copies, drains those in flight and exits.
 #include <atomic>
@@ -69,6 +75,15 @@ struct FmtArgs {
     int nstages;
     int xs_stride;
     uint32_t off_ring, off_x, off_s, off_z, off_red;
+    // Slab addressing in shared memory: the scale of (unit row r, group gi)
+    // sits at off_s + (gi >> 3) * s_blk + r * s_row + 2 (gi & 7), its zero
+    // point at off_z + (gi >> 4) * z_blk + r * z_row + (gi & 15).  Row-major
+    // ([16 T][Gs], one bulk copy): s_blk = 16, s_row = 2 Gs.  Group-blocked
+    // ([Gs / 8][16 T][8], one 3-D tensor-map copy, s_blk = 256 T, s_row = 16):
+    // the 8 rows a warp reads at one group then fill 8 distinct 16-byte bank
+    // groups instead of one bank (rows 2 Gs bytes apart, a multiple of 128).
+    int s_tma, z_tma;       // the slab (zero-point slab) comes group-blocked
+    uint32_t s_blk, s_row, z_blk, z_row;
 };
 
 // (nib - z) * s for one lane's 32-bit word of a chunk: rows r0 in registers
@@ -125,19 +140,24 @@ __device__ __forceinline__ void dequant8_zq(uint32_t w, __half2 zc0, __half2 nzc
 // products summed in a fresh FP32 fragment, scaled once per row.
 template <int MT, bool CHUNK_SCALE>
 __device__ __forceinline__ void mma_group_fmt(uint32_t w_addr, uint32_t cs, uint32_t x0_addr,
-                                              uint32_t x1_addr, const __half* sc0,
-                                              const __half* sc1, const uint8_t* zr0,
-                                              const uint8_t* zr1, int gi0, int gi1,
+                                              uint32_t x1_addr, const uint8_t* sr0,
+                                              const uint8_t* sr1, const uint8_t* zr0,
+                                              const uint8_t* zr1, uint32_t so0, uint32_t so1,
+                                              uint32_t zo0, uint32_t zo1,
                                               float (&acc)[2][MT][4]) {
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
-        const int gi = c == 0 ? gi0 : gi1;
-        const __half2 s0 = __half2half2(sc0[gi]);
-        const __half2 s1 = __half2half2(sc1[gi]);
-        const int z0 = zr0 ? (int)zr0[gi] : 8;
-        const int z1 = zr1 ? (int)zr1[gi] : 8;
-        const __half2 zc0 = __half2half2(__int2half_rn(1024 + z0));
-        const __half2 zc1 = __half2half2(__int2half_rn(64 + z1));
+        const uint32_t so = c == 0 ? so0 : so1, zo = c == 0 ? zo0 : zo1;
+        const __half2 s0 = __half2half2(*reinterpret_cast<const __half*>(sr0 + so));
+        const __half2 s1 = __half2half2(*reinterpret_cast<const __half*>(sr1 + so));
+        const uint32_t z0 = zr0 ? zr0[zo] : 8u;
+        const uint32_t z1 = zr1 ? zr1[zo] : 8u;
+        // 1024 + z0 is the fp16 bit pattern 0x6400 + z0 (exact for z0 < 1024);
+        // 64 + z1 = (1024 + z1) - 960, an exact fp16 difference for z1 < 256
+        const uint32_t zb0 = 0x64006400u + z0 * 0x10001u, zb1 = 0x64006400u + z1 * 0x10001u;
+        const __half2 zc0 = *reinterpret_cast<const __half2*>(&zb0);
+        const __half2 zc1 = __hsub2(*reinterpret_cast<const __half2*>(&zb1),
+                                    __half2half2(__ushort_as_half(0x6380)));  // 960
         const uint4 wv = lds128(w_addr + c * cs);
         const uint4 xa = lds128(x0_addr + c * 128);
         const uint4 xb = lds128(x0_addr + c * 128 + 16);
@@ -188,10 +208,13 @@ __device__ __forceinline__ void mma_group_fmt(uint32_t w_addr, uint32_t cs, uint
     }
 }
 
-template <int MT, bool CHUNK_SCALE>
+// GSH: log2 of the group size (5, 6, 7), or 31 for one group per row.
+template <int MT, int GSH>
 __global__ void __launch_bounds__(kFThreads, MT == 1 ? 3 : 2)
-    gemv_fmt_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ FmtArgs a) {
+    gemv_fmt_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap smap,
+                    const __grid_constant__ CUtensorMap zmap, const __grid_constant__ FmtArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
+    constexpr bool CHUNK_SCALE = GSH >= 6;  // a whole 64-wide chunk in one group
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int T = a.T;
@@ -231,24 +254,38 @@ __global__ void __launch_bounds__(kFThreads, MT == 1 ? 3 : 2)
             const int box_x = t0 * (kFTileBytes / 8);
             const int cy0 = rb * C;
             tma_prefetch_map(&wmap);
-            {   // scale slab (and zero-point slab) of the unit's rows
-                const uint32_t sbytes = (uint32_t)(rows * a.Gs * 2);
-                const uint32_t sbulk = sbytes & ~15u;
+            {   // scale slab (and zero-point slab) of the unit's rows: one
+                // group-blocked tensor-map box (rows past N zero-filled), or
+                // row-major by bulk copy with the unaligned tail by hand
+                const int R = 16 * T;
+                uint32_t sbulk = 0, zbulk = 0, tx = 0;
                 const __half* ssrc = a.scales + (size_t)r0 * a.Gs;
-                __half* sdst = reinterpret_cast<__half*>(smem + a.off_s);
-                for (uint32_t e = sbulk / 2; e < sbytes / 2; ++e) sdst[e] = ssrc[e];
-                uint32_t zbulk = 0;
-                const uint8_t* zsrc = nullptr;
-                if (a.zeros) {
-                    const uint32_t zbytes = (uint32_t)(rows * a.Gs);
-                    zbulk = zbytes & ~15u;
-                    zsrc = a.zeros + (size_t)r0 * a.Gs;
-                    uint8_t* zdst = smem + a.off_z;
-                    for (uint32_t e = zbulk; e < zbytes; ++e) zdst[e] = zsrc[e];
+                const uint8_t* zsrc = a.zeros ? a.zeros + (size_t)r0 * a.Gs : nullptr;
+                if (a.s_tma) {
+                    tx += (uint32_t)(R * a.Gs * 2);
+                } else {
+                    const uint32_t sbytes = (uint32_t)(rows * a.Gs * 2);
+                    sbulk = sbytes & ~15u;
+                    __half* sdst = reinterpret_cast<__half*>(smem + a.off_s);
+                    for (uint32_t e = sbulk / 2; e < sbytes / 2; ++e) sdst[e] = ssrc[e];
+                    tx += sbulk;
                 }
-                mbar_arrive_expect_tx(sbase + kFBarS, sbulk + zbulk);
-                if (sbulk) bulk_g2s(sbase + a.off_s, ssrc, sbulk, sbase + kFBarS);
-                if (zbulk) bulk_g2s(sbase + a.off_z, zsrc, zbulk, sbase + kFBarS);
+                if (a.zeros) {
+                    if (a.z_tma) {
+                        tx += (uint32_t)(R * a.Gs);
+                    } else {
+                        const uint32_t zbytes = (uint32_t)(rows * a.Gs);
+                        zbulk = zbytes & ~15u;
+                        uint8_t* zdst = smem + a.off_z;
+                        for (uint32_t e = zbulk; e < zbytes; ++e) zdst[e] = zsrc[e];
+                        tx += zbulk;
+                    }
+                }
+                mbar_arrive_expect_tx(sbase + kFBarS, tx);
+                if (a.s_tma) tma_load_3d(sbase + a.off_s, &smap, 0, r0, 0, sbase + kFBarS);
+                else if (sbulk) bulk_g2s(sbase + a.off_s, ssrc, sbulk, sbase + kFBarS);
+                if (a.zeros && a.z_tma) tma_load_3d(sbase + a.off_z, &zmap, 0, r0, 0, sbase + kFBarS);
+                else if (zbulk) bulk_g2s(sbase + a.off_z, zsrc, zbulk, sbase + kFBarS);
             }
             bool x_issued = false;
             auto issue_x = [&]() {
@@ -317,10 +354,10 @@ __global__ void __launch_bounds__(kFThreads, MT == 1 ? 3 : 2)
     const uint32_t x1 = sbase + a.off_x + xr1 * a.xs_stride + t * 32;
     const uint32_t cs = (uint32_t)(T * kFTileBytes);
     const uint32_t wl = ring + ti * kFTileBytes + lane * 16;
-    const __half* sc0 = reinterpret_cast<const __half*>(smem + a.off_s) + row0 * a.Gs;
-    const __half* sc1 = sc0 + 8 * a.Gs;
-    const uint8_t* zr0 = a.zeros ? smem + a.off_z + row0 * a.Gs : nullptr;
-    const uint8_t* zr1 = a.zeros ? zr0 + 8 * a.Gs : nullptr;
+    const uint8_t* sr0 = smem + a.off_s + row0 * a.s_row;
+    const uint8_t* sr1 = sr0 + 8 * a.s_row;
+    const uint8_t* zr0 = a.zeros ? smem + a.off_z + row0 * a.z_row : nullptr;
+    const uint8_t* zr1 = a.zeros ? zr0 + 8 * a.z_row : nullptr;
 
     bool ok = mbar_wait(sbase + kFBarX, 0, a.timeout_ns, a.status);
     if (a.alpha) {
@@ -361,11 +398,21 @@ __global__ void __launch_bounds__(kFThreads, MT == 1 ? 3 : 2)
                 const int gsl = ks * 2 + gi;        // this warp's group within the stage
                 if (gsl < gs) {
                     const int gl = st * GPS + gsl;  // 128-group index along the row
-                    // the scale group of this lane's k in chunks 2 gl and 2 gl + 1
-                    const int k0 = gl * 128 + 16 * t;
-                    mma_group_fmt<MT, CHUNK_SCALE>(wl + slot * kFStageBytes + gsl * 2 * cs, cs, x0 + gl * 256,
-                                      x1 + gl * 256, sc0, sc1, zr0, zr1, k0 >> a.gshift,
-                                      (k0 + 64) >> a.gshift, acc);
+                    // The scale group of this lane's k (16 t .. 16 t + 15 of
+                    // each chunk) in chunks 2 gl and 2 gl + 1: gi0 and gi1.
+                    // They share a run of 8 scales and of 16 zero points, so
+                    // the second chunk's offsets are the first's plus
+                    // 2 (gi1 - gi0) and gi1 - gi0 in either slab layout.
+                    uint32_t so = 0, zo = 0;
+                    constexpr uint32_t dg = GSH == 5 ? 2 : GSH == 6 ? 1 : 0;  // gi1 - gi0
+                    if constexpr (GSH < 31) {
+                        const uint32_t gi0 = GSH == 5 ? 4 * gl + (t >> 1) : GSH == 6 ? 2 * gl : gl;
+                        so = (gi0 >> 3) * a.s_blk + ((gi0 & 7) << 1);
+                        zo = (gi0 >> 4) * a.z_blk + (gi0 & 15);
+                    }
+                    mma_group_fmt<MT, CHUNK_SCALE>(wl + slot * kFStageBytes + gsl * 2 * cs, cs,
+                                                   x0 + gl * 256, x1 + gl * 256, sr0, sr1, zr0, zr1,
+                                                   so, so + 2 * dg, zo, zo + dg, acc);
                 }
             }
         }
@@ -424,14 +471,19 @@ struct FmtPlan {
 
 template <int MT>
 int fmt_occupancy(uint32_t smem) {
-    // both scale modes have the same launch bounds; the larger register count decides
-    int b0 = 0, b1 = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b0, gemv_fmt_kernel<MT, false>, kFThreads,
-                                                      smem) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, gemv_fmt_kernel<MT, true>, kFThreads,
-                                                      smem) != cudaSuccess)
-        return 0;
-    return b0 < b1 ? b0 : b1;
+    // every group size has the same launch bounds; the largest register count decides
+    const void* fns[4] = {reinterpret_cast<const void*>(gemv_fmt_kernel<MT, 5>),
+                          reinterpret_cast<const void*>(gemv_fmt_kernel<MT, 6>),
+                          reinterpret_cast<const void*>(gemv_fmt_kernel<MT, 7>),
+                          reinterpret_cast<const void*>(gemv_fmt_kernel<MT, 31>)};
+    int occ = 0;
+    for (int i = 0; i < 4; ++i) {
+        int b = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fns[i], kFThreads, smem) != cudaSuccess)
+            return 0;
+        occ = i == 0 || b < occ ? b : occ;
+    }
+    return occ;
 }
 
 template <int MT>
@@ -440,11 +492,13 @@ cudaError_t ensure_fmt_attr() {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(
-        gemv_fmt_kernel<MT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(gemv_fmt_kernel<MT, true>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    const void* fns[4] = {reinterpret_cast<const void*>(gemv_fmt_kernel<MT, 5>),
+                          reinterpret_cast<const void*>(gemv_fmt_kernel<MT, 6>),
+                          reinterpret_cast<const void*>(gemv_fmt_kernel<MT, 7>),
+                          reinterpret_cast<const void*>(gemv_fmt_kernel<MT, 31>)};
+    cudaError_t e = cudaSuccess;
+    for (int i = 0; i < 4 && e == cudaSuccess; ++i)
+        e = cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev].store(true, std::memory_order_release);
     return e;
 }
@@ -497,6 +551,52 @@ FmtPlan plan_fmt(int M, int N, int K, int Gs, bool zp, const DeviceCtx& ctx) {
     return best;
 }
 
+// The group-blocked view of a [N, Gs] slab of `eb`-byte elements (fp16
+// scales or byte zero points): dimension 0 is one 16-byte run of groups,
+// dimension 1 the rows (stride Gs * eb), dimension 2 the runs of a row
+// (stride 16 bytes); a box of R rows lands in shared memory as
+// [Gs * eb / 16][R][16 bytes].  Encoded once per (slab, shape, R).  Returns
+// false when the slab does not fit the view (rows not a whole number of
+// 16-byte runs, more than 256 runs, or an unaligned base); the launch then
+// copies the slab row-major.
+bool slab_map(const void* base, int eb, int N, int Gs, int R, CUtensorMap* out) {
+    const int runs = Gs * eb / 16;
+    if ((Gs * eb) % 16 != 0 || runs < 1 || runs > 256 || R > 256 ||
+        (reinterpret_cast<uintptr_t>(base) & 15) != 0)
+        return false;
+    struct Entry {
+        const void* base;
+        int eb, N, Gs, R;
+        CUtensorMap map;
+    };
+    static std::mutex mu;
+    static std::vector<Entry> cache;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (const Entry& e : cache)
+            if (e.base == base && e.eb == eb && e.N == N && e.Gs == Gs && e.R == R) {
+                *out = e.map;
+                return true;
+            }
+    }
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode) return false;
+    Entry e{base, eb, N, Gs, R, {}};
+    const cuuint64_t dims[3] = {(cuuint64_t)(16 / eb), (cuuint64_t)N, (cuuint64_t)runs};
+    const cuuint64_t strides[2] = {(cuuint64_t)Gs * eb, 16};
+    const cuuint32_t box[3] = {(cuuint32_t)(16 / eb), (cuuint32_t)R, (cuuint32_t)runs};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (encode(&e.map, eb == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+               const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    *out = e.map;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache.size() < 4096) cache.push_back(e);
+    return true;
+}
+
 template <int MT>
 cudaError_t launch_fmt_mt(FmtArgs a, cudaStream_t stream, const DeviceCtx& ctx) {
     cudaError_t e = ensure_fmt_attr<MT>();
@@ -534,6 +634,14 @@ cudaError_t launch_fmt_mt(FmtArgs a, cudaStream_t stream, const DeviceCtx& ctx) 
     CUtensorMap wmap;
     e = gemv_weight_map(a.wq, a.N, a.K, p.T, &wmap);
     if (e != cudaSuccess) return e;
+    const int R = 16 * p.T;
+    CUtensorMap smap{}, zmap{};
+    a.s_tma = slab_map(a.scales, 2, a.N, a.Gs, R, &smap) ? 1 : 0;
+    a.z_tma = a.zeros && slab_map(a.zeros, 1, a.N, a.Gs, R, &zmap) ? 1 : 0;
+    a.s_blk = a.s_tma ? (uint32_t)R * 16 : 16;
+    a.s_row = a.s_tma ? 16 : (uint32_t)a.Gs * 2;
+    a.z_blk = a.z_tma ? (uint32_t)R * 16 : 16;
+    a.z_row = a.z_tma ? 16 : (uint32_t)a.Gs;
     const long long units = ((long long)a.N + 16 * p.T - 1) / (16 * p.T);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, (unsigned)units, 1);
@@ -546,8 +654,12 @@ cudaError_t launch_fmt_mt(FmtArgs a, cudaStream_t stream, const DeviceCtx& ctx) 
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     // groups of 64 and more: a whole chunk in one group, scaled in FP32
-    if (a.gshift >= 6) return cudaLaunchKernelEx(&cfg, gemv_fmt_kernel<MT, true>, wmap, a);
-    return cudaLaunchKernelEx(&cfg, gemv_fmt_kernel<MT, false>, wmap, a);
+    switch (a.gshift) {
+    case 5: return cudaLaunchKernelEx(&cfg, gemv_fmt_kernel<MT, 5>, wmap, smap, zmap, a);
+    case 6: return cudaLaunchKernelEx(&cfg, gemv_fmt_kernel<MT, 6>, wmap, smap, zmap, a);
+    case 7: return cudaLaunchKernelEx(&cfg, gemv_fmt_kernel<MT, 7>, wmap, smap, zmap, a);
+    default: return cudaLaunchKernelEx(&cfg, gemv_fmt_kernel<MT, 31>, wmap, smap, zmap, a);
+    }
 }
 
 }  // namespace

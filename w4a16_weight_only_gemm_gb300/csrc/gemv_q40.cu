@@ -15,10 +15,11 @@
 // aligned when K % 256 == 0, which the path requires.  Per block a lane
 // holds bytes 4 t .. 4 t + 3 of the quants of rows g and g + 8 (elements
 // 8 t .. 8 t + 7, read as two 16-bit halves: blocks are 2-byte aligned);
-// prmt, lop3 and one fp16 fma turn a byte into (lo - 8, hi - 8) exactly; two
-// mma.m16n8k16 (the activations' k order permuted the same way) fill a fresh
-// FP32 fragment, scaled once by each row's block scale into the sum.  Every
-// wait is bounded.
+// four lop3 with the fp16 magic 1024 and four fp16 subtractions or fmas
+// turn those 8 nibbles into exact q - 8 pairs of elements (e, e + 4); two
+// mma.m16n8k16 take them against x stored in the same pairing (permuted in
+// shared memory once per CTA) into a fresh FP32 fragment, scaled once by
+// each row's block scale into the sum.  Every wait is bounded.
 #include <atomic>
 #include <mutex>
 #include <utility>
@@ -58,19 +59,33 @@ struct Q40Args {
     uint32_t off_ring, off_x, off_red;
 };
 
-// Byte `sel` of w as the fp16 pair (lo - 8, hi - 8), exact: prmt puts the
-// byte in the low byte of both halves, lop3 keeps the low nibble in half 0
-// and the high nibble (times 16) in half 1 under the fp16 1024 exponent, and
-// one fma rescales half 1 by 1/16 and removes 1032 / 72.
-__device__ __forceinline__ uint32_t byte_to_half2(uint32_t w, uint32_t sel) {
-    uint32_t t;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(t) : "r"(w), "r"(0u), "r"(sel));
+// A lane's 4 quant bytes of one row (elements e0 .. e7 of the block, byte b
+// holding e_2b low and e_2b+1 high) as four exact fp16 pairs of q - 8:
+// r = {(e0, e4), (e1, e5), (e2, e6), (e3, e7)}.  lop3 ORs the low nibbles of
+// bytes 0 and 2 (of w >> 8: 1 and 3) into the mantissa of 1024.0, the high
+// nibbles as 16 n; one subtraction of 1032, or a multiply by 1/16 and
+// subtraction of 72, leaves n - 8 exactly.  The activations are stored with
+// the same pairing, (x0, x4, x1, x5, x2, x6, x3, x7) per 8 elements.
+__device__ __forceinline__ void dequant8_q40(uint32_t w, uint32_t (&r)[4]) {
+    constexpr uint32_t kMagic = 0x64006400u;         // (1024.0, 1024.0)
     constexpr uint32_t kLut = (0xF0 & 0xCC) | 0xAA;  // (a & b) | c
-    const uint32_t v = lop3<kLut>(t, 0x00F0000Fu, 0x64006400u);
-    const __half2 mul = __halves2half2(__ushort_as_half(0x3C00), __ushort_as_half(0x2C00));  // 1, 1/16
-    const __half2 add = __halves2half2(__ushort_as_half(0xE408), __ushort_as_half(0xD480));  // -1032, -72
-    __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&v), mul, add);
-    return *reinterpret_cast<uint32_t*>(&r);
+    const uint32_t w8 = w >> 8;
+    const uint32_t lo0 = lop3<kLut>(w, 0x000F000Fu, kMagic);
+    const uint32_t hi0 = lop3<kLut>(w, 0x00F000F0u, kMagic);
+    const uint32_t lo1 = lop3<kLut>(w8, 0x000F000Fu, kMagic);
+    const uint32_t hi1 = lop3<kLut>(w8, 0x00F000F0u, kMagic);
+    const __half2 k1032 = __half2half2(__ushort_as_half(0x6408));
+    const __half2 k16th = __half2half2(__ushort_as_half(0x2C00));
+    const __half2 km72 = __half2half2(__ushort_as_half(0xD480));
+    __half2 v;
+    v = __hsub2(*reinterpret_cast<const __half2*>(&lo0), k1032);
+    r[0] = *reinterpret_cast<uint32_t*>(&v);
+    v = __hfma2(*reinterpret_cast<const __half2*>(&hi0), k16th, km72);
+    r[1] = *reinterpret_cast<uint32_t*>(&v);
+    v = __hsub2(*reinterpret_cast<const __half2*>(&lo1), k1032);
+    r[2] = *reinterpret_cast<uint32_t*>(&v);
+    v = __hfma2(*reinterpret_cast<const __half2*>(&hi1), k16th, km72);
+    r[3] = *reinterpret_cast<uint32_t*>(&v);
 }
 
 __device__ __forceinline__ uint32_t lds16(uint32_t addr) {
@@ -173,6 +188,24 @@ __global__ void __launch_bounds__(kQThreads, MT == 1 ? 3 : 2)
     const uint32_t x0 = sbase + a.off_x + xr0 * a.xs_stride + t * 16;
     const uint32_t x1 = sbase + a.off_x + xr1 * a.xs_stride + t * 16;
     bool ok = mbar_wait(sbase + kQBarX, 0, a.timeout_ns, a.status);
+    // x in the decode's pairing: (x0, x4, x1, x5, x2, x6, x3, x7) per 8
+    // elements, in place, 16 bytes per thread per step; every consumer thread
+    // takes part in the barrier below
+    {
+        const int per_row = a.K / 8;
+        for (int q = (int)threadIdx.x; ok && q < a.M * per_row; q += kQConsumers) {
+            const int m = q / per_row, off = q - m * per_row;
+            uint4* xp = reinterpret_cast<uint4*>(smem + a.off_x + m * a.xs_stride + off * 16);
+            const uint4 v = *xp;
+            uint4 o;
+            asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(o.x) : "r"(v.x), "r"(v.z));
+            asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(o.y) : "r"(v.x), "r"(v.z));
+            asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(o.z) : "r"(v.y), "r"(v.w));
+            asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(o.w) : "r"(v.y), "r"(v.w));
+            *xp = o;
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kQConsumers) : "memory");
+    }
     ok = __all_sync(0xffffffffu, ok);
     float acc[MT][4];
 #pragma unroll
@@ -204,18 +237,18 @@ __global__ void __launch_bounds__(kQThreads, MT == 1 ? 3 : 2)
                 for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) f[mt][e] = 0.0f;
-                // MMA 0: elements 8t .. 8t + 3 (bytes 0, 1); MMA 1: 8t + 4 .. 8t + 7 (bytes 2, 3)
-                uint32_t af[4];
-                af[0] = byte_to_half2(q0, 0x4040);
-                af[1] = byte_to_half2(q1, 0x4040);
-                af[2] = byte_to_half2(q0, 0x4141);
-                af[3] = byte_to_half2(q1, 0x4141);
+                // MMA 0: elements (8t, 8t + 4), (8t + 1, 8t + 5) of rows g and
+                // g + 8; MMA 1: (8t + 2, 8t + 6), (8t + 3, 8t + 7)
+                uint32_t p0[4], p1[4];
+                dequant8_q40(q0, p0);
+                dequant8_q40(q1, p1);
+                uint32_t af[4] = {p0[0], p1[0], p0[1], p1[1]};
                 mma_16816(f[0], af, xa.x, xa.y, f[0]);
                 if (MT == 2) mma_16816(f[MT - 1], af, xb.x, xb.y, f[MT - 1]);
-                af[0] = byte_to_half2(q0, 0x4242);
-                af[1] = byte_to_half2(q1, 0x4242);
-                af[2] = byte_to_half2(q0, 0x4343);
-                af[3] = byte_to_half2(q1, 0x4343);
+                af[0] = p0[2];
+                af[1] = p1[2];
+                af[2] = p0[3];
+                af[3] = p1[3];
                 mma_16816(f[0], af, xa.z, xa.w, f[0]);
                 if (MT == 2) mma_16816(f[MT - 1], af, xb.z, xb.w, f[MT - 1]);
 #pragma unroll
