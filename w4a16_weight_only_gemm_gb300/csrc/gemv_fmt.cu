@@ -393,27 +393,34 @@ __global__ void __launch_bounds__(kFThreads, MT == 1 ? 3 : 2)
         ok = __all_sync(0xffffffffu, ok);
         if (ok) {
             const int gs = min(GPS, G - st * GPS);  // 128-groups in this stage
-#pragma unroll
-            for (int gi = 0; gi < 2; ++gi) {
+            // the warp's two groups of the stage; at MT = 1 both unguarded
+            // unless the last stage is short, so that the common case is
+            // straight-line code (at MT = 2 that code spills)
+            auto group = [&](int gi) __attribute__((always_inline)) {
                 const int gsl = ks * 2 + gi;        // this warp's group within the stage
-                if (gsl < gs) {
-                    const int gl = st * GPS + gsl;  // 128-group index along the row
-                    // The scale group of this lane's k (16 t .. 16 t + 15 of
-                    // each chunk) in chunks 2 gl and 2 gl + 1: gi0 and gi1.
-                    // They share a run of 8 scales and of 16 zero points, so
-                    // the second chunk's offsets are the first's plus
-                    // 2 (gi1 - gi0) and gi1 - gi0 in either slab layout.
-                    uint32_t so = 0, zo = 0;
-                    constexpr uint32_t dg = GSH == 5 ? 2 : GSH == 6 ? 1 : 0;  // gi1 - gi0
-                    if constexpr (GSH < 31) {
-                        const uint32_t gi0 = GSH == 5 ? 4 * gl + (t >> 1) : GSH == 6 ? 2 * gl : gl;
-                        so = (gi0 >> 3) * a.s_blk + ((gi0 & 7) << 1);
-                        zo = (gi0 >> 4) * a.z_blk + (gi0 & 15);
-                    }
-                    mma_group_fmt<MT, CHUNK_SCALE>(wl + slot * kFStageBytes + gsl * 2 * cs, cs,
-                                                   x0 + gl * 256, x1 + gl * 256, sr0, sr1, zr0, zr1,
-                                                   so, so + 2 * dg, zo, zo + dg, acc);
+                const int gl = st * GPS + gsl;  // 128-group index along the row
+                // The scale group of this lane's k (16 t .. 16 t + 15 of
+                // each chunk) in chunks 2 gl and 2 gl + 1: gi0 and gi1.
+                // They share a run of 8 scales and of 16 zero points, so
+                // the second chunk's offsets are the first's plus
+                // 2 (gi1 - gi0) and gi1 - gi0 in either slab layout.
+                uint32_t so = 0, zo = 0;
+                constexpr uint32_t dg = GSH == 5 ? 2 : GSH == 6 ? 1 : 0;  // gi1 - gi0
+                if constexpr (GSH < 31) {
+                    const uint32_t gi0 = GSH == 5 ? 4 * gl + (t >> 1) : GSH == 6 ? 2 * gl : gl;
+                    so = (gi0 >> 3) * a.s_blk + ((gi0 & 7) << 1);
+                    zo = (gi0 >> 4) * a.z_blk + (gi0 & 15);
                 }
+                mma_group_fmt<MT, CHUNK_SCALE>(wl + slot * kFStageBytes + gsl * 2 * cs, cs,
+                                               x0 + gl * 256, x1 + gl * 256, sr0, sr1, zr0, zr1,
+                                               so, so + 2 * dg, zo, zo + dg, acc);
+            };
+            if (MT == 1 && ks * 2 + 1 < gs) {
+                group(0);
+                group(1);
+            } else {
+                if (ks * 2 < gs) group(0);
+                if (ks * 2 + 1 < gs) group(1);
             }
         }
         __syncwarp();

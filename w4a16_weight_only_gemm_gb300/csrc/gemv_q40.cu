@@ -88,13 +88,9 @@ __device__ __forceinline__ void dequant8_q40(uint32_t w, uint32_t (&r)[4]) {
     r[3] = *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ uint32_t lds16(uint32_t addr) {
-    uint16_t v;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
-    return v;
-}
-
-template <int MT>
+// M1: a single activation row, so only output column 0 is ever stored and
+// the odd columns' rescale is skipped.
+template <int MT, bool M1>
 __global__ void __launch_bounds__(kQThreads, MT == 1 ? 3 : 2)
     gemv_q40_kernel(const __grid_constant__ CUtensorMap bmap, const __grid_constant__ Q40Args a) {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -219,16 +215,28 @@ __global__ void __launch_bounds__(kQThreads, MT == 1 ? 3 : 2)
         ok = __all_sync(0xffffffffu, ok);
         const int kb = st * kps + ks * kQBoxK;       // this warp's box
         if (ok && kb < a.K) {
-            const uint32_t box = ring + slot * kQStageBytes + ks * box_bytes;
-            const uint32_t rA = box + (uint32_t)row0 * kQBoxBytesRow;   // row r0
-            const uint32_t rB = rA + 8 * kQBoxBytesRow;                  // row r0 + 8
-#pragma unroll 2
+            // rows r0 and r0 + 8 of this warp's box (144-byte rows, 16-byte aligned)
+            const uint8_t* bA = smem + a.off_ring + slot * kQStageBytes + ks * box_bytes +
+                                row0 * kQBoxBytesRow;
+            const uint8_t* bB = bA + 8 * kQBoxBytesRow;
+#pragma unroll
             for (int j = 0; j < kQBoxBlocks; ++j) {
-                const uint32_t bo = (uint32_t)(j * kQBlockBytes);
-                const float d0 = __half2float(__ushort_as_half((unsigned short)lds16(rA + bo)));
-                const float d1 = __half2float(__ushort_as_half((unsigned short)lds16(rB + bo)));
-                const uint32_t q0 = lds16(rA + bo + 2 + 4 * t) | (lds16(rA + bo + 4 + 4 * t) << 16);
-                const uint32_t q1 = lds16(rB + bo + 2 + 4 * t) | (lds16(rB + bo + 4 + 4 * t) << 16);
+                const int bo = j * kQBlockBytes;
+                const float d0 = __half2float(*reinterpret_cast<const __half*>(bA + bo));
+                const float d1 = __half2float(*reinterpret_cast<const __half*>(bB + bo));
+                // the lane's quant bytes 2 + 4 t .. 5 + 4 t of the block: one
+                // aligned word in odd blocks (18 j = 2 mod 4), two aligned
+                // words joined in even ones
+                uint32_t q0, q1;
+                if (j & 1) {
+                    q0 = *reinterpret_cast<const uint32_t*>(bA + bo + 2 + 4 * t);
+                    q1 = *reinterpret_cast<const uint32_t*>(bB + bo + 2 + 4 * t);
+                } else {
+                    const uint32_t* wA = reinterpret_cast<const uint32_t*>(bA + bo + 4 * t);
+                    const uint32_t* wB = reinterpret_cast<const uint32_t*>(bB + bo + 4 * t);
+                    q0 = __funnelshift_r(wA[0], wA[1], 16);
+                    q1 = __funnelshift_r(wB[0], wB[1], 16);
+                }
                 const uint4 xa = lds128(x0 + (uint32_t)(kb + 32 * j) * 2);
                 uint4 xb = xa;
                 if (MT == 2) xb = lds128(x1 + (uint32_t)(kb + 32 * j) * 2);
@@ -254,9 +262,11 @@ __global__ void __launch_bounds__(kQThreads, MT == 1 ? 3 : 2)
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt) {
                     acc[mt][0] = fmaf(d0, f[mt][0], acc[mt][0]);
-                    acc[mt][1] = fmaf(d0, f[mt][1], acc[mt][1]);
                     acc[mt][2] = fmaf(d1, f[mt][2], acc[mt][2]);
-                    acc[mt][3] = fmaf(d1, f[mt][3], acc[mt][3]);
+                    if (!M1) {
+                        acc[mt][1] = fmaf(d0, f[mt][1], acc[mt][1]);
+                        acc[mt][3] = fmaf(d1, f[mt][3], acc[mt][3]);
+                    }
                 }
             }
         }
@@ -310,11 +320,15 @@ struct Q40Plan {
 
 template <int MT>
 int q40_occupancy(uint32_t smem) {
-    int blocks = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, gemv_q40_kernel<MT>, kQThreads,
+    // at MT = 1 both column variants; the larger register count decides
+    int b0 = 0, b1 = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b0, gemv_q40_kernel<MT, false>, kQThreads,
                                                       smem) != cudaSuccess)
         return 0;
-    return blocks;
+    if (MT == 1 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                       &b1, gemv_q40_kernel<1, true>, kQThreads, smem) == cudaSuccess)
+        return b1 < b0 ? b1 : b0;
+    return b0;
 }
 
 template <int MT>
@@ -323,8 +337,11 @@ cudaError_t ensure_q40_attr() {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
-    const cudaError_t e = cudaFuncSetAttribute(
-        gemv_q40_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    cudaError_t e = cudaFuncSetAttribute(
+        gemv_q40_kernel<MT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e == cudaSuccess && MT == 1)
+        e = cudaFuncSetAttribute(gemv_q40_kernel<1, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev].store(true, std::memory_order_release);
     return e;
 }
@@ -457,7 +474,8 @@ cudaError_t launch_q40_mt(const uint8_t* blocks, Q40Args a, cudaStream_t stream,
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_q40_kernel<MT>, bmap, a);
+    if (MT == 1 && a.M == 1) return cudaLaunchKernelEx(&cfg, gemv_q40_kernel<1, true>, bmap, a);
+    return cudaLaunchKernelEx(&cfg, gemv_q40_kernel<MT, false>, bmap, a);
 }
 
 }  // namespace
