@@ -527,7 +527,7 @@ bool fmt_layout(FmtPlan& p, int M, int K, int Gs, bool zp, int T, int nst, const
 }
 
 // The unit size: the fewest waves of CTAs, then the most CTAs per wave,
-// with the deepest ring (up to 6 stages) that keeps the CTAs per SM.
+// with the deepest ring (2 to 6 stages) that keeps the CTAs per SM.
 template <int MT>
 FmtPlan plan_fmt(int M, int N, int K, int Gs, bool zp, const DeviceCtx& ctx) {
     FmtPlan best;
@@ -535,6 +535,13 @@ FmtPlan plan_fmt(int M, int N, int K, int Gs, bool zp, const DeviceCtx& ctx) {
     for (int T = 1; T <= 4; T *= 2) {
         FmtPlan p;
         if (!fmt_layout<MT>(p, M, K, Gs, zp, T, 3, ctx)) continue;
+        {   // a 2-stage ring when that fits more CTAs per SM (the large
+            // slabs of groups of 32: 64-row units at K = 4096 go from 2 to 3)
+            FmtPlan q2;
+            if (fmt_layout<MT>(q2, M, K, Gs, zp, T, 2, ctx) &&
+                fmt_occupancy<MT>(q2.smem) > fmt_occupancy<MT>(p.smem))
+                p = q2;
+        }
         const int occ = fmt_occupancy<MT>(p.smem);
         const long long units = ((long long)N + 16 * T - 1) / (16 * T);
         if (occ == 0 || units > 65535) continue;
