@@ -1055,7 +1055,7 @@ constexpr int kSubnormalMinGroups = 16;  // groups per warp and x-sum round
 constexpr double kSmBytesPerUs = 36.0e3;
 constexpr double kCtaBytesPerUs = 14.0e3;
 constexpr double kXBytesPerUs = 32.0e3;
-constexpr double kSplitReduceUs = 1.6;
+constexpr double kSplitReduceUs = 3.5;
 
 template <int MT>
 double launch_cost(long long units, long long slots, double w_bytes, double x_bytes, int S,
