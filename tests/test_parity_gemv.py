@@ -210,7 +210,9 @@ def test_long_units_all_rows(w4lib, kind, M):
 # partial ring stage (K = 11008: 172 chunks; K = 1920: 30).
 SUB_BLOCK_CASES = [(1000, 2048, 1), (1000, 2048, 4), (4096, 4096, 1),
                    (4096, 4096, 2), (6144, 4096, 1), (4136, 11008, 1), (8000, 1920, 1),
-                   (8000, 1920, 4), (24000, 1024, 1), (24000, 1024, 3), (16384, 2048, 2)]
+                   (8000, 1920, 4), (24000, 1024, 1), (24000, 1024, 3), (16384, 2048, 2),
+                   # x slices of 8 rows (M = 5..8 units: 16-row units beat K splits there)
+                   (4096, 4096, 8), (3584, 3584, 8), (4608, 3584, 7)]
 
 
 @pytest.mark.parametrize("N,K,M", SUB_BLOCK_CASES)
