@@ -117,6 +117,26 @@ def test_persistent_tail_units_all_rows(w4lib, M, K, tail_rows):
     assert np.array_equal(run_gemm(x16, q, s), y)
 
 
+@pytest.mark.parametrize("M", [1, 4])
+def test_persistent_short_k_many_blocks_all_rows(w4lib, M):
+    """A persistent launch at K = 256 (one ring stage per block) whose CTAs
+    walk three or more blocks: the producer reuses a scale-slab buffer before
+    its ring wraps, so it must have issued x before it waits for the
+    consumers to free that buffer.  N ends in a ragged block; every row is
+    checked."""
+    K = 256
+    G = w4.gemm_plan(M, 200_000, K)["ctas"]
+    N = 128 * (3 * G) + 128 * (G // 5) - 37
+    plan = w4.gemm_plan(M, N, K)
+    assert plan["blocks_per_cta"] >= 3 and plan["ctas"] == G, plan
+    w16, q, s = quantized(N, K, 75)
+    x16 = acts(M, K, 76 + M)
+    w4.device_status()  # clear
+    y = run_gemm(x16, q, s)
+    assert w4.device_status() == 0  # no wait timed out
+    assert_close(y, oracle.gemm(x16, q, s), f"M={M} N={N} K={K} {plan}")
+
+
 @pytest.mark.parametrize("M", [5, 9, 16])
 @pytest.mark.parametrize("K", [256, 1152])
 def test_persistent_x_in_ring_all_rows(w4lib, M, K):

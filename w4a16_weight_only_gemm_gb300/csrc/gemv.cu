@@ -494,6 +494,9 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const CUtenso
                     const int rb = (int)blockIdx.y + j * (int)gridDim.y;
                     // --- scale slab of block rb ---
                     const int sbuf = j & (a.n_sbuf - 1);
+                    // a slab buffer frees only after the consumers, who need
+                    // x first, finish a block with it
+                    if (j >= a.n_sbuf && !x_issued) issue_x();
                     if (j >= a.n_sbuf &&
                         !mbar_wait(sbase + kBarSEmpty + 8 * sbuf, ((j >> (a.n_sbuf - 1)) - 1) & 1,
                                    a.timeout_ns, a.status)) {
@@ -547,6 +550,7 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap* wmap, const CUtenso
                     // tT tiles x 32 / tT chunks through the tensor map.
                     W4A16_TAIL_GEOMETRY
                     const int sbuf = nblk & (a.n_sbuf - 1);
+                    if (nblk >= a.n_sbuf && !x_issued) issue_x();
                     if (nblk >= a.n_sbuf &&
                         !mbar_wait(sbase + kBarSEmpty + 8 * sbuf, ((nblk >> (a.n_sbuf - 1)) - 1) & 1,
                                    a.timeout_ns, a.status))
