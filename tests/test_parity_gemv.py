@@ -117,11 +117,12 @@ def test_persistent_tail_units_all_rows(w4lib, M, K, tail_rows):
     assert np.array_equal(run_gemm(x16, q, s), y)
 
 
-@pytest.mark.parametrize("M", [1, 4])
+@pytest.mark.parametrize("M", [1, 4, 9, 16])
 def test_persistent_short_k_many_blocks_all_rows(w4lib, M):
     """A persistent launch at K = 256 (one ring stage per block) whose CTAs
     walk three or more blocks: the producer reuses a scale-slab buffer before
-    its ring wraps, so it must have issued x before it waits for the
+    its ring wraps, so it must have issued x (M <= 4: the CTA-wide slice;
+    M > 4: the boxes of the stages issued so far) before it waits for the
     consumers to free that buffer.  N ends in a ragged block; every row is
     checked."""
     K = 256
