@@ -288,3 +288,40 @@ def test_llama3_8b_decode_shapes(w4lib, idx):
 def test_decode_sweep(w4lib, M, idx):
     shapes = workloads.LLAMA3_8B + workloads.QWEN25_7B
     _sampled(shapes[idx], M, "decode_sweep", idx)
+
+
+def _fuzz_cases():
+    """Seeded shapes across the planner's regimes: unit launches, K splits,
+    persistent grids with and without partial last rounds, short and long K
+    (weights kept under ~60 M so the oracle quantizes them in a second)."""
+    rng = np.random.default_rng(20261203)
+    ks = [128, 256, 384, 512, 768, 1152, 2048, 3584, 4096]
+    cases = []
+    for _ in range(24):
+        M = int(rng.integers(1, 17))
+        K = int(rng.choice(ks))
+        N = int(rng.integers(1000, max(4096, 60_000_000 // K)))
+        cases.append((M, N, K))
+    return cases
+
+
+@pytest.mark.parametrize("M,N,K", _fuzz_cases())
+def test_planner_regimes_fuzz(w4lib, M, N, K):
+    """Whatever launch the planner picks: no wait times out, sampled rows
+    (the first and last of a block included) meet the bar, and a repeat call
+    is bit-identical."""
+    plan = w4.gemm_plan(M, N, K)
+    w16, q, s = quantized.__wrapped__(N, K, 90 + M)
+    x16 = acts.__wrapped__(M, K, 91 + M)
+    w4.device_status()  # clear
+    qt, st = as_device(q, s)
+    r = w4.repack(qt)
+    x = from_bits16(x16)
+    y1 = w4.gemm(x, r, st)
+    y2 = w4.gemm(x, r, st)
+    torch.cuda.synchronize()
+    assert w4.device_status() == 0, plan
+    y = y1.float().cpu().numpy().astype(np.float64)
+    assert np.array_equal(y, y2.float().cpu().numpy().astype(np.float64)), plan
+    rows = sample_rows(N, 192, 92 + M)
+    assert_close(y[:, rows], oracle.gemm_rows(x16, q, s, rows), f"M={M} N={N} K={K} {plan}")
