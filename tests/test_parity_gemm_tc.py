@@ -152,3 +152,37 @@ def test_prefill_full_size(w4lib, idx):
     y = run_gemm(x16, q, s)
     rows = sample_rows(lin.N, 96, sw)
     assert_close(y[:, rows], oracle.gemm_rows(x16, q, s, rows), lin.name)
+
+
+def _fuzz_cases():
+    """Seeded prefill shapes across the tile plans: single CTAs, CTA pairs of
+    128- and 96-row CTAs, K split over clusters; ragged M, N and K tails."""
+    rng = np.random.default_rng(20261204)
+    cases = []
+    for _ in range(12):
+        M = int(rng.integers(17, 700))
+        K = 128 * int(rng.integers(1, 65))
+        N = int(rng.integers(100, max(200, min(30000, 40_000_000 // K))))
+        cases.append((M, N, K))
+    return cases
+
+
+@pytest.mark.parametrize("M,N,K", _fuzz_cases())
+def test_tile_plans_fuzz(w4lib, M, N, K):
+    """Whatever tile plan a shape gets: no wait times out, sampled columns
+    (the first and last weight rows of a block included) meet the bar for
+    every x row, and a repeat call is bit-identical."""
+    w16, q, s = quantized.__wrapped__(N, K, 95)
+    x16 = acts.__wrapped__(M, K, 96)
+    qt, st = as_device(q, s)
+    r = w4.repack(qt)
+    x = from_bits16(x16)
+    w4.device_status()  # clear
+    y1 = w4.gemm(x, r, st)
+    y2 = w4.gemm(x, r, st)
+    torch.cuda.synchronize()
+    assert w4.device_status() == 0
+    y = y1.float().cpu().numpy().astype(np.float64)
+    assert np.array_equal(y, y2.float().cpu().numpy().astype(np.float64))
+    rows = sample_rows(N, 96, 97)
+    assert_close(y[:, rows], oracle.gemm_rows(x16, q, s, rows), f"M={M} N={N} K={K}")
