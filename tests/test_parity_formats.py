@@ -216,3 +216,42 @@ def test_awq_llama3_8b_gate_up_m1(w4lib):
     rows = sample_rows(lin.N, 256, sw)
     y_ref = oracle.gemm_rows(oracle.scale_activations(x16, alpha16), q, s, rows, 128)
     assert_close(y[:, rows].float().cpu().numpy(), y_ref, "awq gate_up")
+
+
+def _fuzz_cases():
+    """Seeded format calls across the unit plans (16/32/64-row units, 2- to
+    6-stage rings, group-blocked and row-major slabs) and, for M > 16, the
+    tensor-core path; ragged N, every group size."""
+    rng = np.random.default_rng(20261205)
+    groups = [32, 64, 128, w4.PER_CHANNEL]
+    cases = []
+    for _ in range(16):
+        M = int(rng.choice([1, 2, 3, 4, 7, 8, 9, 13, 16, 40, 300]))
+        group = int(rng.choice(groups))
+        asym = bool(rng.integers(0, 2))
+        K = 128 * int(rng.integers(1, 48))
+        N = int(rng.integers(100, max(200, min(60000, 30_000_000 // K))))
+        cases.append((M, N, K, group, asym))
+    return cases
+
+
+@pytest.mark.parametrize("M,N,K,group,asym", _fuzz_cases())
+def test_formats_plans_fuzz(w4lib, M, N, K, group, asym):
+    """Whatever launch a format call gets: no wait times out, sampled rows
+    meet the bar, and a repeat call is bit-identical."""
+    q, s, z = quantized_fmt.__wrapped__(N, K, 310, group, asym)
+    x16 = acts.__wrapped__(M, K, 311 + M)
+    r = w4.repack(u8(q))
+    st = from_bits16(s)
+    zt = u8(z) if z is not None else None
+    x = from_bits16(x16)
+    w4.device_status()  # clear
+    y1 = w4.gemm_ex(x, r, st, zt, group)
+    y2 = w4.gemm_ex(x, r, st, zt, group)
+    torch.cuda.synchronize()
+    assert w4.device_status() == 0
+    y = y1.float().cpu().numpy().astype(np.float64)
+    assert np.array_equal(y, y2.float().cpu().numpy().astype(np.float64))
+    rows = sample_rows(N, 96, 312)
+    y_ref = oracle.gemm_rows(x16, q, s, rows, group, zeros=z)
+    assert_close(y[:, rows], y_ref, f"g={group} asym={asym} M={M} N={N} K={K}")
