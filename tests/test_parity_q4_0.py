@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import assert_close, from_bits16, u8
+from gpu_util import assert_close, bits16, from_bits16, u8
 from parity_data import acts, quantized, sample_rows
 import w4a16_weight_only_gemm_gb300 as w4
 from w4a16_weight_only_gemm_gb300 import synthetic, workloads
@@ -83,3 +83,36 @@ def test_llama3_8b_shapes_m1(w4lib, idx):
     torch.cuda.synchronize()
     rows = sample_rows(lin.N, 256, sw)
     assert_close(y[:, rows].float().cpu().numpy(), oracle.gemm_q4_0(x16, blocks, rows), lin.name)
+
+
+def _fuzz_cases():
+    """Seeded Q4_0 calls across the unit plans (16 to 128 rows per CTA, one
+    or several waves), M = 1 (the odd-column skip) and M > 1, ragged N."""
+    rng = np.random.default_rng(20261206)
+    cases = []
+    for _ in range(10):
+        M = int(rng.choice([1, 1, 2, 4, 8, 9, 16]))
+        K = 256 * int(rng.integers(1, 40))
+        N = int(rng.integers(50, max(100, min(150000, 30_000_000 // K))))
+        cases.append((M, N, K))
+    return cases
+
+
+@pytest.mark.parametrize("M,N,K", _fuzz_cases())
+def test_q4_0_plans_fuzz(w4lib, M, N, K):
+    """Whatever unit plan a call gets: no wait times out, sampled rows meet
+    the bar, and a repeat call is bit-identical."""
+    w16 = bits16(synthetic.master_weight(N, K, 630))
+    blocks = oracle.quantize_q4_0(w16)
+    x16 = acts.__wrapped__(M, K, 631 + M)
+    bt = u8(blocks)
+    x = from_bits16(x16)
+    w4.device_status()  # clear
+    y1 = w4.gemm_q4_0(x, bt)
+    y2 = w4.gemm_q4_0(x, bt)
+    torch.cuda.synchronize()
+    assert w4.device_status() == 0
+    y = y1.float().cpu().numpy()
+    assert np.array_equal(y, y2.float().cpu().numpy())
+    rows = sample_rows(N, 96, 632)
+    assert_close(y[:, rows], oracle.gemm_q4_0(x16, blocks, rows), f"q4_0 M={M} N={N} K={K}")

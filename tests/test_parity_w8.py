@@ -69,3 +69,34 @@ def test_llama3_8b_shapes_m1(w4lib, idx):
     torch.cuda.synchronize()
     rows = sample_rows(lin.N, 256, sw)
     assert_close(y[:, rows].float().cpu().numpy(), oracle.gemm_rows_w8(x16, q, s, rows), lin.name)
+
+
+def _fuzz_cases():
+    """Seeded W8A16 calls across the unit plans, ragged N and K tails."""
+    rng = np.random.default_rng(20261207)
+    cases = []
+    for _ in range(8):
+        M = int(rng.choice([1, 3, 8, 9, 16]))
+        K = 128 * int(rng.integers(1, 60))
+        N = int(rng.integers(50, max(100, min(100000, 20_000_000 // K))))
+        cases.append((M, N, K))
+    return cases
+
+
+@pytest.mark.parametrize("M,N,K", _fuzz_cases())
+def test_w8_plans_fuzz(w4lib, M, N, K):
+    """Whatever unit plan a call gets: no wait times out, sampled rows meet
+    the bar, and a repeat call is bit-identical."""
+    q8, s8 = oracle.quantize_w8(bits16(synthetic.master_weight(N, K, 640)))
+    x16 = acts.__wrapped__(M, K, 641 + M)
+    qt, st = u8(q8), from_bits16(s8)
+    x = from_bits16(x16)
+    w4.device_status()  # clear
+    y1 = w4.gemm_w8(x, qt, st)
+    y2 = w4.gemm_w8(x, qt, st)
+    torch.cuda.synchronize()
+    assert w4.device_status() == 0
+    y = y1.float().cpu().numpy()
+    assert np.array_equal(y, y2.float().cpu().numpy())
+    rows = sample_rows(N, 96, 642)
+    assert_close(y[:, rows], oracle.gemm_rows_w8(x16, q8, s8, rows), f"w8 M={M} N={N} K={K}")
